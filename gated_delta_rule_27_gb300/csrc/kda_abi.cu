@@ -1,0 +1,106 @@
+// kda_abi.cu -- the extern "C" entry points of libkda: argument checks,
+// path selection and launches.  Every check here runs on the host before
+// anything is enqueued; the kernels themselves live in the other files.
+#include <limits.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool supported_d(int32_t d) { return d == 16 || d == 64 || d == 128; }
+bool supported_chunk(int32_t L) { return L == 16 || L == 32 || L == 64; }
+bool valid_dtype(kda_dtype dt) { return dt == KDA_F32 || dt == KDA_BF16; }
+
+kda::Path prefill_path(int32_t d, kda_dtype dt, int32_t L) {
+    (void)d; (void)dt; (void)L;
+    return kda::PATH_SIMT;
+}
+
+kda_status shape_check(int32_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                       kda_dtype dt, int32_t chunk) {
+    if (total_tokens < 0 || num_seqs < 0 || H <= 0 || H > 65535) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dt)) return KDA_ERR_INVALID_ARG;
+    if (d_k != d_v || !supported_d(d_k) || !supported_chunk(chunk)) return KDA_ERR_UNSUPPORTED;
+    // every row index (token * H + head) * d must fit the kernels' 32-bit token arithmetic
+    if ((int64_t)total_tokens * H > INT_MAX || (int64_t)num_seqs * H * 8 > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+size_t kda_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                                  kda_dtype in_dtype, int32_t chunk_size) {
+    const int32_t L = chunk_size == 0 ? 64 : chunk_size;
+    if (shape_check(total_tokens, num_seqs, H, d_k, d_v, in_dtype, L) != KDA_OK) return 0;
+    return kda::ws_layout(total_tokens, num_seqs, H, d_k, d_v, L, prefill_path(d_k, in_dtype, L)).total;
+}
+
+kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
+                               int32_t d_k, int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0,
+                               void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    const int32_t L = chunk_size == 0 ? 64 : chunk_size;
+    kda_status st = shape_check(total_tokens, num_seqs, H, d_k, d_v, in_dtype, L);
+    if (st != KDA_OK) return st;
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o)) return KDA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
+        if (o == q || o == k || o == v || o == (const void *)g) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned16(S0) || !aligned16(S_final)) return KDA_ERR_INVALID_ARG;
+    const kda::Path path = prefill_path(d_k, in_dtype, L);
+    const kda::WsLayout lay = kda::ws_layout(total_tokens, num_seqs, H, d_k, d_v, L, path);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < lay.total)
+        return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0,
+                                     o, S_final, workspace, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_prefill_check(const void *workspace, void *stream) {
+    if (!workspace) return KDA_ERR_INVALID_ARG;
+    int32_t flag = -1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    return flag == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                           float *S_inout, void *o, void *stream) {
+    if (num_seqs < 0 || H <= 0 || !valid_dtype(in_dtype)) return KDA_ERR_INVALID_ARG;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * H > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !S_inout || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(S_inout) || !aligned16(o))
+        return KDA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v || o == (const void *)S_inout) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_seqs, H, d_k, in_dtype, S_inout, o,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

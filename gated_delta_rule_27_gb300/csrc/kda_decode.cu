@@ -1,0 +1,130 @@
+// kda_decode.cu -- fused recurrent decode step (one new token per sequence).
+//
+// Lecture 04, section 2: in decode the state is already in memory and one
+// fused step is the natural operation.  Per (sequence, head):
+//
+//     S' = D S                 (D = diag(exp(g)), scales the d_k rows)
+//     x  = S'^T k,  y = S'^T q
+//     u  = beta (v - x)
+//     S  = S' + k u^T          (= (I - beta k k^T) D S + beta k v^T)
+//     o  = S^T q = y + (q . k) u
+//
+// The step is bound by HBM: the fp32 state is read once and written once and
+// every other operand is tiny.  One CTA owns one (sequence, head) state; each
+// warp owns a band of 16 rows and each lane four adjacent d_v columns, so a
+// warp's row load is one contiguous 512-byte transaction (d = 128).  The
+// band's 16 float4 loads are all issued before any arithmetic, the decayed
+// band stays in registers, and the two d_k reductions (x, y) are finished
+// through shared memory in a fixed order, so the result is deterministic.
+// State traffic uses streaming (evict-first) loads and stores: the state is
+// touched once per step and is far larger than L2.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kRows = 16;  // rows of S per thread
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__((D / 4) * (D / kRows))
+decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+                   const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ S,
+                   Tin *__restrict__ o) {
+    constexpr int CG = D / 4;        // column groups (float4)
+    constexpr int RG = D / kRows;    // row bands
+    constexpr int NT = CG * RG;
+    __shared__ float s_q[D], s_k[D], s_dec[D], s_u[D];
+    __shared__ float s_x[RG][D], s_y[RG][D];
+    __shared__ float s_qk;
+
+    const int head = blockIdx.x;  // flattened (seq, head)
+    const int tid = threadIdx.x;
+    const int cg = tid % CG, rg = tid / CG;
+    const size_t vec = (size_t)head * D;
+    float4 *Sv = reinterpret_cast<float4 *>(S + (size_t)head * D * D);
+
+    // Issue the state loads first: they are the long pole.
+    float4 s[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) s[j] = __ldcs(&Sv[(size_t)(rg * kRows + j) * CG + cg]);
+
+    for (int i = tid; i < D; i += NT) {
+        s_q[i] = to_f32(q[vec + i]);
+        s_k[i] = to_f32(k[vec + i]);
+        s_dec[i] = expf(g[vec + i]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int i = 0; i < D; ++i) acc = fmaf(s_q[i], s_k[i], acc);
+        s_qk = acc;
+    }
+
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const int r = rg * kRows + j;
+        const float d = s_dec[r], kr = s_k[r], qr = s_q[r];
+        s[j].x *= d; s[j].y *= d; s[j].z *= d; s[j].w *= d;
+        x.x = fmaf(kr, s[j].x, x.x); x.y = fmaf(kr, s[j].y, x.y);
+        x.z = fmaf(kr, s[j].z, x.z); x.w = fmaf(kr, s[j].w, x.w);
+        y.x = fmaf(qr, s[j].x, y.x); y.y = fmaf(qr, s[j].y, y.y);
+        y.z = fmaf(qr, s[j].z, y.z); y.w = fmaf(qr, s[j].w, y.w);
+    }
+    *reinterpret_cast<float4 *>(&s_x[rg][cg * 4]) = x;
+    *reinterpret_cast<float4 *>(&s_y[rg][cg * 4]) = y;
+    __syncthreads();
+
+    const float b = beta[head];
+    for (int c = tid; c < D; c += NT) {
+        float xs = 0.f, ys = 0.f;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) { xs += s_x[r][c]; ys += s_y[r][c]; }
+        const float u = b * (to_f32(v[vec + c]) - xs);
+        s_u[c] = u;
+        o[vec + c] = from_f32<Tin>(fmaf(s_qk, u, ys));
+    }
+    __syncthreads();
+
+    const float4 u = *reinterpret_cast<const float4 *>(&s_u[cg * 4]);
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const float kr = s_k[rg * kRows + j];
+        float4 n;
+        n.x = fmaf(kr, u.x, s[j].x); n.y = fmaf(kr, u.y, s[j].y);
+        n.z = fmaf(kr, u.z, s[j].z); n.w = fmaf(kr, u.w, s[j].w);
+        __stcs(&Sv[(size_t)(rg * kRows + j) * CG + cg], n);
+    }
+}
+
+template <typename Tin, int D>
+cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
+                     float *S, void *o, cudaStream_t st) {
+    constexpr int NT = (D / 4) * (D / kRows);
+    decode_step_kernel<Tin, D><<<heads, NT, 0, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, S,
+                                                     (Tin *)o);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
+                     int d, float *S, void *o, cudaStream_t st) {
+    switch (d) {
+        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, heads, S, o, st);
+        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, heads, S, o, st);
+        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, heads, S, o, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st) {
+    const int heads = num_seqs * H;
+    if (heads == 0) return cudaSuccess;
+    if (dt == KDA_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, beta, heads, d, S, o, st);
+    return launch_t<float>(q, k, v, g, beta, heads, d, S, o, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,132 @@
+// kda_internal.cuh -- shared definitions of libkda's CUDA sources (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------------------
+// Element access.  Inputs q, k, v and the output o are bf16 or fp32; all
+// arithmetic is fp32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// Prefill workspace.  Everything of a chunk that does not depend on the
+// incoming state is written by the chunk-parallel pass and read by the
+// sequential state pass.
+//
+//   [0, 256)            int32 status word (0 = cu_seqlens valid), then padding
+//   doc_slot0           int32 [num_seqs + 1]: first chunk slot of each document
+//                       (exclusive prefix sum of ceil(len / L)), 256-byte padded
+//   records             one per (chunk slot, head), `record_bytes` each
+//
+// The number of chunk slots is bounded by total_tokens / L + num_seqs, so the
+// size depends only on the call's scalar arguments.
+// ---------------------------------------------------------------------------
+enum Path { PATH_SIMT = 0, PATH_TC = 1 };
+
+struct WsLayout {
+    size_t doc_slot0_off;
+    size_t records_off;
+    size_t record_bytes;
+    int64_t max_slots;
+    size_t total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// SIMT record (fp32): W [L,dk] | Ut [L,dv] | Qp [L,dk] | Oloc [L,dv] | Kend [L,dk] | gamma [dk]
+struct SimtRecord {
+    size_t W, Ut, Qp, Oloc, Kend, gamma, bytes;
+};
+__host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
+    SimtRecord r;
+    size_t off = 0;
+    r.W = off;     off += (size_t)L * dk * 4;
+    r.Ut = off;    off += (size_t)L * dv * 4;
+    r.Qp = off;    off += (size_t)L * dk * 4;
+    r.Oloc = off;  off += (size_t)L * dv * 4;
+    r.Kend = off;  off += (size_t)L * dk * 4;
+    r.gamma = off; off += (size_t)dk * 4;
+    r.bytes = align256(off);
+    return r;
+}
+
+// Tensor-core record (d = 128, L = 64).  The MMA operands are bf16 tiles in
+// the exact shared-memory image the tcgen05 state pass consumes (128-byte
+// swizzled, K-major, 8 KB per 64x64 panel), so that pass copies them with one
+// bulk copy each; the epilogue operands stay fp32.
+//   WQ   bf16 [128 rows = 64 rows of W then 64 rows of Qp] x [128 d_k], 4 panels  32 KB
+//   KendT bf16 [128 d_k] x [64 tokens], 2 panels                                  16 KB
+//   Ut   fp32 [64, 128]                                                           32 KB
+//   Oloc fp32 [64, 128]                                                           32 KB
+//   gamma fp32 [128]                                                              512 B
+struct TcRecord {
+    size_t WQ, KendT, Ut, Oloc, gamma, bytes;
+};
+__host__ __device__ inline TcRecord tc_record() {
+    TcRecord r;
+    size_t off = 0;
+    r.WQ = off;    off += 128 * 128 * 2;
+    r.KendT = off; off += 128 * 64 * 2;
+    r.Ut = off;    off += 64 * 128 * 4;
+    r.Oloc = off;  off += 64 * 128 * 4;
+    r.gamma = off; off += 128 * 4;
+    r.bytes = align256(off);
+    return r;
+}
+
+inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {
+    WsLayout w;
+    w.doc_slot0_off = 256;
+    w.records_off = w.doc_slot0_off + align256((size_t)(num_seqs + 1) * 4);
+    w.record_bytes = path == PATH_TC ? tc_record().bytes : simt_record(L, dk, dv).bytes;
+    w.max_slots = total_tokens / L + num_seqs;
+    w.total = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;
+    return w;
+}
+
+// Locates the document and chunk of a chunk slot by binary search over the
+// per-document first-slot table.  Returns false for slots past the last chunk.
+__device__ __forceinline__ bool locate_slot(const int32_t *__restrict__ doc_slot0, const int32_t *__restrict__ cu,
+                                            int num_seqs, int L, int slot, int *doc, int *t0, int *len) {
+    if (slot >= doc_slot0[num_seqs]) return false;
+    int lo = 0, hi = num_seqs - 1;  // find the last doc with doc_slot0[doc] <= slot
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (doc_slot0[mid] <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int start = cu[lo] + (slot - doc_slot0[lo]) * L;
+    *doc = lo;
+    *t0 = start;
+    *len = min(L, cu[lo + 1] - start);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (each returns cudaSuccess or the launch error).
+// ---------------------------------------------------------------------------
+cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st);
+
+cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
+                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st);
+
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                              const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
+                              float *S_final, void *ws, cudaStream_t st);
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st);
+
+}  // namespace kda

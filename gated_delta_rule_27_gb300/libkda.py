@@ -1,0 +1,146 @@
+"""Python binding of libkda's C ABI (include/kda.h).
+
+Argument marshalling only: every step of the recurrence runs in libkda's
+CUDA kernels.  torch supplies device memory and streams.  There is no CPU or
+PyTorch fallback: if libkda.so cannot be loaded, or a tensor is not on a CUDA
+device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+KDA_F32, KDA_BF16 = 0, 1
+
+SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_check",
+           "kda_decode_step")
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, status_string(status)))
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Loads libkda.so (building it first when it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libkda.so is not built (%s); run gated_delta_rule_27_gb300.build" % _build.LIB)
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, fp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, ctypes.c_int, i32]
+    lib.kda_prefill_chunked.restype = ctypes.c_int
+    lib.kda_prefill_chunked.argtypes = [vp, vp, vp, fp, fp, vp, i32, i32, i32, i32, i32, ctypes.c_int, i32,
+                                        fp, vp, fp, vp, ctypes.c_size_t, vp]
+    lib.kda_prefill_check.restype = ctypes.c_int
+    lib.kda_prefill_check.argtypes = [vp, vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, i32, i32, i32, i32, ctypes.c_int, fp, vp, vp]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError("libkda takes bf16 or fp32 q/k/v, got %s" % t.dtype)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libkda takes device tensors; got a %s tensor" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("libkda takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kda_prefill_workspace_size(total_tokens: int, num_seqs: int, H: int, d_k: int, d_v: int, in_dtype: int,
+                               chunk_size: int = 64) -> int:
+    return int(load().kda_prefill_workspace_size(total_tokens, num_seqs, H, d_k, d_v, in_dtype, chunk_size))
+
+
+def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, o, S0=None, S_final=None, workspace=None, chunk_size=64,
+                        stream=None) -> None:
+    """Calls kda_prefill_chunked on caller-owned device tensors (see include/kda.h)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if workspace is None:
+        workspace = new_workspace(T, N, H, d_k, d_v, dt, chunk_size, q.device)
+    rc = load().kda_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H,
+                                    d_k, d_v, dt, chunk_size, _ptr(S0), _ptr(o), _ptr(S_final), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_chunked")
+
+
+def kda_prefill_check(workspace, stream=None) -> int:
+    return int(load().kda_prefill_check(_ptr(workspace), _stream(stream)))
+
+
+def kda_decode_step(q, k, v, g, beta, S_inout, o, stream=None) -> None:
+    """Calls kda_decode_step on caller-owned device tensors (see include/kda.h)."""
+    N, H, d_k = q.shape
+    d_v = v.shape[2]
+    rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), N, H, d_k, d_v, _dtype_code(q),
+                                _ptr(S_inout), _ptr(o), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+
+
+def new_workspace(T, N, H, d_k, d_v, in_dtype, chunk_size, device) -> torch.Tensor:
+    n = kda_prefill_workspace_size(T, N, H, d_k, d_v, in_dtype, chunk_size)
+    if n == 0:
+        raise KdaError(KDA_ERR_UNSUPPORTED, "kda_prefill_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def prefill(q, k, v, g, beta, cu_seqlens, S0=None, chunk_size=64, want_state=True, workspace=None, stream=None):
+    """Allocates o (and S_final) with torch and runs kda_prefill_chunked; returns (o, S_final)."""
+    T, H, d_k = q.shape
+    N = cu_seqlens.numel() - 1
+    o = torch.empty((T, H, v.shape[2]), dtype=v.dtype, device=q.device)
+    S_final = torch.empty((N, H, d_k, v.shape[2]), dtype=torch.float32, device=q.device) if want_state else None
+    kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, o, S0=S0, S_final=S_final, workspace=workspace,
+                        chunk_size=chunk_size, stream=stream)
+    return o, S_final
+
+
+def decode_step(q, k, v, g, beta, S_inout, stream=None):
+    """Allocates o with torch, runs kda_decode_step (S_inout updated in place); returns o."""
+    o = torch.empty_like(v)
+    kda_decode_step(q, k, v, g, beta, S_inout, o, stream=stream)
+    return o

@@ -1,0 +1,130 @@
+/*
+ * kda.h -- C ABI of libkda: the Kimi Delta Attention (KDA) state recurrence
+ * on one GB300 GPU (sm_103a).
+ *
+ * The recurrence (GLM-5.3-Flash Architecture Mastery, course index, "Course
+ * Outcomes": the closed form (I - beta k k^T) D S + beta k v^T; Lecture 11,
+ * section 2, KDA row: the operator order is (I - beta k k^T) D, not
+ * D (I - beta k k^T)):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) D_t S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,             D_t = diag(exp(g_t)),
+ *
+ * per (sequence, head), with S a d_k x d_v fp32 matrix.  Lecture 04,
+ * section 2 asks for two kernel families, selected by request phase: a
+ * chunked prefill kernel (kda_prefill_chunked) and a fused recurrent decode
+ * step (kda_decode_step).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, contiguous, row-major, and
+ *     16-byte aligned; anything else returns KDA_ERR_INVALID_ARG.
+ *   - The caller owns every buffer.  The library allocates no device memory
+ *     and keeps no global state; prefill scratch comes from the caller
+ *     through `workspace` (size from kda_prefill_workspace_size).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  No call synchronises.
+ *   - Argument errors are returned before anything is launched; a failed
+ *     launch returns KDA_ERR_CUDA.  No exception crosses this boundary.
+ *   - Results are deterministic: the same inputs give the same bits, and a
+ *     document inside a packed batch gives the same bits as that document
+ *     run alone.
+ *   - Supported sizes: d_k == d_v in {16, 64, 128}; chunk_size in
+ *     {16, 32, 64} (0 selects 64).  bf16 inputs with d = 128 and chunk 64
+ *     take the tensor-core (tcgen05) prefill; every other combination takes
+ *     the fp32 CUDA-core prefill.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad cu_seqlens, small workspace */
+    KDA_ERR_UNSUPPORTED = 2, /* a size or dtype outside the supported set */
+    KDA_ERR_CUDA = 3,        /* a CUDA launch or driver call failed */
+    KDA_ERR_TIMEOUT = 4      /* reserved: a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+KDA_API const char *kda_status_string(kda_status status);
+
+/*
+ * Bytes of device scratch that kda_prefill_chunked needs for these sizes
+ * (0 when the sizes are invalid).  The bound depends only on the arguments,
+ * not on the document lengths inside cu_seqlens.
+ */
+KDA_API size_t kda_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                                  kda_dtype in_dtype, int32_t chunk_size);
+
+/*
+ * Chunked prefill over packed documents (Lecture 04, sections 1 and 2: each
+ * chunk of L tokens reduces to one affine update in structured
+ * diagonal-plus-rank-one form -- a triangular (WY/UT) solve plus dense
+ * intra-chunk q k^T, k k^T and k S contractions -- and the chunk updates are
+ * then composed in order).
+ *
+ *   q, k       [total_tokens, H, d_k]  in_dtype
+ *   v          [total_tokens, H, d_v]  in_dtype
+ *   g          [total_tokens, H, d_k]  fp32 natural-log decay (D_t = diag(exp(g_t)))
+ *   beta       [total_tokens, H]       fp32 write strength
+ *   cu_seqlens [num_seqs + 1]          int32, device; cu[0] = 0, non-decreasing,
+ *                                      cu[num_seqs] = total_tokens.  The state
+ *                                      restarts at every document start
+ *                                      (Lecture 11, section 2, packing row).
+ *   S0         [num_seqs, H, d_k, d_v] fp32 initial state, or NULL for zeros
+ *   o          [total_tokens, H, d_v]  in_dtype output, o_t = S_t^T q_t
+ *   S_final    [num_seqs, H, d_k, d_v] fp32 state after each document, or NULL.
+ *              S_final may alias S0 (in-place continuation); o must not alias
+ *              any input.
+ *   workspace  device scratch of at least kda_prefill_workspace_size(...) bytes,
+ *              256-byte aligned; its contents on entry do not matter.
+ *
+ * cu_seqlens is read on the device only.  If it is not monotone or does not
+ * end at total_tokens, the kernels write nothing to o or S_final (the call
+ * itself has already returned KDA_OK; kda_prefill_check reports it).
+ */
+KDA_API kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
+                               int32_t d_k, int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0,
+                               void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reports whether the last kda_prefill_chunked call that used this workspace
+ * found cu_seqlens valid.  It copies one word back and SYNCHRONISES `stream`.
+ * Returns KDA_OK or KDA_ERR_INVALID_ARG.
+ */
+KDA_API kda_status kda_prefill_check(const void *workspace, void *stream);
+
+/*
+ * One fused recurrent decode step for num_seqs independent sequences
+ * (Lecture 04, section 2: one new token per sequence, the state already in
+ * memory, one fused step):
+ *
+ *   q, k     [num_seqs, H, d_k] in_dtype     v [num_seqs, H, d_v] in_dtype
+ *   g        [num_seqs, H, d_k] fp32         beta [num_seqs, H] fp32
+ *   S_inout  [num_seqs, H, d_k, d_v] fp32, read and overwritten with S_t
+ *   o        [num_seqs, H, d_v] in_dtype, o_t = S_t^T q_t
+ */
+KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                           float *S_inout, void *o, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */
