@@ -1,0 +1,437 @@
+"""Benchmark of libkda on GB300: chunked prefill tokens/s and decode step time.
+
+One step = one kda_prefill_chunked pass over the prefill workload (B=1,
+H=16, T=4096, d=128, bf16 q/k/v, fp32 gates, chunk 64, zero S0), the
+configuration the headline metric is quoted on.  The decode workload (256
+sequences x 32 heads, fp32 state of 512 MiB) is timed in the same run and
+reported under "decode".  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libkda|reference]
+
+Timing: CUDA events on the launching stream, L2 flushed (a 256 MB write)
+before every timed prefill step (the prefill inputs, 101 MB, would otherwise
+sit in the 129 MB L2); the decode state (512 MiB) is larger than L2.
+Under torchrun (N > 1) every rank runs its own copy of the workload (the
+(sequence, head) chains are independent: weak scaling, no data-path
+collective); value = all ranks' tokens / the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gated_delta_rule_27_gb300 import workloads  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode step µs (state GB/s) on 1 GB300, % of roofline"
+WORKLOAD = "prefill"
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # q,k,v bf16 + g fp32 + beta + o bf16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS if k in p}, "measured (MEASURED_PEAKS.json)"
+    return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json on this box)"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        smax.append(float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# profile summaries committed under profiles/ (ncu DRAM traffic per launch)
+# ---------------------------------------------------------------------------
+def source_hash(kernel_file: str) -> str:
+    h = hashlib.sha256()
+    for rel in (kernel_file, "gated_delta_rule_27_gb300/csrc/kda_internal.cuh",
+                "gated_delta_rule_27_gb300/csrc/kda_tc.cuh"):
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "prefill_prepare_simt": "gated_delta_rule_27_gb300/csrc/kda_prefill_simt.cu",
+    "prefill_state_simt": "gated_delta_rule_27_gb300/csrc/kda_prefill_simt.cu",
+    "chunk_index": "gated_delta_rule_27_gb300/csrc/kda_prefill_simt.cu",
+    "prefill_prepare_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_state_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
+}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.json, or None if absent or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    entry = table.get("%s/%s" % (kernel, workload))
+    if not entry or entry.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# libkda arm
+# ---------------------------------------------------------------------------
+def new_events(n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()  # materialise the underlying cudaEvent_t
+    return evs
+
+
+def bench_prefill(libkda, steps, warmup, dev, rank):
+    w = workloads.WORKLOADS[WORKLOAD]
+    inp = workloads.workload_prefill(WORKLOAD, device=dev)
+    q, k, v, g, beta, cu = inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens
+    T, H, d = q.shape
+    N = inp.num_seqs
+    o = torch.empty((T, H, d), dtype=v.dtype, device=dev)
+    S_final = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, w["chunk"], dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    nk = libkda.PREFILL_MAX_KERNELS + 1
+    per_step = [new_events(nk) for _ in range(steps)]
+    names = None
+
+    def one(evs):
+        return libkda.kda_prefill_chunked_profiled(q, k, v, g, beta, cu, o, evs, S_final=S_final, workspace=ws,
+                                                   chunk_size=w["chunk"])
+
+    warm_ev = new_events(nk)
+    for _ in range(warmup):
+        flush.zero_()
+        one(warm_ev)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        names = one(per_step[i])
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t_wall
+    n = len(names)
+    step_ms = [per_step[i][0].elapsed_time(per_step[i][n]) for i in range(steps)]
+    kern_ms = {names[j]: [per_step[i][j].elapsed_time(per_step[i][j + 1]) for i in range(steps)] for j in range(n)}
+    return dict(T=T, H=H, d=d, N=N, chunk=w["chunk"], step_ms=step_ms, kern_ms=kern_ms, names=names,
+                wall_s=wall_s, launches=n * steps, inp=inp)
+
+
+def bench_e2e(libkda, steps, warmup, dev, inp):
+    """Same prefill through the C ABI with pinned HOST buffers; copies inside the timed region."""
+    w = workloads.WORKLOADS[WORKLOAD]
+    host = [x.to("cpu").pin_memory() for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens)]
+    T, H, d = inp.q.shape
+    N = inp.num_seqs
+    dbuf = [torch.empty_like(x, device=dev) for x in host]
+    o = torch.empty((T, H, d), dtype=inp.v.dtype, device=dev)
+    S_final = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S_final.shape, dtype=S_final.dtype).pin_memory()
+    ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, w["chunk"], dev)
+    h2d = sum(x.numel() * x.element_size() for x in host)
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+
+    def one():
+        for dst, src in zip(dbuf, host):
+            dst.copy_(src, non_blocking=True)
+        libkda.kda_prefill_chunked(*dbuf, o, S_final=S_final, workspace=ws, chunk_size=w["chunk"])
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_final, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    ev = new_events(2)
+    ev[0].record()
+    for _ in range(steps):
+        one()
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / steps
+    return dict(ms=ms, h2d=h2d, d2h=d2h, tokens=T)
+
+
+def bench_decode(libkda, steps, warmup, dev):
+    w = workloads.WORKLOADS["decode"]
+    N, H, d = w["N"], w["H"], w["d"]
+    n_inputs = 64
+    dec = workloads.decode_inputs(n_inputs, N, H, d, w["dtype"], seed=workloads.workload_seed("decode"), device=dev)
+    S = dec.S0.clone()
+    o = torch.empty((N, H, d), dtype=w["dtype"], device=dev)
+    args = lambda t: (dec.q[t], dec.k[t], dec.v[t], dec.g[t], dec.beta[t])
+    for t in range(warmup):
+        libkda.kda_decode_step(*args(t % n_inputs), S, o)
+    torch.cuda.synchronize()
+    evs = [new_events(2) for _ in range(steps)]
+    for i in range(steps):
+        evs[i][0].record()
+        libkda.kda_decode_step(*args(i % n_inputs), S, o)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    us = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]
+    state_bytes = N * H * d * d * 4
+    io_bytes = N * H * (3 * d * 2 + d * 4 + 4 + d * 2)
+    return dict(us=us, state_bytes=state_bytes, io_bytes=io_bytes, N=N, H=H, d=d, launches=steps, dec=dec)
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def cpu_baseline_prefill(inp, budget_s=10.0):
+    """The fp64 oracle on the prefill workload, repeated until ~budget_s of CPU time."""
+    from oracle import oracle
+    f = lambda x: x.detach().to("cpu", torch.float64).numpy()
+    args = [f(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    cu = inp.cu_seqlens.cpu().numpy()
+    threads = min(oracle.default_threads(), inp.num_seqs * inp.q.shape[1])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run(*args, cu, threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return dict(value=reps * inp.total_tokens / el, unit="tokens/s", cores=threads, kind="oracle",
+                sample="the full prefill workload (%d tokens x %d heads), %d repetition(s) in %.1f s"
+                       % (inp.total_tokens, inp.q.shape[1], reps, el))
+
+
+def cpu_baseline_decode(dec, steps=4):
+    from oracle import oracle
+    import numpy as np
+    N, H, d = dec.S0.shape[0], dec.S0.shape[1], dec.S0.shape[2]
+    f = lambda x: x.detach().to("cpu", torch.float64).numpy()
+    S = f(dec.S0)
+    threads = oracle.default_threads()
+    cu = np.arange(N + 1)
+    t0 = time.perf_counter()
+    for t in range(steps):
+        _, S, _ = oracle.run(f(dec.q[t]), f(dec.k[t]), f(dec.v[t]), f(dec.g[t]), f(dec.beta[t]), cu, S0=S,
+                             threads=threads)
+    el = time.perf_counter() - t0
+    return dict(value=el / steps * 1e6, unit="us/step", cores=threads, kind="oracle",
+                sample="%d decode steps over all %d x %d chains" % (steps, N, H))
+
+
+def run_libkda(args):
+    from gated_delta_rule_27_gb300 import libkda
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    libkda.load()
+    pk, pk_src = peaks()
+
+    with ClockSampler(local) as clk:
+        pf = bench_prefill(libkda, args.steps, args.warmup, dev, rank)
+        dc = bench_decode(libkda, max(args.steps, 20), max(args.warmup, 3), dev)
+    clocks = clk.summary()
+    e2e = bench_e2e(libkda, args.steps, args.warmup, dev, pf["inp"])
+
+    T, H = pf["T"], pf["H"]
+    total_ms = sum(pf["step_ms"])
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * T * pf["N"] / (ms_per_step * 1e-3)
+    token_heads = T * pf["N"] * H
+    alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * token_heads + pf["N"] * H * pf["d"] * pf["d"] * 4
+    hbm = pk["hbm_gbs"]
+
+    # dominant kernel of the step and its algorithmic bytes per launch
+    kern_avg = {n: statistics.mean(v) for n, v in pf["kern_ms"].items()}
+    dom = max(kern_avg, key=kern_avg.get)
+    read_bytes = (3 * 128 * 2 + 128 * 4 + 4) * token_heads  # q, k, v, g, beta
+    write_bytes = 128 * 2 * token_heads + pf["N"] * H * pf["d"] * pf["d"] * 4  # o, S_final
+    dom_bytes = read_bytes if "prepare" in dom else (write_bytes if "state" in dom else alg_bytes)
+    achieved = dom_bytes / (kern_avg[dom] * 1e-3) / 1e9
+    traffic = ncu_traffic(dom, WORKLOAD)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic, "algorithmic_bytes": dom_bytes,
+                "avg_launch_ms": kern_avg[dom], "peak_source": pk_src,
+                "kernels_ms": {n: round(m, 5) for n, m in kern_avg.items()}}
+    pass_bw = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    pass_roofline = {"bound": "hbm", "algorithmic_bytes": alg_bytes, "achieved": pass_bw, "peak": hbm,
+                     "unit": "GB/s", "frac": pass_bw / hbm, "roofline_us": alg_bytes / (hbm * 1e9) * 1e6}
+
+    us = sorted(dc["us"])
+    dec_us = statistics.median(us)
+    dec_bytes = 2 * dc["state_bytes"] + dc["io_bytes"]
+    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+    decode = {"workload": "decode N=256 H=32 d=128 bf16 q/k/v, fp32 state 512 MiB",
+              "us_per_step_median": dec_us, "us_per_step_mean": statistics.mean(us),
+              "state_gbs": 2 * dc["state_bytes"] / (dec_us * 1e-6) / 1e9,
+              "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+                           "frac": dec_gbs / hbm, "frac_of_8tbs": dec_gbs / 8000.0, "algorithmic_bytes": dec_bytes,
+                           "traffic": ncu_traffic("decode_step", "decode"), "peak_source": pk_src},
+              "steps": len(us), "gpu_launches": dc["launches"]}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill B=1 H=16 T=4096 d_k=d_v=128 chunk=64 bf16 q/k/v fp32 g/beta zero S0",
+                       "global_batch": world * pf["N"], "seq_len": T, "heads": H, "d": pf["d"],
+                       "chunk": pf["chunk"], "l2": "flushed (256 MB write) before every timed prefill step",
+                       "parallelism": "replicas" if world > 1 else "single-gpu"},
+            "roofline": roofline, "pass_roofline": pass_roofline, "decode": decode,
+            "e2e": {"value": world * e2e["tokens"] / (max_over_ranks(e2e["ms"]) * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+            "gpu_launches": pf["launches"], "clocks": clocks,
+            "wall_s_timed_region": pf["wall_s"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(pf["inp"])
+        line["decode"]["cpu_baseline"] = cpu_baseline_decode(dc["dec"])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import oracle
+    inp = workloads.workload_prefill(WORKLOAD, device="cpu")
+    f = lambda x: x.detach().to(torch.float64).numpy()
+    a = [f(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    cu = inp.cu_seqlens.numpy()
+    threads = min(oracle.default_threads(), inp.num_seqs * inp.q.shape[1])
+    for _ in range(args.warmup):
+        oracle.run(*a, cu, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(*a, cu, threads=threads)
+    el = time.perf_counter() - t0
+    value = args.steps * inp.total_tokens / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill B=1 H=16 T=4096 d_k=d_v=128 chunk=64 bf16 q/k/v fp32 g/beta zero S0",
+                   "global_batch": inp.num_seqs, "seq_len": inp.total_tokens, "heads": inp.q.shape[1], "d": 128,
+                   "parallelism": "cpu threads over (sequence, head) chains"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "the full prefill workload per step, %d step(s)" % args.steps},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_libkda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -49,10 +49,14 @@ size_t kda_prefill_workspace_size(int32_t total_tokens, int32_t num_seqs, int32_
     return kda::ws_layout(total_tokens, num_seqs, H, d_k, d_v, L, prefill_path(d_k, in_dtype, L)).total;
 }
 
-kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
-                               int32_t d_k, int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0,
-                               void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+kda_status prefill_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                        const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
+                        float *S_final, void *workspace, size_t workspace_bytes, void *stream, kda::Marks &marks) {
     const int32_t L = chunk_size == 0 ? 64 : chunk_size;
     kda_status st = shape_check(total_tokens, num_seqs, H, d_k, d_v, in_dtype, L);
     if (st != KDA_OK) return st;
@@ -70,11 +74,40 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, cons
         return KDA_ERR_INVALID_ARG;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace, s);
+    cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace, s, marks);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0,
-                                     o, S_final, workspace, s);
+    e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0, o,
+                                 S_final, workspace, s, marks);
+    marks.end(s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
+                               int32_t d_k, int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0,
+                               void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    kda::Marks marks;
+    return prefill_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype, chunk_size, S0,
+                        o, S_final, workspace, workspace_bytes, stream, marks);
+}
+
+kda_status kda_prefill_chunked_profiled(const void *q, const void *k, const void *v, const float *g,
+                                        const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                        kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
+                                        float *S_final, void *workspace, size_t workspace_bytes, void *stream,
+                                        void *const *events, int32_t *num_kernels, const char **kernel_names) {
+    kda::Marks marks;
+    marks.ev = events;
+    marks.names = kernel_names;
+    const kda_status st = prefill_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
+                                       chunk_size, S0, o, S_final, workspace, workspace_bytes, stream, marks);
+    if (num_kernels) *num_kernels = marks.n;
+    return st;
 }
 
 kda_status kda_prefill_check(const void *workspace, void *stream) {

@@ -114,17 +114,37 @@ __device__ __forceinline__ bool locate_slot(const int32_t *__restrict__ doc_slot
 }
 
 // ---------------------------------------------------------------------------
+// Optional profiling marks: an event recorded before every kernel of a call
+// and one after the last, with the kernels' names (all may be null).
+// ---------------------------------------------------------------------------
+struct Marks {
+    void *const *ev = nullptr;
+    const char **names = nullptr;
+    int n = 0;
+    void before(cudaStream_t s, const char *kernel) {
+        if (ev && n <= KDA_PREFILL_MAX_KERNELS && ev[n]) cudaEventRecord(static_cast<cudaEvent_t>(ev[n]), s);
+        if (names && n < KDA_PREFILL_MAX_KERNELS) names[n] = kernel;
+        ++n;
+    }
+    void end(cudaStream_t s) {
+        if (ev && n <= KDA_PREFILL_MAX_KERNELS && ev[n]) cudaEventRecord(static_cast<cudaEvent_t>(ev[n]), s);
+    }
+};
+
+// ---------------------------------------------------------------------------
 // Launchers (each returns cudaSuccess or the launch error).
 // ---------------------------------------------------------------------------
-cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st);
+cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st,
+                               Marks &marks);
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
-                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st);
+                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st,
+                                Marks &marks);
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, cudaStream_t st);
+                              float *S_final, void *ws, cudaStream_t st, Marks &marks);
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st);

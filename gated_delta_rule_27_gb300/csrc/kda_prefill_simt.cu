@@ -312,7 +312,7 @@ prefill_state_simt(const int32_t *__restrict__ cu, int num_seqs, int H, const fl
 template <typename Tin, int D, int L>
 cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                      float *S_final, void *ws, cudaStream_t st) {
+                      float *S_final, void *ws, cudaStream_t st, Marks &marks) {
     constexpr int TILE = D < 32 ? D : 32;
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, D, D, L, PATH_SIMT);
     char *w = static_cast<char *>(ws);
@@ -323,6 +323,7 @@ cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *
         if ((e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_prep)))
             return e;
         dim3 grid((unsigned)lay.max_slots, (unsigned)H);
+        marks.before(st, "prefill_prepare_simt");
         prep<<<grid, kThreads, sm_prep, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, cu,
                                               num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
                                               lay.record_bytes);
@@ -333,6 +334,7 @@ cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *
     const size_t sm_state = StateSmem<D, L, TILE>::bytes;
     if ((e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_state))) return e;
     const unsigned blocks = (unsigned)((size_t)num_seqs * H * (D / TILE));
+    marks.before(st, "prefill_state_simt");
     state<<<blocks, kThreads, sm_state, st>>>(cu, num_seqs, H, S0, (Tin *)o, S_final, w, lay.doc_slot0_off,
                                               lay.records_off, lay.record_bytes);
     return cudaGetLastError();
@@ -341,11 +343,11 @@ cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *
 template <typename Tin, int D>
 cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g, const float *beta,
                      const int32_t *cu, int num_seqs, int total_tokens, int H, int L, const float *S0, void *o,
-                     float *S_final, void *ws, cudaStream_t st) {
+                     float *S_final, void *ws, cudaStream_t st, Marks &marks) {
     switch (L) {
-        case 16: return launch_dl<Tin, D, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st);
-        case 32: return launch_dl<Tin, D, 32>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st);
-        case 64: return launch_dl<Tin, D, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st);
+        case 16: return launch_dl<Tin, D, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
+        case 32: return launch_dl<Tin, D, 32>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
+        case 64: return launch_dl<Tin, D, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -353,21 +355,23 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g
 template <typename Tin>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g, const float *beta,
                      const int32_t *cu, int num_seqs, int total_tokens, int H, int d, int L, const float *S0,
-                     void *o, float *S_final, void *ws, cudaStream_t st) {
+                     void *o, float *S_final, void *ws, cudaStream_t st, Marks &marks) {
     switch (d) {
-        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st);
-        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st);
-        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st);
+        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
+        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
+        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st) {
+cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st,
+                               Marks &marks) {
     char *w = static_cast<char *>(ws);
     const size_t doc_off = 256;
     const int threads = num_seqs >= 512 ? 1024 : (num_seqs >= 128 ? 256 : 64);
+    marks.before(st, "chunk_index");
     chunk_index_kernel<<<1, threads, 0, st>>>(cu, num_seqs, total_tokens, L, reinterpret_cast<int32_t *>(w),
                                               reinterpret_cast<int32_t *>(w + doc_off));
     return cudaGetLastError();
@@ -375,10 +379,12 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
-                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st) {
+                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st,
+                                Marks &marks) {
     if (dt == KDA_BF16)
-        return launch_t<__nv_bfloat16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st);
-    return launch_t<float>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st);
+        return launch_t<__nv_bfloat16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st,
+                                       marks);
+    return launch_t<float>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st, marks);
 }
 
 }  // namespace kda

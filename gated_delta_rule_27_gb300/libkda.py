@@ -17,8 +17,9 @@ from . import build as _build
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
 KDA_F32, KDA_BF16 = 0, 1
 
-SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_check",
-           "kda_decode_step")
+SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_chunked_profiled",
+           "kda_prefill_check", "kda_decode_step")
+PREFILL_MAX_KERNELS = 4
 
 _lib = None
 
@@ -51,6 +52,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.kda_prefill_chunked.restype = ctypes.c_int
     lib.kda_prefill_chunked.argtypes = [vp, vp, vp, fp, fp, vp, i32, i32, i32, i32, i32, ctypes.c_int, i32,
                                         fp, vp, fp, vp, ctypes.c_size_t, vp]
+    lib.kda_prefill_chunked_profiled.restype = ctypes.c_int
+    lib.kda_prefill_chunked_profiled.argtypes = lib.kda_prefill_chunked.argtypes + [
+        ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_char_p)]
     lib.kda_prefill_check.restype = ctypes.c_int
     lib.kda_prefill_check.argtypes = [vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
@@ -105,6 +109,34 @@ def kda_prefill_chunked(q, k, v, g, beta, cu_seqlens, o, S0=None, S_final=None, 
                                     workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_prefill_chunked")
+
+
+def kda_prefill_chunked_profiled(q, k, v, g, beta, cu_seqlens, o, events, S0=None, S_final=None, workspace=None,
+                                 chunk_size=64, stream=None):
+    """kda_prefill_chunked plus CUDA events around its kernels.
+
+    `events` is a list of torch.cuda.Event (len >= PREFILL_MAX_KERNELS + 1,
+    created with enable_timing=True and already initialised by a record).
+    Returns the names of the launched kernels; events[i] precedes kernel i and
+    events[len(names)] follows the last one.
+    """
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if workspace is None:
+        workspace = new_workspace(T, N, H, d_k, d_v, dt, chunk_size, q.device)
+    n_ev = PREFILL_MAX_KERNELS + 1
+    ev_arr = (ctypes.c_void_p * n_ev)(*[ctypes.c_void_p(e.cuda_event) for e in events[:n_ev]])
+    n_k = ctypes.c_int32(0)
+    names = (ctypes.c_char_p * PREFILL_MAX_KERNELS)()
+    rc = load().kda_prefill_chunked_profiled(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T,
+                                             H, d_k, d_v, dt, chunk_size, _ptr(S0), _ptr(o), _ptr(S_final),
+                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             _stream(stream), ev_arr, ctypes.byref(n_k), names)
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_chunked_profiled")
+    return [names[i].decode() for i in range(n_k.value)]
 
 
 def kda_prefill_check(workspace, stream=None) -> int:

@@ -103,6 +103,23 @@ KDA_API kda_status kda_prefill_chunked(const void *q, const void *k, const void 
                                void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Profiling variant: does exactly what kda_prefill_chunked does and, in
+ * addition, records CUDA events on `stream` around its kernels.  events[i]
+ * (a cudaEvent_t passed as void*, or NULL to skip it) is recorded just
+ * before kernel i, and events[n] just after the last kernel; n is written to
+ * *num_kernels and never exceeds KDA_PREFILL_MAX_KERNELS, so `events` must
+ * hold KDA_PREFILL_MAX_KERNELS + 1 entries.  kernel_names, if not NULL,
+ * receives n static strings naming the kernels in launch order.
+ */
+#define KDA_PREFILL_MAX_KERNELS 4
+KDA_API kda_status kda_prefill_chunked_profiled(const void *q, const void *k, const void *v, const float *g,
+                                        const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                        kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
+                                        float *S_final, void *workspace, size_t workspace_bytes, void *stream,
+                                        void *const *events, int32_t *num_kernels, const char **kernel_names);
+
+/*
  * Reports whether the last kda_prefill_chunked call that used this workspace
  * found cu_seqlens valid.  It copies one word back and SYNCHRONISES `stream`.
  * Returns KDA_OK or KDA_ERR_INVALID_ARG.
