@@ -176,3 +176,31 @@ def decode_step(q, k, v, g, beta, S_inout, stream=None):
     o = torch.empty_like(v)
     kda_decode_step(q, k, v, g, beta, S_inout, o, stream=stream)
     return o
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+_noalloc_ready = False
+
+
+def kda_prefill_chunked_noalloc(q, k, v, g, beta, cu_seqlens, o, S0=None, S_final=None, chunk_size=64,
+                                stream=None) -> None:
+    """Calls kda_prefill_chunked_noalloc: the prefill with the library's static scratch, no workspace argument.
+
+    For callers that must not allocate device memory; see include/kda.h for
+    the scratch limit and the rule that overlapping calls on one GPU race.
+    """
+    global _noalloc_ready
+    lib = load()
+    if not _noalloc_ready:
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+        lib.kda_prefill_chunked_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
+                                                    i32, vp, vp, vp, vp]
+        _noalloc_ready = True
+    T, H, d_k = q.shape
+    N = cu_seqlens.numel() - 1
+    rc = lib.kda_prefill_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H,
+                                         d_k, v.shape[2], _dtype_code(q), chunk_size, _ptr(S0), _ptr(o),
+                                         _ptr(S_final), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_chunked_noalloc")

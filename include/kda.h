@@ -140,6 +140,39 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                            int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
                            float *S_inout, void *o, void *stream);
 
+/*
+ * Chunked prefill that allocates nothing.  The course pages have no
+ * counterpart to this entry point; it repackages kda_prefill_chunked for
+ * callers that cannot give the library device scratch: code that runs while a
+ * stream is being captured into a graph, serving loops whose device memory is
+ * pooled up front and must never see a cudaMalloc (an allocation can also
+ * synchronise the device), and plugins that are handed only their inputs and
+ * outputs.
+ *
+ * Arguments and results are those of kda_prefill_chunked without the
+ * workspace.  The scratch is a static device array of
+ * KDA_NOALLOC_SCRATCH_BYTES inside the library; every GPU that loads the
+ * library's device code holds it until the process exits.  Limit: a call
+ * whose kda_prefill_workspace_size(...) exceeds KDA_NOALLOC_SCRATCH_BYTES
+ * returns KDA_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls on one device share the array: calls whose kernels overlap on
+ *     the GPU (unordered streams) race and corrupt each other's results.
+ *     Calls ordered on one stream are safe.  Nothing in the array needs to
+ *     start at zero.
+ *   - kda_prefill_check is not available for these calls (the status word
+ *     sits in the shared array); invalid cu_seqlens still leave o and S_final
+ *     unwritten.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+KDA_API kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                               int32_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                               kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
+                                               float *S_final, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
