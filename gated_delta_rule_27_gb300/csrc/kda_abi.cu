@@ -13,8 +13,7 @@ bool supported_chunk(int32_t L) { return L == 16 || L == 32 || L == 64; }
 bool valid_dtype(kda_dtype dt) { return dt == KDA_F32 || dt == KDA_BF16; }
 
 kda::Path prefill_path(int32_t d, kda_dtype dt, int32_t L) {
-    (void)d; (void)dt; (void)L;
-    return kda::PATH_SIMT;
+    return (dt == KDA_BF16 && d == 128 && L == 64) ? kda::PATH_TC : kda::PATH_SIMT;
 }
 
 kda_status shape_check(int32_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
@@ -76,8 +75,12 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace, s, marks);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
-    e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0, o,
-                                 S_final, workspace, s, marks);
+    if (path == kda::PATH_TC)
+        e = kda::launch_prefill_tc(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, S0, o, S_final, workspace,
+                                   s, marks);
+    else
+        e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0,
+                                     o, S_final, workspace, s, marks);
     marks.end(s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -62,28 +62,19 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
     return r;
 }
 
-// Tensor-core record (d = 128, L = 64).  The MMA operands are bf16 tiles in
-// the exact shared-memory image the tcgen05 state pass consumes (128-byte
-// swizzled, K-major, 8 KB per 64x64 panel), so that pass copies them with one
-// bulk copy each; the epilogue operands stay fp32.
-//   WQ   bf16 [128 rows = 64 rows of W then 64 rows of Qp] x [128 d_k], 4 panels  32 KB
-//   KendT bf16 [128 d_k] x [64 tokens], 2 panels                                  16 KB
-//   Ut   fp32 [64, 128]                                                           32 KB
-//   Oloc fp32 [64, 128]                                                           32 KB
-//   gamma fp32 [128]                                                              512 B
+// Tensor-core record (d = 128, L = 64).  The state pass's MMA operands are
+// stored as the exact shared-memory images it consumes (bf16, K-major,
+// 128-byte swizzled), so that pass moves each with one bulk copy:
+//   A1    [128 rows: 64 rows of W, then 64 rows of Qp] x [128 d_k]   2 panels  32 KB
+//   A2    Kend^T [128 d_k rows] x [64 tokens]                        1 panel   16 KB
+//   Ut    bf16 [4 column tiles][64 tokens][32 columns]                          16 KB
+//   Oloc  bf16, same tiling as Ut                                               16 KB
+//   gamma fp32 [128]                                                            512 B
 struct TcRecord {
-    size_t WQ, KendT, Ut, Oloc, gamma, bytes;
+    size_t A1, A2, Ut, Oloc, gamma, bytes;
 };
-__host__ __device__ inline TcRecord tc_record() {
-    TcRecord r;
-    size_t off = 0;
-    r.WQ = off;    off += 128 * 128 * 2;
-    r.KendT = off; off += 128 * 64 * 2;
-    r.Ut = off;    off += 64 * 128 * 4;
-    r.Oloc = off;  off += 64 * 128 * 4;
-    r.gamma = off; off += 128 * 4;
-    r.bytes = align256(off);
-    return r;
+__host__ __device__ constexpr TcRecord tc_record() {
+    return TcRecord{0, 32768, 49152, 65536, 81920, 82432};
 }
 
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {
