@@ -62,19 +62,20 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
     return r;
 }
 
-// Tensor-core record (d = 128, L = 64).  The state pass's MMA operands are
-// stored as the exact shared-memory images it consumes (bf16, K-major,
-// 128-byte swizzled), so that pass moves each with one bulk copy:
-//   A1    [128 rows: 64 rows of W, then 64 rows of Qp] x [128 d_k]   2 panels  32 KB
-//   A2    Kend^T [128 d_k rows] x [64 tokens]                        1 panel   16 KB
-//   Ut    bf16 [4 column tiles][64 tokens][32 columns]                          16 KB
-//   Oloc  bf16, same tiling as Ut                                               16 KB
-//   gamma fp32 [128]                                                            512 B
+// Tensor-core record (d = 128, L = 64).  Every state-pass MMA operand is
+// stored as the exact shared-memory image that pass consumes (bf16, 128-byte
+// swizzled), so the state pass moves each with one bulk copy:
+//   Mc    M' = -Kend^T W, K-major [128 d_k rows][128 d_k]        2 panels  32 KB
+//   Kend  MN-major [64 tokens][128 d_k] (A = Kend^T)              2 chunks  16 KB
+//   UtT   K-major [128 d_v rows][64 tokens]; column tile t is rows 32t..  16 KB
+//   Qp    MN-major [128 d_k][64 tokens] (A = Qp, 64 rows)                   16 KB
+//   P     K-major [64 tokens][64 tokens]                                     8 KB
+//   gamma fp32 [128]                                                        512 B
 struct TcRecord {
-    size_t A1, A2, Ut, Oloc, gamma, bytes;
+    size_t Mc, Kend, UtT, Qp, P, gamma, bytes;
 };
 __host__ __device__ constexpr TcRecord tc_record() {
-    return TcRecord{0, 32768, 49152, 65536, 81920, 82432};
+    return TcRecord{0, 32768, 49152, 65536, 81920, 90112, 90624};
 }
 
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {

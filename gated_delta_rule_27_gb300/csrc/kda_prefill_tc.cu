@@ -63,42 +63,46 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     const uint32_t a = tc::smem_u32(p);
     return p + (((a + 1023u) & ~1023u) - a);
 }
+// tcgen05.ld is warp-collective (.sync.aligned): every TMEM load below runs
+// under a warp-uniform condition, and per-lane conditions only guard stores.
+__device__ __forceinline__ bool warp_all(bool b) { return __all_sync(0xffffffffu, b); }
 // Records a timed-out wait in the workspace status word (first writer wins).
 __device__ __forceinline__ void flag_timeout(char *ws) {
     atomicCAS(reinterpret_cast<int32_t *>(ws), 0, (int32_t)KDA_ERR_TIMEOUT);
 }
 
-// Block-major 64 x 64 fp32 matrix: 16 x 16 blocks, block (i, j) contiguous.
-__device__ __forceinline__ int blk_idx(int r, int s) { return (((r >> 4) * 4 + (s >> 4)) << 8) + ((r & 15) << 4) + (s & 15); }
-
 // ---------------------------------------------------------------------------
 // Kernel 1: chunk-parallel preparation
 // ---------------------------------------------------------------------------
+// Compact block-major lower triangle of a 64 x 64 fp32 matrix: the ten
+// 16 x 16 blocks (i, j), j <= i, each contiguous.
+__device__ __forceinline__ int tri_blk(int i, int j) { return ((i * (i + 1)) / 2 + j) << 8; }
+__device__ __forceinline__ int tri_idx(int r, int s) { return tri_blk(r >> 4, s >> 4) + ((r & 15) << 4) + (s & 15); }
+
 struct PrepSmem {
-    static constexpr uint32_t Q = 0;       // q tile (MN-major image, 2 x 8 KB), then exp(b) q in place
-    static constexpr uint32_t K = 16384;   // k tile -> exp(b) k in place (round-2 A) -> W^T (round-3 A, K-major)
-    static constexpr uint32_t V = 32768;   // v tile (round-2 A) -> Ut^T (round-3 A, K-major)
-    static constexpr uint32_t X = 49152;   // round-1 A: 2 panels of 128 rows x 128 B
-    static constexpr uint32_t Y = 81920;   // round-1 B: 2 panels of 64 rows x 128 B
-    // after round 1 the X/Y area is reused
-    static constexpr uint32_t Afp = X;           // fp32 A, block-major (16 KB)
-    static constexpr uint32_t Tfp = X + 16384;   // fp32 T, block-major (16 KB)
-    static constexpr uint32_t P = Y;             // bf16 P, K-major [r][s] (8 KB)
-    static constexpr uint32_t Tb = Y + 8192;     // bf16 T', K-major [r][s] (8 KB)
-    static constexpr uint32_t A1 = X;            // staging of the A1 record image (32 KB), after the solve
-    static constexpr uint32_t Bexact = X;        // fp32 b [64][128] for the exact A/P fallback (32 KB)
+    // X: two 16 KB panels (channels 0-63, 64-127); in each, rows 0-63 hold the k
+    // tile and rows 64-127 the q tile (128-byte swizzled), so that after the
+    // in-place scaling X is round 1's A operand, and its k half (panel stride
+    // 16 KB) is round 2's MN-major A operand.
+    static constexpr uint32_t X = 0;
+    static constexpr uint32_t V = 32768;   // v tile (MN-major chunks of 64 channels), then beta v in place
+    static constexpr uint32_t G = 49152;   // g fp32 [64][128], then b in place; then A, T, T(bf16); then Kend, W^T
+    static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P
+    static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
+    static constexpr uint32_t Tfp = G + 10240;     // compact fp32 T (10 KB)
+    static constexpr uint32_t Tb = G + 20480;      // bf16 T, K-major [r][s] (8 KB)
+    static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB), round-4 A operand
+    static constexpr uint32_t WT = G + 16384;      // W^T, K-major [c][s] (16 KB), round-3 A / round-4 B operand
     static constexpr uint32_t bytes = 98304;
 };
 
-// T = (I + A)^{-1} for A strictly lower triangular (64 x 64, block-major):
+// T = (I + A)^{-1} for A strictly lower triangular (compact block-major):
 // invert the four 16 x 16 diagonal blocks by forward substitution, then fill
-// the sub-diagonals level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+// the sub-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
 __device__ void unit_lower_inverse(float *A, float *T, int tid) {
-    for (int e = tid; e < 4096; e += 128) T[e] = 0.f;
-    __syncthreads();
     if (tid < 64) {
         const int blk = tid >> 4, j = tid & 15;
-        const float *Ab = A + ((blk * 4 + blk) << 8);
+        const float *Ab = A + tri_blk(blk, blk);
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -107,50 +111,95 @@ __device__ void unit_lower_inverse(float *A, float *T, int tid) {
             for (int s = 0; s < r; ++s) acc = fmaf(Ab[(r << 4) + s], x[s], acc);
             x[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
         }
-        float *Tb = T + ((blk * 4 + blk) << 8);
+        float *Td = T + tri_blk(blk, blk);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[(r << 4) + j] = x[r];
+        for (int r = 0; r < 16; ++r) Td[(r << 4) + j] = x[r];
     }
     __syncthreads();
     for (int lvl = 1; lvl < 4; ++lvl) {
         const int nb = 4 - lvl;
-        // M_b = sum_k A_{i,k} T_{k,j}, kept in the (dead) diagonal block b of A
+        // M_b = sum_k A_{i,k} T_{k,j}, kept in the diagonal block b of A (no longer needed)
         for (int e = tid; e < nb * 256; e += 128) {
             const int b = e >> 8, r = (e >> 4) & 15, s = e & 15;
             const int i = b + lvl, j = b;
             float acc = 0.f;
             for (int k = j; k < i; ++k) {
-                const float *Aik = A + ((i * 4 + k) << 8) + (r << 4);
-                const float *Tkj = T + ((k * 4 + j) << 8) + s;
+                const float *Aik = A + tri_blk(i, k) + (r << 4);
+                const float *Tkj = T + tri_blk(k, j) + s;
 #pragma unroll
                 for (int t = 0; t < 16; ++t) acc = fmaf(Aik[t], Tkj[t << 4], acc);
             }
-            A[((b * 4 + b) << 8) + (r << 4) + s] = acc;
+            A[tri_blk(b, b) + (r << 4) + s] = acc;
         }
         __syncthreads();
         for (int e = tid; e < nb * 256; e += 128) {
             const int b = e >> 8, r = (e >> 4) & 15, s = e & 15;
             const int i = b + lvl, j = b;
-            const float *Tii = T + ((i * 4 + i) << 8) + (r << 4);
-            const float *M = A + ((b * 4 + b) << 8) + s;
+            const float *Tii = T + tri_blk(i, i) + (r << 4);
+            const float *M = A + tri_blk(b, b) + s;
             float acc = 0.f;
 #pragma unroll
             for (int t = 0; t < 16; ++t) acc = fmaf(Tii[t], M[t << 4], acc);
-            T[((i * 4 + j) << 8) + (r << 4) + s] = -acc;
+            T[tri_blk(i, j) + (r << 4) + s] = -acc;
         }
         __syncthreads();
     }
 }
 
+// Exact A and P on the CUDA cores for a chunk whose log-decay range is too
+// wide for the factorised tensor-core form: pairwise exp(b_r - b_s) <= 1
+// (s <= r).  Thread t owns row r = t / 2 and the 32 columns s of half t % 2.
+__device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, int Lc, int tid, float (&accA)[32],
+                         float (&accP)[32]) {
+    const int r = tid >> 1, s0 = (tid & 1) * 32;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) { accA[j] = 0.f; accP[j] = 0.f; }
+    if (r >= Lc) return;
+    for (int c = 0; c < kD; ++c) {
+        const uint8_t *panel = X + (uint32_t)(c >> 6) * 16384u;
+        const float brc = B[r * kD + c];
+        const float krc = bf16_at(panel + tc::sw128_offset(r, c & 63));
+        const float qrc = bf16_at(panel + tc::sw128_offset(64 + r, c & 63));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int s = s0 + j;
+            if (s <= r) {
+                const float ks = bf16_at(panel + tc::sw128_offset(s, c & 63)) * expf(brc - B[s * kD + c]);
+                accA[j] = fmaf(krc, ks, accA[j]);
+                accP[j] = fmaf(qrc, ks, accP[j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) accA[j] *= s_beta[r];
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(h[i]);
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
 __global__ void __launch_bounds__(128, 2)
 prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
                    char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t load_bar, mma_bar;
     __shared__ uint32_t tmem_base;
     __shared__ float s_beta[kL];
+    __shared__ __align__(16) float s_bm[kD];
+    __shared__ __align__(16) float s_F[kD];
+    __shared__ __align__(16) float s_Em[kD];
     __shared__ int s_unsafe, s_abort;
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, c = tid;
@@ -167,125 +216,97 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::fence_mbar_init();
         s_unsafe = 0;
         s_abort = 0;
-        tc::mbar_arrive_expect_tx(&load_bar, 3 * 16384);
-        tc::tma_load_3d(sm + PrepSmem::Q, &tm_q, 0, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::Q + 8192, &tm_q, 64, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::K, &tm_k, 0, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::K + 8192, &tm_k, 64, h, t0, &load_bar);
+        tc::mbar_arrive_expect_tx(&load_bar, 6 * 8192 + 32768);
+        tc::tma_load_3d(sm + PrepSmem::X, &tm_k, 0, h, t0, &load_bar);
+        tc::tma_load_3d(sm + PrepSmem::X + 8192, &tm_q, 0, h, t0, &load_bar);
+        tc::tma_load_3d(sm + PrepSmem::X + 16384, &tm_k, 64, h, t0, &load_bar);
+        tc::tma_load_3d(sm + PrepSmem::X + 24576, &tm_q, 64, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::V, &tm_v, 0, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::V + 8192, &tm_v, 64, h, t0, &load_bar);
+        tc::tma_load_3d(sm + PrepSmem::G, &tm_g, 0, h, t0, &load_bar);
     }
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_alloc(&tmem_base, 256);
         tc::tmem_relinquish();
     }
     if (tid < kL) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-
-    // cumulative log-decay of channel c over the chunk, in registers
-    float b[kL];
-    {
-        float acc = 0.f;
-#pragma unroll
-        for (int r = 0; r < kL; ++r) {
-            acc += r < Lc ? g[((size_t)(t0 + r) * H + h) * kD + c] : 0.f;
-            b[r] = acc;
-        }
-    }
-    const int m = (Lc - 1) >> 1;
-    float bm = 0.f, blast = 0.f, bmax = -INFINITY, bmin = INFINITY;
-#pragma unroll
-    for (int r = 0; r < kL; ++r) {
-        if (r == m) bm = b[r];
-        if (r == Lc - 1) blast = b[r];
-        if (r < Lc) { bmax = fmaxf(bmax, b[r]); bmin = fminf(bmin, b[r]); }
-    }
-    if (bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY)) s_unsafe = 1;
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const bool unsafe = s_unsafe != 0;
     if (!tc::mbar_wait(&load_bar, 0)) s_abort = 1;
     __syncthreads();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
 
-    const uint8_t *sq = sm + PrepSmem::Q, *sk = sm + PrepSmem::K;
-    const uint32_t in_off = (uint32_t)(c >> 6) * 8192u;  // channel chunk of the MN-major input tiles
-
+    // cumulative log-decay of channel c, in place; reference token m in the middle
+    float *Gf = reinterpret_cast<float *>(sm + PrepSmem::G);
+    {
+        const int m = (Lc - 1) >> 1;
+        float acc = 0.f, bm = 0.f, blast = 0.f, bmax = -INFINITY, bmin = INFINITY;
+        for (int r = 0; r < Lc; ++r) {
+            acc += Gf[r * kD + c];
+            Gf[r * kD + c] = acc;
+            if (r == m) bm = acc;
+            bmax = fmaxf(bmax, acc);
+            bmin = fminf(bmin, acc);
+        }
+        blast = acc;
+        s_bm[c] = bm;
+        s_F[c] = expf(blast - bm);
+        s_Em[c] = expf(bm);
+        reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
+        if (bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY)) s_unsafe = 1;
+    }
+    __syncthreads();
+    const bool unsafe = s_unsafe != 0;
+    float accA[32], accP[32];
     if (unsafe) {
-        // Exact A and P on the CUDA cores: pairwise exp(b_r - b_s) <= 1 for s <= r.
-        float *Bx = reinterpret_cast<float *>(sm + PrepSmem::Bexact);
-#pragma unroll
-        for (int r = 0; r < kL; ++r) Bx[r * kD + c] = b[r];
-        __syncthreads();
-        float accA[32], accP[32];
-        const int r = tid >> 1, s0 = (tid & 1) * 32;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) { accA[j] = 0.f; accP[j] = 0.f; }
-        for (int cc = 0; cc < kD; ++cc) {
-            const uint32_t off = (uint32_t)(cc >> 6) * 8192u;
-            const float brc = Bx[r * kD + cc];
-            const float krc = bf16_at(sk + off + tc::sw128_offset(r, cc & 63));
-            const float qrc = bf16_at(sq + off + tc::sw128_offset(r, cc & 63));
-#pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const int s = s0 + j;
-                if (s <= r && r < Lc) {
-                    const float e = expf(brc - Bx[s * kD + cc]);
-                    const float ks = bf16_at(sk + off + tc::sw128_offset(s, cc & 63)) * e;
-                    accA[j] = fmaf(krc, ks, accA[j]);
-                    accP[j] = fmaf(qrc, ks, accP[j]);
-                }
-            }
-        }
-        __syncthreads();  // everyone is done with Bx before A overwrites it
-        float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
-        uint8_t *Pb = sm + PrepSmem::P;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int s = s0 + j;
-            Af[blk_idx(r, s)] = s < r ? s_beta[r] * accA[j] : 0.f;
-            st_bf16(Pb + tc::sw128_offset(r, s), s <= r ? accP[j] : 0.f);
-        }
+        exact_ap(sm + PrepSmem::X, Gf, s_beta, Lc, tid, accA, accP);
+        __syncthreads();  // the raw k, q tiles are about to be scaled in place
     }
 
-    // Operands: round-1 A/B (fast path), exp(b) k and exp(b) q in place, Kend^T to the record.
+    // Row-wise operand build: thread t owns token row r = t / 2 and channels 64 (t % 2) .. +63.
+    uint4 kend[8];
     {
-        const float Em = expf(bm), F = expf(blast - bm);
-        uint8_t *X = sm + PrepSmem::X, *Yp = sm + PrepSmem::Y;
-        uint8_t *kq = sm + PrepSmem::K, *qq = sm + PrepSmem::Q;
-        const uint32_t xoff = (uint32_t)(c >> 6) * 16384u, yoff = (uint32_t)(c >> 6) * 8192u;
-        uint8_t *A2row = reinterpret_cast<uint8_t *>(rec + R.A2) + (size_t)c * 128;
-#pragma unroll
-        for (int r8 = 0; r8 < kL; r8 += 8) {
-            uint32_t kend[4];
+        const int r = tid >> 1, half = tid & 1;
+        const bool valid = r < Lc;
+        const float br = s_beta[r];
+        uint8_t *Xp = sm + PrepSmem::X + (uint32_t)half * 16384u;
+        uint8_t *Vp = sm + PrepSmem::V + (uint32_t)half * 8192u;
+        uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)half * 8192u;
+        uint8_t *Kg = reinterpret_cast<uint8_t *>(rec + R.Kend) + (size_t)half * 8192;
+#pragma unroll 2
+        for (int g8 = 0; g8 < 8; ++g8) {
+            const int cc = g8 * 8, c0 = half * 64 + cc;
+            const uint32_t off_k = tc::sw128_offset(r, cc), off_q = tc::sw128_offset(64 + r, cc);
+            float k8[8], q8[8], v8[8], xk[8], xq[8], y8[8], bv[8], ke[8];
+            unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
+            unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
+            unpack8(*reinterpret_cast<const uint4 *>(Vp + off_k), v8);
+            const float4 b0 = *reinterpret_cast<const float4 *>(Gf + r * kD + c0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(Gf + r * kD + c0 + 4);
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int r = r8 + u;
-                const bool valid = r < Lc;
-                const float e1 = valid ? expf(b[r] - bm) : 0.f;
+                const float e1 = valid ? expf(bb[u] - s_bm[c0 + u]) : 0.f;
                 const float inv = valid ? __frcp_rn(e1) : 0.f;
-                const uint32_t io = in_off + tc::sw128_offset(r, c & 63);
-                const float kv = bf16_at(kq + io), qv = bf16_at(qq + io);
-                if (!unsafe) {
-                    st_bf16(X + xoff + tc::sw128_offset(r, c & 63), s_beta[r] * kv * e1);
-                    st_bf16(X + xoff + tc::sw128_offset(64 + r, c & 63), qv * e1);
-                    st_bf16(Yp + yoff + tc::sw128_offset(r, c & 63), kv * inv);
-                }
-                st_bf16(kq + io, kv * e1 * Em);
-                st_bf16(qq + io, qv * e1 * Em);
-                const float ke = kv * F * inv;
-                if (u & 1) kend[u >> 1] |= pack_bf16x2(0.f, ke) & 0xFFFF0000u;
-                else kend[u >> 1] = pack_bf16x2(ke, 0.f) & 0x0000FFFFu;
+                xk[u] = br * k8[u] * e1;
+                xq[u] = q8[u] * e1;
+                y8[u] = k8[u] * inv;
+                bv[u] = br * v8[u];
+                ke[u] = y8[u] * s_F[c0 + u];
             }
-            *reinterpret_cast<uint4 *>(A2row + (((r8 >> 3) ^ (c & 7)) << 4)) =
-                make_uint4(kend[0], kend[1], kend[2], kend[3]);
+            *reinterpret_cast<uint4 *>(Xp + off_k) = pack8(xk);
+            *reinterpret_cast<uint4 *>(Xp + off_q) = pack8(xq);
+            if (!unsafe) *reinterpret_cast<uint4 *>(Yp + off_k) = pack8(y8);
+            *reinterpret_cast<uint4 *>(Vp + off_k) = pack8(bv);
+            kend[g8] = pack8(ke);
+            *reinterpret_cast<uint4 *>(Kg + off_k) = kend[g8];
         }
-        reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
@@ -293,10 +314,27 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_after();
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-    constexpr uint64_t kMnmaj = tc::smem_desc_base(8192, 1024, tc::SW_128B);
     uint32_t mma_phase = 0;
     bool ok = true;
-    if (!unsafe) {
+    float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
+    uint8_t *Pb = sm + PrepSmem::Y;
+    uint8_t *Pg = reinterpret_cast<uint8_t *>(rec + R.P);
+    if (unsafe) {
+        const int r = tid >> 1, s0 = (tid & 1) * 32;
+#pragma unroll
+        for (int j8 = 0; j8 < 32; j8 += 8) {
+            float w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s = s0 + j8 + u;
+                if ((s >> 4) <= (r >> 4)) Af[tri_idx(r, s)] = s < r ? accA[j8 + u] : 0.f;
+                w[u] = s <= r ? accP[j8 + u] : 0.f;
+            }
+            const uint4 pw = pack8(w);
+            *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s0 + j8)) = pw;
+            *reinterpret_cast<uint4 *>(Pg + tc::sw128_offset(r, s0 + j8)) = pw;
+        }
+    } else {
         // round 1: [beta k e1 ; q e1] x (k / e1)^T -> TMEM cols 0..63 (rows 0-63 A, 64-127 P)
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, false, false);
@@ -312,49 +350,56 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = tc::mbar_wait(&mma_bar, mma_phase);
         mma_phase ^= 1;
         tc::tc_fence_after();
-        if (ok) {
-            float v[64];
+        if (warp_all(ok)) {
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float t[16];
-                tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), t);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[q4 * 16 + i] = t[i];
-            }
             if (tid < 64) {
                 const int r = tid;
-                float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
+                const int qmax = (warp * 32 + 31) >> 4;  // warp-uniform trip count
+                for (int q4 = 0; q4 <= qmax; ++q4) {
+                    float t[16];
+                    tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), t);
+                    if (q4 <= (r >> 4)) {
+                        float *dst = Af + tri_blk(r >> 4, q4) + ((r & 15) << 4);
 #pragma unroll
-                for (int s = 0; s < 64; ++s) Af[blk_idx(r, s)] = s < r ? v[s] : 0.f;
+                        for (int i = 0; i < 16; i += 4) {
+                            float4 w;
+                            w.x = q4 * 16 + i + 0 < r ? t[i + 0] : 0.f;
+                            w.y = q4 * 16 + i + 1 < r ? t[i + 1] : 0.f;
+                            w.z = q4 * 16 + i + 2 < r ? t[i + 2] : 0.f;
+                            w.w = q4 * 16 + i + 3 < r ? t[i + 3] : 0.f;
+                            *reinterpret_cast<float4 *>(dst + i) = w;
+                        }
+                    }
+                }
             } else {
                 const int r = tid - 64;
-                uint8_t *Pb = sm + PrepSmem::P;
 #pragma unroll
-                for (int s8 = 0; s8 < 64; s8 += 8) {
-                    float w[8];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float t[16];
+                    tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), t);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) w[u] = (s8 + u) <= r ? v[s8 + u] : 0.f;
-                    *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s8)) =
-                        make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
-                                   pack_bf16x2(w[6], w[7]));
+                    for (int h8 = 0; h8 < 16; h8 += 8) {
+                        float w[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) w[u] = q4 * 16 + h8 + u <= r ? t[h8 + u] : 0.f;
+                        const uint4 pw = pack8(w);
+                        *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, q4 * 16 + h8)) = pw;
+                        *reinterpret_cast<uint4 *>(Pg + tc::sw128_offset(r, q4 * 16 + h8)) = pw;
+                    }
                 }
             }
         }
-        tc::tc_fence_before();
-        if (!ok) s_abort = 1;
-        __syncthreads();
-    } else {
-        __syncthreads();
     }
+    tc::tc_fence_before();
+    if (!ok) s_abort = 1;
+    __syncthreads();
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
 
-    // triangular solve in fp32, then T' = T diag(beta) as the bf16 round-2 B operand
-    float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
+    // triangular solve in fp32, then T as the bf16 round-2 B operand (K-major [r][s])
     float *Tf = reinterpret_cast<float *>(sm + PrepSmem::Tfp);
     unit_lower_inverse(Af, Tf, tid);
     {
@@ -366,10 +411,9 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s = s0 + s8 + u;
-                w[u] = (s <= r ? Tf[blk_idx(r, s)] : 0.f) * s_beta[s];
+                w[u] = s <= r ? Tf[tri_idx(r, s)] : 0.f;
             }
-            *reinterpret_cast<uint4 *>(Tb + tc::sw128_offset(r, s0 + s8)) = make_uint4(
-                pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+            *reinterpret_cast<uint4 *>(Tb + tc::sw128_offset(r, s0 + s8)) = pack8(w);
         }
     }
     tc::fence_async_smem();
@@ -377,14 +421,16 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
 
-    // round 2: W^T = (exp(b) k)^T T'^T -> cols 64..127;  Ut^T = V^T T'^T -> cols 0..63
+    // round 2: (T X_k)^T -> cols 64..127 (W^T once scaled by exp(b_m));  (T beta V)^T = Ut^T -> cols 128..191
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, true, false);
+        constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
+        constexpr uint64_t kVmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
         for (int s = 0; s < 4; ++s) {
             const uint64_t bdesc = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Tb + s * 32));
-            tc::mma_bf16(tmem + 64, tc::smem_desc(kMnmaj, tc::smem_u32(sm + PrepSmem::K + s * 2048)), bdesc, id,
+            tc::mma_bf16(tmem + 64, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + s * 2048)), bdesc, id, s > 0);
+            tc::mma_bf16(tmem + 128, tc::smem_desc(kVmn, tc::smem_u32(sm + PrepSmem::V + s * 2048)), bdesc, id,
                          s > 0);
-            tc::mma_bf16(tmem, tc::smem_desc(kMnmaj, tc::smem_u32(sm + PrepSmem::V + s * 2048)), bdesc, id, s > 0);
         }
         tc::mma_commit(&mma_bar);
     }
@@ -393,35 +439,29 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     mma_phase ^= 1;
     tc::tc_fence_after();
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint8_t *A1s = sm + PrepSmem::A1;
-    const uint32_t a1off = (uint32_t)(c >> 6) * 16384u;
-    __nv_bfloat16 *gUt = reinterpret_cast<__nv_bfloat16 *>(rec + R.Ut) + (size_t)(c >> 5) * 64 * kTile + (c & 31);
-    __nv_bfloat16 *gOl = reinterpret_cast<__nv_bfloat16 *>(rec + R.Oloc) + (size_t)(c >> 5) * 64 * kTile + (c & 31);
-    if (ok) {
-        // W^T and Ut^T rows -> round-3 A operands (K-major [c][s]) over the dead K / V tiles,
-        // W into the A1 staging image, Ut to the record
+    if (warp_all(ok)) {
+        const float em = s_Em[c];
+        uint8_t *UtG = reinterpret_cast<uint8_t *>(rec + R.UtT);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             float w[16], u[16];
             tc::tmem_ld16(tmem + lane_base + 64u + (uint32_t)(q4 * 16), w);
-            tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), u);
+            tc::tmem_ld16(tmem + lane_base + 128u + (uint32_t)(q4 * 16), u);
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8) {
-                const int s8 = q4 * 16 + h8;
-                *reinterpret_cast<uint4 *>(sm + PrepSmem::K + tc::sw128_offset(c, s8)) =
-                    make_uint4(pack_bf16x2(w[h8], w[h8 + 1]), pack_bf16x2(w[h8 + 2], w[h8 + 3]),
-                               pack_bf16x2(w[h8 + 4], w[h8 + 5]), pack_bf16x2(w[h8 + 6], w[h8 + 7]));
-                *reinterpret_cast<uint4 *>(sm + PrepSmem::V + tc::sw128_offset(c, s8)) =
-                    make_uint4(pack_bf16x2(u[h8], u[h8 + 1]), pack_bf16x2(u[h8 + 2], u[h8 + 3]),
-                               pack_bf16x2(u[h8 + 4], u[h8 + 5]), pack_bf16x2(u[h8 + 6], u[h8 + 7]));
-            }
+                float ww[8], uu[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = q4 * 16 + i;
-                st_bf16(A1s + a1off + tc::sw128_offset(r, c & 63), w[i]);
-                gUt[(size_t)r * kTile] = __float2bfloat16_rn(u[i]);
+                for (int i = 0; i < 8; ++i) { ww[i] = w[h8 + i] * em; uu[i] = u[h8 + i]; }
+                const uint32_t off = tc::sw128_offset(c, q4 * 16 + h8);
+                *reinterpret_cast<uint4 *>(sm + PrepSmem::WT + off) = pack8(ww);
+                *reinterpret_cast<uint4 *>(UtG + off) = pack8(uu);
             }
         }
+        // Kend (kept in registers since the operand build) -> round-4 A operand
+        const int r = tid >> 1, half = tid & 1;
+        uint8_t *Ks = sm + PrepSmem::KendS + (uint32_t)half * 8192u;
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) *reinterpret_cast<uint4 *>(Ks + tc::sw128_offset(r, g8 * 8)) = kend[g8];
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
@@ -430,72 +470,92 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_after();
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
 
-    // round 3: (P W)^T = W^T P^T -> cols 64..127;  Oloc^T = Ut^T P^T -> cols 0..63
+    // round 3: W^T P^T = (P W)^T -> cols 0..63;  round 4: Kend^T W -> cols 128..255
     if (tid == 0) {
-        constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id4 = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
         for (int s = 0; s < 4; ++s) {
-            const uint64_t bdesc = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32));
-            tc::mma_bf16(tmem + 64, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::K + s * 32)), bdesc, id, s > 0);
-            tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), bdesc, id, s > 0);
+            const uint64_t wt = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32));
+            tc::mma_bf16(tmem, wt, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + s * 32)), id3, s > 0);
+            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)), wt, id4,
+                         s > 0);
         }
         tc::mma_commit(&mma_bar);
     }
     __syncwarp();
     ok = tc::mbar_wait(&mma_bar, mma_phase);
     tc::tc_fence_after();
-    if (ok) {
-        const uint8_t *qg = sm + PrepSmem::Q;
+    if (warp_all(ok)) {
+        // Qp = exp(b) q - P W, stored MN-major [c][r]; M' = -Kend^T W, stored K-major [c][c']
+        const float em = s_Em[c];
+        const uint8_t *Xq = sm + PrepSmem::X + (uint32_t)(c >> 6) * 16384u;
+        uint8_t *QpG = reinterpret_cast<uint8_t *>(rec + R.Qp);
+        uint8_t *McG = reinterpret_cast<uint8_t *>(rec + R.Mc);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            float pw[16], ol[16];
-            tc::tmem_ld16(tmem + lane_base + 64u + (uint32_t)(q4 * 16), pw);
-            tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), ol);
+            float pw[16];
+            tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), pw);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = q4 * 16 + i;
-                const float qv = bf16_at(qg + in_off + tc::sw128_offset(r, c & 63));
-                st_bf16(A1s + a1off + tc::sw128_offset(64 + r, c & 63), qv - pw[i]);
-                gOl[(size_t)r * kTile] = __float2bfloat16_rn(ol[i]);
+            for (int h8 = 0; h8 < 16; h8 += 8) {
+                float w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = q4 * 16 + h8 + i;
+                    w[i] = bf16_at(Xq + tc::sw128_offset(64 + r, c & 63)) * em - pw[h8 + i];
+                }
+                *reinterpret_cast<uint4 *>(QpG + tc::sw128_offset(c, q4 * 16 + h8)) = pack8(w);
+            }
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            float m[16];
+            tc::tmem_ld16(tmem + lane_base + 128u + (uint32_t)(q8 * 16), m);
+#pragma unroll
+            for (int h8 = 0; h8 < 16; h8 += 8) {
+                float w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = -m[h8 + i];
+                const int cp = q8 * 16 + h8;
+                *reinterpret_cast<uint4 *>(McG + (uint32_t)(cp >> 6) * 16384u + tc::sw128_offset(c, cp & 63)) =
+                    pack8(w);
             }
         }
     }
-    tc::fence_async_smem();
     tc::tc_fence_before();
-    if (!ok) s_abort = 1;
+    if (!ok && tid == 0) flag_timeout(ws);
     __syncthreads();
-    if (s_abort) {
-        if (tid == 0) flag_timeout(ws);
-    } else if (tid == 0) {
-        tc::bulk_s2g(rec + R.A1, A1s, 32768);
-        tc::bulk_commit();
-        tc::bulk_wait_read();
-    }
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
 struct StateSmem {
-    static constexpr uint32_t kBuf = 58368;  // per record buffer (57 KB, 1024-aligned)
-    static constexpr uint32_t A1 = 0, A2 = 32768, Ut = 49152, Ol = 53248, gam = 57344;
-    static constexpr uint32_t SB = 2 * kBuf;       // S^T operand, K-major [32 rows][128 K], 2 panels of 4 KB
-    static constexpr uint32_t UB = SB + 8192;      // U^T operand, K-major [32 rows][64 K], 4 KB
-    static constexpr uint32_t bytes = UB + 4096;
-    static constexpr uint32_t tx = 32768 + 16384 + 4096 + 4096 + 512;
+    // per-chunk record buffer (two of them)
+    static constexpr uint32_t Mc = 0, Kend = 32768, Qp = 49152, P = 65536, UtT = 81920, gam = 86016;
+    static constexpr uint32_t kBuf = 87040;          // 85 KB, 1024-aligned
+    static constexpr uint32_t Zero = 2 * kBuf;       // 16 KB of zeros: rows 64-127 of the Qp operand
+    // S^T operand, K-major [32 rows][128 K], 2 panels of 4 KB, ping-pong: chunk c's MMAs read
+    // SB + (c & 1) * 8 KB while the epilogue writes S_{c+1} into the other half, so the output
+    // MMAs of chunk c (still in flight after the state MMAs complete) never see S_{c+1}.
+    static constexpr uint32_t SB = Zero + 16384;
+    static constexpr uint32_t bytes = SB + 16384;
+    static constexpr uint32_t tx = 32768 + 16384 + 16384 + 8192 + 4096 + 512;
 };
 
 __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int tile, uint64_t *bar) {
     constexpr TcRecord R = tc_record();
     tc::mbar_arrive_expect_tx(bar, StateSmem::tx);
-    tc::bulk_g2s(buf + StateSmem::A1, rec + R.A1, 32768, bar);
-    tc::bulk_g2s(buf + StateSmem::A2, rec + R.A2, 16384, bar);
-    tc::bulk_g2s(buf + StateSmem::Ut, rec + R.Ut + (size_t)tile * 4096, 4096, bar);
-    tc::bulk_g2s(buf + StateSmem::Ol, rec + R.Oloc + (size_t)tile * 4096, 4096, bar);
+    tc::bulk_g2s(buf + StateSmem::Mc, rec + R.Mc, 32768, bar);
+    tc::bulk_g2s(buf + StateSmem::Kend, rec + R.Kend, 16384, bar);
+    tc::bulk_g2s(buf + StateSmem::Qp, rec + R.Qp, 16384, bar);
+    tc::bulk_g2s(buf + StateSmem::P, rec + R.P, 8192, bar);
+    tc::bulk_g2s(buf + StateSmem::UtT, rec + R.UtT + (size_t)tile * 4096, 4096, bar);
     tc::bulk_g2s(buf + StateSmem::gam, rec + R.gamma, 512, bar);
 }
 
@@ -511,7 +571,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                  __nv_bfloat16 *__restrict__ o, float *__restrict__ S_final, char *__restrict__ ws,
                  size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[2], mma1_bar, mma2_bar;
+    __shared__ uint64_t full_bar[2], a_bar, b_bar[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
@@ -532,113 +592,122 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
     if (nchunks > 0) {
+        // zero rows 64-127 of the P operand (both buffers) and the Qp padding block; they are never loaded
+        for (int e = tid; e < 512; e += 128) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm + StateSmem::P + 8192)[e] = z;
+            reinterpret_cast<uint4 *>(sm + StateSmem::kBuf + StateSmem::P + 8192)[e] = z;
+        }
+        for (int e = tid; e < 1024; e += 128) reinterpret_cast<uint4 *>(sm + StateSmem::Zero)[e] = make_uint4(0, 0, 0, 0);
         store_state_operand(sm + StateSmem::SB, i, S);
         tc::fence_async_smem();
+        const char *rec_h = ws + records_off + (size_t)h * record_bytes;
+        const size_t rec_stride = (size_t)H * record_bytes;
         if (tid == 0) {
             tc::mbar_init(&full_bar[0], 1);
             tc::mbar_init(&full_bar[1], 1);
-            tc::mbar_init(&mma1_bar, 1);
-            tc::mbar_init(&mma2_bar, 1);
+            tc::mbar_init(&a_bar, 1);
+            tc::mbar_init(&b_bar[0], 1);
+            tc::mbar_init(&b_bar[1], 1);
             tc::fence_mbar_init();
             s_abort = 0;
-            const char *base = ws + records_off + (size_t)h * record_bytes;
-            for (int c = 0; c < 2 && c < nchunks; ++c)
-                issue_record(sm + c * StateSmem::kBuf, base + (size_t)(first + c) * H * record_bytes, tile,
-                             &full_bar[c]);
+            issue_record(sm, rec_h + (size_t)first * rec_stride, tile, &full_bar[0]);
         }
         if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 64);
+            tc::tmem_alloc(&tmem_base, 128);
             tc::tmem_relinquish();
         }
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
-        const uint32_t tmem = tmem_base;
+        const uint32_t tmem = tmem_base;  // S acc: cols 0..31; O acc: 64..95 / 96..127 (ping-pong)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-        constexpr uint32_t id1 = tc::idesc_bf16_f32(128, kTile, false, false);
-        constexpr uint32_t id2 = tc::idesc_bf16_f32(128, kTile, false, false);
+        constexpr uint64_t kKendMn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
+        constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
+        constexpr uint32_t idMnN = tc::idesc_bf16_f32(128, kTile, true, false);
         const int t_doc = cu[n], t_end = cu[n + 1];
+        bool ok = true;
 
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = 0; c <= nchunks; ++c) {
             const int bsel = c & 1;
             uint8_t *buf = sm + bsel * StateSmem::kBuf;
-            const int t0 = t_doc + c * kL;
-            const int Lc = min(kL, t_end - t0);
-            bool ok = tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
-            if (ok && tid == 0) {
-                // [X; Y] = [W; Qp] S  -> cols 0..31
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
-                    const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                    tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::A1 + ka)),
-                                 tc::smem_desc(kKmaj, tc::smem_u32(sm + StateSmem::SB + kb)), id1, s > 0);
+            if (tid == 0 && c < nchunks) {
+                // B of the previous chunk done -> its buffer is free: prefetch the next record into it
+                if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                if (ok && c + 1 < nchunks)
+                    issue_record(sm + (bsel ^ 1) * StateSmem::kBuf, rec_h + (size_t)(first + c + 1) * rec_stride,
+                                 tile, &full_bar[bsel ^ 1]);
+                ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
+                if (ok) {
+                    tc::tc_fence_after();
+                    // S-critical: Kend^T Ut + M' S -> S acc
+                    for (int s = 0; s < 4; ++s)
+                        tc::mma_bf16(tmem, tc::smem_desc(kKendMn, tc::smem_u32(buf + StateSmem::Kend + s * 2048)),
+                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idMnN, s > 0);
+                    uint8_t *sbc = sm + StateSmem::SB + (uint32_t)bsel * 8192u;
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
+                        const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
+                        tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + ka)),
+                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idN, true);
+                    }
+                    tc::mma_commit(&a_bar);
+                    // output: Qp S + P Ut -> O acc[c & 1] (rows 64..127 of the A operands are zero)
+                    const uint32_t oacc = tmem + 64u + (uint32_t)bsel * 32u;
+                    const uint64_t kQpMn = tc::smem_desc_base(
+                        StateSmem::Zero - (bsel * StateSmem::kBuf + StateSmem::Qp), 1024, tc::SW_128B);
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
+                        tc::mma_bf16(oacc, tc::smem_desc(kQpMn, tc::smem_u32(buf + StateSmem::Qp + s * 2048)),
+                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idMnN, s > 0);
+                    }
+                    for (int s = 0; s < 4; ++s)
+                        tc::mma_bf16(oacc, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::P + s * 32)),
+                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idN, true);
+                    tc::mma_commit(&b_bar[bsel]);
                 }
-                tc::mma_commit(&mma1_bar);
             }
             __syncwarp();
-            ok = ok && tc::mbar_wait(&mma1_bar, (uint32_t)(c & 1));
-            tc::tc_fence_after();
-            float acc[kTile];
-            if (ok) {
-                float t[16];
-                tc::tmem_ld16(tmem + lane_base, t);
+            if (c < nchunks) {
+                // S <- gamma * S + (Kend^T Ut + M' S)
+                ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
+                tc::tc_fence_after();
+                if (warp_all(ok)) {
+                    const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+                    float t[16];
+                    tc::tmem_ld16(tmem + lane_base, t);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = t[j];
-                tc::tmem_ld16(tmem + lane_base + 16u, t);
+                    for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], t[j]);
+                    tc::tmem_ld16(tmem + lane_base + 16u, t);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[16 + j] = t[j];
+                    for (int j = 0; j < 16; ++j) S[16 + j] = fmaf(gam, S[16 + j], t[j]);
+                    store_state_operand(sm + StateSmem::SB + (uint32_t)(bsel ^ 1) * 8192u, i, S);
+                }
             }
-            if (tid < 64) {
-                // U = Ut - X for token row r = tid -> U^T operand (K-major [j][r])
+            if (c > 0 && tid < 64) {
+                // O rows of the previous chunk
+                if (tid != 0 || c == nchunks)
+                    ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                tc::tc_fence_after();
                 const int r = tid;
-                const uint8_t *ut = buf + StateSmem::Ut + r * 64;
-                uint8_t *UB = sm + StateSmem::UB;
+                const int t0p = t_doc + (c - 1) * kL;
+                if (warp_all(ok)) {
+                    const uint32_t oacc = tmem + lane_base + 64u + (uint32_t)((c - 1) & 1) * 32u;
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0p + r) * H + h) * kD + col0);
 #pragma unroll
-                for (int j = 0; j < kTile; ++j) {
-                    const float u = ok ? bf16_at(ut + 2 * j) - acc[j] : 0.f;
-                    st_bf16(UB + tc::sw128_offset(j, r), u);
-                }
-                tc::fence_async_smem();
-                tc::tc_fence_before();
-                tc::named_barrier(1, 64);
-                if (tid == 0 && ok) {
-                    tc::tc_fence_after();
-                    // Kend^T U -> cols 32..63
-                    for (int s = 0; s < 4; ++s)
-                        tc::mma_bf16(tmem + 32, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::A2 + s * 32)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(sm + StateSmem::UB + s * 32)), id2, s > 0);
-                    tc::mma_commit(&mma2_bar);
-                }
-            } else if (ok) {
-                // O = Y + Oloc for token row r = tid - 64
-                const int r = tid - 64;
-                if (r < Lc) {
-                    const uint8_t *ol = buf + StateSmem::Ol + r * 64;
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * kD + col0);
+                    for (int half = 0; half < 2; ++half) {
+                        float t[16];
+                        tc::tmem_ld16(oacc + (uint32_t)(half * 16), t);
+                        float w0[8], w1[8];
 #pragma unroll
-                    for (int j8 = 0; j8 < kTile; j8 += 8) {
-                        float w[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) w[u] = acc[j8 + u] + bf16_at(ol + 2 * (j8 + u));
-                        dst[j8 >> 3] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                                                  pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+                        for (int u = 0; u < 8; ++u) { w0[u] = t[u]; w1[u] = t[8 + u]; }
+                        if (t0p + r < t_end) {
+                            dst[half * 2] = pack8(w0);
+                            dst[half * 2 + 1] = pack8(w1);
+                        }
                     }
                 }
-            }
-            __syncwarp();
-            ok = ok && tc::mbar_wait(&mma2_bar, (uint32_t)(c & 1));
-            tc::tc_fence_after();
-            if (ok) {
-                float t[16];
-                const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-                tc::tmem_ld16(tmem + lane_base + 32u, t);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], t[j]);
-                tc::tmem_ld16(tmem + lane_base + 48u, t);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) S[16 + j] = fmaf(gam, S[16 + j], t[j]);
-                store_state_operand(sm + StateSmem::SB, i, S);
             }
             tc::fence_async_smem();
             tc::tc_fence_before();
@@ -646,19 +715,16 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             __syncthreads();
             tc::tc_fence_after();
             if (s_abort) break;
-            if (tid == 0 && c + 2 < nchunks)
-                issue_record(buf, ws + records_off + ((size_t)(first + c + 2) * H + h) * record_bytes, tile,
-                             &full_bar[bsel]);
         }
         if (s_abort) {
-            // Let any copy still in flight land before the CTA's shared memory goes away.
+            // let any copy still in flight land before the CTA's shared memory goes away
             if (tid == 0) {
                 flag_timeout(ws);
                 for (int b = 0; b < 2; ++b) tc::mbar_wait(&full_bar[b], 0, 10000000ull);
             }
             __syncthreads();
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 64);
+        if (warp == 0) tc::tmem_dealloc(tmem, 128);
         if (s_abort) return;
     }
     if (S_final) {
@@ -698,6 +764,19 @@ bool make_input_map(CUtensorMap *map, const void *base, int total_tokens, int H)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T, H, 128] fp32 gates, boxes of 128 channels x 1 head x 64 tokens, unswizzled rows.
+bool make_gate_map(CUtensorMap *map, const float *base, int total_tokens, int H) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)H * kD * 4};
+    cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)kL};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -707,16 +786,16 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     char *w = static_cast<char *>(ws);
     cudaError_t e;
     if (lay.max_slots > 0 && total_tokens > 0) {
-        CUtensorMap mq, mk, mv;
+        CUtensorMap mq, mk, mv, mg;
         if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
-            !make_input_map(&mv, v, total_tokens, H))
+            !make_input_map(&mv, v, total_tokens, H) || !make_gate_map(&mg, g, total_tokens, H))
             return cudaErrorInvalidValue;
         const int smem = PrepSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
             return e;
         marks.before(st, "prefill_prepare_tc");
         prefill_prepare_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem, st>>>(
-            mq, mk, mv, g, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
+            mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
         if ((e = cudaGetLastError())) return e;
     }
     if (num_seqs == 0) return cudaSuccess;

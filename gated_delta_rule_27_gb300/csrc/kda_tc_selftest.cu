@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const uint4 *__restric
         tc::mma_commit(&bar);
     }
     __syncwarp();
-    const bool ok = tc::mbar_wait(&bar, 0);
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar, 0));  // warp-uniform: tcgen05.ld is collective
     if (!ok && lane == 0) atomicExch(status, 1);
     tc::tc_fence_after();
     if (ok) {
