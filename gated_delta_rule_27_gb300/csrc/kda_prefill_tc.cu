@@ -56,9 +56,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_at(const uint8_t *p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
 }
-__device__ __forceinline__ void st_bf16(uint8_t *p, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
-}
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     const uint32_t a = tc::smem_u32(p);
     return p + (((a + 1023u) & ~1023u) - a);
@@ -78,27 +75,75 @@ __device__ __forceinline__ void flag_timeout(char *ws) {
 // 16 x 16 blocks (i, j), j <= i, each contiguous.
 __device__ __forceinline__ int tri_blk(int i, int j) { return ((i * (i + 1)) / 2 + j) << 8; }
 __device__ __forceinline__ int tri_idx(int r, int s) { return tri_blk(r >> 4, s >> 4) + ((r & 15) << 4) + (s & 15); }
+// Cumulative log-decay b[r][c] lives in a [64][128] fp32 array whose float4
+// groups are XOR-swizzled by (r mod 8), so that row-wise float4 reads by
+// eight consecutive rows hit eight different bank groups.
+__device__ __forceinline__ int bswz(int r, int c) { return r * kD + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
 
 struct PrepSmem {
     // X: two 16 KB panels (channels 0-63, 64-127); in each, rows 0-63 hold the k
     // tile and rows 64-127 the q tile (128-byte swizzled), so that after the
-    // in-place scaling X is round 1's A operand, and its k half (panel stride
-    // 16 KB) is round 2's MN-major A operand.
+    // in-place scaling X is round 1's A operand, its k rows (panel stride
+    // 16 KB) are round 2's MN-major A operand and its q rows round 3's.
     static constexpr uint32_t X = 0;
-    static constexpr uint32_t V = 32768;   // v tile (MN-major chunks of 64 channels), then beta v in place
-    static constexpr uint32_t G = 49152;   // g fp32 [64][128], then b in place; then A, T, T(bf16); then Kend, W^T
-    static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P
+    static constexpr uint32_t V = 32768;   // v tile (MN-major), beta v in place; then Ut^T, K-major [j][s]
+    static constexpr uint32_t G = 49152;   // g fp32 [64][128] -> b (swizzled); then A, T, T(bf16); then Kend, W'^T
+    static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB) and the identity (8 KB)
     static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
     static constexpr uint32_t Tfp = G + 10240;     // compact fp32 T (10 KB)
     static constexpr uint32_t Tb = G + 20480;      // bf16 T, K-major [r][s] (8 KB)
-    static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB), round-4 A operand
-    static constexpr uint32_t WT = G + 16384;      // W^T, K-major [c][s] (16 KB), round-3 A / round-4 B operand
+    static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB)
+    static constexpr uint32_t WT = G + 16384;      // W'^T, K-major [c][s] (16 KB)
+    static constexpr uint32_t P = Y;               // P, K-major [r][s] (8 KB)
+    static constexpr uint32_t Id = Y + 8192;       // identity, K-major [r][r'] (8 KB)
     static constexpr uint32_t bytes = 98304;
 };
 
 // T = (I + A)^{-1} for A strictly lower triangular (compact block-major):
 // invert the four 16 x 16 diagonal blocks by forward substitution, then fill
 // the sub-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+template <int LVL>
+__device__ __forceinline__ void inverse_level(float *A, float *T, int tid) {
+    constexpr int NB = 4 - LVL;
+#pragma unroll
+    for (int q = 0; q < (NB * 256 + 127) / 128; ++q) {  // M_b = sum_k A_{i,k} T_{k,j} -> diagonal block b of A
+        const int e = tid + q * 128;
+        if (e < NB * 256) {
+            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15, i = b + LVL;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < LVL; ++kk) {
+                const float *Aik = A + tri_blk(i, b + kk) + (r << 4);
+                const float *Tkj = T + tri_blk(b + kk, b) + s;
+#pragma unroll
+                for (int t = 0; t < 16; t += 2) {
+                    acc0 = fmaf(Aik[t], Tkj[t << 4], acc0);
+                    acc1 = fmaf(Aik[t + 1], Tkj[(t + 1) << 4], acc1);
+                }
+            }
+            A[tri_blk(b, b) + (r << 4) + s] = acc0 + acc1;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < (NB * 256 + 127) / 128; ++q) {
+        const int e = tid + q * 128;
+        if (e < NB * 256) {
+            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15, i = b + LVL;
+            const float *Tii = T + tri_blk(i, i) + (r << 4);
+            const float *M = A + tri_blk(b, b) + s;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int t = 0; t < 16; t += 2) {
+                acc0 = fmaf(Tii[t], M[t << 4], acc0);
+                acc1 = fmaf(Tii[t + 1], M[(t + 1) << 4], acc1);
+            }
+            T[tri_blk(i, b) + (r << 4) + s] = -(acc0 + acc1);
+        }
+    }
+    __syncthreads();
+}
+
 __device__ void unit_lower_inverse(float *A, float *T, int tid) {
     if (tid < 64) {
         const int blk = tid >> 4, j = tid & 15;
@@ -116,34 +161,9 @@ __device__ void unit_lower_inverse(float *A, float *T, int tid) {
         for (int r = 0; r < 16; ++r) Td[(r << 4) + j] = x[r];
     }
     __syncthreads();
-    for (int lvl = 1; lvl < 4; ++lvl) {
-        const int nb = 4 - lvl;
-        // M_b = sum_k A_{i,k} T_{k,j}, kept in the diagonal block b of A (no longer needed)
-        for (int e = tid; e < nb * 256; e += 128) {
-            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15;
-            const int i = b + lvl, j = b;
-            float acc = 0.f;
-            for (int k = j; k < i; ++k) {
-                const float *Aik = A + tri_blk(i, k) + (r << 4);
-                const float *Tkj = T + tri_blk(k, j) + s;
-#pragma unroll
-                for (int t = 0; t < 16; ++t) acc = fmaf(Aik[t], Tkj[t << 4], acc);
-            }
-            A[tri_blk(b, b) + (r << 4) + s] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nb * 256; e += 128) {
-            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15;
-            const int i = b + lvl, j = b;
-            const float *Tii = T + tri_blk(i, i) + (r << 4);
-            const float *M = A + tri_blk(b, b) + s;
-            float acc = 0.f;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) acc = fmaf(Tii[t], M[t << 4], acc);
-            T[tri_blk(i, j) + (r << 4) + s] = -acc;
-        }
-        __syncthreads();
-    }
+    inverse_level<1>(A, T, tid);
+    inverse_level<2>(A, T, tid);
+    inverse_level<3>(A, T, tid);
 }
 
 // Exact A and P on the CUDA cores for a chunk whose log-decay range is too
@@ -157,14 +177,14 @@ __device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, 
     if (r >= Lc) return;
     for (int c = 0; c < kD; ++c) {
         const uint8_t *panel = X + (uint32_t)(c >> 6) * 16384u;
-        const float brc = B[r * kD + c];
+        const float brc = B[bswz(r, c)];
         const float krc = bf16_at(panel + tc::sw128_offset(r, c & 63));
         const float qrc = bf16_at(panel + tc::sw128_offset(64 + r, c & 63));
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int s = s0 + j;
             if (s <= r) {
-                const float ks = bf16_at(panel + tc::sw128_offset(s, c & 63)) * expf(brc - B[s * kD + c]);
+                const float ks = bf16_at(panel + tc::sw128_offset(s, c & 63)) * expf(brc - B[bswz(s, c)]);
                 accA[j] = fmaf(krc, ks, accA[j]);
                 accP[j] = fmaf(qrc, ks, accP[j]);
             }
@@ -184,6 +204,10 @@ __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
     }
 }
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack8_at(const float *f) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
 }
@@ -234,6 +258,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = tmem_base;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     if (!tc::mbar_wait(&load_bar, 0)) s_abort = 1;
     __syncthreads();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
@@ -242,24 +267,28 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return;
     }
 
-    // cumulative log-decay of channel c, in place; reference token m in the middle
+    // cumulative log-decay of channel c (registers), reference token m in the middle
     float *Gf = reinterpret_cast<float *>(sm + PrepSmem::G);
     {
+        float bcol[kL];
         const int m = (Lc - 1) >> 1;
-        float acc = 0.f, bm = 0.f, blast = 0.f, bmax = -INFINITY, bmin = INFINITY;
-        for (int r = 0; r < Lc; ++r) {
-            acc += Gf[r * kD + c];
-            Gf[r * kD + c] = acc;
+        float acc = 0.f, bm = 0.f, bmax = -INFINITY, bmin = INFINITY;
+#pragma unroll
+        for (int r = 0; r < kL; ++r) {
+            acc += r < Lc ? Gf[r * kD + c] : 0.f;
+            bcol[r] = acc;
             if (r == m) bm = acc;
-            bmax = fmaxf(bmax, acc);
-            bmin = fminf(bmin, acc);
+            if (r < Lc) { bmax = fmaxf(bmax, acc); bmin = fminf(bmin, acc); }
         }
-        blast = acc;
+        const float blast = acc;
         s_bm[c] = bm;
         s_F[c] = expf(blast - bm);
         s_Em[c] = expf(bm);
         reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
         if (bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY)) s_unsafe = 1;
+        __syncthreads();  // all of g has been read: b may now go to its swizzled places
+#pragma unroll
+        for (int r = 0; r < kL; ++r) Gf[bswz(r, c)] = bcol[r];
     }
     __syncthreads();
     const bool unsafe = s_unsafe != 0;
@@ -287,13 +316,14 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
             unpack8(*reinterpret_cast<const uint4 *>(Vp + off_k), v8);
-            const float4 b0 = *reinterpret_cast<const float4 *>(Gf + r * kD + c0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(Gf + r * kD + c0 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0));
+            const float4 b1 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0 + 4));
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float e1 = valid ? expf(bb[u] - s_bm[c0 + u]) : 0.f;
-                const float inv = valid ? __frcp_rn(e1) : 0.f;
+                const float d = bb[u] - s_bm[c0 + u];
+                const float e1 = valid ? __expf(d) : 0.f;
+                const float inv = valid ? __expf(-d) : 0.f;
                 xk[u] = br * k8[u] * e1;
                 xq[u] = q8[u] * e1;
                 y8[u] = k8[u] * inv;
@@ -317,8 +347,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint32_t mma_phase = 0;
     bool ok = true;
     float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
-    uint8_t *Pb = sm + PrepSmem::Y;
-    uint8_t *Pg = reinterpret_cast<uint8_t *>(rec + R.P);
+    uint8_t *Pb = sm + PrepSmem::P;
     if (unsafe) {
         const int r = tid >> 1, s0 = (tid & 1) * 32;
 #pragma unroll
@@ -330,9 +359,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if ((s >> 4) <= (r >> 4)) Af[tri_idx(r, s)] = s < r ? accA[j8 + u] : 0.f;
                 w[u] = s <= r ? accP[j8 + u] : 0.f;
             }
-            const uint4 pw = pack8(w);
-            *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s0 + j8)) = pw;
-            *reinterpret_cast<uint4 *>(Pg + tc::sw128_offset(r, s0 + j8)) = pw;
+            *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s0 + j8)) = pack8(w);
         }
     } else {
         // round 1: [beta k e1 ; q e1] x (k / e1)^T -> TMEM cols 0..63 (rows 0-63 A, 64-127 P)
@@ -351,22 +378,23 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mma_phase ^= 1;
         tc::tc_fence_after();
         if (warp_all(ok)) {
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+            float v[64];
+            tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(v));
+            tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(v + 32));
+            __syncthreads();  // every lane has read round 1 before P overwrites the B operand
             if (tid < 64) {
                 const int r = tid;
-                const int qmax = (warp * 32 + 31) >> 4;  // warp-uniform trip count
-                for (int q4 = 0; q4 <= qmax; ++q4) {
-                    float t[16];
-                    tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), t);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
                     if (q4 <= (r >> 4)) {
                         float *dst = Af + tri_blk(r >> 4, q4) + ((r & 15) << 4);
 #pragma unroll
                         for (int i = 0; i < 16; i += 4) {
                             float4 w;
-                            w.x = q4 * 16 + i + 0 < r ? t[i + 0] : 0.f;
-                            w.y = q4 * 16 + i + 1 < r ? t[i + 1] : 0.f;
-                            w.z = q4 * 16 + i + 2 < r ? t[i + 2] : 0.f;
-                            w.w = q4 * 16 + i + 3 < r ? t[i + 3] : 0.f;
+                            w.x = q4 * 16 + i + 0 < r ? v[q4 * 16 + i + 0] : 0.f;
+                            w.y = q4 * 16 + i + 1 < r ? v[q4 * 16 + i + 1] : 0.f;
+                            w.z = q4 * 16 + i + 2 < r ? v[q4 * 16 + i + 2] : 0.f;
+                            w.w = q4 * 16 + i + 3 < r ? v[q4 * 16 + i + 3] : 0.f;
                             *reinterpret_cast<float4 *>(dst + i) = w;
                         }
                     }
@@ -374,20 +402,26 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             } else {
                 const int r = tid - 64;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    float t[16];
-                    tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), t);
+                for (int s8 = 0; s8 < 64; s8 += 8) {
+                    float w[8];
 #pragma unroll
-                    for (int h8 = 0; h8 < 16; h8 += 8) {
-                        float w[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) w[u] = q4 * 16 + h8 + u <= r ? t[h8 + u] : 0.f;
-                        const uint4 pw = pack8(w);
-                        *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, q4 * 16 + h8)) = pw;
-                        *reinterpret_cast<uint4 *>(Pg + tc::sw128_offset(r, q4 * 16 + h8)) = pw;
-                    }
+                    for (int u = 0; u < 8; ++u) w[u] = s8 + u <= r ? v[s8 + u] : 0.f;
+                    *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s8)) = pack8(w);
                 }
             }
+        } else {
+            __syncthreads();
+        }
+    }
+    // identity (K-major [r][r']) for round 3, in the dead second half of the round-1 B operand
+    {
+        const int r = tid >> 1, s0 = (tid & 1) * 32;
+#pragma unroll
+        for (int s8 = 0; s8 < 32; s8 += 8) {
+            float w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w[u] = (s0 + s8 + u) == r ? 1.f : 0.f;
+            *reinterpret_cast<uint4 *>(sm + PrepSmem::Id + tc::sw128_offset(r, s0 + s8)) = pack8(w);
         }
     }
     tc::tc_fence_before();
@@ -421,7 +455,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
 
-    // round 2: (T X_k)^T -> cols 64..127 (W^T once scaled by exp(b_m));  (T beta V)^T = Ut^T -> cols 128..191
+    // round 2: W'^T = (T X_k)^T -> cols 64..127;  Ut^T = (T beta V)^T -> cols 128..191
     if (tid == 0) {
         constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, true, false);
         constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
@@ -438,30 +472,28 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     ok = tc::mbar_wait(&mma_bar, mma_phase);
     mma_phase ^= 1;
     tc::tc_fence_after();
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     if (warp_all(ok)) {
-        const float em = s_Em[c];
-        uint8_t *UtG = reinterpret_cast<uint8_t *>(rec + R.UtT);
+        float w[64], u[64];
+        tc::tmem_ld32(tmem + lane_base + 64u, *reinterpret_cast<float(*)[32]>(w));
+        tc::tmem_ld32(tmem + lane_base + 96u, *reinterpret_cast<float(*)[32]>(w + 32));
+        tc::tmem_ld32(tmem + lane_base + 128u, *reinterpret_cast<float(*)[32]>(u));
+        tc::tmem_ld32(tmem + lane_base + 160u, *reinterpret_cast<float(*)[32]>(u + 32));
+        __syncthreads();  // round 2 has consumed beta V before Ut^T replaces it
+        uint8_t *UtTile = reinterpret_cast<uint8_t *>(rec + R.tiles) + (size_t)(c >> 5) * R.tile_bytes;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float w[16], u[16];
-            tc::tmem_ld16(tmem + lane_base + 64u + (uint32_t)(q4 * 16), w);
-            tc::tmem_ld16(tmem + lane_base + 128u + (uint32_t)(q4 * 16), u);
-#pragma unroll
-            for (int h8 = 0; h8 < 16; h8 += 8) {
-                float ww[8], uu[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) { ww[i] = w[h8 + i] * em; uu[i] = u[h8 + i]; }
-                const uint32_t off = tc::sw128_offset(c, q4 * 16 + h8);
-                *reinterpret_cast<uint4 *>(sm + PrepSmem::WT + off) = pack8(ww);
-                *reinterpret_cast<uint4 *>(UtG + off) = pack8(uu);
-            }
+        for (int s8 = 0; s8 < 64; s8 += 8) {
+            *reinterpret_cast<uint4 *>(sm + PrepSmem::WT + tc::sw128_offset(c, s8)) = pack8_at(w + s8);
+            const uint4 uu = pack8_at(u + s8);
+            *reinterpret_cast<uint4 *>(sm + PrepSmem::V + tc::sw128_offset(c, s8)) = uu;
+            *reinterpret_cast<uint4 *>(UtTile + tc::sw128_offset(c & 31, s8)) = uu;
         }
-        // Kend (kept in registers since the operand build) -> round-4 A operand
+        // Kend (kept in registers since the operand build) -> MN-major [s][c] operand
         const int r = tid >> 1, half = tid & 1;
         uint8_t *Ks = sm + PrepSmem::KendS + (uint32_t)half * 8192u;
 #pragma unroll
         for (int g8 = 0; g8 < 8; ++g8) *reinterpret_cast<uint4 *>(Ks + tc::sw128_offset(r, g8 * 8)) = kend[g8];
+    } else {
+        __syncthreads();
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
@@ -474,55 +506,63 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return;
     }
 
-    // round 3: W^T P^T = (P W)^T -> cols 0..63;  round 4: Kend^T W -> cols 128..255
+    // round 3:  (X_q - P W')^T -> cols 0..63;  Oloc^T = Ut^T P^T -> cols 64..127;
+    //           Kend^T W' -> cols 128..255
     if (tid == 0) {
-        constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 64, false, false);
-        constexpr uint32_t id4 = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint32_t id_neg = tc::idesc_bf16_f32(128, 64, false, false) | (1u << 14);  // negate B
+        constexpr uint32_t id_xq = tc::idesc_bf16_f32(128, 64, true, false);
+        constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
         constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
         for (int s = 0; s < 4; ++s) {
+            const uint64_t pdesc = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32));
             const uint64_t wt = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32));
-            tc::mma_bf16(tmem, wt, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + s * 32)), id3, s > 0);
-            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)), wt, id4,
+            tc::mma_bf16(tmem, wt, pdesc, id_neg, s > 0);
+            tc::mma_bf16(tmem + 64, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), pdesc, id64,
+                         s > 0);
+            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)), wt, id128,
                          s > 0);
         }
+        for (int s = 0; s < 4; ++s)
+            tc::mma_bf16(tmem, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + 8192 + s * 2048)),
+                         tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Id + s * 32)), id_xq, true);
         tc::mma_commit(&mma_bar);
     }
     __syncwarp();
     ok = tc::mbar_wait(&mma_bar, mma_phase);
     tc::tc_fence_after();
     if (warp_all(ok)) {
-        // Qp = exp(b) q - P W, stored MN-major [c][r]; M' = -Kend^T W, stored K-major [c][c']
         const float em = s_Em[c];
-        const uint8_t *Xq = sm + PrepSmem::X + (uint32_t)(c >> 6) * 16384u;
         uint8_t *QpG = reinterpret_cast<uint8_t *>(rec + R.Qp);
         uint8_t *McG = reinterpret_cast<uint8_t *>(rec + R.Mc);
+        uint8_t *OlG = reinterpret_cast<uint8_t *>(rec + R.tiles) + (size_t)(c >> 5) * R.tile_bytes + 4096 +
+                       (size_t)(c & 31) * 128;
+        {
+            float qv[64], ol[64];
+            tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(qv));
+            tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(qv + 32));
+            tc::tmem_ld32(tmem + lane_base + 64u, *reinterpret_cast<float(*)[32]>(ol));
+            tc::tmem_ld32(tmem + lane_base + 96u, *reinterpret_cast<float(*)[32]>(ol + 32));
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float pw[16];
-            tc::tmem_ld16(tmem + lane_base + (uint32_t)(q4 * 16), pw);
+            for (int i = 0; i < 64; ++i) qv[i] *= em;
 #pragma unroll
-            for (int h8 = 0; h8 < 16; h8 += 8) {
-                float w[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = q4 * 16 + h8 + i;
-                    w[i] = bf16_at(Xq + tc::sw128_offset(64 + r, c & 63)) * em - pw[h8 + i];
-                }
-                *reinterpret_cast<uint4 *>(QpG + tc::sw128_offset(c, q4 * 16 + h8)) = pack8(w);
+            for (int s8 = 0; s8 < 64; s8 += 8) {
+                *reinterpret_cast<uint4 *>(QpG + tc::sw128_offset(c, s8)) = pack8_at(qv + s8);
+                *reinterpret_cast<uint4 *>(OlG + s8 * 2) = pack8_at(ol + s8);
             }
         }
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-            float m[16];
-            tc::tmem_ld16(tmem + lane_base + 128u + (uint32_t)(q8 * 16), m);
+        for (int q32 = 0; q32 < 4; ++q32) {
+            float mv[32];
+            tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(q32 * 32), mv);
 #pragma unroll
-            for (int h8 = 0; h8 < 16; h8 += 8) {
-                float w[8];
+            for (int i = 0; i < 32; ++i) mv[i] *= -s_Em[q32 * 32 + i];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = -m[h8 + i];
-                const int cp = q8 * 16 + h8;
+            for (int h8 = 0; h8 < 32; h8 += 8) {
+                const int cp = q32 * 32 + h8;
                 *reinterpret_cast<uint4 *>(McG + (uint32_t)(cp >> 6) * 16384u + tc::sw128_offset(c, cp & 63)) =
-                    pack8(w);
+                    pack8_at(mv + h8);
             }
         }
     }
@@ -536,34 +576,40 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
 struct StateSmem {
-    // per-chunk record buffer (two of them)
-    static constexpr uint32_t Mc = 0, Kend = 32768, Qp = 49152, P = 65536, UtT = 81920, gam = 86016;
-    static constexpr uint32_t kBuf = 87040;          // 85 KB, 1024-aligned
-    static constexpr uint32_t Zero = 2 * kBuf;       // 16 KB of zeros: rows 64-127 of the Qp operand
+    static constexpr uint32_t Zero = 0;        // 16 KB of zeros: rows 0-63 of the output MMA's A operand
+    static constexpr uint32_t Buf = 16384;     // two record buffers
+    static constexpr uint32_t kBuf = 74752;    // shared record part (65 KB) + this CTA's tile (8 KB)
+    static constexpr uint32_t Mc = 0, Kend = 32768, Qp = 49152, gam = 65536, UtT = 66560, Ol = 66560 + 4096;
     // S^T operand, K-major [32 rows][128 K], 2 panels of 4 KB, ping-pong: chunk c's MMAs read
-    // SB + (c & 1) * 8 KB while the epilogue writes S_{c+1} into the other half, so the output
-    // MMAs of chunk c (still in flight after the state MMAs complete) never see S_{c+1}.
-    static constexpr uint32_t SB = Zero + 16384;
+    // half (c & 1) while the epilogue writes S_{c+1} into the other half, so the output MMAs of
+    // chunk c (still in flight after the state MMAs complete) never see S_{c+1}.
+    static constexpr uint32_t SB = Buf + 2 * kBuf;
     static constexpr uint32_t bytes = SB + 16384;
-    static constexpr uint32_t tx = 32768 + 16384 + 16384 + 8192 + 4096 + 512;
 };
 
 __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int tile, uint64_t *bar) {
     constexpr TcRecord R = tc_record();
-    tc::mbar_arrive_expect_tx(bar, StateSmem::tx);
-    tc::bulk_g2s(buf + StateSmem::Mc, rec + R.Mc, 32768, bar);
-    tc::bulk_g2s(buf + StateSmem::Kend, rec + R.Kend, 16384, bar);
-    tc::bulk_g2s(buf + StateSmem::Qp, rec + R.Qp, 16384, bar);
-    tc::bulk_g2s(buf + StateSmem::P, rec + R.P, 8192, bar);
-    tc::bulk_g2s(buf + StateSmem::UtT, rec + R.UtT + (size_t)tile * 4096, 4096, bar);
-    tc::bulk_g2s(buf + StateSmem::gam, rec + R.gamma, 512, bar);
+    tc::mbar_arrive_expect_tx(bar, StateSmem::kBuf);
+    tc::bulk_g2s(buf, rec, (uint32_t)R.shared_bytes, bar);
+    tc::bulk_g2s(buf + R.shared_bytes, rec + R.tiles + (size_t)tile * R.tile_bytes, (uint32_t)R.tile_bytes, bar);
 }
 
-// Writes row i of S (32 values) into the K-major S^T operand: element (j, i).
+// Writes row i of S (32 values) into the K-major S^T operand: element (j, i),
+// two adjacent rows per 4-byte store (rows i and i ^ 1 swap halves of their values).
 __device__ __forceinline__ void store_state_operand(uint8_t *SB, int i, const float (&S)[kTile]) {
     uint8_t *p = SB + (uint32_t)(i >> 6) * 4096u;
+    const int odd = i & 1, ie = i & ~1;
 #pragma unroll
-    for (int j = 0; j < kTile; ++j) st_bf16(p + tc::sw128_offset(j, i & 63), S[j]);
+    for (int j2 = 0; j2 < kTile / 2; ++j2) {
+        // even lanes store columns 0..15, odd lanes 16..31; each needs its partner's value
+        const int j_even = j2, j_odd = j2 + kTile / 2;
+        const float mine = odd ? S[j_odd] : S[j_even];
+        const float other_give = odd ? S[j_even] : S[j_odd];
+        const float partner = __shfl_xor_sync(0xffffffffu, other_give, 1);
+        const int j = odd ? j_odd : j_even;
+        const float lo = odd ? partner : mine, hi = odd ? mine : partner;
+        *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
+    }
 }
 
 __global__ void __launch_bounds__(128, 1)
@@ -576,7 +622,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     __shared__ int s_abort;
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, i = tid;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, i = tid;
     const int tile = blockIdx.x % kNTile;
     const int h = (blockIdx.x / kNTile) % H;
     const int n = blockIdx.x / (kNTile * H);
@@ -592,12 +638,6 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
     if (nchunks > 0) {
-        // zero rows 64-127 of the P operand (both buffers) and the Qp padding block; they are never loaded
-        for (int e = tid; e < 512; e += 128) {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4 *>(sm + StateSmem::P + 8192)[e] = z;
-            reinterpret_cast<uint4 *>(sm + StateSmem::kBuf + StateSmem::P + 8192)[e] = z;
-        }
         for (int e = tid; e < 1024; e += 128) reinterpret_cast<uint4 *>(sm + StateSmem::Zero)[e] = make_uint4(0, 0, 0, 0);
         store_state_operand(sm + StateSmem::SB, i, S);
         tc::fence_async_smem();
@@ -611,7 +651,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             tc::mbar_init(&b_bar[1], 1);
             tc::fence_mbar_init();
             s_abort = 0;
-            issue_record(sm, rec_h + (size_t)first * rec_stride, tile, &full_bar[0]);
+            issue_record(sm + StateSmem::Buf, rec_h + (size_t)first * rec_stride, tile, &full_bar[0]);
         }
         if (warp == 0) {
             tc::tmem_alloc(&tmem_base, 128);
@@ -620,7 +660,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
-        const uint32_t tmem = tmem_base;  // S acc: cols 0..31; O acc: 64..95 / 96..127 (ping-pong)
+        const uint32_t tmem = tmem_base;  // S acc: cols 0..31; O acc: 32..63 / 64..95 (ping-pong, rows 64-127)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
         constexpr uint64_t kKendMn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
@@ -628,85 +668,109 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         constexpr uint32_t idMnN = tc::idesc_bf16_f32(128, kTile, true, false);
         const int t_doc = cu[n], t_end = cu[n + 1];
         bool ok = true;
+        uint32_t oloc[kTile / 2];  // this thread's output row of Oloc for the chunk in flight (warps 2-3)
 
         for (int c = 0; c <= nchunks; ++c) {
             const int bsel = c & 1;
-            uint8_t *buf = sm + bsel * StateSmem::kBuf;
-            if (tid == 0 && c < nchunks) {
-                // B of the previous chunk done -> its buffer is free: prefetch the next record into it
-                if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
-                if (ok && c + 1 < nchunks)
-                    issue_record(sm + (bsel ^ 1) * StateSmem::kBuf, rec_h + (size_t)(first + c + 1) * rec_stride,
-                                 tile, &full_bar[bsel ^ 1]);
-                ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
-                if (ok) {
-                    tc::tc_fence_after();
-                    // S-critical: Kend^T Ut + M' S -> S acc
-                    for (int s = 0; s < 4; ++s)
-                        tc::mma_bf16(tmem, tc::smem_desc(kKendMn, tc::smem_u32(buf + StateSmem::Kend + s * 2048)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idMnN, s > 0);
-                    uint8_t *sbc = sm + StateSmem::SB + (uint32_t)bsel * 8192u;
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
-                        const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                        tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + ka)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idN, true);
+            uint8_t *buf = sm + StateSmem::Buf + bsel * StateSmem::kBuf;
+            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)bsel * 8192u;
+            if (c < nchunks) {
+                if (tid == 0) {
+                    // output MMAs of the previous chunk done -> its buffer is free for chunk c + 1
+                    if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                    if (ok && c + 1 < nchunks)
+                        issue_record(sm + StateSmem::Buf + (bsel ^ 1) * StateSmem::kBuf,
+                                     rec_h + (size_t)(first + c + 1) * rec_stride, tile, &full_bar[bsel ^ 1]);
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
+                    if (ok) {
+                        tc::tc_fence_after();
+                        // state: Kend^T Ut + M' S -> S acc
+                        for (int s = 0; s < 4; ++s)
+                            tc::mma_bf16(tmem, tc::smem_desc(kKendMn, tc::smem_u32(buf + StateSmem::Kend + s * 2048)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idMnN,
+                                         s > 0);
+                        for (int s = 0; s < 8; ++s) {
+                            const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
+                            const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
+                            tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + ka)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idN, true);
+                        }
+                        tc::mma_commit(&a_bar);
                     }
-                    tc::mma_commit(&a_bar);
-                    // output: Qp S + P Ut -> O acc[c & 1] (rows 64..127 of the A operands are zero)
-                    const uint32_t oacc = tmem + 64u + (uint32_t)bsel * 32u;
-                    const uint64_t kQpMn = tc::smem_desc_base(
-                        StateSmem::Zero - (bsel * StateSmem::kBuf + StateSmem::Qp), 1024, tc::SW_128B);
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                        tc::mma_bf16(oacc, tc::smem_desc(kQpMn, tc::smem_u32(buf + StateSmem::Qp + s * 2048)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idMnN, s > 0);
+                }
+                if (warp == 0) {
+                    __syncwarp();
+                    tc::named_barrier_arrive(2, 64);
+                } else if (warp == 2) {
+                    tc::named_barrier(2, 64);
+                    if (lane == 0) {
+                        // output: [0 ; Qp] S -> O acc[c & 1] rows 64..127
+                        tc::tc_fence_after();
+                        const uint32_t oacc = tmem + 32u + (uint32_t)bsel * 32u;
+                        const uint64_t kQp = tc::smem_desc_base(
+                            (uint32_t)(StateSmem::Buf + bsel * StateSmem::kBuf + StateSmem::Qp - StateSmem::Zero), 1024,
+                            tc::SW_128B);
+                        for (int s = 0; s < 8; ++s) {
+                            const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
+                            tc::mma_bf16(oacc, tc::smem_desc(kQp, tc::smem_u32(sm + StateSmem::Zero + s * 2048)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idMnN, s > 0);
+                        }
+                        tc::mma_commit(&b_bar[bsel]);
                     }
-                    for (int s = 0; s < 4; ++s)
-                        tc::mma_bf16(oacc, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::P + s * 32)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idN, true);
-                    tc::mma_commit(&b_bar[bsel]);
+                    __syncwarp();
                 }
             }
-            __syncwarp();
+            if (warp >= 2) {
+                const int r = tid - 64;
+                if (c > 0) {
+                    // O of the previous chunk: [0 ; Qp] S rows 64-127 + Oloc
+                    ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                    tc::tc_fence_after();
+                    if (warp_all(ok)) {
+                        float t[32];
+                        tc::tmem_ld32(tmem + lane_base + 32u + (uint32_t)((c - 1) & 1) * 32u, t);
+                        const int t0p = t_doc + (c - 1) * kL;
+                        if (t0p + r < t_end) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0p + r) * H + h) * kD + col0);
+#pragma unroll
+                            for (int q8 = 0; q8 < 4; ++q8) {
+                                float w[8];
+#pragma unroll
+                                for (int u = 0; u < 8; u += 2) {
+                                    const __nv_bfloat162 ob =
+                                        *reinterpret_cast<const __nv_bfloat162 *>(&oloc[(q8 * 8 + u) >> 1]);
+                                    const float2 of = __bfloat1622float2(ob);
+                                    w[u] = t[q8 * 8 + u] + of.x;
+                                    w[u + 1] = t[q8 * 8 + u + 1] + of.y;
+                                }
+                                dst[q8] = pack8(w);
+                            }
+                        }
+                    }
+                }
+                if (c < nchunks) {
+                    // this chunk's Oloc row, kept for next iteration's output
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
+                    const uint8_t *ol = buf + StateSmem::Ol + r * 2;
+#pragma unroll
+                    for (int j2 = 0; j2 < kTile / 2; ++j2) {
+                        const uint16_t lo = *reinterpret_cast<const uint16_t *>(ol + (2 * j2) * 128);
+                        const uint16_t hi = *reinterpret_cast<const uint16_t *>(ol + (2 * j2 + 1) * 128);
+                        oloc[j2] = (uint32_t)lo | ((uint32_t)hi << 16);
+                    }
+                }
+            }
             if (c < nchunks) {
                 // S <- gamma * S + (Kend^T Ut + M' S)
                 ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
                 tc::tc_fence_after();
                 if (warp_all(ok)) {
                     const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-                    float t[16];
-                    tc::tmem_ld16(tmem + lane_base, t);
+                    float t[32];
+                    tc::tmem_ld32(tmem + lane_base, t);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], t[j]);
-                    tc::tmem_ld16(tmem + lane_base + 16u, t);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) S[16 + j] = fmaf(gam, S[16 + j], t[j]);
+                    for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], t[j]);
                     store_state_operand(sm + StateSmem::SB + (uint32_t)(bsel ^ 1) * 8192u, i, S);
-                }
-            }
-            if (c > 0 && tid < 64) {
-                // O rows of the previous chunk
-                if (tid != 0 || c == nchunks)
-                    ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
-                tc::tc_fence_after();
-                const int r = tid;
-                const int t0p = t_doc + (c - 1) * kL;
-                if (warp_all(ok)) {
-                    const uint32_t oacc = tmem + lane_base + 64u + (uint32_t)((c - 1) & 1) * 32u;
-                    uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0p + r) * H + h) * kD + col0);
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float t[16];
-                        tc::tmem_ld16(oacc + (uint32_t)(half * 16), t);
-                        float w0[8], w1[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) { w0[u] = t[u]; w1[u] = t[8 + u]; }
-                        if (t0p + r < t_end) {
-                            dst[half * 2] = pack8(w0);
-                            dst[half * 2 + 1] = pack8(w1);
-                        }
-                    }
                 }
             }
             tc::fence_async_smem();
