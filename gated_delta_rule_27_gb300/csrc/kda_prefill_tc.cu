@@ -218,7 +218,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
                    char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t load_bar, mma_bar;
+    __shared__ uint64_t load_bar, r1_bar, r2_bar, r3_bar, r4_bar;  // one barrier per MMA round
     __shared__ uint32_t tmem_base;
     __shared__ float s_beta[kL];
     __shared__ __align__(16) float s_bm[kD];
@@ -236,7 +236,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (tid == 0) {
         tc::mbar_init(&load_bar, 1);
-        tc::mbar_init(&mma_bar, 1);
+        tc::mbar_init(&r1_bar, 2);  // rounds are issued by several warps, one commit each
+        tc::mbar_init(&r2_bar, 2);
+        tc::mbar_init(&r3_bar, 2);
+        tc::mbar_init(&r4_bar, 2);
         tc::fence_mbar_init();
         s_unsafe = 0;
         s_abort = 0;
@@ -307,7 +310,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         uint8_t *Xp = sm + PrepSmem::X + (uint32_t)half * 16384u;
         uint8_t *Vp = sm + PrepSmem::V + (uint32_t)half * 8192u;
         uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)half * 8192u;
-        uint8_t *Kg = reinterpret_cast<uint8_t *>(rec + R.Kend) + (size_t)half * 8192;
 #pragma unroll 2
         for (int g8 = 0; g8 < 8; ++g8) {
             const int cc = g8 * 8, c0 = half * 64 + cc;
@@ -335,7 +337,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!unsafe) *reinterpret_cast<uint4 *>(Yp + off_k) = pack8(y8);
             *reinterpret_cast<uint4 *>(Vp + off_k) = pack8(bv);
             kend[g8] = pack8(ke);
-            *reinterpret_cast<uint4 *>(Kg + off_k) = kend[g8];
         }
     }
     tc::fence_async_smem();
@@ -344,7 +345,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_after();
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-    uint32_t mma_phase = 0;
+    const int lane = tid & 31;
     bool ok = true;
     float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
     uint8_t *Pb = sm + PrepSmem::P;
@@ -362,25 +363,31 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s0 + j8)) = pack8(w);
         }
     } else {
-        // round 1: [beta k e1 ; q e1] x (k / e1)^T -> TMEM cols 0..63 (rows 0-63 A, 64-127 P)
-        if (tid == 0) {
+        // round 1: [beta k e1 ; q e1] x (k / e1)^T (rows 0-63 A, 64-127 P), the two K panels
+        // issued by warps 0 and 1 into TMEM cols 0..63 and 128..191
+        if (lane == 0 && warp < 2) {
             constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, false, false);
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
-                const uint32_t kb = (uint32_t)(s >> 2) * 8192u + (uint32_t)(s & 3) * 32u;
-                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::X + ka)),
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ka = (uint32_t)warp * 16384u + (uint32_t)s * 32u;
+                const uint32_t kb = (uint32_t)warp * 8192u + (uint32_t)s * 32u;
+                tc::mma_bf16(tmem + 128u * (uint32_t)warp, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::X + ka)),
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + kb)), id, s > 0);
             }
-            tc::mma_commit(&mma_bar);
+            tc::mma_commit(&r1_bar);
         }
         __syncwarp();
-        ok = tc::mbar_wait(&mma_bar, mma_phase);
-        mma_phase ^= 1;
+        ok = tc::mbar_wait(&r1_bar, 0);
         tc::tc_fence_after();
         if (warp_all(ok)) {
-            float v[64];
+            float v[64], v2[32];
             tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(v));
+            tc::tmem_ld32(tmem + lane_base + 128u, v2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += v2[i];
             tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(v + 32));
+            tc::tmem_ld32(tmem + lane_base + 160u, v2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 + i] += v2[i];
             __syncthreads();  // every lane has read round 1 before P overwrites the B operand
             if (tid < 64) {
                 const int r = tid;
@@ -456,21 +463,18 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_after();
 
     // round 2: W'^T = (T X_k)^T -> cols 64..127;  Ut^T = (T beta V)^T -> cols 128..191
-    if (tid == 0) {
+    if (lane == 0 && warp < 2) {  // warp 0: W', warp 1: Ut
         constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, true, false);
-        constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
-        constexpr uint64_t kVmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t bdesc = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Tb + s * 32));
-            tc::mma_bf16(tmem + 64, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + s * 2048)), bdesc, id, s > 0);
-            tc::mma_bf16(tmem + 128, tc::smem_desc(kVmn, tc::smem_u32(sm + PrepSmem::V + s * 2048)), bdesc, id,
-                         s > 0);
-        }
-        tc::mma_commit(&mma_bar);
+        const uint64_t amn = warp == 0 ? tc::smem_desc_base(16384, 1024, tc::SW_128B)
+                                       : tc::smem_desc_base(8192, 1024, tc::SW_128B);
+        uint8_t *abase = sm + (warp == 0 ? PrepSmem::X : PrepSmem::V);
+        for (int s = 0; s < 4; ++s)
+            tc::mma_bf16(tmem + 64u * (uint32_t)(warp + 1), tc::smem_desc(amn, tc::smem_u32(abase + s * 2048)),
+                         tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Tb + s * 32)), id, s > 0);
+        tc::mma_commit(&r2_bar);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&mma_bar, mma_phase);
-    mma_phase ^= 1;
+    ok = tc::mbar_wait(&r2_bar, 0);
     tc::tc_fence_after();
     if (warp_all(ok)) {
         float w[64], u[64];
@@ -479,13 +483,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::tmem_ld32(tmem + lane_base + 128u, *reinterpret_cast<float(*)[32]>(u));
         tc::tmem_ld32(tmem + lane_base + 160u, *reinterpret_cast<float(*)[32]>(u + 32));
         __syncthreads();  // round 2 has consumed beta V before Ut^T replaces it
-        uint8_t *UtTile = reinterpret_cast<uint8_t *>(rec + R.tiles) + (size_t)(c >> 5) * R.tile_bytes;
 #pragma unroll
         for (int s8 = 0; s8 < 64; s8 += 8) {
             *reinterpret_cast<uint4 *>(sm + PrepSmem::WT + tc::sw128_offset(c, s8)) = pack8_at(w + s8);
-            const uint4 uu = pack8_at(u + s8);
-            *reinterpret_cast<uint4 *>(sm + PrepSmem::V + tc::sw128_offset(c, s8)) = uu;
-            *reinterpret_cast<uint4 *>(UtTile + tc::sw128_offset(c & 31, s8)) = uu;
+            *reinterpret_cast<uint4 *>(sm + PrepSmem::V + tc::sw128_offset(c, s8)) = pack8_at(u + s8);
         }
         // Kend (kept in registers since the operand build) -> MN-major [s][c] operand
         const int r = tid >> 1, half = tid & 1;
@@ -506,51 +507,44 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return;
     }
 
-    // round 3:  (X_q - P W')^T -> cols 0..63;  Oloc^T = Ut^T P^T -> cols 64..127;
-    //           Kend^T W' -> cols 128..255
-    if (tid == 0) {
-        constexpr uint32_t id_neg = tc::idesc_bf16_f32(128, 64, false, false) | (1u << 14);  // negate B
-        constexpr uint32_t id_xq = tc::idesc_bf16_f32(128, 64, true, false);
-        constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64, false, false);
-        constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
-        constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
-        constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t pdesc = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32));
-            const uint64_t wt = tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32));
-            tc::mma_bf16(tmem, wt, pdesc, id_neg, s > 0);
-            tc::mma_bf16(tmem + 64, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), pdesc, id64,
-                         s > 0);
-            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)), wt, id128,
-                         s > 0);
+    // round 3:  (X_q - P W')^T -> cols 0..63 (warp 0);  Kend^T W' -> cols 128..255 (warp 1)
+    if (lane == 0 && warp < 2) {
+        if (warp == 0) {
+            constexpr uint32_t id_neg = tc::idesc_bf16_f32(128, 64, false, false) | (1u << 14);  // negate B
+            constexpr uint32_t id_xq = tc::idesc_bf16_f32(128, 64, true, false);
+            constexpr uint64_t kXmn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
+            for (int s = 0; s < 4; ++s)
+                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32)), id_neg, s > 0);
+            for (int s = 0; s < 4; ++s)
+                tc::mma_bf16(tmem, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + 8192 + s * 2048)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Id + s * 32)), id_xq, true);
+        } else {
+            constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
+            constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
+            for (int s = 0; s < 4; ++s)
+                tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32)), id128, s > 0);
         }
-        for (int s = 0; s < 4; ++s)
-            tc::mma_bf16(tmem, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + 8192 + s * 2048)),
-                         tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Id + s * 32)), id_xq, true);
-        tc::mma_commit(&mma_bar);
+        tc::mma_commit(&r3_bar);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&mma_bar, mma_phase);
+    ok = tc::mbar_wait(&r3_bar, 0);
     tc::tc_fence_after();
     if (warp_all(ok)) {
+        // Qp = (X_q - P W') exp(b_m), stored MN-major [c][r]; M' = -Kend^T W' exp(b_m), K-major [c][c']
         const float em = s_Em[c];
         uint8_t *QpG = reinterpret_cast<uint8_t *>(rec + R.Qp);
         uint8_t *McG = reinterpret_cast<uint8_t *>(rec + R.Mc);
-        uint8_t *OlG = reinterpret_cast<uint8_t *>(rec + R.tiles) + (size_t)(c >> 5) * R.tile_bytes + 4096 +
-                       (size_t)(c & 31) * 128;
         {
-            float qv[64], ol[64];
+            float qv[64];
             tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(qv));
             tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(qv + 32));
-            tc::tmem_ld32(tmem + lane_base + 64u, *reinterpret_cast<float(*)[32]>(ol));
-            tc::tmem_ld32(tmem + lane_base + 96u, *reinterpret_cast<float(*)[32]>(ol + 32));
 #pragma unroll
             for (int i = 0; i < 64; ++i) qv[i] *= em;
 #pragma unroll
-            for (int s8 = 0; s8 < 64; s8 += 8) {
+            for (int s8 = 0; s8 < 64; s8 += 8)
                 *reinterpret_cast<uint4 *>(QpG + tc::sw128_offset(c, s8)) = pack8_at(qv + s8);
-                *reinterpret_cast<uint4 *>(OlG + s8 * 2) = pack8_at(ol + s8);
-            }
         }
 #pragma unroll
         for (int q32 = 0; q32 < 4; ++q32) {
@@ -567,6 +561,71 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     }
     tc::tc_fence_before();
+    if (!ok) s_abort = 1;
+    __syncthreads();
+    tc::tc_fence_after();
+    if (s_abort) {
+        if (tid == 0) flag_timeout(ws);
+        if (warp == 0) tc::tmem_dealloc(tmem, 256);
+        return;
+    }
+
+    // round 4:  Oloc^T = Ut^T P^T -> cols 0..63 (warp 0);  Bc = Kend^T Ut -> cols 128..255 (warp 1)
+    if (lane == 0 && warp < 2) {
+        if (warp == 0) {
+            constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64, false, false);
+            for (int s = 0; s < 4; ++s)
+                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32)), id64, s > 0);
+        } else {
+            constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
+            constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
+            for (int s = 0; s < 4; ++s)
+                tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), id128, s > 0);
+        }
+        tc::mma_commit(&r4_bar);
+    }
+    __syncwarp();
+    ok = tc::mbar_wait(&r4_bar, 0);
+    tc::tc_fence_after();
+    if (warp_all(ok)) {
+        uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R.tiles);
+        {
+            // Oloc column j = c into tile j / 32, pair-interleaved [16 pairs][64 tokens][2]: lanes j and
+            // j ^ 1 trade halves so that each writes 32 tokens of its pair as whole 4-byte words
+            float ol[64];
+            tc::tmem_ld64(tmem + lane_base, ol);
+            const int odd = c & 1;
+            uint8_t *OlG = tiles + (size_t)(c >> 5) * R.tile_bytes + 8192 + (size_t)((c & 31) >> 1) * 256 +
+                           (size_t)odd * 128;
+#pragma unroll
+            for (int r4 = 0; r4 < 32; r4 += 4) {
+                uint32_t wd[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = r4 + u;
+                    // even lane writes tokens 0..31, odd lane 32..63, each as (even column, odd column)
+                    const float give = odd ? ol[r] : ol[32 + r];
+                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                    const float mine = odd ? ol[32 + r] : ol[r];
+                    wd[u] = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
+                }
+                *reinterpret_cast<uint4 *>(OlG + r4 * 4) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kNTile; ++t) {
+            // Bc row c, columns of tile t: four 16-byte chunks, chunk k stored at k ^ ((c >> 1) & 3)
+            float bv[32];
+            tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(t * 32), bv);
+            uint8_t *BcG = tiles + (size_t)t * R.tile_bytes + (size_t)c * 64;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(BcG + ((k ^ ((c >> 1) & 3)) << 4)) = pack8_at(bv + 8 * k);
+        }
+    }
+    tc::tc_fence_before();
     if (!ok && tid == 0) flag_timeout(ws);
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -575,15 +634,16 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // ---------------------------------------------------------------------------
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
+constexpr int kNBuf = 3;  // record buffers: chunk c + 2 streams in while chunk c computes
 struct StateSmem {
-    static constexpr uint32_t Zero = 0;        // 16 KB of zeros: rows 0-63 of the output MMA's A operand
-    static constexpr uint32_t Buf = 16384;     // two record buffers
-    static constexpr uint32_t kBuf = 74752;    // shared record part (65 KB) + this CTA's tile (8 KB)
-    static constexpr uint32_t Mc = 0, Kend = 32768, Qp = 49152, gam = 65536, UtT = 66560, Ol = 66560 + 4096;
+    static constexpr uint32_t Buf = 0;
+    static constexpr uint32_t kBuf = 62464;  // shared record part (49 KB) + this CTA's tile (12 KB)
+    static constexpr uint32_t Mc = 0, Qp = 32768, gam = 49152, Bc = 50176, Ol = 50176 + 8192;
+    static constexpr uint32_t Zero = Buf + kNBuf * kBuf;  // 16 KB of zeros: rows 64-127 of the output operand
     // S^T operand, K-major [32 rows][128 K], 2 panels of 4 KB, ping-pong: chunk c's MMAs read
     // half (c & 1) while the epilogue writes S_{c+1} into the other half, so the output MMAs of
     // chunk c (still in flight after the state MMAs complete) never see S_{c+1}.
-    static constexpr uint32_t SB = Buf + 2 * kBuf;
+    static constexpr uint32_t SB = Zero + 16384;
     static constexpr uint32_t bytes = SB + 16384;
 };
 
@@ -612,12 +672,17 @@ __device__ __forceinline__ void store_state_operand(uint8_t *SB, int i, const fl
     }
 }
 
+// Roles per chunk (128 threads, thread i <-> state row i <-> TMEM lane i):
+//   warps 0, 1 (lane 0)  issue M' S over the two K panels (state, critical path)
+//   warp 3 (lane 0)      issues [Qp ; 0] S after them (output, rows 0-63 of its accumulator)
+//   warps 0, 1           finish the previous chunk's outputs while the state MMAs run
+//   all                  S <- gamma S + Bc + M' S, and the bf16 copy for the next chunk
 __global__ void __launch_bounds__(128, 1)
 prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  __nv_bfloat16 *__restrict__ o, float *__restrict__ S_final, char *__restrict__ ws,
                  size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[2], a_bar, b_bar[2];
+    __shared__ uint64_t full_bar[kNBuf], a_bar, b_bar[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
@@ -644,14 +709,15 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         const char *rec_h = ws + records_off + (size_t)h * record_bytes;
         const size_t rec_stride = (size_t)H * record_bytes;
         if (tid == 0) {
-            tc::mbar_init(&full_bar[0], 1);
-            tc::mbar_init(&full_bar[1], 1);
-            tc::mbar_init(&a_bar, 1);
+            for (int b = 0; b < kNBuf; ++b) tc::mbar_init(&full_bar[b], 1);
+            tc::mbar_init(&a_bar, 2);  // one commit from each of the two state-MMA issuers
             tc::mbar_init(&b_bar[0], 1);
             tc::mbar_init(&b_bar[1], 1);
             tc::fence_mbar_init();
             s_abort = 0;
-            issue_record(sm + StateSmem::Buf, rec_h + (size_t)first * rec_stride, tile, &full_bar[0]);
+            for (int c = 0; c < 2 && c < nchunks; ++c)
+                issue_record(sm + StateSmem::Buf + c * StateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride,
+                             tile, &full_bar[c]);
         }
         if (warp == 0) {
             tc::tmem_alloc(&tmem_base, 128);
@@ -660,75 +726,78 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
-        const uint32_t tmem = tmem_base;  // S acc: cols 0..31; O acc: 32..63 / 64..95 (ping-pong, rows 64-127)
+        // TMEM: M' S over the two K panels in cols 0..31 and 32..63; the output accumulator
+        // ping-pongs between cols 64 and 96 (its rows 0-63 hold O).
+        const uint32_t tmem = tmem_base;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-        constexpr uint64_t kKendMn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
         constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
         constexpr uint32_t idMnN = tc::idesc_bf16_f32(128, kTile, true, false);
         const int t_doc = cu[n], t_end = cu[n + 1];
         bool ok = true;
-        uint32_t oloc[kTile / 2];  // this thread's output row of Oloc for the chunk in flight (warps 2-3)
+        uint32_t oloc[kTile / 2];  // this thread's output row of Oloc for the chunk in flight (warps 0-1)
 
         for (int c = 0; c <= nchunks; ++c) {
-            const int bsel = c & 1;
+            const int bsel = c % kNBuf;
+            const uint32_t fpar = (uint32_t)((c / kNBuf) & 1);
             uint8_t *buf = sm + StateSmem::Buf + bsel * StateSmem::kBuf;
-            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)bsel * 8192u;
+            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c & 1) * 8192u;
             if (c < nchunks) {
-                if (tid == 0) {
-                    // output MMAs of the previous chunk done -> its buffer is free for chunk c + 1
-                    if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
-                    if (ok && c + 1 < nchunks)
-                        issue_record(sm + StateSmem::Buf + (bsel ^ 1) * StateSmem::kBuf,
-                                     rec_h + (size_t)(first + c + 1) * rec_stride, tile, &full_bar[bsel ^ 1]);
-                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
+                if (lane == 0 && warp < 2) {
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
                     if (ok) {
                         tc::tc_fence_after();
-                        // state: Kend^T Ut + M' S -> S acc
+                        const uint32_t panel = (uint32_t)warp;
                         for (int s = 0; s < 4; ++s)
-                            tc::mma_bf16(tmem, tc::smem_desc(kKendMn, tc::smem_u32(buf + StateSmem::Kend + s * 2048)),
-                                         tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::UtT + s * 32)), idMnN,
-                                         s > 0);
-                        for (int s = 0; s < 8; ++s) {
-                            const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
-                            const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                            tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + ka)),
-                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idN, true);
-                        }
+                            tc::mma_bf16(tmem + 32u * panel,
+                                         tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u +
+                                                                           (uint32_t)s * 32u)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u + (uint32_t)s * 32u)),
+                                         idN, s > 0);
                         tc::mma_commit(&a_bar);
                     }
                 }
-                if (warp == 0) {
-                    __syncwarp();
-                    tc::named_barrier_arrive(2, 64);
-                } else if (warp == 2) {
-                    tc::named_barrier(2, 64);
+                __syncwarp();
+                if (warp < 2) {
+                    tc::named_barrier_arrive(2, 96);
+                } else if (warp == 3) {
+                    tc::named_barrier(2, 96);
                     if (lane == 0) {
-                        // output: [0 ; Qp] S -> O acc[c & 1] rows 64..127
+                        ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
                         tc::tc_fence_after();
-                        const uint32_t oacc = tmem + 32u + (uint32_t)bsel * 32u;
+                        // output: [Qp ; 0] S -> O acc[c & 1], queued behind the state MMAs
+                        const uint32_t oacc = tmem + 64u + (uint32_t)(c & 1) * 32u;
                         const uint64_t kQp = tc::smem_desc_base(
-                            (uint32_t)(StateSmem::Buf + bsel * StateSmem::kBuf + StateSmem::Qp - StateSmem::Zero), 1024,
-                            tc::SW_128B);
+                            (uint32_t)(StateSmem::Zero - (StateSmem::Buf + bsel * StateSmem::kBuf + StateSmem::Qp)),
+                            1024, tc::SW_128B);
                         for (int s = 0; s < 8; ++s) {
                             const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                            tc::mma_bf16(oacc, tc::smem_desc(kQp, tc::smem_u32(sm + StateSmem::Zero + s * 2048)),
+                            tc::mma_bf16(oacc, tc::smem_desc(kQp, tc::smem_u32(buf + StateSmem::Qp + s * 2048)),
                                          tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idMnN, s > 0);
                         }
-                        tc::mma_commit(&b_bar[bsel]);
+                        tc::mma_commit(&b_bar[c & 1]);
+                        // the previous chunk's output MMAs are done too (in order) -> its buffer is free
+                        // for chunk c + 2
+                        if (c + 2 < nchunks) {
+                            if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                            if (ok)
+                                issue_record(sm + StateSmem::Buf + ((c + 2) % kNBuf) * StateSmem::kBuf,
+                                             rec_h + (size_t)(first + c + 2) * rec_stride, tile,
+                                             &full_bar[(c + 2) % kNBuf]);
+                        }
                     }
                     __syncwarp();
                 }
             }
-            if (warp >= 2) {
-                const int r = tid - 64;
+            if (warp < 2) {
+                const int r = tid;
                 if (c > 0) {
-                    // O of the previous chunk: [0 ; Qp] S rows 64-127 + Oloc
+                    // O of the previous chunk: rows 0-63 of [Qp ; 0] S, plus Oloc
                     ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
                     tc::tc_fence_after();
                     if (warp_all(ok)) {
                         float t[32];
-                        tc::tmem_ld32(tmem + lane_base + 32u + (uint32_t)((c - 1) & 1) * 32u, t);
+                        tc::tmem_ld32(tmem + lane_base + 64u + (uint32_t)((c - 1) & 1) * 32u, t);
                         const int t0p = t_doc + (c - 1) * kL;
                         if (t0p + r < t_end) {
                             uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0p + r) * H + h) * kD + col0);
@@ -750,27 +819,32 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 }
                 if (c < nchunks) {
                     // this chunk's Oloc row, kept for next iteration's output
-                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c >> 1) & 1));
-                    const uint8_t *ol = buf + StateSmem::Ol + r * 2;
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
+                    const uint32_t *ol = reinterpret_cast<const uint32_t *>(buf + StateSmem::Ol) + r;
 #pragma unroll
-                    for (int j2 = 0; j2 < kTile / 2; ++j2) {
-                        const uint16_t lo = *reinterpret_cast<const uint16_t *>(ol + (2 * j2) * 128);
-                        const uint16_t hi = *reinterpret_cast<const uint16_t *>(ol + (2 * j2 + 1) * 128);
-                        oloc[j2] = (uint32_t)lo | ((uint32_t)hi << 16);
-                    }
+                    for (int p2 = 0; p2 < kTile / 2; ++p2) oloc[p2] = ol[p2 * 64];
                 }
             }
             if (c < nchunks) {
-                // S <- gamma * S + (Kend^T Ut + M' S)
+                // S <- gamma * S + Kend^T Ut + M' S (the last term in two K halves)
                 ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
                 tc::tc_fence_after();
                 if (warp_all(ok)) {
                     const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-                    float t[32];
-                    tc::tmem_ld32(tmem + lane_base, t);
+                    float bc[32];
+                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
 #pragma unroll
-                    for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], t[j]);
-                    store_state_operand(sm + StateSmem::SB + (uint32_t)(bsel ^ 1) * 8192u, i, S);
+                    for (int k = 0; k < 4; ++k) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), f);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) bc[8 * k + u] = f[u];
+                    }
+                    float t[64];
+                    tc::tmem_ld64(tmem + lane_base, t);
+#pragma unroll
+                    for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t[j] + t[32 + j]));
+                    store_state_operand(sm + StateSmem::SB + (uint32_t)((c + 1) & 1) * 8192u, i, S);
                 }
             }
             tc::fence_async_smem();
@@ -784,7 +858,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             // let any copy still in flight land before the CTA's shared memory goes away
             if (tid == 0) {
                 flag_timeout(ws);
-                for (int b = 0; b < 2; ++b) tc::mbar_wait(&full_bar[b], 0, 10000000ull);
+                for (int b = 0; b < kNBuf; ++b) tc::mbar_wait(&full_bar[b], 0, 10000000ull);
             }
             __syncthreads();
         }
