@@ -224,6 +224,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __shared__ __align__(16) float s_bm[kD];
     __shared__ __align__(16) float s_F[kD];
     __shared__ __align__(16) float s_Em[kD];
+    __shared__ __align__(16) float s_blast[kD];
     __shared__ int s_unsafe, s_abort;
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, c = tid;
@@ -284,12 +285,17 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (r < Lc) { bmax = fmaxf(bmax, acc); bmin = fminf(bmin, acc); }
         }
         const float blast = acc;
-        s_bm[c] = bm;
-        s_F[c] = expf(blast - bm);
-        s_Em[c] = expf(bm);
         reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
         if (bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY)) s_unsafe = 1;
-        __syncthreads();  // all of g has been read: b may now go to its swizzled places
+        __syncthreads();  // all of g has been read (b may now go to its swizzled places); s_unsafe is final
+        // Reference point of the factorised exponentials: the middle token; a chunk whose range is too
+        // wide for that takes exact A and P and the chunk start as reference (exp(b_r) <= 1 for
+        // non-positive gates), so no operand can overflow.
+        const float bref = s_unsafe ? 0.f : bm;
+        s_bm[c] = bref;
+        s_F[c] = expf(blast - bref);
+        s_Em[c] = expf(bref);
+        s_blast[c] = blast;
 #pragma unroll
         for (int r = 0; r < kL; ++r) Gf[bswz(r, c)] = bcol[r];
     }
@@ -325,12 +331,13 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int u = 0; u < 8; ++u) {
                 const float d = bb[u] - s_bm[c0 + u];
                 const float e1 = valid ? __expf(d) : 0.f;
-                const float inv = valid ? __expf(-d) : 0.f;
+                const float inv = valid && !unsafe ? __expf(-d) : 0.f;
                 xk[u] = br * k8[u] * e1;
                 xq[u] = q8[u] * e1;
                 y8[u] = k8[u] * inv;
                 bv[u] = br * v8[u];
-                ke[u] = y8[u] * s_F[c0 + u];
+                // Kend = k exp(b_last - b_r) <= |k|: via the bounded factors, or directly when unsafe
+                ke[u] = unsafe ? (valid ? k8[u] * __expf(s_blast[c0 + u] - bb[u]) : 0.f) : y8[u] * s_F[c0 + u];
             }
             *reinterpret_cast<uint4 *>(Xp + off_k) = pack8(xk);
             *reinterpret_cast<uint4 *>(Xp + off_q) = pack8(xq);

@@ -211,3 +211,25 @@ def test_deterministic_inplace_and_guarded():
     libkda.kda_prefill_chunked(q, k, v, g, beta, cu, o, S0=S_in, S_final=S_in, chunk_size=64)
     torch.cuda.synchronize()
     assert torch.equal(S_in, S_first)
+
+
+@pytest.mark.parametrize("channels", ["all", "one"])
+def test_extreme_gates(channels):
+    """Runs of log-decay -10 (the extreme-gate values) inside a chunk, and write strengths 0 or 1.
+
+    A chunk whose cumulative log-decay spans more than the tensor-core form's
+    bounded range (here about 400 on one side of the chunk's middle token)
+    must still match the oracle; so must the chunks around it.
+    """
+    T, H, d = 200, 2, 128
+    inp = workloads.prefill_inputs([T], H=H, d=d, dtype=torch.bfloat16, seed=77, s0_std=0.1)
+    sel = slice(None) if channels == "all" else slice(5, 6)
+    inp.g[70:111, :, sel] = -10.0
+    inp.g[140:142, :, sel] = -1e-4
+    inp.beta[75:80] = 1.0
+    inp.beta[80:85] = 0.0
+    o_ref, S_ref, _ = oracle_prefill(inp, S0=inp.S0)
+    for chunk in (64, 32):
+        o, S = _run(inp, chunk, S0=inp.S0)
+        assert rel(o, o_ref) <= TOL[torch.bfloat16], (chunk, rel(o, o_ref))
+        assert rel(S, S_ref) <= TOL[torch.bfloat16], (chunk, rel(S, S_ref))
