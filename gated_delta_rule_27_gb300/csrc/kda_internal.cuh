@@ -64,21 +64,20 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
 
 // Tensor-core record (d = 128, L = 64).  Every operand of the state pass is
 // stored as the exact shared-memory image that pass consumes (bf16, 128-byte
-// swizzled), so the state pass moves a record with two bulk copies: the part
-// every column tile needs, then its own tile.
+// swizzled), so the state pass moves a record with three bulk copies: the part
+// every column tile needs, then its own tile of Bc and of Oloc.
 //   Mc     M' = -Kend^T W, K-major [128 d_k rows][128 d_k]          2 panels  32 KB
 //   Qp     MN-major [128 d_k][64 tokens] (operand Qp, 64 rows)                16 KB
 //   gamma  fp32 [128], padded to 1 KB
-//   tiles  4 x 12 KB, one per 32-column tile t of S:
-//          Bc   Kend^T Ut rows [128 d_k][32 d_v] bf16, 64-byte rows whose
-//               16-byte chunks are XOR-swizzled by (row mod 4)            8 KB
-//          Oloc P Ut: bf16 [16 column pairs][64 tokens][2], so that token
-//               row r reads its 32 values as 16 consecutive-word loads     4 KB
+//   Bc     Kend^T Ut, per 32-column tile t: bf16 [128 d_k][32 d_v], 64-byte rows
+//          whose 16-byte chunks are XOR-swizzled by ((row / 2) mod 4)   4 x 8 KB
+//   Oloc   P Ut, per tile t: bf16 [16 column pairs][64 tokens][2], so that
+//          token row r reads its 32 values as 16 consecutive-word loads  4 x 4 KB
 struct TcRecord {
-    size_t Mc, Qp, gamma, tiles, tile_bytes, shared_bytes, bytes;
+    size_t Mc, Qp, gamma, Bc, Oloc, shared_bytes, bytes;
 };
 __host__ __device__ constexpr TcRecord tc_record() {
-    return TcRecord{0, 32768, 49152, 50176, 12288, 50176, 50176 + 4 * 12288};
+    return TcRecord{0, 32768, 49152, 50176, 50176 + 32768, 50176, 50176 + 32768 + 16384};
 }
 
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {

@@ -104,41 +104,56 @@ struct PrepSmem {
 // the sub-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
 template <int LVL>
 __device__ __forceinline__ void inverse_level(float *A, float *T, int tid) {
-    constexpr int NB = 4 - LVL;
+    constexpr int NB = 4 - LVL;          // blocks on this sub-diagonal
+    constexpr int ITEMS = NB * 64;       // 4-wide row pieces: (block, row, 4 columns)
+    // M_b = sum_k A_{i,k} T_{k,j} -> diagonal block b of A (no longer needed there)
 #pragma unroll
-    for (int q = 0; q < (NB * 256 + 127) / 128; ++q) {  // M_b = sum_k A_{i,k} T_{k,j} -> diagonal block b of A
+    for (int q = 0; q < (ITEMS + 127) / 128; ++q) {
         const int e = tid + q * 128;
-        if (e < NB * 256) {
-            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15, i = b + LVL;
-            float acc0 = 0.f, acc1 = 0.f;
+        if (e < ITEMS) {
+            const int b = e >> 6, r = (e >> 2) & 15, s0 = (e & 3) * 4, i = b + LVL;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int kk = 0; kk < LVL; ++kk) {
                 const float *Aik = A + tri_blk(i, b + kk) + (r << 4);
-                const float *Tkj = T + tri_blk(b + kk, b) + s;
+                const float *Tkj = T + tri_blk(b + kk, b) + s0;
 #pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    acc0 = fmaf(Aik[t], Tkj[t << 4], acc0);
-                    acc1 = fmaf(Aik[t + 1], Tkj[(t + 1) << 4], acc1);
+                for (int t4 = 0; t4 < 16; t4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(Aik + t4);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 tv = *reinterpret_cast<const float4 *>(Tkj + ((t4 + u) << 4));
+                        acc.x = fmaf(av[u], tv.x, acc.x); acc.y = fmaf(av[u], tv.y, acc.y);
+                        acc.z = fmaf(av[u], tv.z, acc.z); acc.w = fmaf(av[u], tv.w, acc.w);
+                    }
                 }
             }
-            A[tri_blk(b, b) + (r << 4) + s] = acc0 + acc1;
+            *reinterpret_cast<float4 *>(A + tri_blk(b, b) + (r << 4) + s0) = acc;
         }
     }
     __syncthreads();
 #pragma unroll
-    for (int q = 0; q < (NB * 256 + 127) / 128; ++q) {
+    for (int q = 0; q < (ITEMS + 127) / 128; ++q) {
         const int e = tid + q * 128;
-        if (e < NB * 256) {
-            const int b = e >> 8, r = (e >> 4) & 15, s = e & 15, i = b + LVL;
+        if (e < ITEMS) {
+            const int b = e >> 6, r = (e >> 2) & 15, s0 = (e & 3) * 4, i = b + LVL;
             const float *Tii = T + tri_blk(i, i) + (r << 4);
-            const float *M = A + tri_blk(b, b) + s;
-            float acc0 = 0.f, acc1 = 0.f;
+            const float *M = A + tri_blk(b, b) + s0;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < 16; t += 2) {
-                acc0 = fmaf(Tii[t], M[t << 4], acc0);
-                acc1 = fmaf(Tii[t + 1], M[(t + 1) << 4], acc1);
+            for (int t4 = 0; t4 < 16; t4 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Tii + t4);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 mv = *reinterpret_cast<const float4 *>(M + ((t4 + u) << 4));
+                    acc.x = fmaf(av[u], mv.x, acc.x); acc.y = fmaf(av[u], mv.y, acc.y);
+                    acc.z = fmaf(av[u], mv.z, acc.z); acc.w = fmaf(av[u], mv.w, acc.w);
+                }
             }
-            T[tri_blk(i, b) + (r << 4) + s] = -(acc0 + acc1);
+            *reinterpret_cast<float4 *>(T + tri_blk(i, b) + (r << 4) + s0) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
     }
     __syncthreads();
@@ -221,7 +236,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __shared__ uint64_t load_bar, r1_bar, r2_bar, r3_bar, r4_bar;  // one barrier per MMA round
     __shared__ uint32_t tmem_base;
     __shared__ float s_beta[kL];
-    __shared__ __align__(16) float s_bm[kD];
+    __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
     __shared__ __align__(16) float s_F[kD];
     __shared__ __align__(16) float s_Em[kD];
     __shared__ __align__(16) float s_blast[kD];
@@ -327,9 +342,14 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const float4 b0 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0));
             const float4 b1 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0 + 4));
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            float bmv[8], fv[8];
+            *reinterpret_cast<float4 *>(bmv) = *reinterpret_cast<const float4 *>(s_bm + c0);
+            *reinterpret_cast<float4 *>(bmv + 4) = *reinterpret_cast<const float4 *>(s_bm + c0 + 4);
+            *reinterpret_cast<float4 *>(fv) = *reinterpret_cast<const float4 *>(s_F + c0);
+            *reinterpret_cast<float4 *>(fv + 4) = *reinterpret_cast<const float4 *>(s_F + c0 + 4);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const float d = bb[u] - s_bm[c0 + u];
+                const float d = bb[u] - bmv[u];
                 const float e1 = valid ? __expf(d) : 0.f;
                 const float inv = valid && !unsafe ? __expf(-d) : 0.f;
                 xk[u] = br * k8[u] * e1;
@@ -337,7 +357,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 y8[u] = k8[u] * inv;
                 bv[u] = br * v8[u];
                 // Kend = k exp(b_last - b_r) <= |k|: via the bounded factors, or directly when unsafe
-                ke[u] = unsafe ? (valid ? k8[u] * __expf(s_blast[c0 + u] - bb[u]) : 0.f) : y8[u] * s_F[c0 + u];
+                ke[u] = unsafe ? (valid ? k8[u] * __expf(s_blast[c0 + u] - bb[u]) : 0.f) : y8[u] * fv[u];
             }
             *reinterpret_cast<uint4 *>(Xp + off_k) = pack8(xk);
             *reinterpret_cast<uint4 *>(Xp + off_q) = pack8(xq);
@@ -539,34 +559,38 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     ok = tc::mbar_wait(&r3_bar, 0);
     tc::tc_fence_after();
     if (warp_all(ok)) {
-        // Qp = (X_q - P W') exp(b_m), stored MN-major [c][r]; M' = -Kend^T W' exp(b_m), K-major [c][c']
+        // Qp = (X_q - P W') exp(b_m), MN-major [c][r]; M' = -Kend^T W' exp(b_m), K-major [c][c'].
+        // Both are staged in shared memory (round 3 has consumed X and W'^T) and leave by bulk copy.
         const float em = s_Em[c];
-        uint8_t *QpG = reinterpret_cast<uint8_t *>(rec + R.Qp);
-        uint8_t *McG = reinterpret_cast<uint8_t *>(rec + R.Mc);
+        uint8_t *QpS = sm + PrepSmem::WT;
+        uint8_t *McS = sm + PrepSmem::X;
         {
             float qv[64];
-            tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(qv));
-            tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(qv + 32));
+            tc::tmem_ld64(tmem + lane_base, qv);
 #pragma unroll
             for (int i = 0; i < 64; ++i) qv[i] *= em;
 #pragma unroll
             for (int s8 = 0; s8 < 64; s8 += 8)
-                *reinterpret_cast<uint4 *>(QpG + tc::sw128_offset(c, s8)) = pack8_at(qv + s8);
+                *reinterpret_cast<uint4 *>(QpS + tc::sw128_offset(c, s8)) = pack8_at(qv + s8);
         }
 #pragma unroll
         for (int q32 = 0; q32 < 4; ++q32) {
             float mv[32];
             tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(q32 * 32), mv);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mv[i] *= -s_Em[q32 * 32 + i];
+            for (int i4 = 0; i4 < 32; i4 += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(s_Em + q32 * 32 + i4);
+                mv[i4] *= -e4.x; mv[i4 + 1] *= -e4.y; mv[i4 + 2] *= -e4.z; mv[i4 + 3] *= -e4.w;
+            }
 #pragma unroll
             for (int h8 = 0; h8 < 32; h8 += 8) {
                 const int cp = q32 * 32 + h8;
-                *reinterpret_cast<uint4 *>(McG + (uint32_t)(cp >> 6) * 16384u + tc::sw128_offset(c, cp & 63)) =
+                *reinterpret_cast<uint4 *>(McS + (uint32_t)(cp >> 6) * 16384u + tc::sw128_offset(c, cp & 63)) =
                     pack8_at(mv + h8);
             }
         }
     }
+    tc::fence_async_smem();
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
     __syncthreads();
@@ -575,6 +599,11 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (tid == 0) flag_timeout(ws);
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
+    }
+    if (tid == 0) {
+        tc::bulk_s2g(rec + R.Mc, sm + PrepSmem::X, 32768);
+        tc::bulk_s2g(rec + R.Qp, sm + PrepSmem::WT, 16384);
+        tc::bulk_commit();
     }
 
     // round 4:  Oloc^T = Ut^T P^T -> cols 0..63 (warp 0);  Bc = Kend^T Ut -> cols 128..255 (warp 1)
@@ -596,16 +625,17 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncwarp();
     ok = tc::mbar_wait(&r4_bar, 0);
     tc::tc_fence_after();
+    if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
+    __syncthreads();
     if (warp_all(ok)) {
-        uint8_t *tiles = reinterpret_cast<uint8_t *>(rec + R.tiles);
         {
             // Oloc column j = c into tile j / 32, pair-interleaved [16 pairs][64 tokens][2]: lanes j and
             // j ^ 1 trade halves so that each writes 32 tokens of its pair as whole 4-byte words
             float ol[64];
             tc::tmem_ld64(tmem + lane_base, ol);
             const int odd = c & 1;
-            uint8_t *OlG = tiles + (size_t)(c >> 5) * R.tile_bytes + 8192 + (size_t)((c & 31) >> 1) * 256 +
-                           (size_t)odd * 128;
+            uint8_t *OlG = reinterpret_cast<uint8_t *>(rec + R.Oloc) + (size_t)(c >> 5) * 4096 +
+                           (size_t)((c & 31) >> 1) * 256 + (size_t)odd * 128;
 #pragma unroll
             for (int r4 = 0; r4 < 32; r4 += 4) {
                 uint32_t wd[4];
@@ -626,15 +656,23 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // Bc row c, columns of tile t: four 16-byte chunks, chunk k stored at k ^ ((c >> 1) & 3)
             float bv[32];
             tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(t * 32), bv);
-            uint8_t *BcG = tiles + (size_t)t * R.tile_bytes + (size_t)c * 64;
+            uint8_t *BcS = sm + PrepSmem::X + t * 8192 + c * 64;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(BcG + ((k ^ ((c >> 1) & 3)) << 4)) = pack8_at(bv + 8 * k);
+                *reinterpret_cast<uint4 *>(BcS + ((k ^ ((c >> 1) & 3)) << 4)) = pack8_at(bv + 8 * k);
         }
     }
+    tc::fence_async_smem();
     tc::tc_fence_before();
     if (!ok && tid == 0) flag_timeout(ws);
     __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            tc::bulk_s2g(rec + R.Bc, sm + PrepSmem::X, 32768);
+            tc::bulk_commit();
+        }
+        tc::bulk_wait_read();  // shared memory must outlive the copies' reads
+    }
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
@@ -658,7 +696,8 @@ __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int 
     constexpr TcRecord R = tc_record();
     tc::mbar_arrive_expect_tx(bar, StateSmem::kBuf);
     tc::bulk_g2s(buf, rec, (uint32_t)R.shared_bytes, bar);
-    tc::bulk_g2s(buf + R.shared_bytes, rec + R.tiles + (size_t)tile * R.tile_bytes, (uint32_t)R.tile_bytes, bar);
+    tc::bulk_g2s(buf + StateSmem::Bc, rec + R.Bc + (size_t)tile * 8192, 8192, bar);
+    tc::bulk_g2s(buf + StateSmem::Ol, rec + R.Oloc + (size_t)tile * 4096, 4096, bar);
 }
 
 // Writes row i of S (32 values) into the K-major S^T operand: element (j, i),
