@@ -270,11 +270,20 @@ def barrier():
 
 
 def max_over_ranks(x: float) -> float:
+    """The slowest rank's value (timing control plane only; no data-path collective)."""
     if torch.distributed.is_available() and torch.distributed.is_initialized():
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
     return x
+
+
+def weak_scaling_value(units_per_rank: float, seconds_per_rank: float) -> float:
+    """Whole-job throughput: every rank processes its own copy of the workload, the job ends with the
+    slowest rank."""
+    world = torch.distributed.get_world_size() if torch.distributed.is_initialized() else 1
+    return world * units_per_rank / max_over_ranks(seconds_per_rank)
 
 
 def cpu_baseline_prefill(inp, budget_s=10.0):
