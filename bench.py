@@ -7,6 +7,7 @@ sequences x 32 heads, fp32 state of 512 MiB) is timed in the same run and
 reported under "decode".  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libkda|reference]
+  python bench.py --profile-case prefill|decode-n64 [--repeat R]   (untimed, for ncu)
 
 Timing: CUDA events on the launching stream, L2 flushed (a 256 MB write)
 before every timed prefill step (the prefill inputs, 101 MB, would otherwise
@@ -426,6 +427,36 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile_case(case: str, repeat: int):
+    """Untimed launches of one workload, for an external profiler (ncu) to capture.
+
+    'prefill' runs the prefill workload through kda_prefill_chunked; 'decode-n64' runs decode steps over
+    a quarter of the decode workload's sequences (64 x 32 heads, 128 MiB of state), small enough for a
+    many-pass capture.
+    """
+    from gated_delta_rule_27_gb300 import libkda
+    torch.cuda.set_device(0)
+    if case == "prefill":
+        inp = workloads.workload_prefill(WORKLOAD, device="cuda")
+        T, N = inp.total_tokens, inp.num_seqs
+        H, d = inp.q.shape[1], inp.q.shape[2]
+        o = torch.empty_like(inp.v)
+        S = torch.empty((N, H, d, d), device="cuda")
+        ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, 64, "cuda")
+        for _ in range(repeat):
+            libkda.kda_prefill_chunked(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, o, S_final=S,
+                                       workspace=ws)
+    else:
+        dec = workloads.decode_inputs(repeat, 64, 32, 128, torch.bfloat16, seed=workloads.workload_seed("decode"),
+                                      device="cuda")
+        S = dec.S0.clone()
+        o = torch.empty((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+        for t in range(repeat):
+            libkda.kda_decode_step(dec.q[t], dec.k[t], dec.v[t], dec.g[t], dec.beta[t], S, o)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": case, "repeat": repeat, "status": "ok"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,7 +464,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode-n64"], default=None,
+                    help="run untimed launches of one workload for a profiler, print a status line, exit")
+    ap.add_argument("--repeat", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.repeat)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
