@@ -62,22 +62,26 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
     return r;
 }
 
-// Tensor-core record (d = 128, L = 64).  Every operand of the state pass is
-// stored as the exact shared-memory image that pass consumes (bf16, 128-byte
-// swizzled), so the state pass moves a record with three bulk copies: the part
-// every column tile needs, then its own tile of Bc and of Oloc.
-//   Mc     M' = -Kend^T W, K-major [128 d_k rows][128 d_k]          2 panels  32 KB
-//   Qp     MN-major [128 d_k][64 tokens] (operand Qp, 64 rows)                16 KB
+// Tensor-core record (d = 128, L = 64).  Every operand is stored as the exact
+// shared-memory image its consumer loads (bf16, 128-byte swizzled unless
+// noted), so each consumer moves its part of a record with one or two bulk
+// copies.  The state pass reads [Mc, Bc) plus its own column tile of Bc and
+// writes S; the output pass reads [Qp, bytes) in one piece.
+//   Mc     M' = -Kend^T W, K-major [128 d_k rows][128 d_k], 2 panels          32 KB
 //   gamma  fp32 [128], padded to 1 KB
 //   Bc     Kend^T Ut, per 32-column tile t: bf16 [128 d_k][32 d_v], 64-byte rows
-//          whose 16-byte chunks are XOR-swizzled by ((row / 2) mod 4)   4 x 8 KB
-//   Oloc   P Ut, per tile t: bf16 [16 column pairs][64 tokens][2], so that
-//          token row r reads its 32 values as 16 consecutive-word loads  4 x 4 KB
+//          whose 16-byte chunks are XOR-swizzled by ((row / 2) mod 4)    4 x 8 KB
+//   Qp     MN-major [128 d_k][64 tokens]                                       16 KB
+//   P      intra-chunk scores, K-major [64 tokens][64 tokens]                   8 KB
+//   Ut     Ut^T, K-major [128 d_v][64 tokens]                                  16 KB
+//   S      the chunk's incoming state as the state pass multiplied it: bf16
+//          K-major [128 d_v rows][128 d_k], 2 panels of 16 KB (written by the
+//          state pass, tile t filling rows 32t .. 32t + 31 of both panels)     32 KB
 struct TcRecord {
-    size_t Mc, Qp, gamma, Bc, Oloc, shared_bytes, bytes;
+    size_t Mc, gamma, Bc, Qp, P, Ut, S, state_part, out_part, bytes;
 };
 __host__ __device__ constexpr TcRecord tc_record() {
-    return TcRecord{0, 32768, 49152, 50176, 50176 + 32768, 50176, 50176 + 32768 + 16384};
+    return TcRecord{0, 32768, 33792, 66560, 82944, 91136, 107520, 33792, 140288 - 66560, 140288};
 }
 
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {

@@ -1,38 +1,36 @@
 // kda_prefill_tc.cu -- chunked prefill on the Blackwell tensor cores (tcgen05),
 // bf16 inputs, d_k = d_v = 128, 64-token chunks.
 //
-// Same chunk algebra as the CUDA-core path (Lecture 04, section 1: a chunk's
-// effect on the incoming state is one affine update formed without that
-// state, kept in structured diagonal-plus-rank-one form):
-//     A[r,s] = beta_r sum_c k_rc k_sc exp(b_rc - b_sc)  (s < r),   b_r = sum_{s<=r} g_s
+// Chunk algebra (Lecture 04, section 1: a chunk's effect on the incoming state
+// is one affine update formed without that state).  With b_r = sum_{s<=r} g_s
+// per channel, a reference point b_m and X_k = beta k exp(b - b_m),
+// X_q = q exp(b - b_m), Kend = k exp(b_last - b):
+//     A[r,s] = beta_r sum_c k_rc k_sc exp(b_rc - b_sc)  (s < r)
 //     P[r,s] = sum_c q_rc k_sc exp(b_rc - b_sc)         (s <= r)
-//     T' = (I + A)^{-1} diag(beta)
-//     W = T' (exp(b) * K),   Ut = T' V,   Qp = exp(b) * Q - P W,   Oloc = P Ut
-//     Kend = exp(b_last - b) * K,   gamma = exp(b_last)
-// and per document, chunk after chunk, with S the incoming state:
-//     U = Ut - W S;   O = Qp S + Oloc;   S <- gamma * S + Kend^T U.
+//     T = (I + A)^{-1},  W' = T X_k,  Ut = T (beta V)
+//     Qp = (X_q - P W') exp(b_m),  M' = -Kend^T W' exp(b_m),  Bc = Kend^T Ut,  gamma = exp(b_last)
+// and per document, chunk after chunk, with S_c the state entering chunk c:
+//     S_{c+1} = gamma S_c + M' S_c + Bc,      O_c = Qp S_c + P Ut.
 //
 // Kernel 1, prefill_prepare_tc: one CTA (128 threads, thread c <-> channel c
-// <-> TMEM lane c) per (chunk, head).  q, k, v tiles arrive by TMA (128-byte
-// swizzle).  The dense contractions run as three rounds of tcgen05.mma with
-// fp32 accumulators in TMEM:
-//     round 1  [beta k e1 ; q e1] (128 x 128) x [k / e1]^T (64)   -> A and P
-//     round 2  (exp(b) k)^T T'^T and V^T T'^T                     -> W^T, Ut^T
-//     round 3  W^T P^T and Ut^T P^T                                -> (P W)^T, Oloc^T
-// where e1 = exp(b_r - b_m) is taken about the chunk's middle token m, so
-// every factor is bounded by exp(+-80) as long as the chunk's log-decay range
-// on each side of m stays within 80; a chunk outside that range takes exact
-// pairwise exponentials on the CUDA cores for A and P instead.  The gates,
-// the cumulative sums and the triangular solve stay in fp32 (registers and
-// shared memory); nothing d_k x d_k is ever formed.  The state pass's
-// operands are written to the workspace as ready-made shared-memory images.
+// <-> TMEM lane c) per (chunk, head).  q, k, v, g tiles arrive by TMA.  The
+// dense contractions run as four rounds of tcgen05.mma with fp32 accumulators
+// in TMEM (A and P; W' and Ut; Qp and M'; Bc); the gates, their cumulative
+// sums and the triangular solve stay fp32 on the CUDA cores, and nothing
+// d_k x d_k is formed from a single token.  b_m is the chunk's middle token,
+// so every factor is bounded by exp(+-80) while the chunk's log-decay range on
+// each side of m stays within 80; a chunk outside that range takes exact
+// pairwise exponentials for A and P and reference 0 instead.  Every result is
+// written to the chunk's workspace record as a ready shared-memory image.
 //
-// Kernel 2, prefill_state_tc: one CTA (128 threads, thread i <-> state row i)
-// per (document, head, 32-column tile of S), sequential over the document's
-// chunks.  Per chunk: one bulk copy per operand (double-buffered, one chunk
-// ahead), MMA [W; Qp] (128 x 128) x S (128 x 32) -> [X; Y], U = Ut - X,
-// O = Y + Oloc, MMA Kend^T (128 x 64) x U (64 x 32), S = gamma * S + that.
-// S stays fp32 in registers; its bf16 copy in shared memory feeds the MMA.
+// Kernel 2, prefill_state_tc: one CTA per (document, head, 32-column tile of
+// S), sequential over the document's chunks: one MMA group M' S per chunk,
+// S kept fp32 in registers, its bf16 image in shared memory feeding the next
+// MMA and copied to the chunk's record.
+//
+// Kernel 3, prefill_output_tc: one CTA per (chunk, head), O = Qp S_c + P Ut
+// from the record, written as bf16.
+//
 // Every mbarrier wait is bounded: on expiry the kernel records
 // KDA_ERR_TIMEOUT in the workspace status word and stops.
 #include <cuda.h>
@@ -255,7 +253,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::mbar_init(&r1_bar, 2);  // rounds are issued by several warps, one commit each
         tc::mbar_init(&r2_bar, 2);
         tc::mbar_init(&r3_bar, 2);
-        tc::mbar_init(&r4_bar, 2);
+        tc::mbar_init(&r4_bar, 1);
         tc::fence_mbar_init();
         s_unsafe = 0;
         s_abort = 0;
@@ -462,7 +460,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (!ok) s_abort = 1;
     __syncthreads();
     if (s_abort) {
-        if (tid == 0) flag_timeout(ws);
+        if (tid == 0) {
+            flag_timeout(ws);
+            tc::bulk_wait_read();  // record images already on their way still read shared memory
+        }
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
@@ -488,6 +489,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    if (tid == 0) {  // P is final: its image goes to the record for the output pass
+        tc::bulk_s2g(rec + R.P, sm + PrepSmem::P, 8192);
+        tc::bulk_commit();
+    }
 
     // round 2: W'^T = (T X_k)^T -> cols 64..127;  Ut^T = (T beta V)^T -> cols 128..191
     if (lane == 0 && warp < 2) {  // warp 0: W', warp 1: Ut
@@ -529,9 +534,17 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
     if (s_abort) {
-        if (tid == 0) flag_timeout(ws);
+        if (tid == 0) {
+            flag_timeout(ws);
+            tc::bulk_wait_read();  // record images already on their way still read shared memory
+        }
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
+    }
+
+    if (tid == 0) {  // so is Ut^T
+        tc::bulk_s2g(rec + R.Ut, sm + PrepSmem::V, 16384);
+        tc::bulk_commit();
     }
 
     // round 3:  (X_q - P W')^T -> cols 0..63 (warp 0);  Kend^T W' -> cols 128..255 (warp 1)
@@ -596,7 +609,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
     if (s_abort) {
-        if (tid == 0) flag_timeout(ws);
+        if (tid == 0) {
+            flag_timeout(ws);
+            tc::bulk_wait_read();  // record images already on their way still read shared memory
+        }
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
@@ -606,20 +622,13 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::bulk_commit();
     }
 
-    // round 4:  Oloc^T = Ut^T P^T -> cols 0..63 (warp 0);  Bc = Kend^T Ut -> cols 128..255 (warp 1)
-    if (lane == 0 && warp < 2) {
-        if (warp == 0) {
-            constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64, false, false);
-            for (int s = 0; s < 4; ++s)
-                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32)), id64, s > 0);
-        } else {
-            constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
-            constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
-            for (int s = 0; s < 4; ++s)
-                tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), id128, s > 0);
-        }
+    // round 4:  Bc = Kend^T Ut -> cols 128..255
+    if (tid == 32) {
+        constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
+        for (int s = 0; s < 4; ++s)
+            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
+                         tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), id128, s > 0);
         tc::mma_commit(&r4_bar);
     }
     __syncwarp();
@@ -628,29 +637,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
     __syncthreads();
     if (warp_all(ok)) {
-        {
-            // Oloc column j = c into tile j / 32, pair-interleaved [16 pairs][64 tokens][2]: lanes j and
-            // j ^ 1 trade halves so that each writes 32 tokens of its pair as whole 4-byte words
-            float ol[64];
-            tc::tmem_ld64(tmem + lane_base, ol);
-            const int odd = c & 1;
-            uint8_t *OlG = reinterpret_cast<uint8_t *>(rec + R.Oloc) + (size_t)(c >> 5) * 4096 +
-                           (size_t)((c & 31) >> 1) * 256 + (size_t)odd * 128;
-#pragma unroll
-            for (int r4 = 0; r4 < 32; r4 += 4) {
-                uint32_t wd[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int r = r4 + u;
-                    // even lane writes tokens 0..31, odd lane 32..63, each as (even column, odd column)
-                    const float give = odd ? ol[r] : ol[32 + r];
-                    const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-                    const float mine = odd ? ol[32 + r] : ol[r];
-                    wd[u] = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
-                }
-                *reinterpret_cast<uint4 *>(OlG + r4 * 4) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            }
-        }
 #pragma unroll
         for (int t = 0; t < kNTile; ++t) {
             // Bc row c, columns of tile t: four 16-byte chunks, chunk k stored at k ^ ((c >> 1) & 3)
@@ -679,25 +665,23 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // ---------------------------------------------------------------------------
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
-constexpr int kNBuf = 3;  // record buffers: chunk c + 2 streams in while chunk c computes
+constexpr int kNBuf = 4;  // record buffers: chunks c + 1 .. c + 3 stream in while chunk c computes
+constexpr int kNSb = 3;   // bf16 state images: multiplied (and copied out), being written, spare
 struct StateSmem {
-    static constexpr uint32_t Buf = 0;
-    static constexpr uint32_t kBuf = 62464;  // shared record part (49 KB) + this CTA's tile (12 KB)
-    static constexpr uint32_t Mc = 0, Qp = 32768, gam = 49152, Bc = 50176, Ol = 50176 + 8192;
-    static constexpr uint32_t Zero = Buf + kNBuf * kBuf;  // 16 KB of zeros: rows 64-127 of the output operand
-    // S^T operand, K-major [32 rows][128 K], 2 panels of 4 KB, ping-pong: chunk c's MMAs read
-    // half (c & 1) while the epilogue writes S_{c+1} into the other half, so the output MMAs of
-    // chunk c (still in flight after the state MMAs complete) never see S_{c+1}.
-    static constexpr uint32_t SB = Zero + 16384;
-    static constexpr uint32_t bytes = SB + 16384;
+    static constexpr uint32_t kBuf = 43008;  // M' and gamma (33 KB) + this CTA's Bc tile (8 KB), 1 KB aligned
+    static constexpr uint32_t Mc = 0, gam = 32768, Bc = 33792;
+    // S^T operand, K-major [32 rows][128 K] in 2 panels of 4 KB, a ring of three: chunk c's MMAs
+    // read image c % 3, which is also copied to chunk c's record for the output pass, while the
+    // epilogue writes image (c + 1) % 3.
+    static constexpr uint32_t SB = kNBuf * kBuf;
+    static constexpr uint32_t bytes = SB + kNSb * 8192;
 };
 
 __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int tile, uint64_t *bar) {
     constexpr TcRecord R = tc_record();
-    tc::mbar_arrive_expect_tx(bar, StateSmem::kBuf);
-    tc::bulk_g2s(buf, rec, (uint32_t)R.shared_bytes, bar);
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)R.state_part + 8192u);
+    tc::bulk_g2s(buf, rec, (uint32_t)R.state_part, bar);
     tc::bulk_g2s(buf + StateSmem::Bc, rec + R.Bc + (size_t)tile * 8192, 8192, bar);
-    tc::bulk_g2s(buf + StateSmem::Ol, rec + R.Oloc + (size_t)tile * 4096, 4096, bar);
 }
 
 // Writes row i of S (32 values) into the K-major S^T operand: element (j, i),
@@ -718,17 +702,17 @@ __device__ __forceinline__ void store_state_operand(uint8_t *SB, int i, const fl
     }
 }
 
-// Roles per chunk (128 threads, thread i <-> state row i <-> TMEM lane i):
-//   warps 0, 1 (lane 0)  issue M' S over the two K panels (state, critical path)
-//   warp 3 (lane 0)      issues [Qp ; 0] S after them (output, rows 0-63 of its accumulator)
-//   warps 0, 1           finish the previous chunk's outputs while the state MMAs run
-//   all                  S <- gamma S + Bc + M' S, and the bf16 copy for the next chunk
+// One CTA per (document, head, 32-column tile of S); roles per chunk c
+// (128 threads, thread i <-> state row i <-> TMEM lane i):
+//   warps 0, 1 (lane 0)  issue M' S over the two K panels of S (the critical path)
+//   warp 3 (lane 0)      copies the image of S_c to chunk c's record, prefetches record c + 3
+//   all                  S <- gamma S + Bc + M' S, and the bf16 image of the new S
 __global__ void __launch_bounds__(128, 1)
 prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
-                 __nv_bfloat16 *__restrict__ o, float *__restrict__ S_final, char *__restrict__ ws,
-                 size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+                 float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
+                 size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[kNBuf], a_bar, b_bar[2];
+    __shared__ uint64_t full_bar[kNBuf], a_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
@@ -741,6 +725,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
     const int col0 = tile * kTile;
     const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + col0;
+    constexpr TcRecord R = tc_record();
 
     float S[kTile];
 #pragma unroll
@@ -749,149 +734,87 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
     if (nchunks > 0) {
-        for (int e = tid; e < 1024; e += 128) reinterpret_cast<uint4 *>(sm + StateSmem::Zero)[e] = make_uint4(0, 0, 0, 0);
         store_state_operand(sm + StateSmem::SB, i, S);
         tc::fence_async_smem();
-        const char *rec_h = ws + records_off + (size_t)h * record_bytes;
-        const size_t rec_stride = (size_t)H * record_bytes;
+        char *rec_h = ws + records_off + (size_t)h * record_bytes;  // record of (slot 0, head h)
+        const size_t rec_stride = (size_t)H * record_bytes;          // one chunk slot further
         if (tid == 0) {
             for (int b = 0; b < kNBuf; ++b) tc::mbar_init(&full_bar[b], 1);
             tc::mbar_init(&a_bar, 2);  // one commit from each of the two state-MMA issuers
-            tc::mbar_init(&b_bar[0], 1);
-            tc::mbar_init(&b_bar[1], 1);
             tc::fence_mbar_init();
             s_abort = 0;
-            for (int c = 0; c < 2 && c < nchunks; ++c)
-                issue_record(sm + StateSmem::Buf + c * StateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride,
-                             tile, &full_bar[c]);
+            for (int c = 0; c < kNBuf - 1 && c < nchunks; ++c)
+                issue_record(sm + c * StateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[c]);
         }
         if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 128);
+            tc::tmem_alloc(&tmem_base, 64);
             tc::tmem_relinquish();
         }
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
-        // TMEM: M' S over the two K panels in cols 0..31 and 32..63; the output accumulator
-        // ping-pongs between cols 64 and 96 (its rows 0-63 hold O).
+        // TMEM: M' S over the two K panels in cols 0..31 and 32..63
         const uint32_t tmem = tmem_base;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
         constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
-        constexpr uint32_t idMnN = tc::idesc_bf16_f32(128, kTile, true, false);
-        const int t_doc = cu[n], t_end = cu[n + 1];
         bool ok = true;
-        uint32_t oloc[kTile / 2];  // this thread's output row of Oloc for the chunk in flight (warps 0-1)
 
-        for (int c = 0; c <= nchunks; ++c) {
+        for (int c = 0; c < nchunks; ++c) {
             const int bsel = c % kNBuf;
             const uint32_t fpar = (uint32_t)((c / kNBuf) & 1);
-            uint8_t *buf = sm + StateSmem::Buf + bsel * StateSmem::kBuf;
-            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c & 1) * 8192u;
-            if (c < nchunks) {
-                if (lane == 0 && warp < 2) {
-                    ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
-                    if (ok) {
-                        tc::tc_fence_after();
-                        const uint32_t panel = (uint32_t)warp;
-                        for (int s = 0; s < 4; ++s)
-                            tc::mma_bf16(tmem + 32u * panel,
-                                         tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u +
-                                                                           (uint32_t)s * 32u)),
-                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u + (uint32_t)s * 32u)),
-                                         idN, s > 0);
-                        tc::mma_commit(&a_bar);
-                    }
-                }
-                __syncwarp();
-                if (warp < 2) {
-                    tc::named_barrier_arrive(2, 96);
-                } else if (warp == 3) {
-                    tc::named_barrier(2, 96);
-                    if (lane == 0) {
-                        ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
-                        tc::tc_fence_after();
-                        // output: [Qp ; 0] S -> O acc[c & 1], queued behind the state MMAs
-                        const uint32_t oacc = tmem + 64u + (uint32_t)(c & 1) * 32u;
-                        const uint64_t kQp = tc::smem_desc_base(
-                            (uint32_t)(StateSmem::Zero - (StateSmem::Buf + bsel * StateSmem::kBuf + StateSmem::Qp)),
-                            1024, tc::SW_128B);
-                        for (int s = 0; s < 8; ++s) {
-                            const uint32_t kb = (uint32_t)(s >> 2) * 4096u + (uint32_t)(s & 3) * 32u;
-                            tc::mma_bf16(oacc, tc::smem_desc(kQp, tc::smem_u32(buf + StateSmem::Qp + s * 2048)),
-                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + kb)), idMnN, s > 0);
-                        }
-                        tc::mma_commit(&b_bar[c & 1]);
-                        // the previous chunk's output MMAs are done too (in order) -> its buffer is free
-                        // for chunk c + 2
-                        if (c + 2 < nchunks) {
-                            if (c > 0) ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
-                            if (ok)
-                                issue_record(sm + StateSmem::Buf + ((c + 2) % kNBuf) * StateSmem::kBuf,
-                                             rec_h + (size_t)(first + c + 2) * rec_stride, tile,
-                                             &full_bar[(c + 2) % kNBuf]);
-                        }
-                    }
-                    __syncwarp();
-                }
-            }
-            if (warp < 2) {
-                const int r = tid;
-                if (c > 0) {
-                    // O of the previous chunk: rows 0-63 of [Qp ; 0] S, plus Oloc
-                    ok = ok && tc::mbar_wait(&b_bar[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+            uint8_t *buf = sm + bsel * StateSmem::kBuf;
+            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c % kNSb) * 8192u;
+            if (lane == 0 && warp < 2) {
+                ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
+                if (ok) {
                     tc::tc_fence_after();
-                    if (warp_all(ok)) {
-                        float t[32];
-                        tc::tmem_ld32(tmem + lane_base + 64u + (uint32_t)((c - 1) & 1) * 32u, t);
-                        const int t0p = t_doc + (c - 1) * kL;
-                        if (t0p + r < t_end) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0p + r) * H + h) * kD + col0);
-#pragma unroll
-                            for (int q8 = 0; q8 < 4; ++q8) {
-                                float w[8];
-#pragma unroll
-                                for (int u = 0; u < 8; u += 2) {
-                                    const __nv_bfloat162 ob =
-                                        *reinterpret_cast<const __nv_bfloat162 *>(&oloc[(q8 * 8 + u) >> 1]);
-                                    const float2 of = __bfloat1622float2(ob);
-                                    w[u] = t[q8 * 8 + u] + of.x;
-                                    w[u + 1] = t[q8 * 8 + u + 1] + of.y;
-                                }
-                                dst[q8] = pack8(w);
-                            }
-                        }
-                    }
+                    const uint32_t panel = (uint32_t)warp;
+                    for (int s = 0; s < 4; ++s)
+                        tc::mma_bf16(tmem + 32u * panel,
+                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u +
+                                                                       (uint32_t)s * 32u)),
+                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u + (uint32_t)s * 32u)),
+                                     idN, s > 0);
+                    tc::mma_commit(&a_bar);
                 }
-                if (c < nchunks) {
-                    // this chunk's Oloc row, kept for next iteration's output
-                    ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
-                    const uint32_t *ol = reinterpret_cast<const uint32_t *>(buf + StateSmem::Ol) + r;
+            } else if (lane == 0 && warp == 3) {
+                // S_c's image, tile rows of both panels, into chunk c's record
+                char *rec = rec_h + (size_t)(first + c) * rec_stride;
+                tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
+                tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
+                tc::bulk_commit();
+                tc::bulk_wait_read_but_last();  // image c - 1 is free again: the epilogue of chunk c + 1 reuses it
+                // the buffer chunk c - 1 used was released by the barrier that ended that chunk
+                const int cn = c + kNBuf - 1;
+                if (cn < nchunks)
+                    issue_record(sm + (cn % kNBuf) * StateSmem::kBuf, rec_h + (size_t)(first + cn) * rec_stride,
+                                 tile, &full_bar[cn % kNBuf]);
+            }
+            __syncwarp();
+            // S <- gamma * S + Kend^T Ut + M' S (the last term in two K halves); gamma and the Bc row
+            // are read while the MMAs run
+            ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
+            const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+            float bc[32];
+            {
+                const uint8_t *brow = buf + StateSmem::Bc + i * 64;
 #pragma unroll
-                    for (int p2 = 0; p2 < kTile / 2; ++p2) oloc[p2] = ol[p2 * 64];
+                for (int k = 0; k < 4; ++k) {
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), f);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) bc[8 * k + u] = f[u];
                 }
             }
-            if (c < nchunks) {
-                // S <- gamma * S + Kend^T Ut + M' S (the last term in two K halves)
-                ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
-                tc::tc_fence_after();
-                if (warp_all(ok)) {
-                    const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-                    float bc[32];
-                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
+            ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
+            tc::tc_fence_after();
+            if (warp_all(ok)) {
+                float t[64];
+                tc::tmem_ld64(tmem + lane_base, t);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float f[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), f);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) bc[8 * k + u] = f[u];
-                    }
-                    float t[64];
-                    tc::tmem_ld64(tmem + lane_base, t);
-#pragma unroll
-                    for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t[j] + t[32 + j]));
-                    store_state_operand(sm + StateSmem::SB + (uint32_t)((c + 1) & 1) * 8192u, i, S);
-                }
+                for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t[j] + t[32 + j]));
+                store_state_operand(sm + StateSmem::SB + (uint32_t)((c + 1) % kNSb) * 8192u, i, S);
             }
             tc::fence_async_smem();
             tc::tc_fence_before();
@@ -900,15 +823,16 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             tc::tc_fence_after();
             if (s_abort) break;
         }
+        if (warp == 3 && lane == 0) tc::bulk_wait_read();  // shared memory must outlive the image copies
         if (s_abort) {
-            // let any copy still in flight land before the CTA's shared memory goes away
+            // let any record copy still in flight land before the CTA's shared memory goes away
             if (tid == 0) {
                 flag_timeout(ws);
                 for (int b = 0; b < kNBuf; ++b) tc::mbar_wait(&full_bar[b], 0, 10000000ull);
             }
             __syncthreads();
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem, 64);
         if (s_abort) return;
     }
     if (S_final) {
@@ -916,6 +840,101 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         for (int j = 0; j < kTile; j += 4)
             *reinterpret_cast<float4 *>(S_final + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel 3: chunk-parallel output
+// ---------------------------------------------------------------------------
+// One CTA (128 threads) per (chunk, head):  O = Qp S_c + P Ut, with S_c the
+// state entering the chunk (its bf16 image, written by the state pass).  Both
+// products accumulate into one 128-lane TMEM tile whose lanes 0-63 are the
+// chunk's tokens: A = [Qp ; *] (MN-major) and [P ; *] (K-major) are read as
+// 128-row operands whose upper 64 rows fall on other record images and give
+// accumulator rows nobody reads.
+struct OutSmem {
+    static constexpr uint32_t Qp = 0, P = 16384, Ut = 24576, S = 40960;  // the record's [Qp, end) as stored
+    static constexpr uint32_t bytes = 73728;
+};
+
+__global__ void __launch_bounds__(128)
+prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o,
+                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t load_bar, mma_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_ok;
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid input or an earlier timeout
+    uint8_t *sm = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    int doc, t0, Lc;
+    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
+    constexpr TcRecord R = tc_record();
+    static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
+                      R.S - R.Qp == OutSmem::S,
+                  "output pass loads the record tail as one image");
+    const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
+    if (tid == 0) {
+        tc::mbar_init(&load_bar, 1);
+        tc::mbar_init(&mma_bar, 1);
+        tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(&load_bar, OutSmem::bytes);
+        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::bytes, &load_bar);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    if (tid == 0) {
+        const bool ok = tc::mbar_wait(&load_bar, 0);
+        s_ok = ok;
+        if (ok) {
+            tc::tc_fence_after();
+            constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+            constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
+            constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, false);
+            constexpr uint32_t id_k = tc::idesc_bf16_f32(128, 128, false, false);
+            for (int s = 0; s < 8; ++s)  // Qp S_c over d_k
+                tc::mma_bf16(tmem, tc::smem_desc(kQpMn, tc::smem_u32(sm + OutSmem::Qp + s * 2048)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::S + (s >> 2) * 16384 + (s & 3) * 32)),
+                             id_mn, s > 0);
+            for (int s = 0; s < 4; ++s)  // + P Ut over the chunk's tokens
+                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::P + s * 32)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::Ut + s * 32)), id_k, true);
+        }
+        tc::mma_commit(&mma_bar);  // arrives at once when nothing was issued
+    }
+    __syncwarp();
+    if (warp < 2) {
+        // token row r = tid: 128 fp32 accumulators -> 256 bytes of o
+        const bool done = tc::mbar_wait(&mma_bar, 0);
+        tc::tc_fence_after();
+        if (warp_all(done)) {
+            const int r = tid;
+            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+            uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * kD);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float v[32];
+                tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                if (r < Lc) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[q * 4 + u] = pack8_at(v + 8 * u);
+                }
+            }
+        } else if ((tid & 31) == 0) {
+            flag_timeout(ws);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && !s_ok) flag_timeout(ws);
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -987,9 +1006,19 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if ((e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
     marks.before(st, "prefill_state_tc");
     prefill_state_tc<<<(unsigned)((size_t)num_seqs * H * kNTile), 128, smem, st>>>(
-        cu, num_seqs, H, S0, static_cast<__nv_bfloat16 *>(o), S_final, w, lay.doc_slot0_off, lay.records_off,
-        lay.record_bytes);
-    return cudaGetLastError();
+        cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
+    if ((e = cudaGetLastError())) return e;
+    if (lay.max_slots > 0 && total_tokens > 0) {
+        const int smem_o = OutSmem::bytes + 1024;
+        if ((e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_o)))
+            return e;
+        marks.before(st, "prefill_output_tc");
+        prefill_output_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem_o, st>>>(
+            cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,
+            lay.record_bytes);
+        if ((e = cudaGetLastError())) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kda
