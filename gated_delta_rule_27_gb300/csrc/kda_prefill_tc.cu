@@ -12,10 +12,10 @@
 // and per document, chunk after chunk, with S_c the state entering chunk c:
 //     S_{c+1} = gamma S_c + M' S_c + Bc,      O_c = Qp S_c + P Ut.
 //
-// Kernel 1, prefill_prepare_tc: one CTA (128 threads, thread c <-> channel c
-// <-> TMEM lane c) per (chunk, head).  q, k, v, g tiles arrive by TMA.  The
-// dense contractions run as four rounds of tcgen05.mma with fp32 accumulators
-// in TMEM (A and P; W' and Ut; Qp and M'; Bc); the gates, their cumulative
+// Kernel 1, prefill_prepare_tc: one CTA (256 threads, two per SM) per (chunk,
+// head).  q, k, v, g tiles arrive by TMA.  The dense contractions run as four
+// rounds of tcgen05.mma with fp32 accumulators in TMEM (A and P; W' and Ut; Qp
+// and M'; Bc); the gates, their cumulative
 // sums and the triangular solve stay fp32 on the CUDA cores, and nothing
 // d_k x d_k is formed from a single token.  b_m is the chunk's middle token,
 // so every factor is bounded by exp(+-80) while the chunk's log-decay range on
@@ -73,10 +73,17 @@ __device__ __forceinline__ void flag_timeout(char *ws) {
 // 16 x 16 blocks (i, j), j <= i, each contiguous.
 __device__ __forceinline__ int tri_blk(int i, int j) { return ((i * (i + 1)) / 2 + j) << 8; }
 __device__ __forceinline__ int tri_idx(int r, int s) { return tri_blk(r >> 4, s >> 4) + ((r & 15) << 4) + (s & 15); }
-// Cumulative log-decay b[r][c] lives in a [64][128] fp32 array whose float4
-// groups are XOR-swizzled by (r mod 8), so that row-wise float4 reads by
-// eight consecutive rows hit eight different bank groups.
-__device__ __forceinline__ int bswz(int r, int c) { return r * kD + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
+// Cumulative log-decay b[r][c] lives in a [64][128] fp32 array.  Within row r,
+// channel c sits in half h = (c / 4) mod 2 at position (c / 8) * 4 + c mod 4,
+// rotated by 16 h inside the half: a warp writing 32 consecutive channels of
+// one row, and eight threads reading one float4 each of eight consecutive
+// channel octets, both touch 32 distinct banks.
+__device__ __forceinline__ int bswz(int r, int c) {
+    const int hf = (c >> 2) & 1;
+    return r * kD + hf * 64 + ((((c >> 3) << 2) + (c & 3) + 16 * hf) & 63);
+}
+
+constexpr int kPrepThreads = 256;
 
 struct PrepSmem {
     // X: two 16 KB panels (channels 0-63, 64-127); in each, rows 0-63 hold the k
@@ -89,7 +96,8 @@ struct PrepSmem {
     static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB) and the identity (8 KB)
     static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
     static constexpr uint32_t Tfp = G + 10240;     // compact fp32 T (10 KB)
-    static constexpr uint32_t Tb = G + 20480;      // bf16 T, K-major [r][s] (8 KB)
+    static constexpr uint32_t Scr = G + 20480;     // the solve's scratch (6 KB) ...
+    static constexpr uint32_t Tb = G + 20480;      // ... then bf16 T, K-major [r][s] (8 KB)
     static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB)
     static constexpr uint32_t WT = G + 16384;      // W'^T, K-major [c][s] (16 KB)
     static constexpr uint32_t P = Y;               // P, K-major [r][s] (8 KB)
@@ -97,96 +105,122 @@ struct PrepSmem {
     static constexpr uint32_t bytes = 98304;
 };
 
-// T = (I + A)^{-1} for A strictly lower triangular (compact block-major):
-// invert the four 16 x 16 diagonal blocks by forward substitution, then fill
-// the sub-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-template <int LVL>
-__device__ __forceinline__ void inverse_level(float *A, float *T, int tid) {
-    constexpr int NB = 4 - LVL;          // blocks on this sub-diagonal
-    constexpr int ITEMS = NB * 64;       // 4-wide row pieces: (block, row, 4 columns)
-    // M_b = sum_k A_{i,k} T_{k,j} -> diagonal block b of A (no longer needed there)
-#pragma unroll
-    for (int q = 0; q < (ITEMS + 127) / 128; ++q) {
-        const int e = tid + q * 128;
-        if (e < ITEMS) {
-            const int b = e >> 6, r = (e >> 2) & 15, s0 = (e & 3) * 4, i = b + LVL;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < LVL; ++kk) {
-                const float *Aik = A + tri_blk(i, b + kk) + (r << 4);
-                const float *Tkj = T + tri_blk(b + kk, b) + s0;
-#pragma unroll
-                for (int t4 = 0; t4 < 16; t4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(Aik + t4);
-                    const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 tv = *reinterpret_cast<const float4 *>(Tkj + ((t4 + u) << 4));
-                        acc.x = fmaf(av[u], tv.x, acc.x); acc.y = fmaf(av[u], tv.y, acc.y);
-                        acc.z = fmaf(av[u], tv.z, acc.z); acc.w = fmaf(av[u], tv.w, acc.w);
-                    }
-                }
-            }
-            *reinterpret_cast<float4 *>(A + tri_blk(b, b) + (r << 4) + s0) = acc;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < (ITEMS + 127) / 128; ++q) {
-        const int e = tid + q * 128;
-        if (e < ITEMS) {
-            const int b = e >> 6, r = (e >> 2) & 15, s0 = (e & 3) * 4, i = b + LVL;
-            const float *Tii = T + tri_blk(i, i) + (r << 4);
-            const float *M = A + tri_blk(b, b) + s0;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int t4 = 0; t4 < 16; t4 += 4) {
-                const float4 a = *reinterpret_cast<const float4 *>(Tii + t4);
-                const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 mv = *reinterpret_cast<const float4 *>(M + ((t4 + u) << 4));
-                    acc.x = fmaf(av[u], mv.x, acc.x); acc.y = fmaf(av[u], mv.y, acc.y);
-                    acc.z = fmaf(av[u], mv.z, acc.z); acc.w = fmaf(av[u], mv.w, acc.w);
-                }
-            }
-            *reinterpret_cast<float4 *>(T + tri_blk(i, b) + (r << 4) + s0) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-    }
-    __syncthreads();
-}
-
-__device__ void unit_lower_inverse(float *A, float *T, int tid) {
-    if (tid < 64) {
+// T = (I + A)^{-1} for A strictly lower triangular (compact block-major, four
+// 16-row blocks), 256 threads.  The diagonal blocks are inverted by forward
+// substitution; then, with L = I + A split into 32-row halves
+// [[L_lo, 0], [A_hl, L_hi]], each half's lower block is -T_ii A_ij T_jj and
+// the lower-left quarter is -T_hi (A_hl T_lo): four phases of 256 equal items.
+__device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid) {
+    if (tid < 64) {  // diagonal block blk, column j: (I + A_bb) x = e_j
         const int blk = tid >> 4, j = tid & 15;
         const float *Ab = A + tri_blk(blk, blk);
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(Ab[(r << 4) + s], x[s], acc);
-            x[r] = r < j ? 0.f : (r == j ? 1.f : -acc);
+            for (int s = 0; s + 1 < r; s += 2) {
+                a0 = fmaf(Ab[(r << 4) + s], x[s], a0);
+                a1 = fmaf(Ab[(r << 4) + s + 1], x[s + 1], a1);
+            }
+            if (r & 1) a0 = fmaf(Ab[(r << 4) + r - 1], x[r - 1], a0);
+            x[r] = r < j ? 0.f : (r == j ? 1.f : -(a0 + a1));
         }
         float *Td = T + tri_blk(blk, blk);
 #pragma unroll
         for (int r = 0; r < 16; ++r) Td[(r << 4) + j] = x[r];
     }
     __syncthreads();
-    inverse_level<1>(A, T, tid);
-    inverse_level<2>(A, T, tid);
-    inverse_level<3>(A, T, tid);
+    {  // F = T_ii A_{i,i-1} for i = 1, 3 (scratch blocks 0, 1): item (b, row, column pair)
+        const int b = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2, i = 1 + 2 * b;
+        const float *Ti = T + tri_blk(i, i) + (r << 4);
+        const float *Ai = A + tri_blk(i, i - 1) + c2;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(Ti + k4);
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 a = *reinterpret_cast<const float2 *>(Ai + ((k4 + u) << 4));
+                acc.x = fmaf(tv[u], a.x, acc.x);
+                acc.y = fmaf(tv[u], a.y, acc.y);
+            }
+        }
+        *reinterpret_cast<float2 *>(scr + (b << 8) + (r << 4) + c2) = acc;
+    }
+    __syncthreads();
+    {  // T_{i,i-1} = -F T_{i-1,i-1}
+        const int b = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2, i = 1 + 2 * b;
+        const float *F = scr + (b << 8) + (r << 4);
+        const float *Tj = T + tri_blk(i - 1, i - 1) + c2;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(F + k4);
+            const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 t = *reinterpret_cast<const float2 *>(Tj + ((k4 + u) << 4));
+                acc.x = fmaf(fv[u], t.x, acc.x);
+                acc.y = fmaf(fv[u], t.y, acc.y);
+            }
+        }
+        *reinterpret_cast<float2 *>(T + tri_blk(i, i - 1) + (r << 4) + c2) = make_float2(-acc.x, -acc.y);
+    }
+    __syncthreads();
+    {  // X_ij = sum_{k=j}^{1} A_ik T_kj for (i, j) in {2, 3} x {0, 1} (scratch blocks 2..5)
+        const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = j; k < 2; ++k) {
+            const float *Ai = A + tri_blk(i, k) + (r << 4);
+            const float *Tk = T + tri_blk(k, j) + c4;
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Ai + k4);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 t = *reinterpret_cast<const float4 *>(Tk + ((k4 + u) << 4));
+                    acc.x = fmaf(av[u], t.x, acc.x); acc.y = fmaf(av[u], t.y, acc.y);
+                    acc.z = fmaf(av[u], t.z, acc.z); acc.w = fmaf(av[u], t.w, acc.w);
+                }
+            }
+        }
+        *reinterpret_cast<float4 *>(scr + 512 + (xb << 8) + (r << 4) + c4) = acc;
+    }
+    __syncthreads();
+    {  // T_ij = -sum_{k=2}^{i} T_ik X_kj
+        const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 2; k <= i; ++k) {
+            const float *Ti = T + tri_blk(i, k) + (r << 4);
+            const float *Xk = scr + 512 + ((((k - 2) << 1) + j) << 8) + c4;
+#pragma unroll
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(Ti + k4);
+                const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = *reinterpret_cast<const float4 *>(Xk + ((k4 + u) << 4));
+                    acc.x = fmaf(tv[u], x.x, acc.x); acc.y = fmaf(tv[u], x.y, acc.y);
+                    acc.z = fmaf(tv[u], x.z, acc.z); acc.w = fmaf(tv[u], x.w, acc.w);
+                }
+            }
+        }
+        *reinterpret_cast<float4 *>(T + tri_blk(i, j) + (r << 4) + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
 }
 
 // Exact A and P on the CUDA cores for a chunk whose log-decay range is too
 // wide for the factorised tensor-core form: pairwise exp(b_r - b_s) <= 1
-// (s <= r).  Thread t owns row r = t / 2 and the 32 columns s of half t % 2.
-__device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, int Lc, int tid, float (&accA)[32],
-                         float (&accP)[32]) {
-    const int r = tid >> 1, s0 = (tid & 1) * 32;
+// (s <= r).  Thread t owns row r = t / 4 and the 16 columns s of quarter t % 4.
+__device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, int Lc, int tid, float (&accA)[16],
+                         float (&accP)[16]) {
+    const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) { accA[j] = 0.f; accP[j] = 0.f; }
+    for (int j = 0; j < 16; ++j) { accA[j] = 0.f; accP[j] = 0.f; }
     if (r >= Lc) return;
     for (int c = 0; c < kD; ++c) {
         const uint8_t *panel = X + (uint32_t)(c >> 6) * 16384u;
@@ -194,7 +228,7 @@ __device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, 
         const float krc = bf16_at(panel + tc::sw128_offset(r, c & 63));
         const float qrc = bf16_at(panel + tc::sw128_offset(64 + r, c & 63));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const int s = s0 + j;
             if (s <= r) {
                 const float ks = bf16_at(panel + tc::sw128_offset(s, c & 63)) * expf(brc - B[bswz(s, c)]);
@@ -204,7 +238,7 @@ __device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, 
         }
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) accA[j] *= s_beta[r];
+    for (int j = 0; j < 16; ++j) accA[j] *= s_beta[r];
 }
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -225,22 +259,29 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
                       pack_bf16x2(f[6], f[7]));
 }
 
-__global__ void __launch_bounds__(128, 2)
+// Roles (256 threads).  Channel-wise steps: thread t <-> channel t % 128 and
+// half t / 128 of the chunk's rows.  Row-wise steps: thread t <-> token row
+// t / 4 and channel quarter t % 4.  TMEM epilogues: warp w reads lanes
+// 32 (w % 4) .. + 31 (channel or token rows), warps w and w + 4 splitting the
+// accumulator's columns.  MMAs are issued by lane 0 of warps 0 and 1.
+__global__ void __launch_bounds__(kPrepThreads, 2)
 prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
-                   char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+                   char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
+                   int resident) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t load_bar, r1_bar, r2_bar, r3_bar, r4_bar;  // one barrier per MMA round
+    __shared__ uint64_t g_bar, load_bar, r1_bar, r2_bar, r3_bar, r4_bar;  // gates; k, q, v; MMA rounds
     __shared__ uint32_t tmem_base;
     __shared__ float s_beta[kL];
     __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
     __shared__ __align__(16) float s_F[kD];
     __shared__ __align__(16) float s_Em[kD];
     __shared__ __align__(16) float s_blast[kD];
-    __shared__ int s_unsafe, s_abort;
+    __shared__ float s_half[kD], s_mid[kD], s_lo[2][kD], s_hi[2][kD];
+    __shared__ int s_abort;
     uint8_t *sm = align1024(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, c = tid;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slot = blockIdx.x, h = blockIdx.y;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     int doc, t0, Lc;
@@ -249,22 +290,24 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
 
     if (tid == 0) {
+        tc::mbar_init(&g_bar, 1);
         tc::mbar_init(&load_bar, 1);
-        tc::mbar_init(&r1_bar, 2);  // rounds are issued by several warps, one commit each
+        tc::mbar_init(&r1_bar, 2);  // rounds 1-3 are issued by two warps, one commit each
         tc::mbar_init(&r2_bar, 2);
         tc::mbar_init(&r3_bar, 2);
         tc::mbar_init(&r4_bar, 1);
         tc::fence_mbar_init();
-        s_unsafe = 0;
         s_abort = 0;
-        tc::mbar_arrive_expect_tx(&load_bar, 6 * 8192 + 32768);
+        // the gates first: the cumulative sums run while k, q, v are still arriving
+        tc::mbar_arrive_expect_tx(&g_bar, 32768);
+        tc::tma_load_3d(sm + PrepSmem::G, &tm_g, 0, h, t0, &g_bar);
+        tc::mbar_arrive_expect_tx(&load_bar, 6 * 8192);
         tc::tma_load_3d(sm + PrepSmem::X, &tm_k, 0, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::X + 8192, &tm_q, 0, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::X + 16384, &tm_k, 64, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::X + 24576, &tm_q, 64, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::V, &tm_v, 0, h, t0, &load_bar);
         tc::tma_load_3d(sm + PrepSmem::V + 8192, &tm_v, 64, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::G, &tm_g, 0, h, t0, &load_bar);
     }
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 256);
@@ -275,8 +318,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    if (!tc::mbar_wait(&load_bar, 0)) s_abort = 1;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int trow = (warp & 3) * 32 + lane;  // this thread's TMEM lane
+    const int hs = warp >> 2;                 // this warp's half of an accumulator's columns
+    if (!tc::mbar_wait(&g_bar, 0)) s_abort = 1;
     __syncthreads();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
         if (tid == 0) flag_timeout(ws);
@@ -284,55 +329,106 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         return;
     }
 
-    // cumulative log-decay of channel c (registers), reference token m in the middle
+    // cumulative log-decay of channel c over this thread's 32 rows; reference token m in the middle
     float *Gf = reinterpret_cast<float *>(sm + PrepSmem::G);
+    bool unsafe;
     {
-        float bcol[kL];
-        const int m = (Lc - 1) >> 1;
-        float acc = 0.f, bm = 0.f, bmax = -INFINITY, bmin = INFINITY;
+        const int c = tid & (kD - 1), hh = tid >> 7, r0 = hh * 32;
+        const int m = (Lc - 1) >> 1, last = Lc - 1;
+        float bcol[32];
+        float acc = 0.f;
 #pragma unroll
-        for (int r = 0; r < kL; ++r) {
-            acc += r < Lc ? Gf[r * kD + c] : 0.f;
-            bcol[r] = acc;
-            if (r == m) bm = acc;
-            if (r < Lc) { bmax = fmaxf(bmax, acc); bmin = fminf(bmin, acc); }
+        for (int u = 0; u < 32; ++u) {
+            acc += r0 + u < Lc ? Gf[(r0 + u) * kD + c] : 0.f;
+            bcol[u] = acc;
         }
-        const float blast = acc;
-        reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
-        if (bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY)) s_unsafe = 1;
-        __syncthreads();  // all of g has been read (b may now go to its swizzled places); s_unsafe is final
+        if (hh == 0) s_half[c] = acc;
+        __syncthreads();  // all of g has been read (b may now go to its swizzled places); s_half is final
+        const float off = hh ? s_half[c] : 0.f;
+        float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int r = r0 + u;
+            const float b = bcol[u] + off;
+            if (r < Lc) { lo = fminf(lo, b); hi = fmaxf(hi, b); }
+            if (r == m) s_mid[c] = b;
+            if (r == last) s_blast[c] = b;
+            Gf[bswz(r, c)] = b;
+        }
+        s_lo[hh][c] = lo;
+        s_hi[hh][c] = hi;
+        __syncthreads();
+        bool bad = false;
+        if (tid < kD) {
+            const float bm = s_mid[c];
+            const float bmin = fminf(s_lo[0][c], s_lo[1][c]), bmax = fmaxf(s_hi[0][c], s_hi[1][c]);
+            bad = bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY);
+        }
         // Reference point of the factorised exponentials: the middle token; a chunk whose range is too
         // wide for that takes exact A and P and the chunk start as reference (exp(b_r) <= 1 for
         // non-positive gates), so no operand can overflow.
-        const float bref = s_unsafe ? 0.f : bm;
-        s_bm[c] = bref;
-        s_F[c] = expf(blast - bref);
-        s_Em[c] = expf(bref);
-        s_blast[c] = blast;
-#pragma unroll
-        for (int r = 0; r < kL; ++r) Gf[bswz(r, c)] = bcol[r];
+        unsafe = __syncthreads_or(bad) != 0;
+        if (tid < kD) {
+            const float blast = s_blast[c];
+            const float bref = unsafe ? 0.f : s_mid[c];
+            s_bm[c] = bref;
+            s_F[c] = expf(blast - bref);
+            s_Em[c] = expf(bref);
+            reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
+        }
+        if (!tc::mbar_wait(&load_bar, 0)) s_abort = 1;
+        if (tid == 0) {
+            // CTAs start in launch order as slots free up, so the one `resident` places further on takes this
+            // CTA's place next: pull its tiles into L2 while this chunk computes
+            const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
+            int ndoc, nt0, nLc;
+            if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) &&
+                locate_slot(doc_slot0, cu, num_seqs, kL, nxt % gridDim.x, &ndoc, &nt0, &nLc)) {
+                const int nh = nxt / gridDim.x;
+                tc::tma_prefetch_3d(&tm_g, 0, nh, nt0);
+                tc::tma_prefetch_3d(&tm_k, 0, nh, nt0);
+                tc::tma_prefetch_3d(&tm_k, 64, nh, nt0);
+                tc::tma_prefetch_3d(&tm_q, 0, nh, nt0);
+                tc::tma_prefetch_3d(&tm_q, 64, nh, nt0);
+                tc::tma_prefetch_3d(&tm_v, 0, nh, nt0);
+                tc::tma_prefetch_3d(&tm_v, 64, nh, nt0);
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    const bool unsafe = s_unsafe != 0;
-    float accA[32], accP[32];
+    if (s_abort) {
+        if (tid == 0) flag_timeout(ws);
+        if (warp == 0) tc::tmem_dealloc(tmem, 256);
+        return;
+    }
+    float accA[16], accP[16];
     if (unsafe) {
         exact_ap(sm + PrepSmem::X, Gf, s_beta, Lc, tid, accA, accP);
         __syncthreads();  // the raw k, q tiles are about to be scaled in place
     }
 
-    // Row-wise operand build: thread t owns token row r = t / 2 and channels 64 (t % 2) .. +63.
-    uint4 kend[8];
+    // Operand build: thread t owns channel octet o = t % 16 (channels 8 o .. 8 o + 7) of token rows
+    // t / 16 + 16 i, i = 0..3; the octet's per-channel factors are read once.
+    uint4 kend[4];
+    const int oct = tid & 15, opanel = oct >> 3, ocol = (oct & 7) * 8, orow = tid >> 4;
     {
-        const int r = tid >> 1, half = tid & 1;
-        const bool valid = r < Lc;
-        const float br = s_beta[r];
-        uint8_t *Xp = sm + PrepSmem::X + (uint32_t)half * 16384u;
-        uint8_t *Vp = sm + PrepSmem::V + (uint32_t)half * 8192u;
-        uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)half * 8192u;
-#pragma unroll 2
-        for (int g8 = 0; g8 < 8; ++g8) {
-            const int cc = g8 * 8, c0 = half * 64 + cc;
-            const uint32_t off_k = tc::sw128_offset(r, cc), off_q = tc::sw128_offset(64 + r, cc);
+        const int c0 = oct * 8;
+        float bmv[8], fv[8], blv[8];
+        *reinterpret_cast<float4 *>(bmv) = *reinterpret_cast<const float4 *>(s_bm + c0);
+        *reinterpret_cast<float4 *>(bmv + 4) = *reinterpret_cast<const float4 *>(s_bm + c0 + 4);
+        *reinterpret_cast<float4 *>(fv) = *reinterpret_cast<const float4 *>(s_F + c0);
+        *reinterpret_cast<float4 *>(fv + 4) = *reinterpret_cast<const float4 *>(s_F + c0 + 4);
+        *reinterpret_cast<float4 *>(blv) = *reinterpret_cast<const float4 *>(s_blast + c0);
+        *reinterpret_cast<float4 *>(blv + 4) = *reinterpret_cast<const float4 *>(s_blast + c0 + 4);
+        uint8_t *Xp = sm + PrepSmem::X + (uint32_t)opanel * 16384u;
+        uint8_t *Vp = sm + PrepSmem::V + (uint32_t)opanel * 8192u;
+        uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)opanel * 8192u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = orow + 16 * i;
+            const bool valid = r < Lc;
+            const float br = s_beta[r];
+            const uint32_t off_k = tc::sw128_offset(r, ocol), off_q = tc::sw128_offset(64 + r, ocol);
             float k8[8], q8[8], v8[8], xk[8], xq[8], y8[8], bv[8], ke[8];
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
@@ -340,11 +436,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const float4 b0 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0));
             const float4 b1 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0 + 4));
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            float bmv[8], fv[8];
-            *reinterpret_cast<float4 *>(bmv) = *reinterpret_cast<const float4 *>(s_bm + c0);
-            *reinterpret_cast<float4 *>(bmv + 4) = *reinterpret_cast<const float4 *>(s_bm + c0 + 4);
-            *reinterpret_cast<float4 *>(fv) = *reinterpret_cast<const float4 *>(s_F + c0);
-            *reinterpret_cast<float4 *>(fv + 4) = *reinterpret_cast<const float4 *>(s_F + c0 + 4);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float d = bb[u] - bmv[u];
@@ -355,13 +446,13 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 y8[u] = k8[u] * inv;
                 bv[u] = br * v8[u];
                 // Kend = k exp(b_last - b_r) <= |k|: via the bounded factors, or directly when unsafe
-                ke[u] = unsafe ? (valid ? k8[u] * __expf(s_blast[c0 + u] - bb[u]) : 0.f) : y8[u] * fv[u];
+                ke[u] = unsafe ? (valid ? k8[u] * __expf(blv[u] - bb[u]) : 0.f) : y8[u] * fv[u];
             }
             *reinterpret_cast<uint4 *>(Xp + off_k) = pack8(xk);
             *reinterpret_cast<uint4 *>(Xp + off_q) = pack8(xq);
             if (!unsafe) *reinterpret_cast<uint4 *>(Yp + off_k) = pack8(y8);
             *reinterpret_cast<uint4 *>(Vp + off_k) = pack8(bv);
-            kend[g8] = pack8(ke);
+            kend[i] = pack8(ke);
         }
     }
     tc::fence_async_smem();
@@ -370,14 +461,13 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_after();
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-    const int lane = tid & 31;
     bool ok = true;
     float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
     uint8_t *Pb = sm + PrepSmem::P;
     if (unsafe) {
-        const int r = tid >> 1, s0 = (tid & 1) * 32;
+        const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
-        for (int j8 = 0; j8 < 32; j8 += 8) {
+        for (int j8 = 0; j8 < 16; j8 += 8) {
             float w[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -403,53 +493,48 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         __syncwarp();
         ok = tc::mbar_wait(&r1_bar, 0);
         tc::tc_fence_after();
-        if (warp_all(ok)) {
-            float v[64], v2[32];
-            tc::tmem_ld32(tmem + lane_base, *reinterpret_cast<float(*)[32]>(v));
-            tc::tmem_ld32(tmem + lane_base + 128u, v2);
+        if (warp_all(ok)) {  // the MMAs are complete: their operand Y may be overwritten by P
+            float v[32], v2[32];
+            tc::tmem_ld32(tmem + lane_base + 32u * (uint32_t)hs, v);
+            tc::tmem_ld32(tmem + lane_base + 128u + 32u * (uint32_t)hs, v2);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] += v2[i];
-            tc::tmem_ld32(tmem + lane_base + 32u, *reinterpret_cast<float(*)[32]>(v + 32));
-            tc::tmem_ld32(tmem + lane_base + 160u, v2);
+            if (trow < 64) {
+                const int r = trow;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[32 + i] += v2[i];
-            __syncthreads();  // every lane has read round 1 before P overwrites the B operand
-            if (tid < 64) {
-                const int r = tid;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int qb = 0; qb < 2; ++qb) {
+                    const int q4 = 2 * hs + qb;
                     if (q4 <= (r >> 4)) {
                         float *dst = Af + tri_blk(r >> 4, q4) + ((r & 15) << 4);
 #pragma unroll
                         for (int i = 0; i < 16; i += 4) {
                             float4 w;
-                            w.x = q4 * 16 + i + 0 < r ? v[q4 * 16 + i + 0] : 0.f;
-                            w.y = q4 * 16 + i + 1 < r ? v[q4 * 16 + i + 1] : 0.f;
-                            w.z = q4 * 16 + i + 2 < r ? v[q4 * 16 + i + 2] : 0.f;
-                            w.w = q4 * 16 + i + 3 < r ? v[q4 * 16 + i + 3] : 0.f;
+                            w.x = q4 * 16 + i + 0 < r ? v[qb * 16 + i + 0] : 0.f;
+                            w.y = q4 * 16 + i + 1 < r ? v[qb * 16 + i + 1] : 0.f;
+                            w.z = q4 * 16 + i + 2 < r ? v[qb * 16 + i + 2] : 0.f;
+                            w.w = q4 * 16 + i + 3 < r ? v[qb * 16 + i + 3] : 0.f;
                             *reinterpret_cast<float4 *>(dst + i) = w;
                         }
                     }
                 }
             } else {
-                const int r = tid - 64;
+                const int r = trow - 64;
 #pragma unroll
-                for (int s8 = 0; s8 < 64; s8 += 8) {
+                for (int s8 = 0; s8 < 32; s8 += 8) {
+                    const int s = 32 * hs + s8;
                     float w[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) w[u] = s8 + u <= r ? v[s8 + u] : 0.f;
-                    *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s8)) = pack8(w);
+                    for (int u = 0; u < 8; ++u) w[u] = s + u <= r ? v[s8 + u] : 0.f;
+                    *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s)) = pack8(w);
                 }
             }
-        } else {
-            __syncthreads();
         }
     }
     // identity (K-major [r][r']) for round 3, in the dead second half of the round-1 B operand
     {
-        const int r = tid >> 1, s0 = (tid & 1) * 32;
+        const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
-        for (int s8 = 0; s8 < 32; s8 += 8) {
+        for (int s8 = 0; s8 < 16; s8 += 8) {
             float w[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) w[u] = (s0 + s8 + u) == r ? 1.f : 0.f;
@@ -460,22 +545,19 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (!ok) s_abort = 1;
     __syncthreads();
     if (s_abort) {
-        if (tid == 0) {
-            flag_timeout(ws);
-            tc::bulk_wait_read();  // record images already on their way still read shared memory
-        }
+        if (tid == 0) flag_timeout(ws);
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
 
     // triangular solve in fp32, then T as the bf16 round-2 B operand (K-major [r][s])
     float *Tf = reinterpret_cast<float *>(sm + PrepSmem::Tfp);
-    unit_lower_inverse(Af, Tf, tid);
+    unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), tid);
     {
-        const int r = tid >> 1, s0 = (tid & 1) * 32;
+        const int r = tid >> 2, s0 = (tid & 3) * 16;
         uint8_t *Tb = sm + PrepSmem::Tb;
 #pragma unroll
-        for (int s8 = 0; s8 < 32; s8 += 8) {
+        for (int s8 = 0; s8 < 16; s8 += 8) {
             float w[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -509,24 +591,18 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     ok = tc::mbar_wait(&r2_bar, 0);
     tc::tc_fence_after();
     if (warp_all(ok)) {
-        float w[64], u[64];
-        tc::tmem_ld32(tmem + lane_base + 64u, *reinterpret_cast<float(*)[32]>(w));
-        tc::tmem_ld32(tmem + lane_base + 96u, *reinterpret_cast<float(*)[32]>(w + 32));
-        tc::tmem_ld32(tmem + lane_base + 128u, *reinterpret_cast<float(*)[32]>(u));
-        tc::tmem_ld32(tmem + lane_base + 160u, *reinterpret_cast<float(*)[32]>(u + 32));
-        __syncthreads();  // round 2 has consumed beta V before Ut^T replaces it
+        // warps 0-3: W'^T row c -> WT;  warps 4-7: Ut^T row c -> V (round 2 has consumed beta V)
+        float w[64];
+        tc::tmem_ld64(tmem + lane_base + 64u + 64u * (uint32_t)hs, w);
+        uint8_t *dst = sm + (hs ? PrepSmem::V : PrepSmem::WT);
 #pragma unroll
-        for (int s8 = 0; s8 < 64; s8 += 8) {
-            *reinterpret_cast<uint4 *>(sm + PrepSmem::WT + tc::sw128_offset(c, s8)) = pack8_at(w + s8);
-            *reinterpret_cast<uint4 *>(sm + PrepSmem::V + tc::sw128_offset(c, s8)) = pack8_at(u + s8);
-        }
+        for (int s8 = 0; s8 < 64; s8 += 8)
+            *reinterpret_cast<uint4 *>(dst + tc::sw128_offset(trow, s8)) = pack8_at(w + s8);
         // Kend (kept in registers since the operand build) -> MN-major [s][c] operand
-        const int r = tid >> 1, half = tid & 1;
-        uint8_t *Ks = sm + PrepSmem::KendS + (uint32_t)half * 8192u;
+        uint8_t *Ks = sm + PrepSmem::KendS + (uint32_t)opanel * 8192u;
 #pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) *reinterpret_cast<uint4 *>(Ks + tc::sw128_offset(r, g8 * 8)) = kend[g8];
-    } else {
-        __syncthreads();
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(Ks + tc::sw128_offset(orow + 16 * i, ocol)) = kend[i];
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
@@ -541,7 +617,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (warp == 0) tc::tmem_dealloc(tmem, 256);
         return;
     }
-
     if (tid == 0) {  // so is Ut^T
         tc::bulk_s2g(rec + R.Ut, sm + PrepSmem::V, 16384);
         tc::bulk_commit();
@@ -574,10 +649,12 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (warp_all(ok)) {
         // Qp = (X_q - P W') exp(b_m), MN-major [c][r]; M' = -Kend^T W' exp(b_m), K-major [c][c'].
         // Both are staged in shared memory (round 3 has consumed X and W'^T) and leave by bulk copy.
-        const float em = s_Em[c];
+        // Warps 0-3: Qp and M' columns 0-31; warps 4-7: M' columns 32-127.
+        const int c = trow;
         uint8_t *QpS = sm + PrepSmem::WT;
         uint8_t *McS = sm + PrepSmem::X;
-        {
+        if (hs == 0) {
+            const float em = s_Em[c];
             float qv[64];
             tc::tmem_ld64(tmem + lane_base, qv);
 #pragma unroll
@@ -586,8 +663,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             for (int s8 = 0; s8 < 64; s8 += 8)
                 *reinterpret_cast<uint4 *>(QpS + tc::sw128_offset(c, s8)) = pack8_at(qv + s8);
         }
-#pragma unroll
-        for (int q32 = 0; q32 < 4; ++q32) {
+        for (int q32 = hs ? 1 : 0; q32 < (hs ? 4 : 1); ++q32) {
             float mv[32];
             tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(q32 * 32), mv);
 #pragma unroll
@@ -637,9 +713,11 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
     __syncthreads();
     if (warp_all(ok)) {
+        const int c = trow;
 #pragma unroll
-        for (int t = 0; t < kNTile; ++t) {
+        for (int tt = 0; tt < 2; ++tt) {
             // Bc row c, columns of tile t: four 16-byte chunks, chunk k stored at k ^ ((c >> 1) & 3)
+            const int t = 2 * hs + tt;
             float bv[32];
             tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(t * 32), bv);
             uint8_t *BcS = sm + PrepSmem::X + t * 8192 + c * 64;
@@ -858,7 +936,8 @@ struct OutSmem {
 
 __global__ void __launch_bounds__(128)
 prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o,
-                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
+                  int resident) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t load_bar, mma_bar;
     __shared__ uint32_t tmem_base;
@@ -881,6 +960,12 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
         tc::fence_mbar_init();
         tc::mbar_arrive_expect_tx(&load_bar, OutSmem::bytes);
         tc::bulk_g2s(sm, rec + R.Qp, OutSmem::bytes, &load_bar);
+        // the CTA that takes this one's place next (CTAs start in launch order): its record into L2
+        const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
+        if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) && (nxt % gridDim.x) < doc_slot0[num_seqs])
+            tc::bulk_prefetch_l2(ws + records_off + ((size_t)(nxt % gridDim.x) * H + nxt / gridDim.x) * record_bytes +
+                                     R.Qp,
+                                 OutSmem::bytes);
     }
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 128);
@@ -980,6 +1065,24 @@ bool make_gate_map(CUtensorMap *map, const float *base, int total_tokens, int H)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTAs of `kernel` resident on the whole device at once (0 if unknown), cached per device.
+template <typename K>
+int resident_ctas(K kernel, int threads, int smem) {
+    static std::mutex lock;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> g(lock);
+    if (!cached[dev]) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cached[dev] = per_sm * sms;
+    }
+    return cached[dev];
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -996,9 +1099,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         const int smem = PrepSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
             return e;
+        const int resident = resident_ctas(prefill_prepare_tc, kPrepThreads, smem);
         marks.before(st, "prefill_prepare_tc");
-        prefill_prepare_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem, st>>>(
-            mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
+        prefill_prepare_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), kPrepThreads, smem, st>>>(
+            mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, resident);
         if ((e = cudaGetLastError())) return e;
     }
     if (num_seqs == 0) return cudaSuccess;
@@ -1012,10 +1116,11 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         const int smem_o = OutSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_o)))
             return e;
+        const int resident = resident_ctas(prefill_output_tc, 128, smem_o);
         marks.before(st, "prefill_output_tc");
         prefill_output_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem_o, st>>>(
             cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,
-            lay.record_bytes);
+            lay.record_bytes, resident);
         if ((e = cudaGetLastError())) return e;
     }
     return cudaSuccess;

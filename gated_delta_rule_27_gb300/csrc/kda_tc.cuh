@@ -126,6 +126,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
         : "memory");
 }
 
+// Prefetches a 3-D tile into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
+// Prefetches `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy shared -> global (bulk-group completion); both addresses
 // 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes) {
