@@ -762,30 +762,38 @@ __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int 
     tc::bulk_g2s(buf + StateSmem::Bc, rec + R.Bc + (size_t)tile * 8192, 8192, bar);
 }
 
-// Writes row i of S (32 values) into the K-major S^T operand: element (j, i),
-// two adjacent rows per 4-byte store (rows i and i ^ 1 swap halves of their values).
-__device__ __forceinline__ void store_state_operand(uint8_t *SB, int i, const float (&S)[kTile]) {
+// Writes S[i][16 h + j] (j < 16, this thread's half h of the tile's columns)
+// into the K-major S^T operand, element (16 h + j, i).  Rows i and i ^ 1 (lanes
+// of one warp) trade values so that each stores whole 4-byte words holding
+// rows (i & ~1, i | 1) of one column: the even lane columns 16 h + u, the odd
+// lane columns 16 h + 8 + ((u + 4) mod 8), which keeps the 32 stores of a warp
+// instruction on 32 distinct banks.
+__device__ __forceinline__ void store_state_half(uint8_t *SB, int i, int h, const float (&S)[16]) {
     uint8_t *p = SB + (uint32_t)(i >> 6) * 4096u;
     const int odd = i & 1, ie = i & ~1;
 #pragma unroll
-    for (int j2 = 0; j2 < kTile / 2; ++j2) {
-        // even lanes store columns 0..15, odd lanes 16..31; each needs its partner's value
-        const int j_even = j2, j_odd = j2 + kTile / 2;
-        const float mine = odd ? S[j_odd] : S[j_even];
-        const float other_give = odd ? S[j_even] : S[j_odd];
-        const float partner = __shfl_xor_sync(0xffffffffu, other_give, 1);
-        const int j = odd ? j_odd : j_even;
-        const float lo = odd ? partner : mine, hi = odd ? mine : partner;
+    for (int u = 0; u < 8; ++u) {
+        const int ja = u, jb = 8 + ((u + 4) & 7);  // the even and the odd lane's column of this step
+        const float give = odd ? S[ja] : S[jb];   // what the partner needs from this row
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const int j = 16 * h + (odd ? jb : ja);
+        const float lo = odd ? got : S[ja], hi = odd ? S[jb] : got;
         *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
     }
 }
 
-// One CTA per (document, head, 32-column tile of S); roles per chunk c
-// (128 threads, thread i <-> state row i <-> TMEM lane i):
-//   warps 0, 1 (lane 0)  issue M' S over the two K panels of S (the critical path)
-//   warp 3 (lane 0)      copies the image of S_c to chunk c's record, prefetches record c + 3
-//   all                  S <- gamma S + Bc + M' S, and the bf16 image of the new S
-__global__ void __launch_bounds__(128, 1)
+// One CTA per (document, head, 32-column tile of S), 320 threads:
+//   warps 0-7   epilogue: thread <-> state row i = 32 (w % 4) + lane (its TMEM lane) and column half
+//               h = w / 4; S[i][16 h ..] stays fp32 in registers
+//   warps 8, 9  lane 0 issues M' S over K panel w - 8 of S; warp 9 also copies each chunk's S image
+//               to its record and keeps records streaming three chunks ahead
+// Per chunk c:  issuers (after the epilogue warps' arrival on the operand barrier) -> MMAs ->
+// a_bar -> epilogue S <- gamma S + Bc + M' S, image of S_{c+1} -> arrival on the operand barrier.
+constexpr int kStateEpiWarps = 8;
+constexpr int kStateThreads = (kStateEpiWarps + 2) * 32;
+constexpr uint32_t kBarOperand = 1;  // named barrier: the next S image is complete
+
+__global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
                  size_t record_bytes) {
@@ -795,30 +803,34 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     __shared__ int s_abort;
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, i = tid;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer = warp >= kStateEpiWarps;
+    const int i = (warp & 3) * 32 + lane, hcol = (warp >> 2) & 1;
     const int tile = blockIdx.x % kNTile;
     const int h = (blockIdx.x / kNTile) % H;
     const int n = blockIdx.x / (kNTile * H);
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
-    const int col0 = tile * kTile;
+    const int col0 = tile * kTile + 16 * hcol;
     const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + col0;
     constexpr TcRecord R = tc_record();
 
-    float S[kTile];
+    float S[16];
 #pragma unroll
-    for (int j = 0; j < kTile; j += 4) {
-        const float4 v = S0 ? *reinterpret_cast<const float4 *>(S0 + state_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 16; j += 4) {
+        const float4 v = (S0 && !issuer) ? *reinterpret_cast<const float4 *>(S0 + state_off + j)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
+    bool ok = true;
     if (nchunks > 0) {
-        store_state_operand(sm + StateSmem::SB, i, S);
+        if (!issuer) store_state_half(sm + StateSmem::SB, i, hcol, S);
         tc::fence_async_smem();
         char *rec_h = ws + records_off + (size_t)h * record_bytes;  // record of (slot 0, head h)
         const size_t rec_stride = (size_t)H * record_bytes;          // one chunk slot further
         if (tid == 0) {
             for (int b = 0; b < kNBuf; ++b) tc::mbar_init(&full_bar[b], 1);
-            tc::mbar_init(&a_bar, 2);  // one commit from each of the two state-MMA issuers
+            tc::mbar_init(&a_bar, 2);  // one commit from each issuer
             tc::fence_mbar_init();
             s_abort = 0;
             for (int c = 0; c < kNBuf - 1 && c < nchunks; ++c)
@@ -833,75 +845,78 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         tc::tc_fence_after();
         // TMEM: M' S over the two K panels in cols 0..31 and 32..63
         const uint32_t tmem = tmem_base;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-        constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
-        bool ok = true;
 
-        for (int c = 0; c < nchunks; ++c) {
-            const int bsel = c % kNBuf;
-            const uint32_t fpar = (uint32_t)((c / kNBuf) & 1);
-            uint8_t *buf = sm + bsel * StateSmem::kBuf;
-            uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c % kNSb) * 8192u;
-            if (lane == 0 && warp < 2) {
-                ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
-                if (ok) {
-                    tc::tc_fence_after();
-                    const uint32_t panel = (uint32_t)warp;
-                    for (int s = 0; s < 4; ++s)
-                        tc::mma_bf16(tmem + 32u * panel,
-                                     tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u +
-                                                                       (uint32_t)s * 32u)),
-                                     tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u + (uint32_t)s * 32u)),
-                                     idN, s > 0);
-                    tc::mma_commit(&a_bar);
+        if (issuer) {
+            const uint32_t panel = (uint32_t)(warp - kStateEpiWarps);
+            constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+            constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
+            for (int c = 0; c < nchunks; ++c) {
+                const int bsel = c % kNBuf;
+                uint8_t *buf = sm + bsel * StateSmem::kBuf;
+                uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c % kNSb) * 8192u;
+                if (c > 0) tc::named_barrier(kBarOperand, kStateThreads);  // S_c's image is complete
+                tc::tc_fence_after();
+                if (lane == 0) {
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
+                    if (ok) {
+                        const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u));
+                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u));
+                        for (int s = 0; s < 4; ++s)  // K steps of 16: +32 bytes, +2 in the start-address field
+                            tc::mma_bf16(tmem + 32u * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, s > 0);
+                    }
+                    tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
+                    if (panel == 1 && ok) {
+                        // S_c's image, tile rows of both panels, into chunk c's record
+                        char *rec = rec_h + (size_t)(first + c) * rec_stride;
+                        tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
+                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
+                        tc::bulk_commit();
+                        tc::bulk_wait_read_but_last();  // image c - 1 is free again for chunk c + 1's epilogue
+                        // the buffer chunk c - 1 used was released by the operand barrier of this chunk
+                        const int cn = c + kNBuf - 1;
+                        if (cn < nchunks)
+                            issue_record(sm + (cn % kNBuf) * StateSmem::kBuf,
+                                         rec_h + (size_t)(first + cn) * rec_stride, tile, &full_bar[cn % kNBuf]);
+                    }
                 }
-            } else if (lane == 0 && warp == 3) {
-                // S_c's image, tile rows of both panels, into chunk c's record
-                char *rec = rec_h + (size_t)(first + c) * rec_stride;
-                tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
-                tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
-                tc::bulk_commit();
-                tc::bulk_wait_read_but_last();  // image c - 1 is free again: the epilogue of chunk c + 1 reuses it
-                // the buffer chunk c - 1 used was released by the barrier that ended that chunk
-                const int cn = c + kNBuf - 1;
-                if (cn < nchunks)
-                    issue_record(sm + (cn % kNBuf) * StateSmem::kBuf, rec_h + (size_t)(first + cn) * rec_stride,
-                                 tile, &full_bar[cn % kNBuf]);
+                __syncwarp();
             }
-            __syncwarp();
-            // S <- gamma * S + Kend^T Ut + M' S (the last term in two K halves); gamma and the Bc row
-            // are read while the MMAs run
-            ok = ok && tc::mbar_wait(&full_bar[bsel], fpar);
-            const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-            float bc[32];
-            {
-                const uint8_t *brow = buf + StateSmem::Bc + i * 64;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
+            if (lane == 0 && panel == 1) tc::bulk_wait_read();  // shared memory must outlive the image copies
+        } else {
+            const uint32_t tacc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 16u * (uint32_t)hcol;
+            for (int c = 0; c < nchunks; ++c) {
+                const int bsel = c % kNBuf;
+                const uint8_t *buf = sm + bsel * StateSmem::kBuf;
+                // gamma and this thread's 16 Bc values, read while the MMAs run
+                ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
+                const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+                float bc[16];
+                {
+                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
                     float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), f);
+                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((2 * hcol) ^ ((i >> 1) & 3)) << 4)), f);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) bc[8 * k + u] = f[u];
+                    for (int u = 0; u < 8; ++u) bc[u] = f[u];
+                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((2 * hcol + 1) ^ ((i >> 1) & 3)) << 4)), f);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) bc[8 + u] = f[u];
                 }
-            }
-            ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
-            tc::tc_fence_after();
-            if (warp_all(ok)) {
-                float t[64];
-                tc::tmem_ld64(tmem + lane_base, t);
+                ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
+                tc::tc_fence_after();
+                if (warp_all(ok)) {
+                    float t0[16], t1[16];
+                    tc::tmem_ld16x2(tacc, tacc + 32u, t0, t1);
 #pragma unroll
-                for (int j = 0; j < kTile; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t[j] + t[32 + j]));
-                store_state_operand(sm + StateSmem::SB + (uint32_t)((c + 1) % kNSb) * 8192u, i, S);
+                    for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t0[j] + t1[j]));
+                    store_state_half(sm + StateSmem::SB + (uint32_t)((c + 1) % kNSb) * 8192u, i, hcol, S);
+                }
+                tc::fence_async_smem();
+                tc::tc_fence_before();
+                if (c + 1 < nchunks) tc::named_barrier_arrive(kBarOperand, kStateThreads);
             }
-            tc::fence_async_smem();
-            tc::tc_fence_before();
-            if (!ok) s_abort = 1;
-            __syncthreads();
-            tc::tc_fence_after();
-            if (s_abort) break;
         }
-        if (warp == 3 && lane == 0) tc::bulk_wait_read();  // shared memory must outlive the image copies
+        if (!ok) s_abort = 1;
+        __syncthreads();
         if (s_abort) {
             // let any record copy still in flight land before the CTA's shared memory goes away
             if (tid == 0) {
@@ -913,9 +928,9 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         if (warp == 0) tc::tmem_dealloc(tmem, 64);
         if (s_abort) return;
     }
-    if (S_final) {
+    if (S_final && !issuer) {
 #pragma unroll
-        for (int j = 0; j < kTile; j += 4)
+        for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<float4 *>(S_final + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
 }
@@ -1109,7 +1124,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const int smem = StateSmem::bytes + 1024;
     if ((e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
     marks.before(st, "prefill_state_tc");
-    prefill_state_tc<<<(unsigned)((size_t)num_seqs * H * kNTile), 128, smem, st>>>(
+    prefill_state_tc<<<(unsigned)((size_t)num_seqs * H * kNTile), kStateThreads, smem, st>>>(
         cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
     if ((e = cudaGetLastError())) return e;
     if (lay.max_slots > 0 && total_tokens > 0) {
