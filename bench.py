@@ -141,6 +141,7 @@ KERNEL_SOURCES = {
     "prefill_prepare_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_state_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_output_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_fused_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
 }
 

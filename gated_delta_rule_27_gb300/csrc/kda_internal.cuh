@@ -29,6 +29,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 //   doc_slot0           int32 [num_seqs + 1]: first chunk slot of each document
 //                       (exclusive prefix sum of ceil(len / L)), 256-byte padded
 //   records             one per (chunk slot, head), `record_bytes` each
+//   flags               (tensor-core path) the single-launch pipeline's progress flags
 //
 // The number of chunk slots is bounded by total_tokens / L + num_seqs, so the
 // size depends only on the call's scalar arguments.
@@ -40,6 +41,9 @@ struct WsLayout {
     size_t records_off;
     size_t record_bytes;
     int64_t max_slots;
+    size_t flags_off;    // tensor-core path: int32 [max_slots * H] record-ready flags, then int32
+                         // [max_slots * H] state-image counters, then two int32 unit counters
+    size_t flags_bytes;  // 0 on the CUDA-core path
     size_t total;
 };
 
@@ -90,7 +94,9 @@ inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int
     w.records_off = w.doc_slot0_off + align256((size_t)(num_seqs + 1) * 4);
     w.record_bytes = path == PATH_TC ? tc_record().bytes : simt_record(L, dk, dv).bytes;
     w.max_slots = total_tokens / L + num_seqs;
-    w.total = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;
+    w.flags_off = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;
+    w.flags_bytes = path == PATH_TC ? align256(((size_t)2 * w.max_slots * H + 2) * 4) : 0;
+    w.total = w.flags_off + w.flags_bytes;
     return w;
 }
 

@@ -36,6 +36,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -264,15 +266,35 @@ __device__ __forceinline__ uint4 pack8_at(const float *f) {
 // t / 4 and channel quarter t % 4.  TMEM epilogues: warp w reads lanes
 // 32 (w % 4) .. + 31 (channel or token rows), warps w and w + 4 splitting the
 // accumulator's columns.  MMAs are issued by lane 0 of warps 0 and 1.
-__global__ void __launch_bounds__(kPrepThreads, 2)
-prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                   const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
-                   char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
-                   int resident) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t g_bar, load_bar, r1_bar, r2_bar, r3_bar, r4_bar;  // gates; k, q, v; MMA rounds
-    __shared__ uint32_t tmem_base;
+struct PrepParams {
+    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_g;  // tensor maps in kernel-parameter space
+    const float *beta;
+    const int32_t *cu;
+    int num_seqs, H;
+    char *ws;
+    size_t doc_slot0_off, records_off, record_bytes;
+};
+// mbarriers of one preparation, each completing exactly once per unit: the gate tile, the k, q, v
+// tiles, and the four MMA rounds
+struct PrepBars {
+    uint64_t g, load, r1, r2, r3, r4;
+};
+__device__ __forceinline__ void prep_bars_init(PrepBars *b) {
+    tc::mbar_init(&b->g, 1);
+    tc::mbar_init(&b->load, 1);
+    tc::mbar_init(&b->r1, 2);  // rounds 1-3 are issued by two warps, one commit each
+    tc::mbar_init(&b->r2, 2);
+    tc::mbar_init(&b->r3, 2);
+    tc::mbar_init(&b->r4, 1);
+}
+
+// One (chunk slot, head) of the preparation by a CTA of 256 threads whose 256 TMEM
+// columns start at `tmem`; `ph` is the parity of this unit's barrier phases (units
+// a CTA has prepared before, mod 2).  (nslot, nh) is a unit that is likely to
+// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  Returns
+// false after recording a timeout in the status word.
+__device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
+                             uint32_t ph, uint32_t tmem, int nslot, int nh) {
     __shared__ float s_beta[kL];
     __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
     __shared__ __align__(16) float s_F[kD];
@@ -280,53 +302,38 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __shared__ __align__(16) float s_blast[kD];
     __shared__ float s_half[kD], s_mid[kD], s_lo[2][kD], s_hi[2][kD];
     __shared__ int s_abort;
-    uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = blockIdx.x, h = blockIdx.y;
-    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
-    int doc, t0, Lc;
-    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
+    const int H = p.H;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(p.ws + p.doc_slot0_off);
+    char *ws = p.ws;
     constexpr TcRecord R = tc_record();
-    char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
+    char *rec = ws + p.records_off + ((size_t)slot * H + h) * p.record_bytes;
 
     if (tid == 0) {
-        tc::mbar_init(&g_bar, 1);
-        tc::mbar_init(&load_bar, 1);
-        tc::mbar_init(&r1_bar, 2);  // rounds 1-3 are issued by two warps, one commit each
-        tc::mbar_init(&r2_bar, 2);
-        tc::mbar_init(&r3_bar, 2);
-        tc::mbar_init(&r4_bar, 1);
-        tc::fence_mbar_init();
         s_abort = 0;
         // the gates first: the cumulative sums run while k, q, v are still arriving
-        tc::mbar_arrive_expect_tx(&g_bar, 32768);
-        tc::tma_load_3d(sm + PrepSmem::G, &tm_g, 0, h, t0, &g_bar);
-        tc::mbar_arrive_expect_tx(&load_bar, 6 * 8192);
-        tc::tma_load_3d(sm + PrepSmem::X, &tm_k, 0, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::X + 8192, &tm_q, 0, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::X + 16384, &tm_k, 64, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::X + 24576, &tm_q, 64, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::V, &tm_v, 0, h, t0, &load_bar);
-        tc::tma_load_3d(sm + PrepSmem::V + 8192, &tm_v, 64, h, t0, &load_bar);
+        tc::mbar_arrive_expect_tx(&bars->g, 32768);
+        tc::tma_load_3d(sm + PrepSmem::G, p.tm_g, 0, h, t0, &bars->g);
+        tc::mbar_arrive_expect_tx(&bars->load, 6 * 8192);
+        tc::tma_load_3d(sm + PrepSmem::X, p.tm_k, 0, h, t0, &bars->load);
+        tc::tma_load_3d(sm + PrepSmem::X + 8192, p.tm_q, 0, h, t0, &bars->load);
+        tc::tma_load_3d(sm + PrepSmem::X + 16384, p.tm_k, 64, h, t0, &bars->load);
+        tc::tma_load_3d(sm + PrepSmem::X + 24576, p.tm_q, 64, h, t0, &bars->load);
+        tc::tma_load_3d(sm + PrepSmem::V, p.tm_v, 0, h, t0, &bars->load);
+        tc::tma_load_3d(sm + PrepSmem::V + 8192, p.tm_v, 64, h, t0, &bars->load);
     }
-    if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 256);
-        tc::tmem_relinquish();
-    }
-    if (tid < kL) s_beta[tid] = tid < Lc ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (tid < kL) s_beta[tid] = tid < Lc ? p.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = tmem_base;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int trow = (warp & 3) * 32 + lane;  // this thread's TMEM lane
     const int hs = warp >> 2;                 // this warp's half of an accumulator's columns
-    if (!tc::mbar_wait(&g_bar, 0)) s_abort = 1;
+    if (!tc::mbar_wait(&bars->g, ph)) s_abort = 1;
     __syncthreads();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 256);
-        return;
+        return false;
     }
 
     // cumulative log-decay of channel c over this thread's 32 rows; reference token m in the middle
@@ -376,30 +383,24 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             s_Em[c] = expf(bref);
             reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
         }
-        if (!tc::mbar_wait(&load_bar, 0)) s_abort = 1;
+        if (!tc::mbar_wait(&bars->load, ph)) s_abort = 1;
         if (tid == 0) {
-            // CTAs start in launch order as slots free up, so the one `resident` places further on takes this
-            // CTA's place next: pull its tiles into L2 while this chunk computes
-            const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
             int ndoc, nt0, nLc;
-            if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) &&
-                locate_slot(doc_slot0, cu, num_seqs, kL, nxt % gridDim.x, &ndoc, &nt0, &nLc)) {
-                const int nh = nxt / gridDim.x;
-                tc::tma_prefetch_3d(&tm_g, 0, nh, nt0);
-                tc::tma_prefetch_3d(&tm_k, 0, nh, nt0);
-                tc::tma_prefetch_3d(&tm_k, 64, nh, nt0);
-                tc::tma_prefetch_3d(&tm_q, 0, nh, nt0);
-                tc::tma_prefetch_3d(&tm_q, 64, nh, nt0);
-                tc::tma_prefetch_3d(&tm_v, 0, nh, nt0);
-                tc::tma_prefetch_3d(&tm_v, 64, nh, nt0);
+            if (nslot >= 0 && locate_slot(doc_slot0, p.cu, p.num_seqs, kL, nslot, &ndoc, &nt0, &nLc)) {
+                tc::tma_prefetch_3d(p.tm_g, 0, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_k, 0, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_k, 64, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_q, 0, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_q, 64, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_v, 0, nh, nt0);
+                tc::tma_prefetch_3d(p.tm_v, 64, nh, nt0);
             }
         }
         __syncthreads();
     }
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 256);
-        return;
+        return false;
     }
     float accA[16], accP[16];
     if (unsafe) {
@@ -465,6 +466,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     float *Af = reinterpret_cast<float *>(sm + PrepSmem::Afp);
     uint8_t *Pb = sm + PrepSmem::P;
     if (unsafe) {
+        if (lane == 0 && warp < 2) tc::mma_commit(&bars->r1);  // no MMAs: completes round 1's phase at once
         const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
         for (int j8 = 0; j8 < 16; j8 += 8) {
@@ -488,10 +490,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tc::mma_bf16(tmem + 128u * (uint32_t)warp, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::X + ka)),
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + kb)), id, s > 0);
             }
-            tc::mma_commit(&r1_bar);
+            tc::mma_commit(&bars->r1);
         }
         __syncwarp();
-        ok = tc::mbar_wait(&r1_bar, 0);
+        ok = tc::mbar_wait(&bars->r1, ph);
         tc::tc_fence_after();
         if (warp_all(ok)) {  // the MMAs are complete: their operand Y may be overwritten by P
             float v[32], v2[32];
@@ -546,8 +548,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     __syncthreads();
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 256);
-        return;
+        return false;
     }
 
     // triangular solve in fp32, then T as the bf16 round-2 B operand (K-major [r][s])
@@ -585,10 +586,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int s = 0; s < 4; ++s)
             tc::mma_bf16(tmem + 64u * (uint32_t)(warp + 1), tc::smem_desc(amn, tc::smem_u32(abase + s * 2048)),
                          tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Tb + s * 32)), id, s > 0);
-        tc::mma_commit(&r2_bar);
+        tc::mma_commit(&bars->r2);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&r2_bar, 0);
+    ok = tc::mbar_wait(&bars->r2, ph);
     tc::tc_fence_after();
     if (warp_all(ok)) {
         // warps 0-3: W'^T row c -> WT;  warps 4-7: Ut^T row c -> V (round 2 has consumed beta V)
@@ -614,8 +615,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             flag_timeout(ws);
             tc::bulk_wait_read();  // record images already on their way still read shared memory
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 256);
-        return;
+        return false;
     }
     if (tid == 0) {  // so is Ut^T
         tc::bulk_s2g(rec + R.Ut, sm + PrepSmem::V, 16384);
@@ -641,10 +641,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::WT + s * 32)), id128, s > 0);
         }
-        tc::mma_commit(&r3_bar);
+        tc::mma_commit(&bars->r3);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&r3_bar, 0);
+    ok = tc::mbar_wait(&bars->r3, ph);
     tc::tc_fence_after();
     if (warp_all(ok)) {
         // Qp = (X_q - P W') exp(b_m), MN-major [c][r]; M' = -Kend^T W' exp(b_m), K-major [c][c'].
@@ -689,8 +689,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             flag_timeout(ws);
             tc::bulk_wait_read();  // record images already on their way still read shared memory
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 256);
-        return;
+        return false;
     }
     if (tid == 0) {
         tc::bulk_s2g(rec + R.Mc, sm + PrepSmem::X, 32768);
@@ -705,10 +704,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int s = 0; s < 4; ++s)
             tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
                          tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), id128, s > 0);
-        tc::mma_commit(&r4_bar);
+        tc::mma_commit(&bars->r4);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&r4_bar, 0);
+    ok = tc::mbar_wait(&bars->r4, ph);
     tc::tc_fence_after();
     if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
     __syncthreads();
@@ -728,16 +727,56 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
-    if (!ok && tid == 0) flag_timeout(ws);
+    if (!ok) s_abort = 1;
     __syncthreads();
+    const bool done = !s_abort;
     if (tid == 0) {
-        if (ok) {
+        if (done) {
             tc::bulk_s2g(rec + R.Bc, sm + PrepSmem::X, 32768);
             tc::bulk_commit();
+        } else {
+            flag_timeout(ws);
         }
         tc::bulk_wait_read();  // shared memory must outlive the copies' reads
     }
-    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    return done;
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                   const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
+                   char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
+                   int resident) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PrepBars bars;
+    __shared__ uint32_t tmem_base;
+    uint8_t *sm = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    int doc, t0, Lc;
+    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
+    if (tid == 0) {
+        prep_bars_init(&bars);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 256);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    // CTAs start in launch order as slots free up, so the one `resident` places further on takes this
+    // CTA's place next
+    const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
+    const bool has_next = resident > 0 && nxt < (int)(gridDim.x * gridDim.y);
+    const PrepParams prm{&tm_q, &tm_k, &tm_v, &tm_g, beta, cu, num_seqs, H, ws, doc_slot0_off, records_off, record_bytes};
+    prepare_unit(prm, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, has_next ? nxt % (int)gridDim.x : -1,
+                 has_next ? nxt / (int)gridDim.x : 0);
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -949,49 +988,29 @@ struct OutSmem {
     static constexpr uint32_t bytes = 73728;
 };
 
-__global__ void __launch_bounds__(128)
-prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o,
-                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
-                  int resident) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t load_bar, mma_bar;
-    __shared__ uint32_t tmem_base;
+struct OutBars {
+    uint64_t load, mma;
+};
+
+// One (chunk slot, head) of the output pass, t0 / Lc the chunk's first token and
+// length, by a CTA of >= 128 threads (warps 0-1 write the 64 token rows) whose
+// TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's barrier
+// phases.  The record must be complete, S included.  Returns false after
+// recording a timeout in the status word.
+__device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
+                            size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
+                            OutBars *bars, uint32_t ph, uint32_t tmem) {
     __shared__ int s_ok;
-    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid input or an earlier timeout
-    uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int slot = blockIdx.x, h = blockIdx.y;
-    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
-    int doc, t0, Lc;
-    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
                       R.S - R.Qp == OutSmem::S,
                   "output pass loads the record tail as one image");
     const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
     if (tid == 0) {
-        tc::mbar_init(&load_bar, 1);
-        tc::mbar_init(&mma_bar, 1);
-        tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(&load_bar, OutSmem::bytes);
-        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::bytes, &load_bar);
-        // the CTA that takes this one's place next (CTAs start in launch order): its record into L2
-        const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
-        if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) && (nxt % gridDim.x) < doc_slot0[num_seqs])
-            tc::bulk_prefetch_l2(ws + records_off + ((size_t)(nxt % gridDim.x) * H + nxt / gridDim.x) * record_bytes +
-                                     R.Qp,
-                                 OutSmem::bytes);
-    }
-    if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 128);
-        tc::tmem_relinquish();
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = tmem_base;
-    if (tid == 0) {
-        const bool ok = tc::mbar_wait(&load_bar, 0);
+        tc::mbar_arrive_expect_tx(&bars->load, OutSmem::bytes);
+        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::bytes, &bars->load);
+        const bool ok = tc::mbar_wait(&bars->load, ph);
         s_ok = ok;
         if (ok) {
             tc::tc_fence_after();
@@ -1007,12 +1026,12 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
                 tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::P + s * 32)),
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::Ut + s * 32)), id_k, true);
         }
-        tc::mma_commit(&mma_bar);  // arrives at once when nothing was issued
+        tc::mma_commit(&bars->mma);  // arrives at once when nothing was issued
     }
     __syncwarp();
     if (warp < 2) {
         // token row r = tid: 128 fp32 accumulators -> 256 bytes of o
-        const bool done = tc::mbar_wait(&mma_bar, 0);
+        const bool done = tc::mbar_wait(&bars->mma, ph);
         tc::tc_fence_after();
         if (warp_all(done)) {
             const int r = tid;
@@ -1033,8 +1052,369 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !s_ok) flag_timeout(ws);
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    const bool ok = s_ok != 0;
+    if (tid == 0 && !ok) flag_timeout(ws);
+    return ok;
+}
+
+__global__ void __launch_bounds__(128)
+prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o,
+                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
+                  int resident) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ OutBars bars;
+    __shared__ uint32_t tmem_base;
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid input or an earlier timeout
+    uint8_t *sm = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    int doc, t0, Lc;
+    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
+    if (tid == 0) {
+        tc::mbar_init(&bars.load, 1);
+        tc::mbar_init(&bars.mma, 1);
+        tc::fence_mbar_init();
+        // the CTA that takes this one's place next (CTAs start in launch order): its record into L2
+        const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
+        if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) && (nxt % gridDim.x) < doc_slot0[num_seqs])
+            tc::bulk_prefetch_l2(ws + records_off + ((size_t)(nxt % gridDim.x) * H + nxt / gridDim.x) * record_bytes +
+                                     tc_record().Qp,
+                                 OutSmem::bytes);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base);
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
+}
+
+// ---------------------------------------------------------------------------
+// Single-launch pipeline: preparation, state pass and output overlapped
+// ---------------------------------------------------------------------------
+// When a call has few (document, head, column tile) chains, one launch of
+// prefill_fused_tc, with as many CTAs as fit on the GPU at once, replaces the
+// three kernels above, so that the
+// state pass runs while later chunks are still being prepared and the outputs
+// are formed while their records are still in L2:
+//   CTAs [0, n_state)  one chain each (the state pass above, 256 threads:
+//                      warps 0-3 epilogue with 32 columns per thread, warps 4-5
+//                      MMA issuers, warp 6 streams records in as they are
+//                      published, warp 7 copies each state image out and
+//                      publishes it)
+//   other CTAs         take units from a shared counter: the preparation of a
+//                      (chunk slot, head), or its output once its record and
+//                      all its column tiles' state images are published;
+//                      outputs trail the preparations by `lag` chunk slots.
+// Hand-offs go through the flags region of the workspace with GPU-scope
+// release / acquire: a record is published after its bulk stores complete,
+// and a reader fences the async proxy before its bulk loads.  Every wait is
+// bounded.  Progress needs only the state CTAs to be resident (they have the
+// lowest indices, so they are placed first): a state CTA waits for records,
+// and every record it waits for belongs to a unit that a running worker has
+// already claimed and finishes without waiting; a worker waits only for state
+// CTAs.
+
+// Row i of S (32 values) into the K-major S^T operand, element (j, i); rows i
+// and i ^ 1 trade values so that each stores whole 4-byte words.
+__device__ __forceinline__ void store_state_row32(uint8_t *SB, int i, const float (&S)[kTile]) {
+    uint8_t *p = SB + (uint32_t)(i >> 6) * 4096u;
+    const int odd = i & 1, ie = i & ~1;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int ja = u, jb = 16 + ((u + 8) & 15);  // the even and the odd lane's column of this step
+        const float give = odd ? S[ja] : S[jb];
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const int j = odd ? jb : ja;
+        const float lo = odd ? got : S[ja], hi = odd ? S[jb] : got;
+        *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
+    }
+}
+
+struct FusedStateSmem {
+    static constexpr uint32_t kBuf = 43008;  // M' and gamma + this CTA's Bc tile, 1 KB aligned
+    static constexpr uint32_t SB = 2 * kBuf;  // two bf16 images of S
+    static constexpr uint32_t bytes = SB + 2 * 8192;
+};
+constexpr int kFusedMaxChains = 64;   // automatic choice: at most this many chains
+constexpr int kFusedMinWorkers = 32;  // CTAs left for the chunk-parallel units, at least
+constexpr size_t fused_smem_bytes() {
+    return (PrepSmem::bytes > FusedStateSmem::bytes ? (PrepSmem::bytes > OutSmem::bytes ? PrepSmem::bytes : OutSmem::bytes)
+                                                    : (FusedStateSmem::bytes > OutSmem::bytes ? FusedStateSmem::bytes
+                                                                                              : OutSmem::bytes)) +
+           1024;
+}
+
+constexpr uint32_t kBarFusedOp = 1;              // named barrier: the next S image is complete
+constexpr uint32_t kFusedOpCount = 4 * 32 + 3 * 32;  // epilogue warps arrive; issuers and publisher wait
+
+struct FusedArgs {
+    const float *S0;
+    float *S_final;
+    __nv_bfloat16 *o;
+    int32_t *ready;    // [slot * H + h]: the record of (slot, h) is published
+    int32_t *sdone;    // [slot * H + h]: column tiles whose state image is published
+    int32_t *counter;  // next unit
+    int n_state, lag;  // state CTAs; outputs trail the preparations by `lag` chunk slots
+};
+
+// Position u of the worker units -> (output?, slot, head): the first `lag` slots' preparations, then
+// alternately one slot's preparations and the outputs of the slot `lag` earlier, then the last outputs.
+__device__ __forceinline__ void decode_unit(int u, int C, int H, int lag, bool *out, int *slot, int *h) {
+    const int D = min(lag, C);
+    const int lead = D * H, mid = (C - D) * 2 * H;
+    if (u < lead) {
+        *out = false; *slot = u / H; *h = u % H;
+    } else if (u < lead + mid) {
+        const int q = u - lead, b = q / (2 * H), r = q % (2 * H);
+        *out = r >= H; *slot = r < H ? D + b : b; *h = r < H ? r : r - H;
+    } else {
+        const int q = u - lead - mid;
+        *out = true; *slot = C - D + q / H; *h = q % H;
+    }
+}
+
+__device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *sm) {
+    __shared__ uint64_t full_bar[2], empty_bar[2], a_bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = pp.H;
+    const int j = blockIdx.x, tile = j % kNTile, h = (j / kNTile) % H, n = j / (kNTile * H);
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
+    const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
+    const bool epi = warp < 4;
+    const int i = (warp & 3) * 32 + lane;
+    const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + tile * kTile;
+    constexpr TcRecord R = tc_record();
+
+    float S[kTile];
+#pragma unroll
+    for (int c4 = 0; c4 < kTile; c4 += 4) {
+        const float4 v = (f.S0 && epi) ? *reinterpret_cast<const float4 *>(f.S0 + state_off + c4)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[c4] = v.x; S[c4 + 1] = v.y; S[c4 + 2] = v.z; S[c4 + 3] = v.w;
+    }
+    bool ok = true;
+    if (nchunks > 0) {
+        if (epi) store_state_row32(sm + FusedStateSmem::SB, i, S);
+        tc::fence_async_smem();
+        if (tid == 0) {
+            for (int b = 0; b < 2; ++b) {
+                tc::mbar_init(&full_bar[b], 1);
+                tc::mbar_init(&empty_bar[b], 128);  // every epilogue thread releases the buffer
+            }
+            tc::mbar_init(&a_bar, 2);
+            tc::fence_mbar_init();
+            s_abort = 0;
+        }
+        if (warp == 0) {
+            tc::tmem_alloc(&tmem_base, 64);
+            tc::tmem_relinquish();
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+        const uint32_t tmem = tmem_base;
+        char *rec_h = pp.ws + pp.records_off + (size_t)h * pp.record_bytes;
+        const size_t rec_stride = (size_t)H * pp.record_bytes;
+
+        if (warp == 6) {
+            // loader: record c into buffer c % 2 once it is published and the buffer is free
+            if (lane == 0) {
+                int issued = 0;
+                for (int c = 0; c < nchunks; ++c) {
+                    const int b = c & 1;
+                    if (c >= 2) ok = ok && tc::mbar_wait(&empty_bar[b], (uint32_t)(((c - 2) >> 1) & 1));
+                    ok = ok && tc::wait_flag_geq(f.ready + (size_t)(first + c) * H + h, 1);
+                    if (!ok) break;
+                    tc::fence_proxy_async_global();
+                    issue_record(sm + b * FusedStateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile,
+                                 &full_bar[b]);
+                    issued = c + 1;
+                }
+                // copies still on their way land before shared memory can go away
+                for (int c = max(0, issued - 2); c < issued; ++c)
+                    tc::mbar_wait(&full_bar[c & 1], (uint32_t)((c >> 1) & 1), 10000000ull);
+            }
+            __syncwarp();
+        } else if (warp == 4 || warp == 5) {
+            const uint32_t panel = (uint32_t)(warp - 4);
+            constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+            constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
+            for (int c = 0; c < nchunks; ++c) {
+                if (c > 0) tc::named_barrier(kBarFusedOp, kFusedOpCount);  // S_c's image is complete
+                tc::tc_fence_after();
+                if (lane == 0) {
+                    ok = ok && tc::mbar_wait(&full_bar[c & 1], (uint32_t)((c >> 1) & 1));
+                    if (ok) {
+                        uint8_t *buf = sm + (c & 1) * FusedStateSmem::kBuf;
+                        uint8_t *sbc = sm + FusedStateSmem::SB + (uint32_t)(c & 1) * 8192u;
+                        const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u));
+                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u));
+                        for (int s = 0; s < 4; ++s)
+                            tc::mma_bf16(tmem + 32u * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, s > 0);
+                    }
+                    tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
+                }
+                __syncwarp();
+            }
+        } else if (warp == 7) {
+            // publisher: S_c's image into chunk c's record; S_{c-1}'s published once its writes are complete
+            for (int c = 0; c < nchunks; ++c) {
+                if (c > 0) tc::named_barrier(kBarFusedOp, kFusedOpCount);
+                if (lane == 0) {
+                    const uint8_t *sbc = sm + FusedStateSmem::SB + (uint32_t)(c & 1) * 8192u;
+                    char *rec = rec_h + (size_t)(first + c) * rec_stride;
+                    tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
+                    tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
+                    tc::bulk_commit();
+                    tc::bulk_wait_all_but_last();
+                    if (c > 0) {
+                        tc::fence_proxy_async_global();
+                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 1) * H + h, 1);
+                    }
+                    tc::bulk_wait_read();  // image c has been read: the epilogue of chunk c + 1 rewrites it
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                tc::bulk_wait_all();
+                tc::fence_proxy_async_global();
+                tc::red_release_gpu_add(f.sdone + (size_t)(first + nchunks - 1) * H + h, 1);
+            }
+            __syncwarp();
+        } else {
+            // epilogue: S <- gamma S + Bc + M' S for state row i, 32 columns
+            const uint32_t tacc = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int c = 0; c < nchunks; ++c) {
+                const int b = c & 1;
+                const uint8_t *buf = sm + b * FusedStateSmem::kBuf;
+                ok = ok && tc::mbar_wait(&full_bar[b], (uint32_t)((c >> 1) & 1));
+                const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+                float bc[kTile];
+                {
+                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float fv[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), fv);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) bc[8 * k + u] = fv[u];
+                    }
+                }
+                ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
+                tc::tc_fence_after();
+                if (warp_all(ok)) {
+                    float t[64];
+                    tc::tmem_ld64(tacc, t);
+#pragma unroll
+                    for (int jj = 0; jj < kTile; ++jj) S[jj] = fmaf(gam, S[jj], bc[jj] + (t[jj] + t[32 + jj]));
+                    store_state_row32(sm + FusedStateSmem::SB + (uint32_t)((c + 1) & 1) * 8192u, i, S);
+                }
+                tc::fence_async_smem();
+                tc::tc_fence_before();
+                tc::mbar_arrive(&empty_bar[b]);
+                if (c + 1 < nchunks) tc::named_barrier_arrive(kBarFusedOp, kFusedOpCount);
+            }
+        }
+        if (!ok) s_abort = 1;
+        __syncthreads();
+        if (tid == 0 && s_abort) flag_timeout(pp.ws);
+        if (warp == 0) tc::tmem_dealloc(tmem, 64);
+        if (s_abort) return;
+    }
+    if (f.S_final && epi) {
+#pragma unroll
+        for (int c4 = 0; c4 < kTile; c4 += 4)
+            *reinterpret_cast<float4 *>(f.S_final + state_off + c4) = make_float4(S[c4], S[c4 + 1], S[c4 + 2], S[c4 + 3]);
+    }
+}
+
+__device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *sm) {
+    __shared__ PrepBars pbars;
+    __shared__ OutBars obars;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_unit, s_ok;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int H = pp.H;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
+    const int C = doc_slot0[pp.num_seqs];
+    const int total = 2 * C * H;
+    if (tid == 0) {
+        prep_bars_init(&pbars);
+        tc::mbar_init(&obars.load, 1);
+        tc::mbar_init(&obars.mma, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 256);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    uint32_t nprep = 0, nout = 0;
+    for (;;) {
+        if (tid == 0) s_unit = atomicAdd(f.counter, 1);
+        __syncthreads();
+        const int u = s_unit;
+        if (u >= total) break;
+        bool out;
+        int slot, h, doc, t0, Lc;
+        decode_unit(u, C, H, f.lag, &out, &slot, &h);
+        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+        if (!out) {
+            const bool ok = prepare_unit(pp, slot, h, t0, Lc, sm, &pbars, nprep & 1u, tmem, -1, 0);
+            ++nprep;
+            if (!ok) break;
+            if (tid == 0) {
+                tc::bulk_wait_all();  // the record's bulk stores are complete
+                tc::fence_proxy_async_global();
+            }
+            __syncthreads();  // and so are the other threads' direct stores (gamma)
+            if (tid == 0) tc::st_release_gpu(f.ready + (size_t)slot * H + h, 1);
+        } else {
+            if (tid == 0) {
+                // the record itself (its own publication) and every column tile's image of S_c
+                s_ok = tc::wait_flag_geq(f.ready + (size_t)slot * H + h, 1) &&
+                       tc::wait_flag_geq(f.sdone + (size_t)slot * H + h, kNTile);
+                tc::fence_proxy_async_global();
+            }
+            __syncthreads();
+            if (!s_ok) {
+                if (tid == 0) flag_timeout(pp.ws);
+                break;
+            }
+            const bool ok = output_unit(pp.cu, H, f.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, sm,
+                                        &obars, nout & 1u, tmem);
+            ++nout;
+            if (!ok) break;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+prefill_fused_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                 const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
+                 char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, FusedArgs f) {
+    extern __shared__ uint8_t smem_raw[];
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    uint8_t *sm = align1024(smem_raw);
+    const PrepParams pp{&tm_q, &tm_k, &tm_v, &tm_g, beta, cu, num_seqs, H, ws, doc_slot0_off, records_off, record_bytes};
+    if ((int)blockIdx.x < f.n_state)
+        fused_state(pp, f, sm);
+    else
+        fused_worker(pp, f, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -1080,20 +1460,34 @@ bool make_gate_map(CUtensorMap *map, const float *base, int total_tokens, int H)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// CTAs of `kernel` resident on the whole device at once (0 if unknown), cached per device.
+// CTAs of `kernel` that fit on the whole device at once (0 if unknown), cached per device: the smallest of
+// what the SM's registers, shared memory (dynamic + static + the per-CTA reserve), threads and tensor
+// memory (512 columns, `tmem_cols` per CTA) allow, times the SM count.  Worked out here from the
+// kernel's attributes because the runtime's occupancy query answers 1 per SM for these kernels
+// although two or three of them run side by side on an SM.
 template <typename K>
-int resident_ctas(K kernel, int threads, int smem) {
+int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
     static std::mutex lock;
     static int cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     std::lock_guard<std::mutex> g(lock);
     if (!cached[dev]) {
-        int per_sm = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaFuncAttributes fa;
+        int sms = 0, smem_sm = 0, regs_sm = 0, thr_sm = 0, reserve = 0;
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return 0;
-        cached[dev] = per_sm * sms;
+        const int regs_cta = ((fa.numRegs + 7) / 8 * 8) * 32 * ((threads + 31) / 32);
+        int per_sm = smem_sm / (smem + (int)fa.sharedSizeBytes + reserve);
+        per_sm = std::min(per_sm, regs_sm / std::max(regs_cta, 1));
+        per_sm = std::min(per_sm, thr_sm / threads);
+        per_sm = std::min(per_sm, 512 / tmem_cols);
+        cached[dev] = std::max(per_sm, 0) * sms;
     }
     return cached[dev];
 }
@@ -1106,6 +1500,47 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
     cudaError_t e;
+    // The single-launch pipeline, when the chains are few enough to leave most CTAs for the chunk-parallel
+    // units (or when KDA_TC_FUSED=1 asks for it wherever it can run; KDA_TC_FUSED=0 turns it off).
+    const int n_state = num_seqs * H * kNTile;
+    const char *mode = getenv("KDA_TC_FUSED");
+    const bool allow = !(mode && mode[0] == '0');
+    const bool force = mode && mode[0] == '1';
+    if (allow && lay.max_slots > 0 && total_tokens > 0 && (force || n_state <= kFusedMaxChains)) {
+        const int smem_f = (int)fused_smem_bytes();
+        if ((e = cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f)))
+            return e;
+        cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+        const int resident = resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256);
+        if (resident >= n_state + kFusedMinWorkers) {
+            CUtensorMap mq, mk, mv, mg;
+            if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
+                !make_input_map(&mv, v, total_tokens, H) || !make_gate_map(&mg, g, total_tokens, H))
+                return cudaErrorInvalidValue;
+            if ((e = cudaMemsetAsync(w + lay.flags_off, 0, lay.flags_bytes, st))) return e;
+            int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
+            const size_t nflag = (size_t)lay.max_slots * H;
+            FusedArgs f;
+            f.S0 = S0;
+            f.S_final = S_final;
+            f.o = static_cast<__nv_bfloat16 *>(o);
+            f.ready = flags;
+            f.sdone = flags + nflag;
+            f.counter = flags + 2 * nflag;
+            f.n_state = n_state;
+            // outputs trail the preparations by about the chunk slots the workers hold at once, so that an
+            // output's chunk has usually passed the state pass when claimed while its record is still in L2
+            f.lag = max(2, (resident - n_state) / H + 1);
+            // One CTA per resident slot.  The state CTAs have the lowest indices, so they are placed first;
+            // worker CTAs take units from a counter, so one that starts late only finds less to do; and
+            // no wait outlasts its time bound even if a CTA could not be placed.
+            marks.before(st, "prefill_fused_tc");
+            prefill_fused_tc<<<(unsigned)resident, kPrepThreads, smem_f, st>>>(
+                mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, f);
+            return cudaGetLastError();
+        }
+    }
     if (lay.max_slots > 0 && total_tokens > 0) {
         CUtensorMap mq, mk, mv, mg;
         if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
@@ -1114,7 +1549,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         const int smem = PrepSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
             return e;
-        const int resident = resident_ctas(prefill_prepare_tc, kPrepThreads, smem);
+        cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+        const int resident = resident_ctas(prefill_prepare_tc, kPrepThreads, smem, 256);
         marks.before(st, "prefill_prepare_tc");
         prefill_prepare_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), kPrepThreads, smem, st>>>(
             mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, resident);
@@ -1131,7 +1568,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         const int smem_o = OutSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_o)))
             return e;
-        const int resident = resident_ctas(prefill_output_tc, 128, smem_o);
+        cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+        const int resident = resident_ctas(prefill_output_tc, 128, smem_o, 128);
         marks.before(st, "prefill_output_tc");
         prefill_output_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem_o, st>>>(
             cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,

@@ -126,6 +126,37 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
         : "memory");
 }
 
+// Waits until every committed bulk store has completed (its writes performed), or all but the most recent group.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all_but_last() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+// Orders this thread's global-memory accesses of the async proxy (bulk copies) with those of the generic proxy.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// GPU-scope release store / release add / acquire load of an int32 flag in global memory.
+__device__ __forceinline__ void st_release_gpu(int32_t *p, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_gpu_add(int32_t *p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Polls until *p >= v (acquire), giving up after timeout_ns; true if the value was seen.
+__device__ __forceinline__ bool wait_flag_geq(const int32_t *p, int32_t v, uint64_t timeout_ns = 2000000000ull) {
+    if (ld_acquire_gpu(p) >= v) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(32);
+            if (ld_acquire_gpu(p) >= v) return true;
+        }
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // Prefetches a 3-D tile into L2 (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
