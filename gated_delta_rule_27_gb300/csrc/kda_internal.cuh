@@ -138,8 +138,12 @@ struct Marks {
 // ---------------------------------------------------------------------------
 // Launchers (each returns cudaSuccess or the launch error).
 // ---------------------------------------------------------------------------
-cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st,
-                               Marks &marks);
+cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
+                               size_t clear_bytes, cudaStream_t st, Marks &marks);
+
+// Whether a tensor-core prefill of this shape runs as the single-launch pipeline (whose progress flags
+// must then be zeroed before it starts).
+bool tc_fused_plan(int num_seqs, int H, int total_tokens);
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
@@ -148,7 +152,7 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, cudaStream_t st, Marks &marks);
+                              float *S_final, void *ws, bool fused, cudaStream_t st, Marks &marks);
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st);

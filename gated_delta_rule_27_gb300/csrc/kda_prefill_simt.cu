@@ -33,15 +33,18 @@ constexpr int kThreads = 256;
 // ---------------------------------------------------------------------------
 // (1) chunk index: doc_slot0[i] = sum_{j<i} ceil(len_j / L), and validation of
 // cu_seqlens.  On invalid input every document gets zero chunks and the
-// status word is set, so the later kernels write nothing.
+// status word is set, so the later kernels write nothing.  Also zeroes
+// `clear_vec` 16-byte words at `clear` (the single-launch pipeline's progress
+// flags), when asked to.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_tokens, int L, int32_t *status,
-                   int32_t *doc_slot0) {
+                   int32_t *doc_slot0, uint4 *clear, int clear_vec) {
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ int s_carry;
     const int tid = threadIdx.x, nt = blockDim.x;
+    for (int i = tid; i < clear_vec; i += nt) clear[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         s_bad = (cu[0] != 0) || (cu[num_seqs] != total_tokens);
         s_carry = 0;
@@ -366,14 +369,17 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 }  // namespace
 
-cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, cudaStream_t st,
-                               Marks &marks) {
+cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
+                               size_t clear_bytes, cudaStream_t st, Marks &marks) {
     char *w = static_cast<char *>(ws);
     const size_t doc_off = 256;
-    const int threads = num_seqs >= 512 ? 1024 : (num_seqs >= 128 ? 256 : 64);
+    const int clear_vec = (int)(clear_bytes / 16);
+    const int busy = num_seqs > clear_vec ? num_seqs : clear_vec;
+    const int threads = busy >= 512 ? 1024 : (busy >= 128 ? 256 : 64);
     marks.before(st, "chunk_index");
     chunk_index_kernel<<<1, threads, 0, st>>>(cu, num_seqs, total_tokens, L, reinterpret_cast<int32_t *>(w),
-                                              reinterpret_cast<int32_t *>(w + doc_off));
+                                              reinterpret_cast<int32_t *>(w + doc_off), static_cast<uint4 *>(clear),
+                                              clear_vec);
     return cudaGetLastError();
 }
 

@@ -291,10 +291,12 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // One (chunk slot, head) of the preparation by a CTA of 256 threads whose 256 TMEM
 // columns start at `tmem`; `ph` is the parity of this unit's barrier phases (units
 // a CTA has prepared before, mod 2).  (nslot, nh) is a unit that is likely to
-// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  Returns
-// false after recording a timeout in the status word.
+// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  If
+// `publish` is set, the CTA's previous record is published there (release,
+// once its bulk stores are complete) as soon as this unit's loads are on
+// their way.  Returns false after recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
-                             uint32_t ph, uint32_t tmem, int nslot, int nh) {
+                             uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish = nullptr) {
     __shared__ float s_beta[kL];
     __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
     __shared__ __align__(16) float s_F[kD];
@@ -321,6 +323,11 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         tc::tma_load_3d(sm + PrepSmem::X + 24576, p.tm_q, 64, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V, p.tm_v, 0, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V + 8192, p.tm_v, 64, h, t0, &bars->load);
+        if (publish) {
+            tc::bulk_wait_all();
+            tc::fence_proxy_async_global();
+            tc::st_release_gpu(publish, 1);
+        }
     }
     if (tid < kL) s_beta[tid] = tid < Lc ? p.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     tc::tc_fence_before();
@@ -424,8 +431,8 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         uint8_t *Xp = sm + PrepSmem::X + (uint32_t)opanel * 16384u;
         uint8_t *Vp = sm + PrepSmem::V + (uint32_t)opanel * 8192u;
         uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)opanel * 8192u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {  // a loop, not unrolled: one copy of the body stays in the instruction cache
             const int r = orow + 16 * i;
             const bool valid = r < Lc;
             const float br = s_beta[r];
@@ -1142,6 +1149,7 @@ struct FusedStateSmem {
 };
 constexpr int kFusedMaxChains = 64;   // automatic choice: at most this many chains
 constexpr int kFusedMinWorkers = 32;  // CTAs left for the chunk-parallel units, at least
+constexpr int kFusedStaggerNs = 1400;  // about one step of the state pass
 constexpr size_t fused_smem_bytes() {
     return (PrepSmem::bytes > FusedStateSmem::bytes ? (PrepSmem::bytes > OutSmem::bytes ? PrepSmem::bytes : OutSmem::bytes)
                                                     : (FusedStateSmem::bytes > OutSmem::bytes ? FusedStateSmem::bytes
@@ -1160,6 +1168,7 @@ struct FusedArgs {
     int32_t *sdone;    // [slot * H + h]: column tiles whose state image is published
     int32_t *counter;  // next unit
     int n_state, lag;  // state CTAs; outputs trail the preparations by `lag` chunk slots
+    int stagger_ns;    // worker group g (H workers each) starts g * stagger_ns after the kernel
 };
 
 // Position u of the worker units -> (output?, slot, head): the first `lag` slots' preparations, then
@@ -1335,6 +1344,14 @@ __device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *s
     }
 }
 
+// Publishes a record this thread stored with bulk copies: release once the copies are complete.  The other
+// threads' direct stores to it are ordered before by the CTA barriers passed since.
+__device__ __forceinline__ void publish_record(int32_t *flag) {
+    tc::bulk_wait_all();
+    tc::fence_proxy_async_global();
+    tc::st_release_gpu(flag, 1);
+}
+
 __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *sm) {
     __shared__ PrepBars pbars;
     __shared__ OutBars obars;
@@ -1360,6 +1377,15 @@ __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *
     tc::tc_fence_after();
     const uint32_t tmem = tmem_base;
     uint32_t nprep = 0, nout = 0;
+    int32_t *pending = nullptr;  // the last record this CTA prepared, not yet published
+    if (tid == 0 && f.stagger_ns > 0) {
+        // Workers start in groups of H, one chain step apart: the first chunk slots are prepared by
+        // fewer CTAs at a time, so their records (which the state pass needs first) come out sooner,
+        // and the later groups fall into step behind them.
+        const uint64_t t_start = tc::globaltimer_ns();
+        const uint64_t delay = (uint64_t)((blockIdx.x - f.n_state) / H) * (uint64_t)f.stagger_ns;
+        while (tc::globaltimer_ns() - t_start < delay) __nanosleep(256);
+    }
     for (;;) {
         if (tid == 0) s_unit = atomicAdd(f.counter, 1);
         __syncthreads();
@@ -1370,16 +1396,14 @@ __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *
         decode_unit(u, C, H, f.lag, &out, &slot, &h);
         locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
         if (!out) {
-            const bool ok = prepare_unit(pp, slot, h, t0, Lc, sm, &pbars, nprep & 1u, tmem, -1, 0);
+            // the previous record is published once this unit's loads are issued; this one's stays pending
+            const bool ok = prepare_unit(pp, slot, h, t0, Lc, sm, &pbars, nprep & 1u, tmem, -1, 0, pending);
             ++nprep;
             if (!ok) break;
-            if (tid == 0) {
-                tc::bulk_wait_all();  // the record's bulk stores are complete
-                tc::fence_proxy_async_global();
-            }
-            __syncthreads();  // and so are the other threads' direct stores (gamma)
-            if (tid == 0) tc::st_release_gpu(f.ready + (size_t)slot * H + h, 1);
+            pending = f.ready + (size_t)slot * H + h;
         } else {
+            if (tid == 0 && pending) publish_record(pending);
+            pending = nullptr;
             if (tid == 0) {
                 // the record itself (its own publication) and every column tile's image of S_c
                 s_ok = tc::wait_flag_geq(f.ready + (size_t)slot * H + h, 1) &&
@@ -1397,6 +1421,7 @@ __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *
             if (!ok) break;
         }
     }
+    if (tid == 0 && pending) publish_record(pending);
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -1494,31 +1519,38 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
 
 }  // namespace
 
+bool tc_fused_plan(int num_seqs, int H, int total_tokens) {
+    // when the chains are few enough to leave most CTAs for the chunk-parallel units, or wherever it can run
+    // with KDA_TC_FUSED=1; KDA_TC_FUSED=0 turns it off
+    const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
+    const int n_state = num_seqs * H * kNTile;
+    const char *mode = getenv("KDA_TC_FUSED");
+    if ((mode && mode[0] == '0') || lay.max_slots <= 0 || total_tokens <= 0) return false;
+    if (!(mode && mode[0] == '1') && n_state > kFusedMaxChains) return false;
+    const int smem_f = (int)fused_smem_bytes();
+    if (cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f) != cudaSuccess)
+        return false;
+    cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+    return resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256) >= n_state + kFusedMinWorkers;
+}
+
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, cudaStream_t st, Marks &marks) {
+                              float *S_final, void *ws, bool fused, cudaStream_t st, Marks &marks) {
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
     cudaError_t e;
-    // The single-launch pipeline, when the chains are few enough to leave most CTAs for the chunk-parallel
-    // units (or when KDA_TC_FUSED=1 asks for it wherever it can run; KDA_TC_FUSED=0 turns it off).
-    const int n_state = num_seqs * H * kNTile;
-    const char *mode = getenv("KDA_TC_FUSED");
-    const bool allow = !(mode && mode[0] == '0');
-    const bool force = mode && mode[0] == '1';
-    if (allow && lay.max_slots > 0 && total_tokens > 0 && (force || n_state <= kFusedMaxChains)) {
+    // The single-launch pipeline (chosen by tc_fused_plan, its flags zeroed by the chunk index kernel).
+    if (fused) {
+        const int n_state = num_seqs * H * kNTile;
         const int smem_f = (int)fused_smem_bytes();
-        if ((e = cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f)))
-            return e;
-        cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
         const int resident = resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256);
-        if (resident >= n_state + kFusedMinWorkers) {
+        {
             CUtensorMap mq, mk, mv, mg;
             if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
                 !make_input_map(&mv, v, total_tokens, H) || !make_gate_map(&mg, g, total_tokens, H))
                 return cudaErrorInvalidValue;
-            if ((e = cudaMemsetAsync(w + lay.flags_off, 0, lay.flags_bytes, st))) return e;
             int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
             const size_t nflag = (size_t)lay.max_slots * H;
             FusedArgs f;
@@ -1532,6 +1564,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             // outputs trail the preparations by about the chunk slots the workers hold at once, so that an
             // output's chunk has usually passed the state pass when claimed while its record is still in L2
             f.lag = max(2, (resident - n_state) / H + 1);
+            f.stagger_ns = kFusedStaggerNs;
             // One CTA per resident slot.  The state CTAs have the lowest indices, so they are placed first;
             // worker CTAs take units from a counter, so one that starts late only finds less to do; and
             // no wait outlasts its time bound even if a CTA could not be placed.
