@@ -1282,10 +1282,10 @@ __device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *s
                     tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
                     tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
                     tc::bulk_commit();
-                    tc::bulk_wait_all_but_last();
-                    if (c > 0) {
+                    if (c > 1) {  // S_{c-2}'s image, stored two chunks ago: complete, publish it
+                        tc::bulk_wait_all_but_two();
                         tc::fence_proxy_async_global();
-                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 1) * H + h, 1);
+                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 2) * H + h, 1);
                     }
                     tc::bulk_wait_read();  // image c has been read: the epilogue of chunk c + 1 rewrites it
                 }
@@ -1294,7 +1294,8 @@ __device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *s
             if (lane == 0) {
                 tc::bulk_wait_all();
                 tc::fence_proxy_async_global();
-                tc::red_release_gpu_add(f.sdone + (size_t)(first + nchunks - 1) * H + h, 1);
+                for (int c = max(0, nchunks - 2); c < nchunks; ++c)
+                    tc::red_release_gpu_add(f.sdone + (size_t)(first + c) * H + h, 1);
             }
             __syncwarp();
         } else {

@@ -129,6 +129,7 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
 // Waits until every committed bulk store has completed (its writes performed), or all but the most recent group.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all_but_last() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all_but_two() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
 // Orders this thread's global-memory accesses of the async proxy (bulk copies) with those of the generic proxy.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
