@@ -187,26 +187,40 @@ def bench_prefill(libkda, steps, warmup, dev, rank):
         return libkda.kda_prefill_chunked_profiled(q, k, v, g, beta, cu, o, evs, S_final=S_final, workspace=ws,
                                                    chunk_size=w["chunk"])
 
+    def plain():
+        libkda.kda_prefill_chunked(q, k, v, g, beta, cu, o, S_final=S_final, workspace=ws, chunk_size=w["chunk"])
+
     warm_ev = new_events(nk)
     for _ in range(warmup):
         flush.zero_()
+        plain()
+        flush.zero_()
         one(warm_ev)
     torch.cuda.synchronize()
+    # the timed steps: plain calls, an event on each side of every call (after its L2 flush)
+    step_ev = [new_events(2) for _ in range(steps)]
     barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for i in range(steps):
         flush.zero_()
-        names = one(per_step[i])
+        step_ev[i][0].record()
+        plain()
+        step_ev[i][1].record()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_wall
+    step_ms = [step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(steps)]
+    # the per-kernel split: the same number of calls with an event before each kernel
+    for i in range(steps):
+        flush.zero_()
+        names = one(per_step[i])
+    torch.cuda.synchronize()
     n = len(names)
-    step_ms = [per_step[i][0].elapsed_time(per_step[i][n]) for i in range(steps)]
     kern_ms = {names[j]: [per_step[i][j].elapsed_time(per_step[i][j + 1]) for i in range(steps)] for j in range(n)}
     return dict(T=T, H=H, d=d, N=N, chunk=w["chunk"], step_ms=step_ms, kern_ms=kern_ms, names=names,
-                wall_s=wall_s, launches=n * steps, inp=inp)
+                wall_s=wall_s, launches=n * steps, inp=inp)  # launches: the timed steps' kernels
 
 
 def bench_e2e(libkda, steps, warmup, dev, inp):

@@ -44,6 +44,7 @@ chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_token
     __shared__ int s_warp[32];
     __shared__ int s_carry;
     const int tid = threadIdx.x, nt = blockDim.x;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next kernel may get ready meanwhile
     for (int i = tid; i < clear_vec; i += nt) clear[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         s_bad = (cu[0] != 0) || (cu[num_seqs] != total_tokens);

@@ -762,6 +762,8 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5;
     const int slot = blockIdx.x, h = blockIdx.y;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    tc::grid_dep_wait();    // the chunk index kernel's slot table
+    tc::grid_dep_launch();  // the state pass may get ready once every CTA of this grid has started
     int doc, t0, Lc;
     if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
     if (tid == 0) {
@@ -847,6 +849,8 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     __shared__ uint64_t full_bar[kNBuf], a_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
+    tc::grid_dep_wait();  // the preparation's records
+    tc::grid_dep_launch();
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1071,6 +1075,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     extern __shared__ uint8_t smem_raw[];
     __shared__ OutBars bars;
     __shared__ uint32_t tmem_base;
+    tc::grid_dep_wait();  // the state pass's images
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid input or an earlier timeout
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1434,6 +1439,7 @@ prefill_fused_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
                  char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, FusedArgs f) {
     extern __shared__ uint8_t smem_raw[];
+    tc::grid_dep_wait();  // the chunk index kernel: slots, status word, cleared flags
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const PrepParams pp{&tm_q, &tm_k, &tm_v, &tm_g, beta, cu, num_seqs, H, ws, doc_slot0_off, records_off, record_bytes};
@@ -1570,9 +1576,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             // worker CTAs take units from a counter, so one that starts late only finds less to do; and
             // no wait outlasts its time bound even if a CTA could not be placed.
             marks.before(st, "prefill_fused_tc");
-            prefill_fused_tc<<<(unsigned)resident, kPrepThreads, smem_f, st>>>(
-                mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, f);
-            return cudaGetLastError();
+            return launch_dependent(prefill_fused_tc, dim3((unsigned)resident), dim3(kPrepThreads), (size_t)smem_f, st,
+                                    mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
+                                    lay.record_bytes, f);
         }
     }
     if (lay.max_slots > 0 && total_tokens > 0) {
@@ -1587,17 +1593,19 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                              (int)cudaSharedmemCarveoutMaxShared);
         const int resident = resident_ctas(prefill_prepare_tc, kPrepThreads, smem, 256);
         marks.before(st, "prefill_prepare_tc");
-        prefill_prepare_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), kPrepThreads, smem, st>>>(
-            mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, resident);
-        if ((e = cudaGetLastError())) return e;
+        if ((e = launch_dependent(prefill_prepare_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(kPrepThreads),
+                                  (size_t)smem, st, mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off,
+                                  lay.records_off, lay.record_bytes, resident)))
+            return e;
     }
     if (num_seqs == 0) return cudaSuccess;
     const int smem = StateSmem::bytes + 1024;
     if ((e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
     marks.before(st, "prefill_state_tc");
-    prefill_state_tc<<<(unsigned)((size_t)num_seqs * H * kNTile), kStateThreads, smem, st>>>(
-        cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
-    if ((e = cudaGetLastError())) return e;
+    if ((e = launch_dependent(prefill_state_tc, dim3((unsigned)((size_t)num_seqs * H * kNTile)), dim3(kStateThreads),
+                              (size_t)smem, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off,
+                              lay.record_bytes)))
+        return e;
     if (lay.max_slots > 0 && total_tokens > 0) {
         const int smem_o = OutSmem::bytes + 1024;
         if ((e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_o)))
@@ -1606,10 +1614,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                              (int)cudaSharedmemCarveoutMaxShared);
         const int resident = resident_ctas(prefill_output_tc, 128, smem_o, 128);
         marks.before(st, "prefill_output_tc");
-        prefill_output_tc<<<dim3((unsigned)lay.max_slots, (unsigned)H), 128, smem_o, st>>>(
-            cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,
-            lay.record_bytes, resident);
-        if ((e = cudaGetLastError())) return e;
+        if ((e = launch_dependent(prefill_output_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(128),
+                                  (size_t)smem_o, st, cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w,
+                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, resident)))
+            return e;
     }
     return cudaSuccess;
 }

@@ -158,6 +158,12 @@ __device__ __forceinline__ bool wait_flag_geq(const int32_t *p, int32_t v, uint6
     }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
+// while its predecessor in the stream finishes; grid_dep_wait() returns once the predecessor has completed
+// and its writes are visible.  grid_dep_launch() lets the successor start before this kernel ends.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Prefetches a 3-D tile into L2 (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
