@@ -849,8 +849,8 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     __shared__ uint64_t full_bar[kNBuf], a_bar;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
-    tc::grid_dep_wait();  // the preparation's records
-    tc::grid_dep_launch();
+    // (the chunk index kernel's table and status word are complete: the preparation waited for them before
+    // letting this kernel start)
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -883,6 +883,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             tc::mbar_init(&a_bar, 2);  // one commit from each issuer
             tc::fence_mbar_init();
             s_abort = 0;
+            tc::grid_dep_wait();  // the preparation has completed: its records are visible
             for (int c = 0; c < kNBuf - 1 && c < nchunks; ++c)
                 issue_record(sm + c * StateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[c]);
         }
@@ -893,6 +894,9 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         tc::tc_fence_before();
         __syncthreads();
         tc::tc_fence_after();
+        // Only now (after this CTA's wait for the preparation) may the output pass start: it reads the
+        // preparation's part of each record before it waits for this kernel.
+        tc::grid_dep_launch();
         // TMEM: M' S over the two K panels in cols 0..31 and 32..63
         const uint32_t tmem = tmem_base;
 
@@ -1000,17 +1004,19 @@ struct OutSmem {
 };
 
 struct OutBars {
-    uint64_t load, mma;
+    uint64_t load, sload, mma;  // the record's Qp, P, Ut; its state image; the MMAs
 };
 
 // One (chunk slot, head) of the output pass, t0 / Lc the chunk's first token and
 // length, by a CTA of >= 128 threads (warps 0-1 write the 64 token rows) whose
 // TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's barrier
-// phases.  The record must be complete, S included.  Returns false after
-// recording a timeout in the status word.
+// phases.  P Ut is formed first; with `dep_wait` the state image is then
+// awaited through the launch dependency (the state pass is the previous
+// kernel), else it must already be complete.  Returns false after recording a
+// timeout in the status word.
 __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
-                            OutBars *bars, uint32_t ph, uint32_t tmem) {
+                            OutBars *bars, uint32_t ph, uint32_t tmem, bool dep_wait = false) {
     __shared__ int s_ok;
     const int tid = threadIdx.x, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
@@ -1019,23 +1025,32 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
                   "output pass loads the record tail as one image");
     const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
     if (tid == 0) {
-        tc::mbar_arrive_expect_tx(&bars->load, OutSmem::bytes);
-        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::bytes, &bars->load);
-        const bool ok = tc::mbar_wait(&bars->load, ph);
+        // Qp, P, Ut (written by the preparation) ...
+        tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
+        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
+        bool ok = tc::mbar_wait(&bars->load, ph);
+        constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+        constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
+        constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint32_t id_k = tc::idesc_bf16_f32(128, 128, false, false);
+        if (ok) {
+            tc::tc_fence_after();
+            for (int s = 0; s < 4; ++s)  // P Ut over the chunk's tokens
+                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::P + s * 32)),
+                             tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::Ut + s * 32)), id_k, s > 0);
+        }
+        // ... then the image of S_c (written by the state pass)
+        if (dep_wait) tc::grid_dep_wait();
+        tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
+        tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+        ok = tc::mbar_wait(&bars->sload, ph) && ok;
         s_ok = ok;
         if (ok) {
             tc::tc_fence_after();
-            constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-            constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
-            constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, false);
-            constexpr uint32_t id_k = tc::idesc_bf16_f32(128, 128, false, false);
-            for (int s = 0; s < 8; ++s)  // Qp S_c over d_k
+            for (int s = 0; s < 8; ++s)  // + Qp S_c over d_k
                 tc::mma_bf16(tmem, tc::smem_desc(kQpMn, tc::smem_u32(sm + OutSmem::Qp + s * 2048)),
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::S + (s >> 2) * 16384 + (s & 3) * 32)),
-                             id_mn, s > 0);
-            for (int s = 0; s < 4; ++s)  // + P Ut over the chunk's tokens
-                tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::P + s * 32)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::Ut + s * 32)), id_k, true);
+                             id_mn, true);
         }
         tc::mma_commit(&bars->mma);  // arrives at once when nothing was issued
     }
@@ -1075,7 +1090,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     extern __shared__ uint8_t smem_raw[];
     __shared__ OutBars bars;
     __shared__ uint32_t tmem_base;
-    tc::grid_dep_wait();  // the state pass's images
+    // (the chunk index kernel's table and status word are complete: the state pass waited for them)
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid input or an earlier timeout
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1085,6 +1100,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
     if (tid == 0) {
         tc::mbar_init(&bars.load, 1);
+        tc::mbar_init(&bars.sload, 1);
         tc::mbar_init(&bars.mma, 1);
         tc::fence_mbar_init();
         // the CTA that takes this one's place next (CTAs start in launch order): its record into L2
@@ -1101,7 +1117,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base);
+    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, true);
     if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
 }
 
@@ -1371,6 +1387,7 @@ __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *
     if (tid == 0) {
         prep_bars_init(&pbars);
         tc::mbar_init(&obars.load, 1);
+        tc::mbar_init(&obars.sload, 1);
         tc::mbar_init(&obars.mma, 1);
         tc::fence_mbar_init();
     }
