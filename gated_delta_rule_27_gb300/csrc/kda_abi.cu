@@ -73,14 +73,15 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
         return KDA_ERR_INVALID_ARG;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool fused = path == kda::PATH_TC && kda::tc_fused_plan(num_seqs, H, total_tokens);
+    const kda::TcPlan plan = path == kda::PATH_TC ? kda::tc_plan(num_seqs, H, total_tokens) : kda::TC_THREE;
+    const bool flags = plan != kda::TC_THREE;
     cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace,
-                                            fused ? static_cast<char *>(workspace) + lay.flags_off : nullptr,
-                                            fused ? lay.flags_bytes : 0, s, marks);
+                                            flags ? static_cast<char *>(workspace) + lay.flags_off : nullptr,
+                                            flags ? lay.flags_bytes : 0, s, marks);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (path == kda::PATH_TC)
         e = kda::launch_prefill_tc(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, S0, o, S_final, workspace,
-                                   fused, s, marks);
+                                   plan, s, marks);
     else
         e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0,
                                      o, S_final, workspace, s, marks);

@@ -159,9 +159,11 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
                                size_t clear_bytes, cudaStream_t st, Marks &marks);
 
-// Whether a tensor-core prefill of this shape runs as the single-launch pipeline (whose progress flags
-// must then be zeroed before it starts).
-bool tc_fused_plan(int num_seqs, int H, int total_tokens);
+// Launch plans of the tensor-core prefill: three kernels (preparation, state, output); the single-launch
+// pipeline; or the preparation followed by one launch running the state chains with the output units
+// alongside.  The last two need the workspace's progress flags zeroed before they start.
+enum TcPlan { TC_THREE = 0, TC_FUSED = 1, TC_CHAIN = 2 };
+TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
@@ -170,7 +172,7 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, bool fused, cudaStream_t st, Marks &marks);
+                              float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks);
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st);

@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -792,13 +793,13 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
 constexpr int kNBuf = 4;  // record buffers: chunks c + 1 .. c + 3 stream in while chunk c computes
-constexpr int kNSb = 3;   // bf16 state images: multiplied (and copied out), being written, spare
+constexpr int kNSb = 5;   // bf16 state images: multiplied, being written, up to three awaiting their copy out
 struct StateSmem {
     static constexpr uint32_t kBuf = 43008;  // M' and gamma (33 KB) + this CTA's Bc tile (8 KB), 1 KB aligned
     static constexpr uint32_t Mc = 0, gam = 32768, Bc = 33792;
-    // S^T operand, K-major [32 rows][128 K] in 2 panels of 4 KB, a ring of three: chunk c's MMAs
-    // read image c % 3, which is also copied to chunk c's record for the output pass, while the
-    // epilogue writes image (c + 1) % 3.
+    // S^T operand, K-major [32 rows][128 K] in 2 panels of 4 KB, a ring of kNSb: chunk c's MMAs
+    // read image c % kNSb, which the publisher warp also copies to chunk c's record for the output
+    // pass, while the epilogue writes image (c + 1) % kNSb.
     static constexpr uint32_t SB = kNBuf * kBuf;
     static constexpr uint32_t bytes = SB + kNSb * 8192;
 };
@@ -830,23 +831,32 @@ __device__ __forceinline__ void store_state_half(uint8_t *SB, int i, int h, cons
     }
 }
 
-// One CTA per (document, head, 32-column tile of S), 320 threads:
+// One CTA per (document, head, 32-column tile of S), 352 threads:
 //   warps 0-7   epilogue: thread <-> state row i = 32 (w % 4) + lane (its TMEM lane) and column half
 //               h = w / 4; S[i][16 h ..] stays fp32 in registers
-//   warps 8, 9  lane 0 issues M' S over K panel w - 8 of S; warp 9 also copies each chunk's S image
-//               to its record and keeps records streaming three chunks ahead
+//   warps 8, 9  lane 0 issues M' S over K panel w - 8 of S; warp 9 also keeps records streaming
+//               three chunks ahead
+//   warp 10     publisher: copies each chunk's S image to its record and, when asked, publishes it
 // Per chunk c:  issuers (after the epilogue warps' arrival on the operand barrier) -> MMAs ->
-// a_bar -> epilogue S <- gamma S + Bc + M' S, image of S_{c+1} -> arrival on the operand barrier.
+// a_bar -> epilogue S <- gamma S + Bc + M' S, image of S_{c+1} -> arrival on the operand barrier
+// and on img_full.  The publisher hands each image slot back through img_free; it runs behind the
+// chain by up to kNSb - 2 images without holding it up.
 constexpr int kStateEpiWarps = 8;
-constexpr int kStateThreads = (kStateEpiWarps + 2) * 32;
+constexpr int kStatePubWarp = kStateEpiWarps + 2;
+constexpr int kStateThreads = (kStatePubWarp + 1) * 32;
 constexpr uint32_t kBarOperand = 1;  // named barrier: the next S image is complete
+constexpr int kBarOperandThreads = (kStateEpiWarps + 2) * 32;  // epilogue and issuer warps
+constexpr int kStatePubLag = 2;    // images are published once the copy two chunks later is issued ...
+constexpr int kStatePubBatch = 4;  // ... four at a time, behind one release fence
+constexpr int kChainOutGroups = 2;  // output groups of 128 threads in each non-chain CTA of the chain plan
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
-                 float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
-                 size_t record_bytes) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[kNBuf], a_bar;
+// Chain j (document, head, column tile) by a CTA of kStateThreads threads over `smem_raw` (StateSmem).
+// With `sdone` set, each chunk's state image is also published there (release, count per (slot, head))
+// once its copy to the record is complete, for output units running alongside.
+__device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
+                            float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off,
+                            size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw, int32_t *sdone) {
+    __shared__ uint64_t full_bar[kNBuf], a_bar, img_full[kNSb], img_free[kNSb];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     // (the chunk index kernel's table and status word are complete: the preparation waited for them before
@@ -854,11 +864,12 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issuer = warp >= kStateEpiWarps;
+    const bool epi = warp < kStateEpiWarps;
+    const bool issuer = warp == kStateEpiWarps || warp == kStateEpiWarps + 1;
     const int i = (warp & 3) * 32 + lane, hcol = (warp >> 2) & 1;
-    const int tile = blockIdx.x % kNTile;
-    const int h = (blockIdx.x / kNTile) % H;
-    const int n = blockIdx.x / (kNTile * H);
+    const int tile = j % kNTile;
+    const int h = (j / kNTile) % H;
+    const int n = j / (kNTile * H);
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
     const int col0 = tile * kTile + 16 * hcol;
@@ -867,20 +878,24 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
 
     float S[16];
 #pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-        const float4 v = (S0 && !issuer) ? *reinterpret_cast<const float4 *>(S0 + state_off + j)
+    for (int c4 = 0; c4 < 16; c4 += 4) {
+        const float4 v = (S0 && epi) ? *reinterpret_cast<const float4 *>(S0 + state_off + c4)
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+        S[c4] = v.x; S[c4 + 1] = v.y; S[c4 + 2] = v.z; S[c4 + 3] = v.w;
     }
     bool ok = true;
     if (nchunks > 0) {
-        if (!issuer) store_state_half(sm + StateSmem::SB, i, hcol, S);
+        if (epi) store_state_half(sm + StateSmem::SB, i, hcol, S);
         tc::fence_async_smem();
         char *rec_h = ws + records_off + (size_t)h * record_bytes;  // record of (slot 0, head h)
         const size_t rec_stride = (size_t)H * record_bytes;          // one chunk slot further
         if (tid == 0) {
             for (int b = 0; b < kNBuf; ++b) tc::mbar_init(&full_bar[b], 1);
             tc::mbar_init(&a_bar, 2);  // one commit from each issuer
+            for (int b = 0; b < kNSb; ++b) {
+                tc::mbar_init(&img_full[b], kStateEpiWarps);  // one arrival per epilogue warp
+                tc::mbar_init(&img_free[b], 1);               // the publisher's
+            }
             tc::fence_mbar_init();
             s_abort = 0;
             tc::grid_dep_wait();  // the preparation has completed: its records are visible
@@ -908,7 +923,7 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 const int bsel = c % kNBuf;
                 uint8_t *buf = sm + bsel * StateSmem::kBuf;
                 uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c % kNSb) * 8192u;
-                if (c > 0) tc::named_barrier(kBarOperand, kStateThreads);  // S_c's image is complete
+                if (c > 0) tc::named_barrier(kBarOperand, kBarOperandThreads);  // S_c's image is complete
                 tc::tc_fence_after();
                 if (lane == 0) {
                     ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
@@ -920,12 +935,6 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                     }
                     tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
                     if (panel == 1 && ok) {
-                        // S_c's image, tile rows of both panels, into chunk c's record
-                        char *rec = rec_h + (size_t)(first + c) * rec_stride;
-                        tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
-                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
-                        tc::bulk_commit();
-                        tc::bulk_wait_read_but_last();  // image c - 1 is free again for chunk c + 1's epilogue
                         // the buffer chunk c - 1 used was released by the operand barrier of this chunk
                         const int cn = c + kNBuf - 1;
                         if (cn < nchunks)
@@ -935,7 +944,41 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 }
                 __syncwarp();
             }
-            if (lane == 0 && panel == 1) tc::bulk_wait_read();  // shared memory must outlive the image copies
+        } else if (warp == kStatePubWarp) {
+            if (lane == 0) {
+                int pub = 0;  // images published so far
+                for (int c = 0; c < nchunks; ++c) {
+                    const int sl = c % kNSb;
+                    // image 0 was written before the CTA barrier; image c >= 1 by chunk c - 1's epilogue
+                    if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / kNSb) & 1));
+                    if (ok) {
+                        // S_c's image, tile rows of both panels, into chunk c's record
+                        const uint8_t *sbc = sm + StateSmem::SB + (uint32_t)sl * 8192u;
+                        char *rec = rec_h + (size_t)(first + c) * rec_stride;
+                        tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
+                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
+                        tc::bulk_commit();
+                        tc::bulk_wait_read();  // the slot may be rewritten
+                    }
+                    tc::mbar_arrive(&img_free[sl]);  // always: the epilogue counts on one per image
+                    if (ok && sdone && c + 1 - kStatePubLag - pub >= kStatePubBatch) {
+                        // the copies of S_pub .. S_{c-2} have completed: publish them
+                        static_assert(kStatePubLag == 2, "wait_group below");
+                        tc::bulk_wait_all_but_two();
+                        tc::fence_proxy_async_global();
+                        tc::fence_acq_rel_gpu();
+                        for (; pub <= c - kStatePubLag; ++pub)
+                            tc::red_relaxed_gpu_add(sdone + (size_t)(first + pub) * H + h, 1);
+                    }
+                }
+                tc::bulk_wait_all();  // shared memory must outlive the image copies
+                if (sdone && ok) {
+                    tc::fence_proxy_async_global();
+                    tc::fence_acq_rel_gpu();
+                    for (; pub < nchunks; ++pub) tc::red_relaxed_gpu_add(sdone + (size_t)(first + pub) * H + h, 1);
+                }
+            }
+            __syncwarp();
         } else {
             const uint32_t tacc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 16u * (uint32_t)hcol;
             for (int c = 0; c < nchunks; ++c) {
@@ -944,6 +987,9 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 // gamma and this thread's 16 Bc values, read while the MMAs run
                 ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
                 const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+                const int nb = c + 1;                // the image this chunk writes: S_{c+1}, needed by chunk c + 1
+                const bool img = nb < nchunks;
+                uint8_t *sbn = sm + StateSmem::SB + (uint32_t)(nb % kNSb) * 8192u;
                 float bc[16];
                 {
                     const uint8_t *brow = buf + StateSmem::Bc + i * 64;
@@ -955,6 +1001,8 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
 #pragma unroll
                     for (int u = 0; u < 8; ++u) bc[8 + u] = f[u];
                 }
+                // the slot's previous image, S_{c+1-kNSb}, has been copied out
+                if (img && nb >= kNSb) ok = ok && tc::mbar_wait(&img_free[nb % kNSb], (uint32_t)((nb / kNSb - 1) & 1));
                 ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
                 tc::tc_fence_after();
                 if (warp_all(ok)) {
@@ -962,11 +1010,15 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                     tc::tmem_ld16x2(tacc, tacc + 32u, t0, t1);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t0[j] + t1[j]));
-                    store_state_half(sm + StateSmem::SB + (uint32_t)((c + 1) % kNSb) * 8192u, i, hcol, S);
+                    if (img) store_state_half(sbn, i, hcol, S);
                 }
                 tc::fence_async_smem();
                 tc::tc_fence_before();
-                if (c + 1 < nchunks) tc::named_barrier_arrive(kBarOperand, kStateThreads);
+                if (img) {
+                    tc::named_barrier_arrive(kBarOperand, kBarOperandThreads);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&img_full[nb % kNSb]);
+                }
             }
         }
         if (!ok) s_abort = 1;
@@ -982,11 +1034,20 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         if (warp == 0) tc::tmem_dealloc(tmem, 64);
         if (s_abort) return;
     }
-    if (S_final && !issuer) {
+    if (S_final && epi) {
 #pragma unroll
         for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<float4 *>(S_final + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
+}
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
+                 float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
+                 size_t record_bytes) {
+    extern __shared__ uint8_t smem_raw[];
+    state_chain(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x, smem_raw,
+                nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1007,18 +1068,31 @@ struct OutBars {
     uint64_t load, sload, mma;  // the record's Qp, P, Ut; its state image; the MMAs
 };
 
+// A group of 128 threads of a CTA: thread `gtid` of it, synchronised by named
+// barrier `gbar` (0: the whole CTA is the group, __syncthreads).
+struct OutGroup {
+    int gtid;
+    uint32_t gbar;
+    int *ok;  // shared word of the group
+    __device__ __forceinline__ void sync() const {
+        if (gbar == 0) __syncthreads();
+        else tc::named_barrier(gbar, 128);
+    }
+};
+
 // One (chunk slot, head) of the output pass, t0 / Lc the chunk's first token and
-// length, by a CTA of >= 128 threads (warps 0-1 write the 64 token rows) whose
-// TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's barrier
-// phases.  P Ut is formed first; with `dep_wait` the state image is then
-// awaited through the launch dependency (the state pass is the previous
-// kernel), else it must already be complete.  Returns false after recording a
+// length, by a group of 128 threads (warps 0-1 of it write the 64 token rows)
+// whose TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's
+// barrier phases.  P Ut is formed first; the state image is then awaited
+// through the launch dependency with `dep_wait` (the state pass is the
+// previous kernel), or through its publication count at `sflag` (all column
+// tiles), else it must already be complete.  Returns false after recording a
 // timeout in the status word.
 __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
-                            OutBars *bars, uint32_t ph, uint32_t tmem, bool dep_wait = false) {
-    __shared__ int s_ok;
-    const int tid = threadIdx.x, warp = tid >> 5;
+                            OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, bool dep_wait = false,
+                            const int32_t *sflag = nullptr) {
+    const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
                       R.S - R.Qp == OutSmem::S,
@@ -1041,10 +1115,14 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
         }
         // ... then the image of S_c (written by the state pass)
         if (dep_wait) tc::grid_dep_wait();
+        if (sflag) {
+            ok = tc::wait_flag_geq(sflag, kNTile) && ok;
+            tc::fence_proxy_async_global();
+        }
         tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
         tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
         ok = tc::mbar_wait(&bars->sload, ph) && ok;
-        s_ok = ok;
+        *grp.ok = ok;
         if (ok) {
             tc::tc_fence_after();
             for (int s = 0; s < 8; ++s)  // + Qp S_c over d_k
@@ -1077,8 +1155,8 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
         }
     }
     tc::tc_fence_before();
-    __syncthreads();
-    const bool ok = s_ok != 0;
+    grp.sync();
+    const bool ok = *grp.ok != 0;
     if (tid == 0 && !ok) flag_timeout(ws);
     return ok;
 }
@@ -1117,8 +1195,91 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, true);
+    __shared__ int s_ok;
+    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base,
+                OutGroup{tid, 0u, &s_ok}, true);
     if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
+}
+
+// ---------------------------------------------------------------------------
+// State pass with the output pass alongside (one launch after the preparation)
+// ---------------------------------------------------------------------------
+// One CTA per SM.  CTAs [0, n_state) run one chain each (state_chain, which
+// publishes each chunk's state image); in each of the others, two groups of
+// 128 threads take output units in chunk order from a counter, form P Ut at
+// once and Qp S_c as soon as all of S_c's column tiles are published, so that
+// one group's loads overlap the other's products and stores.  Output groups wait only for
+// chain CTAs, which have the lowest indices and are placed first; every wait is
+// bounded.
+__global__ void __launch_bounds__(kStateThreads, 1)
+prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
+                 float *__restrict__ S_final, __nv_bfloat16 *__restrict__ o, char *__restrict__ ws,
+                 size_t doc_slot0_off, size_t records_off, size_t record_bytes, int n_state, int32_t *sdone,
+                 int32_t *counter) {
+    extern __shared__ uint8_t smem_raw[];
+    if ((int)blockIdx.x < n_state) {
+        state_chain(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
+                    smem_raw, sdone);
+        return;
+    }
+    constexpr int kGroups = kChainOutGroups;
+    static_assert(kGroups * 128 <= kStateThreads && kGroups * OutSmem::bytes + 1024 <= StateSmem::bytes + 1024 &&
+                      OutSmem::bytes % 1024 == 0,
+                  "output groups fit the chain CTA");
+    __shared__ OutBars bars[kGroups];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_unit[kGroups], s_uok[kGroups];
+    // (the chunk index kernel's table and status word are complete: the preparation waited for them)
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    uint8_t *sm = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int g = tid >> 7;  // output group; threads of groups >= kGroups only take part in setup and teardown
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    const int units = doc_slot0[num_seqs] * H;
+    const int workers = ((int)gridDim.x - n_state) * kGroups;
+    if (tid == 0) {
+        for (int b = 0; b < kGroups; ++b) {
+            tc::mbar_init(&bars[b].load, 1);
+            tc::mbar_init(&bars[b].sload, 1);
+            tc::mbar_init(&bars[b].mma, 1);
+        }
+        tc::fence_mbar_init();
+        tc::grid_dep_wait();  // the preparation has completed: Qp, P, Ut of every record are visible
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 128 * kGroups);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (g < kGroups) {
+        const OutGroup grp{tid & 127, 2u + (uint32_t)g, &s_uok[g]};
+        const uint32_t tmem = tmem_base + 128u * (uint32_t)g;
+        uint8_t *gsm = sm + (uint32_t)g * OutSmem::bytes;
+        for (uint32_t k = 0;; ++k) {
+            if (grp.gtid == 0) {
+                const int u = atomicAdd(counter, 1);
+                s_unit[g] = u;
+                // the unit some group will take one round later: its Qp, P, Ut into L2 meanwhile
+                const int un = u + workers;
+                if (un < units)
+                    tc::bulk_prefetch_l2(ws + records_off + (size_t)un * record_bytes + tc_record().Qp, OutSmem::S);
+            }
+            grp.sync();
+            const int u = s_unit[g];
+            if (u >= units) break;
+            const int slot = u / H, h = u % H;
+            int doc, t0, Lc;
+            locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
+            if (!output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
+                             grp, false, sdone + u))
+                break;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 128 * kGroups);
 }
 
 // ---------------------------------------------------------------------------
@@ -1171,6 +1332,8 @@ struct FusedStateSmem {
 constexpr int kFusedMaxChains = 64;   // automatic choice: at most this many chains
 constexpr int kFusedMinWorkers = 32;  // CTAs left for the chunk-parallel units, at least
 constexpr int kFusedStaggerNs = 1400;  // about one step of the state pass
+constexpr int kChainMinWorkers = 48;   // output CTAs alongside the chains, at least
+constexpr TcPlan kAutoPlan = TC_CHAIN;  // the plan for few chains
 constexpr size_t fused_smem_bytes() {
     return (PrepSmem::bytes > FusedStateSmem::bytes ? (PrepSmem::bytes > OutSmem::bytes ? PrepSmem::bytes : OutSmem::bytes)
                                                     : (FusedStateSmem::bytes > OutSmem::bytes ? FusedStateSmem::bytes
@@ -1303,10 +1466,10 @@ __device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *s
                     tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
                     tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
                     tc::bulk_commit();
-                    if (c > 1) {  // S_{c-2}'s image, stored two chunks ago: complete, publish it
-                        tc::bulk_wait_all_but_two();
+                    if (c > 3) {  // S_{c-4}'s image, stored four chunks ago: complete, publish it
+                        tc::bulk_wait_all_but_four();
                         tc::fence_proxy_async_global();
-                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 2) * H + h, 1);
+                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 4) * H + h, 1);
                     }
                     tc::bulk_wait_read();  // image c has been read: the epilogue of chunk c + 1 rewrites it
                 }
@@ -1315,7 +1478,7 @@ __device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *s
             if (lane == 0) {
                 tc::bulk_wait_all();
                 tc::fence_proxy_async_global();
-                for (int c = max(0, nchunks - 2); c < nchunks; ++c)
+                for (int c = max(0, nchunks - 4); c < nchunks; ++c)
                     tc::red_release_gpu_add(f.sdone + (size_t)(first + c) * H + h, 1);
             }
             __syncwarp();
@@ -1438,8 +1601,9 @@ __device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *
                 if (tid == 0) flag_timeout(pp.ws);
                 break;
             }
+            __shared__ int s_uok;
             const bool ok = output_unit(pp.cu, H, f.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, sm,
-                                        &obars, nout & 1u, tmem);
+                                        &obars, nout & 1u, tmem, OutGroup{tid, 0u, &s_uok});
             ++nout;
             if (!ok) break;
         }
@@ -1543,30 +1707,52 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
 
 }  // namespace
 
-bool tc_fused_plan(int num_seqs, int H, int total_tokens) {
-    // when the chains are few enough to leave most CTAs for the chunk-parallel units, or wherever it can run
-    // with KDA_TC_FUSED=1; KDA_TC_FUSED=0 turns it off
+// CTAs of the chain-and-output launch: one per SM (its shared memory allows no more), 0 if unknown.
+int chain_ctas() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
+        return 0;
+    return sms;
+}
+
+TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
+    // KDA_TC_PLAN = three | fused | chain picks a plan wherever it can run; KDA_TC_FUSED = 0 / 1 is the same
+    // as three / fused.  Otherwise: the single launch when the chains are few enough to leave most CTAs for
+    // the chunk-parallel units, else three kernels.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
+    if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int n_state = num_seqs * H * kNTile;
-    const char *mode = getenv("KDA_TC_FUSED");
-    if ((mode && mode[0] == '0') || lay.max_slots <= 0 || total_tokens <= 0) return false;
-    if (!(mode && mode[0] == '1') && n_state > kFusedMaxChains) return false;
+    const char *plan = getenv("KDA_TC_PLAN");
+    const char *fused_env = getenv("KDA_TC_FUSED");
+    int want = -1;  // -1 automatic
+    if (plan && !strcmp(plan, "three")) want = TC_THREE;
+    else if (plan && !strcmp(plan, "fused")) want = TC_FUSED;
+    else if (plan && !strcmp(plan, "chain")) want = TC_CHAIN;
+    else if (fused_env && fused_env[0] == '0') want = TC_THREE;
+    else if (fused_env && fused_env[0] == '1') want = TC_FUSED;
+    if (want == TC_THREE) return TC_THREE;
+    if (want == TC_CHAIN || (want < 0 && kAutoPlan == TC_CHAIN)) {
+        if (n_state + kChainMinWorkers <= chain_ctas()) return TC_CHAIN;
+        return TC_THREE;
+    }
+    if (want < 0 && n_state > kFusedMaxChains) return TC_THREE;
     const int smem_f = (int)fused_smem_bytes();
     if (cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f) != cudaSuccess)
-        return false;
+        return TC_THREE;
     cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
-    return resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256) >= n_state + kFusedMinWorkers;
+    return resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256) >= n_state + kFusedMinWorkers ? TC_FUSED
+                                                                                                     : TC_THREE;
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, bool fused, cudaStream_t st, Marks &marks) {
+                              float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks) {
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
     cudaError_t e;
-    // The single-launch pipeline (chosen by tc_fused_plan, its flags zeroed by the chunk index kernel).
-    if (fused) {
+    // The single-launch pipeline (chosen by tc_plan, its flags zeroed by the chunk index kernel).
+    if (plan == TC_FUSED) {
         const int n_state = num_seqs * H * kNTile;
         const int smem_f = (int)fused_smem_bytes();
         const int resident = resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256);
@@ -1617,6 +1803,16 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     if (num_seqs == 0) return cudaSuccess;
     const int smem = StateSmem::bytes + 1024;
+    if (plan == TC_CHAIN) {
+        if ((e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+        int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
+        const size_t nflag = (size_t)lay.max_slots * H;
+        const int n_state = num_seqs * H * kNTile;
+        marks.before(st, "prefill_chain_tc");
+        return launch_dependent(prefill_chain_tc, dim3((unsigned)chain_ctas()), dim3(kStateThreads), (size_t)smem, st,
+                                cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off,
+                                lay.records_off, lay.record_bytes, n_state, flags + nflag, flags + 2 * nflag);
+    }
     if ((e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
     marks.before(st, "prefill_state_tc");
     if ((e = launch_dependent(prefill_state_tc, dim3((unsigned)((size_t)num_seqs * H * kNTile)), dim3(kStateThreads),

@@ -130,6 +130,7 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all_but_last() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all_but_two() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all_but_four() { asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); }
 // Orders this thread's global-memory accesses of the async proxy (bulk copies) with those of the generic proxy.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
@@ -139,6 +140,12 @@ __device__ __forceinline__ void st_release_gpu(int32_t *p, int32_t v) {
 }
 __device__ __forceinline__ void red_release_gpu_add(int32_t *p, int32_t v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// A GPU-scope release fence and a relaxed add: the adds after one fence_acq_rel_gpu() publish every write
+// this thread made (or ordered, e.g. by fence_proxy_async_global) before the fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_relaxed_gpu_add(int32_t *p, int32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
     int32_t v;

@@ -1,11 +1,12 @@
-"""The two launch plans of the tensor-core prefill agree with the oracle and with each other.
+"""The launch plans of the tensor-core prefill agree with the oracle and with each other.
 
 bf16 inputs with d = 128 and 64-token chunks take the tensor-core path.  It runs
-either as three kernels (preparation, state pass, output) or, for calls with few
-(document, head, column tile) chains, as one cooperative launch that overlaps
-them; KDA_TC_FUSED=0 / 1 forces one plan.  Both perform the same arithmetic in
-the same order, so their results must be bitwise identical, and both must meet
-the bf16 tolerance against the fp64 oracle.
+as three kernels (preparation, state pass, output), as one launch that overlaps
+all three, or as the preparation followed by one launch running the state
+chains with the output units alongside; KDA_TC_PLAN (or KDA_TC_FUSED=0 / 1)
+forces a plan.  All perform the same arithmetic in the same order, so their
+results must be bitwise identical, and they must meet the bf16 tolerance
+against the fp64 oracle.
 """
 from __future__ import annotations
 
@@ -23,8 +24,11 @@ pytestmark = pytest.mark.gpu
 def _run(inp, plan, S0=None, poison=0x7F):
     """One call under the given launch plan, on a workspace whose every byte is `poison` beforehand, so that
     nothing a call reads before writing it can pass for a result."""
-    old = os.environ.get("KDA_TC_FUSED")
-    os.environ["KDA_TC_FUSED"] = plan
+    saved = {key: os.environ.pop(key, None) for key in ("KDA_TC_FUSED", "KDA_TC_PLAN")}
+    if plan in ("three", "fused", "chain"):
+        os.environ["KDA_TC_PLAN"] = plan
+    elif plan != "auto":
+        os.environ["KDA_TC_FUSED"] = plan
     try:
         q, k, v, g, beta, cu = to_device(inp)
         T, H, d = q.shape
@@ -38,10 +42,10 @@ def _run(inp, plan, S0=None, poison=0x7F):
         torch.cuda.synchronize()
         assert libkda.kda_prefill_check(ws) == 0
     finally:
-        if old is None:
-            del os.environ["KDA_TC_FUSED"]
-        else:
-            os.environ["KDA_TC_FUSED"] = old
+        for key, val in saved.items():
+            os.environ.pop(key, None)
+            if val is not None:
+                os.environ[key] = val
     return o, S
 
 
@@ -67,8 +71,11 @@ def test_fused_and_three_kernel_plans_agree(case):
     S0 = inp.S0
     o3, S3 = _run(inp, "0", S0, poison=0x00)
     of, Sf = _run(inp, "1", S0, poison=0x7F)
+    oc, Sc = _run(inp, "chain", S0, poison=0x5A)
     assert torch.equal(o3, of), (o3.float() - of.float()).abs().max().item()
     assert torch.equal(S3, Sf), (S3 - Sf).abs().max().item()
+    assert torch.equal(o3, oc), (o3.float() - oc.float()).abs().max().item()
+    assert torch.equal(S3, Sc), (S3 - Sc).abs().max().item()
     o_ref, S_ref, _ = oracle_prefill(inp, S0=S0)
     assert rel(of, o_ref) <= TOL[torch.bfloat16], rel(of, o_ref)
     assert rel(Sf, S_ref) <= TOL[torch.bfloat16], rel(Sf, S_ref)
@@ -92,3 +99,25 @@ def test_fused_plan_on_the_prefill_workload_twice():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     o3, S3 = _run(inp, "0")
     assert torch.equal(o3, outs[0][0]) and torch.equal(S3, outs[0][1])
+
+
+@pytest.mark.parametrize("plan", ["three", "fused", "chain"])
+def test_full_prefill_workload_on_poisoned_workspaces(plan):
+    """The prefill workload under each launch plan on a workspace poisoned with two different patterns: the
+    kernels overlap at their boundaries (and, in the single launch, hand records over through flags), so any
+    read of a record before it is written would show up as a difference."""
+    inp = workloads.workload_prefill("prefill")
+    o_a, S_a = _run(inp, plan, poison=0x00)
+    o_b, S_b = _run(inp, plan, poison=0x7F)
+    assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b)
+    o_ref, S_ref, _ = oracle_prefill(inp, heads=[0, 7, 15])
+    assert rel(o_a[:, [0, 7, 15]], o_ref) <= TOL[torch.bfloat16]
+    assert rel(S_a[:, [0, 7, 15]], S_ref) <= TOL[torch.bfloat16]
+
+
+def test_varlen_workload_on_poisoned_workspaces():
+    """The packed-varlen workload (1024 chains, so three kernels) on two differently poisoned workspaces."""
+    inp = workloads.workload_prefill("varlen")
+    o_a, S_a = _run(inp, "auto", poison=0x00)
+    o_b, S_b = _run(inp, "auto", poison=0x7F)
+    assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b)
