@@ -94,7 +94,7 @@ struct PrepSmem {
     // in-place scaling X is round 1's A operand, its k rows (panel stride
     // 16 KB) are round 2's MN-major A operand and its q rows round 3's.
     static constexpr uint32_t X = 0;
-    static constexpr uint32_t V = 32768;   // v tile (MN-major), beta v in place; then Ut^T, K-major [j][s]
+    static constexpr uint32_t V = 32768;   // v tile (MN-major) as loaded; then Ut^T, K-major [j][s]
     static constexpr uint32_t G = 49152;   // g fp32 [64][128] -> b (swizzled); then A, T, T(bf16); then Kend, W'^T
     static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB) and the identity (8 KB)
     static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
@@ -298,7 +298,7 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // their way.  Returns false after recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
                              uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish = nullptr) {
-    __shared__ float s_beta[kL];
+    __shared__ __align__(16) float s_beta[kL];
     __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
     __shared__ __align__(16) float s_F[kD];
     __shared__ __align__(16) float s_Em[kD];
@@ -430,37 +430,44 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         *reinterpret_cast<float4 *>(blv) = *reinterpret_cast<const float4 *>(s_blast + c0);
         *reinterpret_cast<float4 *>(blv + 4) = *reinterpret_cast<const float4 *>(s_blast + c0 + 4);
         uint8_t *Xp = sm + PrepSmem::X + (uint32_t)opanel * 16384u;
-        uint8_t *Vp = sm + PrepSmem::V + (uint32_t)opanel * 8192u;
         uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)opanel * 8192u;
+        // beta is not applied here: it scales A's rows as they leave TMEM and T's columns in T's bf16
+        // image, so that W' = T diag(beta) (k e1) and Ut = T diag(beta) v take k e1 and v as they are
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {  // a loop, not unrolled: one copy of the body stays in the instruction cache
             const int r = orow + 16 * i;
             const bool valid = r < Lc;
-            const float br = s_beta[r];
             const uint32_t off_k = tc::sw128_offset(r, ocol), off_q = tc::sw128_offset(64 + r, ocol);
-            float k8[8], q8[8], v8[8], xk[8], xq[8], y8[8], bv[8], ke[8];
+            float k8[8], q8[8], xk[8], xq[8], ke[8];
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
-            unpack8(*reinterpret_cast<const uint4 *>(Vp + off_k), v8);
             const float4 b0 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0));
             const float4 b1 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0 + 4));
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            if (!unsafe) {
+                float y8[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float d = bb[u] - bmv[u];
-                const float e1 = valid ? __expf(d) : 0.f;
-                const float inv = valid && !unsafe ? __expf(-d) : 0.f;
-                xk[u] = br * k8[u] * e1;
-                xq[u] = q8[u] * e1;
-                y8[u] = k8[u] * inv;
-                bv[u] = br * v8[u];
-                // Kend = k exp(b_last - b_r) <= |k|: via the bounded factors, or directly when unsafe
-                ke[u] = unsafe ? (valid ? k8[u] * __expf(blv[u] - bb[u]) : 0.f) : y8[u] * fv[u];
+                for (int u = 0; u < 8; ++u) {
+                    const float d = bb[u] - bmv[u];
+                    const float e1 = valid ? __expf(d) : 0.f;
+                    const float inv = valid ? __expf(-d) : 0.f;
+                    xk[u] = k8[u] * e1;
+                    xq[u] = q8[u] * e1;
+                    y8[u] = k8[u] * inv;
+                    ke[u] = y8[u] * fv[u];  // Kend = k exp(b_last - b_r) <= |k| via the bounded factors
+                }
+                *reinterpret_cast<uint4 *>(Yp + off_k) = pack8(y8);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {  // reference 0: exp(b_r) <= 1
+                    const float e1 = valid ? __expf(bb[u] - bmv[u]) : 0.f;
+                    xk[u] = k8[u] * e1;
+                    xq[u] = q8[u] * e1;
+                    ke[u] = valid ? k8[u] * __expf(blv[u] - bb[u]) : 0.f;
+                }
             }
             *reinterpret_cast<uint4 *>(Xp + off_k) = pack8(xk);
             *reinterpret_cast<uint4 *>(Xp + off_q) = pack8(xq);
-            if (!unsafe) *reinterpret_cast<uint4 *>(Yp + off_k) = pack8(y8);
-            *reinterpret_cast<uint4 *>(Vp + off_k) = pack8(bv);
             kend[i] = pack8(ke);
         }
     }
@@ -511,6 +518,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             for (int i = 0; i < 32; ++i) v[i] += v2[i];
             if (trow < 64) {
                 const int r = trow;
+                const float br = s_beta[r];  // A = diag(beta) (k e1)(k / e1)^T, strictly lower
 #pragma unroll
                 for (int qb = 0; qb < 2; ++qb) {
                     const int q4 = 2 * hs + qb;
@@ -519,10 +527,10 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
 #pragma unroll
                         for (int i = 0; i < 16; i += 4) {
                             float4 w;
-                            w.x = q4 * 16 + i + 0 < r ? v[qb * 16 + i + 0] : 0.f;
-                            w.y = q4 * 16 + i + 1 < r ? v[qb * 16 + i + 1] : 0.f;
-                            w.z = q4 * 16 + i + 2 < r ? v[qb * 16 + i + 2] : 0.f;
-                            w.w = q4 * 16 + i + 3 < r ? v[qb * 16 + i + 3] : 0.f;
+                            w.x = q4 * 16 + i + 0 < r ? br * v[qb * 16 + i + 0] : 0.f;
+                            w.y = q4 * 16 + i + 1 < r ? br * v[qb * 16 + i + 1] : 0.f;
+                            w.z = q4 * 16 + i + 2 < r ? br * v[qb * 16 + i + 2] : 0.f;
+                            w.w = q4 * 16 + i + 3 < r ? br * v[qb * 16 + i + 3] : 0.f;
                             *reinterpret_cast<float4 *>(dst + i) = w;
                         }
                     }
@@ -559,21 +567,26 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         return false;
     }
 
-    // triangular solve in fp32, then T as the bf16 round-2 B operand (K-major [r][s])
+    // triangular solve in fp32, then T diag(beta) as the bf16 round-2 B operand (K-major [r][s])
     float *Tf = reinterpret_cast<float *>(sm + PrepSmem::Tfp);
     unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), tid);
     {
-        const int r = tid >> 2, s0 = (tid & 3) * 16;
+        // thread (r, q) takes columns 16 q .. 16 q + 15 of row r (one row of a 16 x 16 block of T, absent
+        // above the diagonal blocks), four at a time in an order rotated by q: the four threads of a row
+        // then read distinct banks
+        const int r = tid >> 2, q = tid & 3;
         uint8_t *Tb = sm + PrepSmem::Tb;
+        const bool blk = q <= (r >> 4);
+        const float *trow = Tf + (blk ? tri_blk(r >> 4, q) + ((r & 15) << 4) : 0);
 #pragma unroll
-        for (int s8 = 0; s8 < 16; s8 += 8) {
-            float w[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int s = s0 + s8 + u;
-                w[u] = s <= r ? Tf[tri_idx(r, s)] : 0.f;
-            }
-            *reinterpret_cast<uint4 *>(Tb + tc::sw128_offset(r, s0 + s8)) = pack8(w);
+        for (int k = 0; k < 4; ++k) {
+            const int j = (k + q) & 3, s = 16 * q + 4 * j;
+            const float4 t = blk ? *reinterpret_cast<const float4 *>(trow + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = *reinterpret_cast<const float4 *>(s_beta + s);
+            uint2 pk;
+            pk.x = pack_bf16x2(s + 0 <= r ? t.x * b.x : 0.f, s + 1 <= r ? t.y * b.y : 0.f);
+            pk.y = pack_bf16x2(s + 2 <= r ? t.z * b.z : 0.f, s + 3 <= r ? t.w * b.w : 0.f);
+            *reinterpret_cast<uint2 *>(Tb + tc::sw128_offset(r, s)) = pk;
         }
     }
     tc::fence_async_smem();
@@ -585,7 +598,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         tc::bulk_commit();
     }
 
-    // round 2: W'^T = (T X_k)^T -> cols 64..127;  Ut^T = (T beta V)^T -> cols 128..191
+    // round 2: W'^T = (T diag(beta) X_k)^T -> cols 64..127;  Ut^T = (T diag(beta) V)^T -> cols 128..191
     if (lane == 0 && warp < 2) {  // warp 0: W', warp 1: Ut
         constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, true, false);
         const uint64_t amn = warp == 0 ? tc::smem_desc_base(16384, 1024, tc::SW_128B)
@@ -600,7 +613,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     ok = tc::mbar_wait(&bars->r2, ph);
     tc::tc_fence_after();
     if (warp_all(ok)) {
-        // warps 0-3: W'^T row c -> WT;  warps 4-7: Ut^T row c -> V (round 2 has consumed beta V)
+        // warps 0-3: W'^T row c -> WT;  warps 4-7: Ut^T row c -> V (round 2 has consumed V)
         float w[64];
         tc::tmem_ld64(tmem + lane_base + 64u + 64u * (uint32_t)hs, w);
         uint8_t *dst = sm + (hs ? PrepSmem::V : PrepSmem::WT);
