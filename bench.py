@@ -250,7 +250,7 @@ def bench_e2e(libkda, steps, warmup, dev, inp):
     comp_done = [torch.cuda.Event() for _ in range(nb)]
     out_done = [torch.cuda.Event() for _ in range(nb)]
 
-    def step(i):
+    def step(i, compute=True):
         b = i % nb
         for gi, (sg, members) in enumerate(zip(s_in, groups)):
             with torch.cuda.stream(sg):
@@ -263,8 +263,9 @@ def bench_e2e(libkda, steps, warmup, dev, inp):
             s_comp.wait_event(e)
         if i >= nb:
             s_comp.wait_event(out_done[b])  # step i - 2's results have left this output set
-        libkda.kda_prefill_chunked(*dbuf[b], o[b], S_final=S_final[b], workspace=ws, chunk_size=w["chunk"],
-                                   stream=s_comp)
+        if compute:
+            libkda.kda_prefill_chunked(*dbuf[b], o[b], S_final=S_final[b], workspace=ws, chunk_size=w["chunk"],
+                                       stream=s_comp)
         comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -272,19 +273,24 @@ def bench_e2e(libkda, steps, warmup, dev, inp):
             S_h[b].copy_(S_final[b], non_blocking=True)
             out_done[b].record(s_out)
 
-    for i in range(warmup):
-        step(i)
-    torch.cuda.synchronize()
-    ev = new_events(2)
-    ev[0].record(s_in[0])
-    for sg in s_in[1:]:
-        sg.wait_event(ev[0])
-    for i in range(steps):
-        step(i)
-    ev[1].record(s_out)
-    torch.cuda.synchronize()
-    ms = ev[0].elapsed_time(ev[1]) / steps
-    return dict(ms=ms, h2d=h2d, d2h=d2h, tokens=T)
+    def timed(compute):
+        for i in range(warmup):
+            step(i, compute)
+        torch.cuda.synchronize()
+        ev = new_events(2)
+        ev[0].record(s_in[0])
+        for sg in s_in[1:]:
+            sg.wait_event(ev[0])
+        for i in range(steps):
+            step(i, compute)
+        ev[1].record(s_out)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / steps
+
+    ms = timed(True)
+    # the same copies in the same pipeline without the prefill: the host link's floor for this step
+    copy_ms = timed(False)
+    return dict(ms=ms, copy_ms=copy_ms, h2d=h2d, d2h=d2h, tokens=T)
 
 
 def bench_decode(libkda, steps, warmup, dev):
@@ -442,7 +448,9 @@ def run_libkda(args):
             "roofline": roofline, "pass_roofline": pass_roofline, "decode": decode,
             "e2e": {"value": world * e2e["tokens"] / (max_over_ranks(e2e["ms"]) * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                    "ms_per_step": e2e["ms"],
+                    "ms_per_step": e2e["ms"], "copy_only_ms_per_step": e2e["copy_ms"],
+                    "link_gbs": (e2e["h2d"] + e2e["d2h"]) / (e2e["copy_ms"] * 1e-3) / 1e9,
+                    "frac_of_copy_floor": e2e["copy_ms"] / e2e["ms"],
                     "note": "pinned host inputs copied in and o, S_final copied out every step; consecutive "
                             "steps pipelined on copy-in / compute / copy-out streams"},
             "gpu_launches": pf["launches"], "clocks": clocks,
