@@ -142,6 +142,7 @@ KERNEL_SOURCES = {
     "prefill_state_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_output_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_fused_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_chain_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
 }
 
@@ -412,6 +413,8 @@ def run_libkda(args):
         dom_bytes = read_bytes
     elif "output" in dom:
         dom_bytes = o_bytes
+    elif "chain" in dom:  # the state pass and the outputs in one launch: S_final and o
+        dom_bytes = s_bytes + o_bytes
     elif "state" in dom:
         dom_bytes = s_bytes + (o_bytes if "simt" in dom else 0)
     else:
