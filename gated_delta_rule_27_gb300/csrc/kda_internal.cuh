@@ -29,7 +29,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 //   doc_slot0           int32 [num_seqs + 1]: first chunk slot of each document
 //                       (exclusive prefix sum of ceil(len / L)), 256-byte padded
 //   records             one per (chunk slot, head), `record_bytes` each
-//   flags               (tensor-core path) the single-launch pipeline's progress flags
+//   flags               (tensor-core path) progress flags of the chain and fused plans
 //
 // The number of chunk slots is bounded by total_tokens / L + num_seqs, so the
 // size depends only on the call's scalar arguments.
@@ -159,9 +159,9 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
                                size_t clear_bytes, cudaStream_t st, Marks &marks);
 
-// Launch plans of the tensor-core prefill: three kernels (preparation, state, output); the single-launch
-// pipeline; or the preparation followed by one launch running the state chains with the output units
-// alongside.  The last two need the workspace's progress flags zeroed before they start.
+// Launch plans of the tensor-core prefill: three kernels (preparation, state, output); one fused launch of
+// all three; or the preparation followed by one launch running the state chains with the output units
+// alongside (chain).  The last two need the workspace's progress flags zeroed before they start.
 enum TcPlan { TC_THREE = 0, TC_FUSED = 1, TC_CHAIN = 2 };
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 

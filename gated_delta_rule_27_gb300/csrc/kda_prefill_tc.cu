@@ -1730,8 +1730,8 @@ int chain_ctas() {
 
 TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     // KDA_TC_PLAN = three | fused | chain picks a plan wherever it can run; KDA_TC_FUSED = 0 / 1 is the same
-    // as three / fused.  Otherwise: the single launch when the chains are few enough to leave most CTAs for
-    // the chunk-parallel units, else three kernels.
+    // as three / fused.  Otherwise (kAutoPlan): the chain plan when the chains leave at least
+    // kChainMinWorkers SMs for the output groups, else three kernels.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int n_state = num_seqs * H * kNTile;
@@ -1764,7 +1764,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
     cudaError_t e;
-    // The single-launch pipeline (chosen by tc_plan, its flags zeroed by the chunk index kernel).
+    // The fused plan (chosen by tc_plan, its flags zeroed by the chunk index kernel).
     if (plan == TC_FUSED) {
         const int n_state = num_seqs * H * kNTile;
         const int smem_f = (int)fused_smem_bytes();

@@ -81,8 +81,8 @@ def test_fused_and_three_kernel_plans_agree(case):
     assert rel(Sf, S_ref) <= TOL[torch.bfloat16], rel(Sf, S_ref)
 
 
-def test_fused_plan_on_the_prefill_workload_twice():
-    """The prefill workload (which picks the single launch by itself) twice on one workspace: the progress
+def test_automatic_plan_on_the_prefill_workload_twice():
+    """The prefill workload (which picks the chain plan by itself) twice on one workspace: the progress
     flags start from zero every call, so both calls match bit for bit and the three-kernel plan."""
     inp = workloads.workload_prefill("prefill")
     q, k, v, g, beta, cu = to_device(inp)
@@ -104,7 +104,7 @@ def test_fused_plan_on_the_prefill_workload_twice():
 @pytest.mark.parametrize("plan", ["three", "fused", "chain"])
 def test_full_prefill_workload_on_poisoned_workspaces(plan):
     """The prefill workload under each launch plan on a workspace poisoned with two different patterns: the
-    kernels overlap at their boundaries (and, in the single launch, hand records over through flags), so any
+    kernels overlap at their boundaries (and, in the chain and fused plans, hand data over through flags), so any
     read of a record before it is written would show up as a difference."""
     inp = workloads.workload_prefill("prefill")
     o_a, S_a = _run(inp, plan, poison=0x00)
