@@ -126,9 +126,9 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
         : "memory");
 }
 
-// Waits until every committed bulk store has completed (its writes performed), or all but the most recent group.
+// Waits until every committed bulk store has completed (its writes performed), or all but the most recent
+// two or four groups.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all_but_last() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all_but_two() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all_but_four() { asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); }
 // Orders this thread's global-memory accesses of the async proxy (bulk copies) with those of the generic proxy.
@@ -193,10 +193,6 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Waits until every committed bulk store but the most recent group has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_but_last() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 
 // Named barrier over `count` threads (a multiple of 32) of the CTA.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
