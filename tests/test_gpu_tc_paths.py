@@ -121,3 +121,39 @@ def test_varlen_workload_on_poisoned_workspaces():
     o_a, S_a = _run(inp, "auto", poison=0x00)
     o_b, S_b = _run(inp, "auto", poison=0x7F)
     assert torch.equal(o_a, o_b) and torch.equal(S_a, S_b)
+
+
+def _kernel_names(inp, S0):
+    """The kernels the automatic plan launches for `inp` (from the profiled entry point)."""
+    q, k, v, g, beta, cu = to_device(inp)
+    T, H, d = q.shape
+    N = cu.numel() - 1
+    ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, 64, dev())
+    o = torch.empty_like(v)
+    S = torch.empty((N, H, d, d), device=dev())
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(libkda.PREFILL_MAX_KERNELS + 1)]
+    for e in events:
+        e.record()
+    names = libkda.kda_prefill_chunked_profiled(q, k, v, g, beta, cu, o, events, S0=S0.to(dev()), S_final=S,
+                                                workspace=ws, chunk_size=64)
+    torch.cuda.synchronize()
+    return names
+
+
+@pytest.mark.parametrize("extra_heads", [0, 1])
+def test_chain_plan_at_its_worker_threshold(extra_heads):
+    """One document with as many heads as leave exactly 48 CTAs beside the chains (4 column tiles a head),
+    the fewest output CTAs the automatic chain plan runs with, and one head more, where it falls back to
+    three kernels: the automatic choice is the expected plan, matches the three-kernel plan bit for bit
+    and meets the bf16 tolerance against the oracle."""
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    H = (sms - 48) // 4 + extra_heads
+    inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=77 + extra_heads, s0_std=0.1)
+    names = _kernel_names(inp, inp.S0)
+    assert ("prefill_chain_tc" in names) == (extra_heads == 0), names
+    o_a, S_a = _run(inp, "auto", inp.S0, poison=0x00)
+    o_3, S_3 = _run(inp, "three", inp.S0, poison=0x7F)
+    assert torch.equal(o_a, o_3) and torch.equal(S_a, S_3)
+    o_ref, S_ref, _ = oracle_prefill(inp, S0=inp.S0)
+    assert rel(o_a, o_ref) <= TOL[torch.bfloat16], rel(o_a, o_ref)
+    assert rel(S_a, S_ref) <= TOL[torch.bfloat16], rel(S_a, S_ref)
