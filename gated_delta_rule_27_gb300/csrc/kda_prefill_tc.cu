@@ -864,8 +864,9 @@ constexpr int kStatePubBatch = 4;  // ... four at a time, behind one release fen
 constexpr int kChainOutGroups = 2;  // output groups of 128 threads in each non-chain CTA of the chain plan
 
 // Chain j (document, head, column tile) by a CTA of kStateThreads threads over `smem_raw` (StateSmem).
-// With `sdone` set, each chunk's state image is also published there (release, count per (slot, head))
-// once its copy to the record is complete, for output units running alongside.
+// With `sdone` set, each chunk's state image is also published there (a count per (slot, head), raised
+// after a GPU-scope release fence, in batches of kStatePubBatch) once its copy to the record is complete,
+// for output units running alongside.
 __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                             float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off,
                             size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw, int32_t *sdone) {
