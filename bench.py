@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -123,14 +124,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # profile summaries committed under profiles/ (ncu DRAM traffic per launch)
 # ---------------------------------------------------------------------------
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed, so that an edit to a comment does not
+    count as a change of the kernel (the sources hold no string literal with a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(kernel_file: str) -> str:
+    """Hash of the code (comments excluded) of a kernel's source file and the two shared headers."""
     h = hashlib.sha256()
     for rel in (kernel_file, "gated_delta_rule_27_gb300/csrc/kda_internal.cuh",
                 "gated_delta_rule_27_gb300/csrc/kda_tc.cuh"):
         p = os.path.join(ROOT, rel)
         if os.path.exists(p):
-            with open(p, "rb") as f:
-                h.update(f.read())
+            with open(p, encoding="utf-8") as f:
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
