@@ -56,3 +56,13 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_entries_ignore_comment_edits():
+    """The source hash that keys the committed DRAM traffic per kernel covers the code only: a comment edit
+    keeps it, a code edit changes it (bench.py then reports the traffic as null)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    code = "int f(int x) {  // doubles x\n    /* body */ return 2 * x;\n}\n"
+    assert bench._code_only(code) == bench._code_only(code.replace("doubles x", "twice x").replace("body", "b"))
+    assert bench._code_only(code) != bench._code_only(code.replace("2 * x", "3 * x"))
