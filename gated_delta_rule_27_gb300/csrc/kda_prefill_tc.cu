@@ -1297,13 +1297,14 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
 }
 
 // ---------------------------------------------------------------------------
-// Single-launch pipeline: preparation, state pass and output overlapped
+// Fused plan (on request): preparation, state pass and output in one launch
 // ---------------------------------------------------------------------------
-// When a call has few (document, head, column tile) chains, one launch of
-// prefill_fused_tc, with as many CTAs as fit on the GPU at once, replaces the
-// three kernels above, so that the
-// state pass runs while later chunks are still being prepared and the outputs
-// are formed while their records are still in L2:
+// One launch of prefill_fused_tc, with as many CTAs as fit on the GPU at once,
+// replaces the three kernels above, so that the state pass runs while later
+// chunks are still being prepared and the outputs are formed while their
+// records are still in L2.  Its chains share their SMs with workers and step
+// more slowly than the chain plan's, which is why that plan is the automatic
+// choice for few chains:
 //   CTAs [0, n_state)  one chain each (the state pass above, 256 threads:
 //                      warps 0-3 epilogue with 32 columns per thread, warps 4-5
 //                      MMA issuers, warp 6 streams records in as they are
