@@ -776,6 +776,20 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5;
     const int slot = blockIdx.x, h = blockIdx.y;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    if (tid == 0 && num_seqs == 1 && (int)(blockIdx.y * gridDim.x + blockIdx.x) < resident) {
+        // First wave of a single document: chunk slot s starts at token 64 s, so this CTA's tiles (inputs
+        // of the call, complete before it) can be pulled into L2 while the chunk index kernel still runs
+        const int64_t tok = (int64_t)slot * kL;
+        if (tok < (int64_t)__ldg(cu + 1)) {
+            tc::tma_prefetch_3d(&tm_g, 0, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_k, 0, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_k, 64, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_q, 0, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_q, 64, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_v, 0, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_v, 64, h, (int)tok);
+        }
+    }
     tc::grid_dep_wait();    // the chunk index kernel's slot table
     tc::grid_dep_launch();  // the state pass may get ready once every CTA of this grid has started
     int doc, t0, Lc;
