@@ -36,3 +36,44 @@ def test_chunked_equals_recurrent_at_every_boundary(chunk, oracle_lib):
     assert oracle.rel_err(S_c, S_r) < 1e-10
     for (n, t), S in bounds.items():
         assert oracle.rel_err(S, snaps[snap.index(t), n]) < 1e-10
+
+
+def test_chunk_pair_composition(oracle_lib):
+    """The composition of two chunk steps, with odd-chunk outputs from the even chunk's incoming state.
+
+    This is the chunk-pair form that the design notes propose for halving the tensor-core state chain; it is
+    checked here in fp64 against the token loop. Per chunk, with G = diag(gamma), M = -Kend^T W and
+    Bc = Kend^T Ut, the step is S' = (G + M) S + Bc. Two steps compose to
+        S'' = G1 G0 S + N S + B2,  N = G1 M0 + M1 G0 + M1 M0,  B2 = (G1 + M1) Bc0 + Bc1,
+    and the second chunk's output needs no second state:
+        O1 = Q2 S + R,  Q2 = Qp1 (G0 + M0),  R = Qp1 Bc0 + P1 Ut1.
+    """
+    from tests.chunked_numpy import chunk_prepare
+    L, d, chunks = 8, 6, 7
+    q, k, v, g, beta, cu = _inputs(3, [L * chunks - 3], 1, d)  # three pairs and a ragged unpaired chunk
+    T = int(cu[-1])
+    rng = np.random.default_rng(4)
+    S0 = rng.standard_normal((1, 1, d, d)) * 0.1
+    snap = list(range(0, T, L))[1:] + [T]
+    o_r, S_r, snaps = oracle.run(q, k, v, g, beta, cu, S0=S0, snap_t=snap, lib=oracle_lib)
+    preps = [chunk_prepare(q[c0:c0 + L, 0], k[c0:c0 + L, 0], v[c0:c0 + L, 0], g[c0:c0 + L, 0], beta[c0:c0 + L, 0])
+             for c0 in range(0, T, L)]
+    step = [(np.diag(p["gamma"]), -p["Kend"].T @ p["W"], p["Kend"].T @ p["Ut"]) for p in preps]
+    S = S0[0, 0].copy()
+    o = np.zeros((T, d))
+    for c in range(0, len(preps), 2):
+        G0, M0, B0 = step[c]
+        o[c * L:(c + 1) * L] = preps[c]["Qp"] @ S + preps[c]["Oloc"]
+        if c + 1 == len(preps):  # an unpaired last chunk: one ordinary step
+            S = (G0 + M0) @ S + B0
+            break
+        G1, M1, B1 = step[c + 1]
+        Q2 = preps[c + 1]["Qp"] @ (G0 + M0)
+        R = preps[c + 1]["Qp"] @ B0 + preps[c + 1]["Oloc"]
+        o[(c + 1) * L:(c + 2) * L] = Q2 @ S + R
+        N = G1 @ M0 + M1 @ G0 + M1 @ M0
+        B2 = (G1 + M1) @ B0 + B1
+        S = G1 @ G0 @ S + N @ S + B2
+        assert oracle.rel_err(S, snaps[snap.index(min((c + 2) * L, T)), 0, 0]) < 1e-10
+    assert oracle.rel_err(o, o_r[:, 0]) < 1e-10
+    assert oracle.rel_err(S, S_r[0, 0]) < 1e-10
