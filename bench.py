@@ -2,20 +2,24 @@
 
 One step = one kda_prefill_chunked pass over the prefill workload (B=1,
 H=16, T=4096, d=128, bf16 q/k/v, fp32 gates, chunk 64, zero S0), the
-configuration the headline metric is quoted on.  The decode workload (256
-sequences x 32 heads, fp32 state of 512 MiB) is timed in the same run and
-reported under "decode".  Prints ONE JSON line on rank 0.
+configuration the headline metric is quoted on.  In the same run, and
+reported under their own keys, the packed-varlen workload (8 documents,
+H=32), the long-context workload (B=2, H=32, T=65536, one pass), the decode
+workload (256 sequences x 32 heads, fp32 state of 512 MiB, 1000 pre-generated
+steps) and the indexed decode over a state pool are timed.  Prints ONE JSON
+line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libkda|reference]
-  python bench.py --profile-case prefill|decode-n64 [--repeat R]   (untimed, for ncu)
+  python bench.py --profile-case prefill|varlen|long|decode-n64 [--repeat R]   (untimed, for ncu)
 
 Timing: CUDA events on the launching stream, L2 flushed (a 256 MB write)
 before every timed prefill step (the prefill inputs, 101 MB, would otherwise
 sit in the 129 MB L2); the decode state (512 MiB) is larger than L2.
-Under torchrun (N > 1) every rank runs its own copy of the workload (the
-(sequence, head) chains are independent: weak scaling, no data-path
-collective); value = all ranks' tokens / the slowest rank's time.
-`--impl reference` times the fp64 CPU oracle on the same workload instead.
+Under torchrun (N > 1) the heads are split across ranks with no collective on
+the data path: the problem has 16 N heads and rank r owns heads
+[16 r, 16 (r + 1)) (weak scaling); value = all ranks' tokens x heads / 16 over
+the slowest rank's time.  `--impl reference` times the fp64 CPU oracle on the
+same workload instead.
 """
 from __future__ import annotations
 
@@ -40,6 +44,12 @@ from gated_delta_rule_27_gb300 import workloads  # noqa: E402
 
 METRIC = "KDA prefill tokens/s and decode step µs (state GB/s) on 1 GB300, % of roofline"
 WORKLOAD = "prefill"
+DESCRIPTION = {
+    "prefill": "prefill B=1 H=16 T=4096 d_k=d_v=128 chunk=64 bf16 q/k/v fp32 g/beta zero S0",
+    "varlen": "packed varlen: 8 documents with seeded lengths U[128,8192], H=32, d=128, chunk 64, bf16 q/k/v, "
+              "fp32 g/beta, state reset per document",
+    "long": "long context B=2 H=32 T=65536 d=128 chunk 64 bf16, one prefill pass",
+}
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # q,k,v bf16 + g fp32 + beta + o bf16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -151,7 +161,6 @@ KERNEL_SOURCES = {
     "prefill_prepare_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_state_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_output_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
-    "prefill_fused_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_chain_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
 }
@@ -180,9 +189,11 @@ def new_events(n):
     return evs
 
 
-def bench_prefill(libkda, steps, warmup, dev, rank):
-    w = workloads.WORKLOADS[WORKLOAD]
-    inp = workloads.workload_prefill(WORKLOAD, device=dev)
+def bench_prefill(libkda, steps, warmup, dev, rank, name=WORKLOAD, head_block=0):
+    """Times kda_prefill_chunked on one prefill workload: `steps` plain calls, each after an L2 flush and
+    bracketed by events, then the same number of profiled calls for the per-kernel split."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.workload_prefill(name, device=dev, head_block=head_block)
     q, k, v, g, beta, cu = inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens
     T, H, d = q.shape
     N = inp.num_seqs
@@ -212,6 +223,7 @@ def bench_prefill(libkda, steps, warmup, dev, rank):
     step_ev = [new_events(2) for _ in range(steps)]
     barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("kda prefill timed: " + name)
     t_wall = time.perf_counter()
     for i in range(steps):
         flush.zero_()
@@ -219,19 +231,24 @@ def bench_prefill(libkda, steps, warmup, dev, rank):
         plain()
         step_ev[i][1].record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier()
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_wall
     step_ms = [step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(steps)]
     # the per-kernel split: the same number of calls with an event before each kernel
+    torch.cuda.nvtx.range_push("kda prefill per-kernel split: " + name)
     for i in range(steps):
         flush.zero_()
         names = one(per_step[i])
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     n = len(names)
     kern_ms = {names[j]: [per_step[i][j].elapsed_time(per_step[i][j + 1]) for i in range(steps)] for j in range(n)}
-    return dict(T=T, H=H, d=d, N=N, chunk=w["chunk"], step_ms=step_ms, kern_ms=kern_ms, names=names,
-                wall_s=wall_s, launches=n * steps, inp=inp)  # launches: the timed steps' kernels
+    token_heads = T * H
+    alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * token_heads + N * H * d * d * 4
+    return dict(name=name, T=T, H=H, d=d, N=N, chunk=w["chunk"], step_ms=step_ms, kern_ms=kern_ms, names=names,
+                wall_s=wall_s, launches=n * steps, inp=inp, alg_bytes=alg_bytes)
 
 
 def bench_e2e(libkda, steps, warmup, dev, inp):
@@ -304,27 +321,58 @@ def bench_e2e(libkda, steps, warmup, dev, inp):
     return dict(ms=ms, copy_ms=copy_ms, h2d=h2d, d2h=d2h, tokens=T)
 
 
-def bench_decode(libkda, steps, warmup, dev):
+def bench_decode(libkda, warmup, dev):
+    """The decode workload as specified: 1000 successive steps whose inputs are all generated on the device
+    beforehand (about 10.5 GB), each step timed alone with events; the median is reported."""
     w = workloads.WORKLOADS["decode"]
-    N, H, d = w["N"], w["H"], w["d"]
-    n_inputs = 64
-    dec = workloads.decode_inputs(n_inputs, N, H, d, w["dtype"], seed=workloads.workload_seed("decode"), device=dev)
+    N, H, d, steps = w["N"], w["H"], w["d"], w["steps"]
+    dec = workloads.decode_inputs(steps, N, H, d, w["dtype"], seed=workloads.workload_seed("decode"), device=dev)
     S = dec.S0.clone()
     o = torch.empty((N, H, d), dtype=w["dtype"], device=dev)
     args = lambda t: (dec.q[t], dec.k[t], dec.v[t], dec.g[t], dec.beta[t])
     for t in range(warmup):
-        libkda.kda_decode_step(*args(t % n_inputs), S, o)
+        libkda.kda_decode_step(*args(t), S, o)
+    S.copy_(dec.S0)
+    torch.cuda.synchronize()
+    evs = [new_events(2) for _ in range(steps)]
+    torch.cuda.nvtx.range_push("kda decode timed: 1000 steps")
+    for i in range(steps):
+        evs[i][0].record()
+        libkda.kda_decode_step(*args(i), S, o)
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    us = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]
+    state_bytes = N * H * d * d * 4
+    io_bytes = N * H * (3 * d * 2 + d * 4 + 4 + d * 2)
+    first = workloads.DecodeInputs(*(x[:4] for x in (dec.q, dec.k, dec.v, dec.g, dec.beta)), dec.S0,
+                                   dec.extreme_steps[:0])
+    del dec
+    return dict(us=us, state_bytes=state_bytes, io_bytes=io_bytes, N=N, H=H, d=d, launches=steps, dec=first)
+
+
+def bench_decode_indexed(libkda, steps, warmup, dev):
+    """Indexed decode over a state pool: 256 of 512 slots (a seeded random choice) active, 32 heads, d = 128."""
+    slots, active, H, d = 512, 256, 32, 128
+    gen = torch.Generator(device="cpu").manual_seed(workloads.BASE_SEED + 11)
+    idx = torch.randperm(slots, generator=gen)[:active].to(torch.int32).to(dev)
+    pool = torch.empty((slots, H, d, d), device=dev).normal_(0.0, 0.1)
+    n_in = 16
+    dec = workloads.decode_inputs(n_in, active, H, d, torch.bfloat16, seed=workloads.BASE_SEED + 12, device=dev)
+    o = torch.empty((active, H, d), dtype=torch.bfloat16, device=dev)
+    args = lambda t: (dec.q[t % n_in], dec.k[t % n_in], dec.v[t % n_in], dec.g[t % n_in], dec.beta[t % n_in])
+    for t in range(warmup):
+        libkda.kda_decode_step_indexed(*args(t), idx, pool, o)
     torch.cuda.synchronize()
     evs = [new_events(2) for _ in range(steps)]
     for i in range(steps):
         evs[i][0].record()
-        libkda.kda_decode_step(*args(i % n_inputs), S, o)
+        libkda.kda_decode_step_indexed(*args(i), idx, pool, o)
         evs[i][1].record()
     torch.cuda.synchronize()
-    us = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]
-    state_bytes = N * H * d * d * 4
-    io_bytes = N * H * (3 * d * 2 + d * 4 + 4 + d * 2)
-    return dict(us=us, state_bytes=state_bytes, io_bytes=io_bytes, N=N, H=H, d=d, launches=steps, dec=dec)
+    us = statistics.median([e[0].elapsed_time(e[1]) * 1e3 for e in evs])
+    nbytes = 2 * active * H * d * d * 4 + active * H * (3 * d * 2 + d * 4 + 4 + d * 2) + active * 4
+    return dict(us=us, bytes=nbytes, slots=slots, active=active, H=H, d=d, steps=steps)
 
 
 def barrier():
@@ -349,13 +397,16 @@ def weak_scaling_value(units_per_rank: float, seconds_per_rank: float) -> float:
     return world * units_per_rank / max_over_ranks(seconds_per_rank)
 
 
-def cpu_baseline_prefill(inp, budget_s=10.0):
-    """The fp64 oracle on the prefill workload, repeated until ~budget_s of CPU time."""
+def cpu_baseline_prefill(inp, budget_s=10.0, heads=None):
+    """The fp64 oracle on a prefill workload (all heads, or the first `heads` of them as a bounded sample),
+    repeated until ~budget_s; the value is scaled to tokens/s of the whole workload."""
     from oracle import oracle
-    f = lambda x: x.detach().to("cpu", torch.float64).numpy()
+    H = inp.q.shape[1]
+    hs = H if heads is None else min(heads, H)
+    f = lambda x: x[:, :hs].detach().to("cpu", torch.float64).contiguous().numpy()
     args = [f(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
     cu = inp.cu_seqlens.cpu().numpy()
-    threads = min(oracle.default_threads(), inp.num_seqs * inp.q.shape[1])
+    threads = min(oracle.default_threads(), inp.num_seqs * hs)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.run(*args, cu, threads=threads)
@@ -363,9 +414,10 @@ def cpu_baseline_prefill(inp, budget_s=10.0):
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 50:
             break
-    return dict(value=reps * inp.total_tokens / el, unit="tokens/s", cores=threads, kind="oracle",
-                sample="the full prefill workload (%d tokens x %d heads), %d repetition(s) in %.1f s"
-                       % (inp.total_tokens, inp.q.shape[1], reps, el))
+    what = "the full workload" if hs == H else "heads 0..%d of %d of the workload" % (hs - 1, H)
+    return dict(value=reps * inp.total_tokens * hs / H / el, unit="tokens/s", cores=threads, kind="oracle",
+                sample="%s (%d tokens x %d heads), %d repetition(s) in %.1f s; scaled to all %d heads"
+                       % (what, inp.total_tokens, hs, reps, el, H))
 
 
 def cpu_baseline_decode(dec, steps=4):
@@ -385,8 +437,45 @@ def cpu_baseline_decode(dec, steps=4):
                 sample="%d decode steps over all %d x %d chains" % (steps, N, H))
 
 
+def prefill_summary(pf, pk, pk_src, world):
+    """Per-pass figures of one prefill workload: time, throughput, roofline of the pass and of its dominant
+    kernel."""
+    T, H, N, d = pf["T"], pf["H"], pf["N"], pf["d"]
+    hbm = pk["hbm_gbs"]
+    ms = max_over_ranks(statistics.mean(pf["step_ms"]))
+    token_heads = T * H
+    kern_avg = {n: statistics.mean(v) for n, v in pf["kern_ms"].items()}
+    dom = max(kern_avg, key=kern_avg.get)
+    # the path's unavoidable bytes, each counted in the kernel that moves it: the inputs are read by the
+    # preparation, the final state written by the state pass, o written by the output pass (the chain
+    # kernel writes both; the SIMT path's state pass writes both); records between kernels do not count
+    read_bytes = (3 * d * 2 + d * 4 + 4) * token_heads  # q, k, v, g, beta
+    s_bytes = N * H * d * d * 4
+    o_bytes = d * 2 * token_heads
+    if "prepare" in dom:
+        dom_bytes = read_bytes
+    elif "output" in dom:
+        dom_bytes = o_bytes
+    elif "chain" in dom:
+        dom_bytes = s_bytes + o_bytes
+    elif "state" in dom:
+        dom_bytes = s_bytes + (o_bytes if "simt" in dom else 0)
+    else:
+        dom_bytes = pf["alg_bytes"]
+    achieved = dom_bytes / (kern_avg[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": ncu_traffic(dom, pf["name"]), "algorithmic_bytes": dom_bytes,
+                "avg_launch_ms": kern_avg[dom], "peak_source": pk_src,
+                "kernels_ms": {n: round(m, 5) for n, m in kern_avg.items()}}
+    pass_bw = pf["alg_bytes"] / (ms * 1e-3) / 1e9
+    pass_roofline = {"bound": "hbm", "algorithmic_bytes": pf["alg_bytes"], "achieved": pass_bw, "peak": hbm,
+                     "unit": "GB/s", "frac": pass_bw / hbm, "roofline_us": pf["alg_bytes"] / (hbm * 1e9) * 1e6}
+    return dict(ms=ms, tokens_per_s=world * T * H / pf["H"] / (ms * 1e-3), roofline=roofline,
+                pass_roofline=pass_roofline)
+
+
 def run_libkda(args):
-    from gated_delta_rule_27_gb300 import libkda
+    from gated_delta_rule_27_gb300 import libkda, shard
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -394,56 +483,35 @@ def run_libkda(args):
         torch.distributed.init_process_group("nccl", device_id=dev)
     libkda.load()
     pk, pk_src = peaks()
+    # head split: the problem has 16 * world heads; this rank owns block `rank` of 16 of them
+    H_block = workloads.WORKLOADS[WORKLOAD]["H"]
+    lo, hi = shard.head_range(H_block * world, world, rank)
+    assert (lo, hi) == (rank * H_block, (rank + 1) * H_block)
 
     with ClockSampler(local) as clk:
-        pf = bench_prefill(libkda, args.steps, args.warmup, dev, rank)
-        dc = bench_decode(libkda, max(args.steps, 20), max(args.warmup, 3), dev)
+        pf = bench_prefill(libkda, args.steps, args.warmup, dev, rank, head_block=rank)
+        dc = bench_decode(libkda, max(args.warmup, 3), dev)
     clocks = clk.summary()
+    others = {}
+    if not args.headline_only:
+        for name in ("varlen", "long"):
+            steps = min(args.steps, 10 if name == "varlen" else 5)
+            others[name] = bench_prefill(libkda, steps, 3, dev, rank, name=name, head_block=rank)
+        di = bench_decode_indexed(libkda, 50, 3, dev)
     e2e = bench_e2e(libkda, args.steps, args.warmup, dev, pf["inp"])
 
-    T, H = pf["T"], pf["H"]
-    total_ms = sum(pf["step_ms"])
-    total_ms = max_over_ranks(total_ms)
-    ms_per_step = total_ms / args.steps
+    T = pf["T"]
+    summ = prefill_summary(pf, pk, pk_src, world)
+    ms_per_step = summ["ms"]
     value = world * T * pf["N"] / (ms_per_step * 1e-3)
-    token_heads = T * pf["N"] * H
-    alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * token_heads + pf["N"] * H * pf["d"] * pf["d"] * 4
     hbm = pk["hbm_gbs"]
-
-    # dominant kernel of the step and its algorithmic bytes per launch
-    kern_avg = {n: statistics.mean(v) for n, v in pf["kern_ms"].items()}
-    dom = max(kern_avg, key=kern_avg.get)
-    # the path's unavoidable bytes, each counted in the kernel that moves it: the inputs are read by the
-    # preparation, the final state written by the state pass, o written by the output pass (the SIMT
-    # path's state pass writes both); records between the kernels are not algorithmic bytes
-    read_bytes = (3 * 128 * 2 + 128 * 4 + 4) * token_heads  # q, k, v, g, beta
-    s_bytes = pf["N"] * H * pf["d"] * pf["d"] * 4  # S_final
-    o_bytes = 128 * 2 * token_heads
-    if "prepare" in dom:
-        dom_bytes = read_bytes
-    elif "output" in dom:
-        dom_bytes = o_bytes
-    elif "chain" in dom:  # the state pass and the outputs in one launch: S_final and o
-        dom_bytes = s_bytes + o_bytes
-    elif "state" in dom:
-        dom_bytes = s_bytes + (o_bytes if "simt" in dom else 0)
-    else:
-        dom_bytes = alg_bytes
-    achieved = dom_bytes / (kern_avg[dom] * 1e-3) / 1e9
-    traffic = ncu_traffic(dom, WORKLOAD)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": traffic, "algorithmic_bytes": dom_bytes,
-                "avg_launch_ms": kern_avg[dom], "peak_source": pk_src,
-                "kernels_ms": {n: round(m, 5) for n, m in kern_avg.items()}}
-    pass_bw = alg_bytes / (ms_per_step * 1e-3) / 1e9
-    pass_roofline = {"bound": "hbm", "algorithmic_bytes": alg_bytes, "achieved": pass_bw, "peak": hbm,
-                     "unit": "GB/s", "frac": pass_bw / hbm, "roofline_us": alg_bytes / (hbm * 1e9) * 1e6}
 
     us = sorted(dc["us"])
     dec_us = statistics.median(us)
     dec_bytes = 2 * dc["state_bytes"] + dc["io_bytes"]
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
-    decode = {"workload": "decode N=256 H=32 d=128 bf16 q/k/v, fp32 state 512 MiB",
+    decode = {"workload": "decode N=256 H=32 d=128 bf16 q/k/v, fp32 state 512 MiB, 1000 pre-generated steps "
+                          "(5% extreme gates), each timed alone",
               "us_per_step_median": dec_us, "us_per_step_mean": statistics.mean(us),
               "state_gbs": 2 * dc["state_bytes"] / (dec_us * 1e-6) / 1e9,
               "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
@@ -454,11 +522,12 @@ def run_libkda(args):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "prefill B=1 H=16 T=4096 d_k=d_v=128 chunk=64 bf16 q/k/v fp32 g/beta zero S0",
-                       "global_batch": world * pf["N"], "seq_len": T, "heads": H, "d": pf["d"],
-                       "chunk": pf["chunk"], "l2": "flushed (256 MB write) before every timed prefill step",
-                       "parallelism": "replicas" if world > 1 else "single-gpu"},
-            "roofline": roofline, "pass_roofline": pass_roofline, "decode": decode,
+            "config": {"workload": DESCRIPTION[WORKLOAD], "global_batch": world * pf["N"], "seq_len": T,
+                       "heads": pf["H"] * world, "d": pf["d"], "chunk": pf["chunk"],
+                       "l2": "flushed (256 MB write) before every timed prefill step",
+                       "parallelism": ("head split: rank r owns heads [16r, 16r+16) of %d, no collective"
+                                       % (16 * world)) if world > 1 else "single-gpu"},
+            "roofline": summ["roofline"], "pass_roofline": summ["pass_roofline"], "decode": decode,
             "e2e": {"value": world * e2e["tokens"] / (max_over_ranks(e2e["ms"]) * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "ms_per_step": e2e["ms"], "copy_only_ms_per_step": e2e["copy_ms"],
@@ -468,9 +537,24 @@ def run_libkda(args):
                             "steps pipelined on copy-in / compute / copy-out streams"},
             "gpu_launches": pf["launches"], "clocks": clocks,
             "wall_s_timed_region": pf["wall_s"]}
+    for name, p in others.items():
+        ps = prefill_summary(p, pk, pk_src, world)
+        line[name] = {"workload": DESCRIPTION[name], "tokens": p["T"], "documents": p["N"], "heads": p["H"],
+                      "ms_per_pass": ps["ms"], "tokens_per_s": ps["tokens_per_s"], "steps": len(p["step_ms"]),
+                      "pass_roofline": ps["pass_roofline"], "roofline": ps["roofline"]}
+    if not args.headline_only:
+        di_gbs = di["bytes"] / (di["us"] * 1e-6) / 1e9
+        line["decode_indexed"] = {
+            "workload": "indexed decode: %d of %d pool slots active (seeded random), H=%d, d=%d, bf16"
+                        % (di["active"], di["slots"], di["H"], di["d"]),
+            "us_per_step_median": di["us"], "steps": di["steps"],
+            "roofline": {"bound": "hbm", "achieved": di_gbs, "peak": hbm, "unit": "GB/s", "frac": di_gbs / hbm,
+                         "algorithmic_bytes": di["bytes"], "peak_source": pk_src}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pf["inp"])
         line["decode"]["cpu_baseline"] = cpu_baseline_decode(dc["dec"])
+        for name, p in others.items():
+            line[name]["cpu_baseline"] = cpu_baseline_prefill(p["inp"], budget_s=5.0, heads=4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -510,14 +594,14 @@ def run_reference(args):
 def run_profile_case(case: str, repeat: int):
     """Untimed launches of one workload, for an external profiler (ncu) to capture.
 
-    'prefill' runs the prefill workload through kda_prefill_chunked; 'decode-n64' runs decode steps over
-    a quarter of the decode workload's sequences (64 x 32 heads, 128 MiB of state), small enough for a
-    many-pass capture.
+    'prefill', 'varlen' and 'long' run that prefill workload through kda_prefill_chunked; 'decode-n64' runs
+    decode steps over a quarter of the decode workload's sequences (64 x 32 heads, 128 MiB of state), small
+    enough for a many-pass capture.
     """
     from gated_delta_rule_27_gb300 import libkda
     torch.cuda.set_device(0)
-    if case == "prefill":
-        inp = workloads.workload_prefill(WORKLOAD, device="cuda")
+    if case in ("prefill", "varlen", "long"):
+        inp = workloads.workload_prefill(case, device="cuda")
         T, N = inp.total_tokens, inp.num_seqs
         H, d = inp.q.shape[1], inp.q.shape[2]
         o = torch.empty_like(inp.v)
@@ -544,7 +628,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode-n64"], default=None,
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the prefill and decode workloads (skip varlen, long, indexed decode)")
+    ap.add_argument("--profile-case", choices=["prefill", "varlen", "long", "decode-n64"], default=None,
                     help="run untimed launches of one workload for a profiler, print a status line, exit")
     ap.add_argument("--repeat", type=int, default=3)
     args = ap.parse_args()

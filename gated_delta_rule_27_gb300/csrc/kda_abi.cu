@@ -4,6 +4,7 @@
 #include <limits.h>
 
 #include "kda_internal.cuh"
+#include "kda_testing.h"
 
 namespace {
 
@@ -123,7 +124,20 @@ kda_status kda_prefill_check(const void *workspace, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
-    return flag == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    return kda::status_from_word(flag);
+}
+
+kda_status kda_testing_set_plan(int32_t plan) {
+    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN) return KDA_ERR_INVALID_ARG;
+    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE ? kda::TC_THREE : plan == -1 ? -1 : kda::TC_CHAIN);
+    return KDA_OK;
+}
+
+kda_status kda_testing_set_fault(int32_t fault, int64_t wait_limit_ns) {
+    if ((fault != KDA_TESTING_FAULT_NONE && fault != KDA_TESTING_FAULT_NO_PUBLISH) || wait_limit_ns < 0)
+        return KDA_ERR_INVALID_ARG;
+    kda::testing_set_fault(fault, (long long)wait_limit_ns);
+    return KDA_OK;
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -138,9 +152,53 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
         return KDA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
     if (o == q || o == k || o == v || o == (const void *)S_inout) return KDA_ERR_INVALID_ARG;
-    cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_seqs, H, d_k, in_dtype, S_inout, o,
-                                       static_cast<cudaStream_t>(stream));
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_seqs, H, d_k, in_dtype, S_inout, o, nullptr, num_seqs,
+                                       nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                   const int32_t *seq_idx, int32_t num_active, int32_t num_slots, int32_t H,
+                                   int32_t d_k, int32_t d_v, kda_dtype in_dtype, float *S_pool, void *o,
+                                   int32_t *status, void *stream) {
+    if (num_active < 0 || num_slots < 0 || H <= 0 || !valid_dtype(in_dtype)) return KDA_ERR_INVALID_ARG;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_active * H > INT_MAX || (int64_t)num_slots * H > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    if (num_active == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !seq_idx || !S_pool || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(S_pool) || !aligned16(o))
+        return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) || (reinterpret_cast<uintptr_t>(seq_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(status) & 3u))
+        return KDA_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v || o == (const void *)S_pool) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_active, H, d_k, in_dtype, S_pool, o, seq_idx, num_slots,
+                                       status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+static kda_status state_copy(const float *src, float *dst, const int32_t *seq_idx, int32_t n, int32_t num_slots,
+                             int32_t H, int32_t d_k, int32_t d_v, bool scatter, int32_t *status, void *stream) {
+    if (n < 0 || num_slots < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)H * d_k * d_v > INT_MAX || (int64_t)n * H > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    if (n == 0) return KDA_OK;
+    if (!src || !dst || !seq_idx || !aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(seq_idx) & 3u) ||
+        (reinterpret_cast<uintptr_t>(status) & 3u) || src == dst)
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_state_copy(src, dst, seq_idx, n, num_slots, H, d_k, scatter, status,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_state_snapshot(const float *S_pool, const int32_t *seq_idx, int32_t n, int32_t num_slots, int32_t H,
+                              int32_t d_k, int32_t d_v, float *S_saved, int32_t *status, void *stream) {
+    return state_copy(S_pool, S_saved, seq_idx, n, num_slots, H, d_k, d_v, false, status, stream);
+}
+
+kda_status kda_state_restore(const float *S_saved, const int32_t *seq_idx, int32_t n, int32_t num_slots, int32_t H,
+                             int32_t d_k, int32_t d_v, float *S_pool, int32_t *status, void *stream) {
+    return state_copy(S_saved, S_pool, seq_idx, n, num_slots, H, d_k, d_v, true, status, stream);
 }
 
 }  // extern "C"

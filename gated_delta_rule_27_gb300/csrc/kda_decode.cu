@@ -18,6 +18,15 @@
 // through shared memory in a fixed order, so the result is deterministic.
 // State traffic uses streaming (evict-first) loads and stores: the state is
 // touched once per step and is far larger than L2.
+//
+// The indexed variant serves a batch that mixes request phases (Lecture 04,
+// section 2: the decode family takes the sequences that are generating,
+// while others are still in prefill): its states live in a pool of slots and
+// an index list names the slot each active sequence's token updates.  Slots
+// not named are not touched.  Two copy kernels take a snapshot of listed
+// slots and put it back, which is what a speculative rollback needs
+// (Lecture 11, section 2, "Serving state" row: rollback must reconcile the
+// KDA state).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -25,11 +34,14 @@ namespace {
 
 constexpr int kRows = 16;  // rows of S per thread
 
+// One CTA per (active sequence, head).  With `idx` null, sequence i's state is S[i]; otherwise it is the
+// pool slot idx[i] (a slot outside [0, num_slots) is skipped and recorded in *status, when given).
 template <typename Tin, int D>
 __global__ void __launch_bounds__((D / 4) * (D / kRows))
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ S,
-                   Tin *__restrict__ o) {
+                   Tin *__restrict__ o, const int32_t *__restrict__ idx, int H, int num_slots,
+                   int32_t *__restrict__ status) {
     constexpr int CG = D / 4;        // column groups (float4)
     constexpr int RG = D / kRows;    // row bands
     constexpr int NT = CG * RG;
@@ -37,11 +49,20 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
     __shared__ float s_x[RG][D], s_y[RG][D];
     __shared__ float s_qk;
 
-    const int head = blockIdx.x;  // flattened (seq, head)
+    const int head = blockIdx.x;  // flattened (active sequence, head): the token's inputs and output
+    size_t state = (size_t)head;  // flattened (slot, head) of its state
+    if (idx) {
+        const int slot = idx[head / H];
+        if (slot < 0 || slot >= num_slots) {
+            if (status && threadIdx.x == 0) atomicCAS(status, 0, (int32_t)KDA_ERR_INVALID_ARG);
+            return;
+        }
+        state = (size_t)slot * H + head % H;
+    }
     const int tid = threadIdx.x;
     const int cg = tid % CG, rg = tid / CG;
     const size_t vec = (size_t)head * D;
-    float4 *Sv = reinterpret_cast<float4 *>(S + (size_t)head * D * D);
+    float4 *Sv = reinterpret_cast<float4 *>(S + state * D * D);
 
     // Issue the state loads first: they are the long pole.
     float4 s[kRows];
@@ -97,22 +118,39 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
     }
 }
 
+// Copies whole (slot, head) states between a pool and a compact buffer: gather (snapshot) writes
+// dst[i] = pool[idx[i]], scatter (restore) writes pool[idx[i]] = src[i].  One CTA per listed state, 16-byte
+// streaming loads and stores; a slot outside [0, num_slots) is skipped and recorded in *status.
+__global__ void __launch_bounds__(256)
+state_copy_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, const int32_t *__restrict__ idx,
+                  int num_slots, int state_vec4, int scatter, int32_t *__restrict__ status) {
+    const int i = blockIdx.x;
+    const int slot = idx[i];
+    if (slot < 0 || slot >= num_slots) {
+        if (status && threadIdx.x == 0) atomicCAS(status, 0, (int32_t)KDA_ERR_INVALID_ARG);
+        return;
+    }
+    const size_t from = (size_t)(scatter ? i : slot) * state_vec4, to = (size_t)(scatter ? slot : i) * state_vec4;
+    for (int j = threadIdx.x; j < state_vec4; j += blockDim.x) __stcs(&dst[to + j], __ldcs(&src[from + j]));
+}
+
 template <typename Tin, int D>
 cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
-                     float *S, void *o, cudaStream_t st) {
+                     float *S, void *o, const int32_t *idx, int H, int num_slots, int32_t *status, cudaStream_t st) {
     constexpr int NT = (D / 4) * (D / kRows);
     decode_step_kernel<Tin, D><<<heads, NT, 0, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, S,
-                                                     (Tin *)o);
+                                                     (Tin *)o, idx, H, num_slots, status);
     return cudaGetLastError();
 }
 
 template <typename Tin>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
-                     int d, float *S, void *o, cudaStream_t st) {
+                     int d, float *S, void *o, const int32_t *idx, int H, int num_slots, int32_t *status,
+                     cudaStream_t st) {
     switch (d) {
-        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, heads, S, o, st);
-        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, heads, S, o, st);
-        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, heads, S, o, st);
+        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
+        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
+        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -120,11 +158,21 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 }  // namespace
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st) {
+                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, const int32_t *idx,
+                          int num_slots, int32_t *status, cudaStream_t st) {
     const int heads = num_seqs * H;
     if (heads == 0) return cudaSuccess;
-    if (dt == KDA_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, beta, heads, d, S, o, st);
-    return launch_t<float>(q, k, v, g, beta, heads, d, S, o, st);
+    if (dt == KDA_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, st);
+    return launch_t<float>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, st);
+}
+
+cudaError_t launch_state_copy(const float *src, float *dst, const int32_t *idx, int n, int num_slots, int H, int d,
+                              bool scatter, int32_t *status, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int state_vec4 = H * d * d / 4;  // one slot: all its heads
+    state_copy_kernel<<<n, 256, 0, st>>>(reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst), idx,
+                                         num_slots, state_vec4, scatter ? 1 : 0, status);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

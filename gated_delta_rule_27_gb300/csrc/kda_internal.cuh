@@ -29,7 +29,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 //   doc_slot0           int32 [num_seqs + 1]: first chunk slot of each document
 //                       (exclusive prefix sum of ceil(len / L)), 256-byte padded
 //   records             one per (chunk slot, head), `record_bytes` each
-//   flags               (tensor-core path) progress flags of the chain and fused plans
+//   flags               (tensor-core path) progress flags of the chain plan
 //
 // The number of chunk slots is bounded by total_tokens / L + num_seqs, so the
 // size depends only on the call's scalar arguments.
@@ -41,8 +41,8 @@ struct WsLayout {
     size_t records_off;
     size_t record_bytes;
     int64_t max_slots;
-    size_t flags_off;    // tensor-core path: int32 [max_slots * H] record-ready flags, then int32
-                         // [max_slots * H] state-image counters, then two int32 unit counters
+    size_t flags_off;    // tensor-core path: int32 [max_slots * H] state-image counters, then two int32
+                         // unit counters (chain plan)
     size_t flags_bytes;  // 0 on the CUDA-core path
     size_t total;
 };
@@ -95,9 +95,17 @@ inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int
     w.record_bytes = path == PATH_TC ? tc_record().bytes : simt_record(L, dk, dv).bytes;
     w.max_slots = total_tokens / L + num_seqs;
     w.flags_off = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;
-    w.flags_bytes = path == PATH_TC ? align256(((size_t)2 * w.max_slots * H + 2) * 4) : 0;
+    w.flags_bytes = path == PATH_TC ? align256(((size_t)w.max_slots * H + 2) * 4) : 0;
     w.total = w.flags_off + w.flags_bytes;
     return w;
+}
+
+// The workspace status word as a status: 0 valid, 1 invalid cu_seqlens (written by the chunk index kernel),
+// KDA_ERR_TIMEOUT a bounded device-side wait that gave up (written by the kernel that waited).
+inline kda_status status_from_word(int32_t word) {
+    if (word == 0) return KDA_OK;
+    if (word == (int32_t)KDA_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
+    return KDA_ERR_INVALID_ARG;
 }
 
 // Locates the document and chunk of a chunk slot by binary search over the
@@ -159,11 +167,15 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
                                size_t clear_bytes, cudaStream_t st, Marks &marks);
 
-// Launch plans of the tensor-core prefill: three kernels (preparation, state, output); one fused launch of
-// all three; or the preparation followed by one launch running the state chains with the output units
-// alongside (chain).  The last two need the workspace's progress flags zeroed before they start.
-enum TcPlan { TC_THREE = 0, TC_FUSED = 1, TC_CHAIN = 2 };
+// Launch plans of the tensor-core prefill: three kernels (preparation, state, output), or the preparation
+// followed by one cooperative launch running the state chains with the output units alongside (chain).  The
+// chain plan needs the workspace's progress flags zeroed before it starts.
+enum TcPlan { TC_THREE = 0, TC_CHAIN = 2 };
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
+
+// Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.
+void testing_set_plan(int plan);
+void testing_set_fault(int fault, long long wait_ns);
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
@@ -174,7 +186,15 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
                               float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks);
 
+// Decode step of num_seqs sequences; with `idx` (device, [num_seqs]) their states are the pool slots idx[i] of
+// S [num_slots, H, d, d], otherwise S[i].
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, cudaStream_t st);
+                          int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, const int32_t *idx,
+                          int num_slots, int32_t *status, cudaStream_t st);
+
+// Snapshot (gather: dst[i] = src[idx[i]]) or restore (scatter: dst[idx[i]] = src[i]) of n whole slots of
+// H heads' d x d fp32 states.
+cudaError_t launch_state_copy(const float *src, float *dst, const int32_t *idx, int n, int num_slots, int H, int d,
+                              bool scatter, int32_t *status, cudaStream_t st);
 
 }  // namespace kda

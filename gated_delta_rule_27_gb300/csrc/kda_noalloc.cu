@@ -69,4 +69,11 @@ kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void 
                                chunk_size, S0, o, S_final, scratch, kScratchBytes, stream);
 }
 
+kda_status kda_prefill_noalloc_check(void *stream) {
+    void *scratch = nullptr;
+    const kda_status st = scratch_for_current_device(&scratch);
+    if (st != KDA_OK) return st;
+    return kda_prefill_check(scratch, stream);
+}
+
 }  // extern "C"

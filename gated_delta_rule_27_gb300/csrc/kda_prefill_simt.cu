@@ -34,8 +34,8 @@ constexpr int kThreads = 256;
 // (1) chunk index: doc_slot0[i] = sum_{j<i} ceil(len_j / L), and validation of
 // cu_seqlens.  On invalid input every document gets zero chunks and the
 // status word is set, so the later kernels write nothing.  Also zeroes
-// `clear_vec` 16-byte words at `clear` (the progress flags of the chain and
-// fused plans), when asked to.
+// `clear_vec` 16-byte words at `clear` (the progress flags of the chain
+// plan), when asked to.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_tokens, int L, int32_t *status,

@@ -37,8 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <cstdlib>
-#include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -49,6 +48,8 @@ namespace {
 
 constexpr int kD = 128, kL = 64, kTile = 32, kNTile = kD / kTile;
 constexpr float kMaxHalfRange = 80.f;  // |b_r - b_m| bound of the tensor-core A/P path
+constexpr uint64_t kFlagWaitNs = 2000000000ull;  // default bound of a wait on another CTA's publication flag
+constexpr int kFaultNoPublish = 1;  // test-only: the chain plan publishes no state image
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -883,7 +884,8 @@ constexpr int kChainOutGroups = 2;  // output groups of 128 threads in each non-
 // for output units running alongside.
 __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                             float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off,
-                            size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw, int32_t *sdone) {
+                            size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw, int32_t *sdone,
+                            bool publish = true) {
     __shared__ uint64_t full_bar[kNBuf], a_bar, img_full[kNSb], img_free[kNSb];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
@@ -989,7 +991,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                         tc::bulk_wait_read();  // the slot may be rewritten
                     }
                     tc::mbar_arrive(&img_free[sl]);  // always: the epilogue counts on one per image
-                    if (ok && sdone && c + 1 - kStatePubLag - pub >= kStatePubBatch) {
+                    if (ok && sdone && publish && c + 1 - kStatePubLag - pub >= kStatePubBatch) {
                         // the copies of S_pub .. S_{c-2} have completed: publish them
                         static_assert(kStatePubLag == 2, "wait_group below");
                         tc::bulk_wait_all_but_two();
@@ -1000,7 +1002,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     }
                 }
                 tc::bulk_wait_all();  // shared memory must outlive the image copies
-                if (sdone && ok) {
+                if (sdone && publish && ok) {
                     tc::fence_proxy_async_global();
                     tc::fence_acq_rel_gpu();
                     for (; pub < nchunks; ++pub) tc::red_relaxed_gpu_add(sdone + (size_t)(first + pub) * H + h, 1);
@@ -1119,7 +1121,7 @@ struct OutGroup {
 __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
                             OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, bool dep_wait = false,
-                            const int32_t *sflag = nullptr) {
+                            const int32_t *sflag = nullptr, uint64_t flag_wait_ns = kFlagWaitNs) {
     const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
@@ -1144,7 +1146,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
         // ... then the image of S_c (written by the state pass)
         if (dep_wait) tc::grid_dep_wait();
         if (sflag) {
-            ok = tc::wait_flag_geq(sflag, kNTile) && ok;
+            ok = tc::wait_flag_geq(sflag, kNTile, flag_wait_ns) && ok;
             tc::fence_proxy_async_global();
         }
         tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
@@ -1243,11 +1245,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  float *__restrict__ S_final, __nv_bfloat16 *__restrict__ o, char *__restrict__ ws,
                  size_t doc_slot0_off, size_t records_off, size_t record_bytes, int n_state, int32_t *sdone,
-                 int32_t *counter) {
+                 int32_t *counter, unsigned long long flag_wait_ns, int fault) {
     extern __shared__ uint8_t smem_raw[];
     if ((int)blockIdx.x < n_state) {
+        // (fault == kFaultNoPublish only in tests of the timeout path: no state image is published, so the
+        // output groups' bounded waits run out)
         state_chain(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
-                    smem_raw, sdone);
+                    smem_raw, sdone, fault != kFaultNoPublish);
         return;
     }
     constexpr int kGroups = kChainOutGroups;
@@ -1301,7 +1305,7 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             int doc, t0, Lc;
             locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
             if (!output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
-                             grp, false, sdone + u))
+                             grp, false, sdone + u, flag_wait_ns))
                 break;
         }
     }
@@ -1310,354 +1314,8 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     if (warp == 0) tc::tmem_dealloc(tmem_base, 128 * kGroups);
 }
 
-// ---------------------------------------------------------------------------
-// Fused plan (on request): preparation, state pass and output in one launch
-// ---------------------------------------------------------------------------
-// One launch of prefill_fused_tc, with as many CTAs as fit on the GPU at once,
-// replaces the three kernels above, so that the state pass runs while later
-// chunks are still being prepared and the outputs are formed while their
-// records are still in L2.  Its chains share their SMs with workers and step
-// more slowly than the chain plan's, which is why that plan is the automatic
-// choice for few chains:
-//   CTAs [0, n_state)  one chain each (the state pass above, 256 threads:
-//                      warps 0-3 epilogue with 32 columns per thread, warps 4-5
-//                      MMA issuers, warp 6 streams records in as they are
-//                      published, warp 7 copies each state image out and
-//                      publishes it)
-//   other CTAs         take units from a shared counter: the preparation of a
-//                      (chunk slot, head), or its output once its record and
-//                      all its column tiles' state images are published;
-//                      outputs trail the preparations by `lag` chunk slots.
-// Hand-offs go through the flags region of the workspace with GPU-scope
-// release / acquire: a record is published after its bulk stores complete,
-// and a reader fences the async proxy before its bulk loads.  Every wait is
-// bounded.  Progress needs only the state CTAs to be resident (they have the
-// lowest indices, so they are placed first): a state CTA waits for records,
-// and every record it waits for belongs to a unit that a running worker has
-// already claimed and finishes without waiting; a worker waits only for state
-// CTAs.
+constexpr int kChainMinWorkers = 48;  // output CTAs alongside the chains, at least
 
-// Row i of S (32 values) into the K-major S^T operand, element (j, i); rows i
-// and i ^ 1 trade values so that each stores whole 4-byte words.
-__device__ __forceinline__ void store_state_row32(uint8_t *SB, int i, const float (&S)[kTile]) {
-    uint8_t *p = SB + (uint32_t)(i >> 6) * 4096u;
-    const int odd = i & 1, ie = i & ~1;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        const int ja = u, jb = 16 + ((u + 8) & 15);  // the even and the odd lane's column of this step
-        const float give = odd ? S[ja] : S[jb];
-        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-        const int j = odd ? jb : ja;
-        const float lo = odd ? got : S[ja], hi = odd ? S[jb] : got;
-        *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
-    }
-}
-
-struct FusedStateSmem {
-    static constexpr uint32_t kBuf = 43008;  // M' and gamma + this CTA's Bc tile, 1 KB aligned
-    static constexpr uint32_t SB = 2 * kBuf;  // two bf16 images of S
-    static constexpr uint32_t bytes = SB + 2 * 8192;
-};
-constexpr int kFusedMaxChains = 64;   // automatic choice: at most this many chains
-constexpr int kFusedMinWorkers = 32;  // CTAs left for the chunk-parallel units, at least
-constexpr int kFusedStaggerNs = 1400;  // about one step of the state pass
-constexpr int kChainMinWorkers = 48;   // output CTAs alongside the chains, at least
-constexpr TcPlan kAutoPlan = TC_CHAIN;  // the plan for few chains
-constexpr size_t fused_smem_bytes() {
-    return (PrepSmem::bytes > FusedStateSmem::bytes ? (PrepSmem::bytes > OutSmem::bytes ? PrepSmem::bytes : OutSmem::bytes)
-                                                    : (FusedStateSmem::bytes > OutSmem::bytes ? FusedStateSmem::bytes
-                                                                                              : OutSmem::bytes)) +
-           1024;
-}
-
-constexpr uint32_t kBarFusedOp = 1;              // named barrier: the next S image is complete
-constexpr uint32_t kFusedOpCount = 4 * 32 + 3 * 32;  // epilogue warps arrive; issuers and publisher wait
-
-struct FusedArgs {
-    const float *S0;
-    float *S_final;
-    __nv_bfloat16 *o;
-    int32_t *ready;    // [slot * H + h]: the record of (slot, h) is published
-    int32_t *sdone;    // [slot * H + h]: column tiles whose state image is published
-    int32_t *counter;  // next unit
-    int n_state, lag;  // state CTAs; outputs trail the preparations by `lag` chunk slots
-    int stagger_ns;    // worker group g (H workers each) starts g * stagger_ns after the kernel
-};
-
-// Position u of the worker units -> (output?, slot, head): the first `lag` slots' preparations, then
-// alternately one slot's preparations and the outputs of the slot `lag` earlier, then the last outputs.
-__device__ __forceinline__ void decode_unit(int u, int C, int H, int lag, bool *out, int *slot, int *h) {
-    const int D = min(lag, C);
-    const int lead = D * H, mid = (C - D) * 2 * H;
-    if (u < lead) {
-        *out = false; *slot = u / H; *h = u % H;
-    } else if (u < lead + mid) {
-        const int q = u - lead, b = q / (2 * H), r = q % (2 * H);
-        *out = r >= H; *slot = r < H ? D + b : b; *h = r < H ? r : r - H;
-    } else {
-        const int q = u - lead - mid;
-        *out = true; *slot = C - D + q / H; *h = q % H;
-    }
-}
-
-__device__ void fused_state(const PrepParams &pp, const FusedArgs &f, uint8_t *sm) {
-    __shared__ uint64_t full_bar[2], empty_bar[2], a_bar;
-    __shared__ uint32_t tmem_base;
-    __shared__ int s_abort;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = pp.H;
-    const int j = blockIdx.x, tile = j % kNTile, h = (j / kNTile) % H, n = j / (kNTile * H);
-    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
-    const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
-    const bool epi = warp < 4;
-    const int i = (warp & 3) * 32 + lane;
-    const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + tile * kTile;
-    constexpr TcRecord R = tc_record();
-
-    float S[kTile];
-#pragma unroll
-    for (int c4 = 0; c4 < kTile; c4 += 4) {
-        const float4 v = (f.S0 && epi) ? *reinterpret_cast<const float4 *>(f.S0 + state_off + c4)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        S[c4] = v.x; S[c4 + 1] = v.y; S[c4 + 2] = v.z; S[c4 + 3] = v.w;
-    }
-    bool ok = true;
-    if (nchunks > 0) {
-        if (epi) store_state_row32(sm + FusedStateSmem::SB, i, S);
-        tc::fence_async_smem();
-        if (tid == 0) {
-            for (int b = 0; b < 2; ++b) {
-                tc::mbar_init(&full_bar[b], 1);
-                tc::mbar_init(&empty_bar[b], 128);  // every epilogue thread releases the buffer
-            }
-            tc::mbar_init(&a_bar, 2);
-            tc::fence_mbar_init();
-            s_abort = 0;
-        }
-        if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 64);
-            tc::tmem_relinquish();
-        }
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
-        const uint32_t tmem = tmem_base;
-        char *rec_h = pp.ws + pp.records_off + (size_t)h * pp.record_bytes;
-        const size_t rec_stride = (size_t)H * pp.record_bytes;
-
-        if (warp == 6) {
-            // loader: record c into buffer c % 2 once it is published and the buffer is free
-            if (lane == 0) {
-                int issued = 0;
-                for (int c = 0; c < nchunks; ++c) {
-                    const int b = c & 1;
-                    if (c >= 2) ok = ok && tc::mbar_wait(&empty_bar[b], (uint32_t)(((c - 2) >> 1) & 1));
-                    ok = ok && tc::wait_flag_geq(f.ready + (size_t)(first + c) * H + h, 1);
-                    if (!ok) break;
-                    tc::fence_proxy_async_global();
-                    issue_record(sm + b * FusedStateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile,
-                                 &full_bar[b]);
-                    issued = c + 1;
-                }
-                // copies still on their way land before shared memory can go away
-                for (int c = max(0, issued - 2); c < issued; ++c)
-                    tc::mbar_wait(&full_bar[c & 1], (uint32_t)((c >> 1) & 1), 10000000ull);
-            }
-            __syncwarp();
-        } else if (warp == 4 || warp == 5) {
-            const uint32_t panel = (uint32_t)(warp - 4);
-            constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-            constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
-            for (int c = 0; c < nchunks; ++c) {
-                if (c > 0) tc::named_barrier(kBarFusedOp, kFusedOpCount);  // S_c's image is complete
-                tc::tc_fence_after();
-                if (lane == 0) {
-                    ok = ok && tc::mbar_wait(&full_bar[c & 1], (uint32_t)((c >> 1) & 1));
-                    if (ok) {
-                        uint8_t *buf = sm + (c & 1) * FusedStateSmem::kBuf;
-                        uint8_t *sbc = sm + FusedStateSmem::SB + (uint32_t)(c & 1) * 8192u;
-                        const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u));
-                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u));
-                        for (int s = 0; s < 4; ++s)
-                            tc::mma_bf16(tmem + 32u * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, s > 0);
-                    }
-                    tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
-                }
-                __syncwarp();
-            }
-        } else if (warp == 7) {
-            // publisher: S_c's image into chunk c's record; S_{c-1}'s published once its writes are complete
-            for (int c = 0; c < nchunks; ++c) {
-                if (c > 0) tc::named_barrier(kBarFusedOp, kFusedOpCount);
-                if (lane == 0) {
-                    const uint8_t *sbc = sm + FusedStateSmem::SB + (uint32_t)(c & 1) * 8192u;
-                    char *rec = rec_h + (size_t)(first + c) * rec_stride;
-                    tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
-                    tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
-                    tc::bulk_commit();
-                    if (c > 3) {  // S_{c-4}'s image, stored four chunks ago: complete, publish it
-                        tc::bulk_wait_all_but_four();
-                        tc::fence_proxy_async_global();
-                        tc::red_release_gpu_add(f.sdone + (size_t)(first + c - 4) * H + h, 1);
-                    }
-                    tc::bulk_wait_read();  // image c has been read: the epilogue of chunk c + 1 rewrites it
-                }
-                __syncwarp();
-            }
-            if (lane == 0) {
-                tc::bulk_wait_all();
-                tc::fence_proxy_async_global();
-                for (int c = max(0, nchunks - 4); c < nchunks; ++c)
-                    tc::red_release_gpu_add(f.sdone + (size_t)(first + c) * H + h, 1);
-            }
-            __syncwarp();
-        } else {
-            // epilogue: S <- gamma S + Bc + M' S for state row i, 32 columns
-            const uint32_t tacc = tmem + ((uint32_t)(warp * 32) << 16);
-            for (int c = 0; c < nchunks; ++c) {
-                const int b = c & 1;
-                const uint8_t *buf = sm + b * FusedStateSmem::kBuf;
-                ok = ok && tc::mbar_wait(&full_bar[b], (uint32_t)((c >> 1) & 1));
-                const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
-                float bc[kTile];
-                {
-                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float fv[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(brow + ((k ^ ((i >> 1) & 3)) << 4)), fv);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) bc[8 * k + u] = fv[u];
-                    }
-                }
-                ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
-                tc::tc_fence_after();
-                if (warp_all(ok)) {
-                    float t[64];
-                    tc::tmem_ld64(tacc, t);
-#pragma unroll
-                    for (int jj = 0; jj < kTile; ++jj) S[jj] = fmaf(gam, S[jj], bc[jj] + (t[jj] + t[32 + jj]));
-                    store_state_row32(sm + FusedStateSmem::SB + (uint32_t)((c + 1) & 1) * 8192u, i, S);
-                }
-                tc::fence_async_smem();
-                tc::tc_fence_before();
-                tc::mbar_arrive(&empty_bar[b]);
-                if (c + 1 < nchunks) tc::named_barrier_arrive(kBarFusedOp, kFusedOpCount);
-            }
-        }
-        if (!ok) s_abort = 1;
-        __syncthreads();
-        if (tid == 0 && s_abort) flag_timeout(pp.ws);
-        if (warp == 0) tc::tmem_dealloc(tmem, 64);
-        if (s_abort) return;
-    }
-    if (f.S_final && epi) {
-#pragma unroll
-        for (int c4 = 0; c4 < kTile; c4 += 4)
-            *reinterpret_cast<float4 *>(f.S_final + state_off + c4) = make_float4(S[c4], S[c4 + 1], S[c4 + 2], S[c4 + 3]);
-    }
-}
-
-// Publishes a record this thread stored with bulk copies: release once the copies are complete.  The other
-// threads' direct stores to it are ordered before by the CTA barriers passed since.
-__device__ __forceinline__ void publish_record(int32_t *flag) {
-    tc::bulk_wait_all();
-    tc::fence_proxy_async_global();
-    tc::st_release_gpu(flag, 1);
-}
-
-__device__ void fused_worker(const PrepParams &pp, const FusedArgs &f, uint8_t *sm) {
-    __shared__ PrepBars pbars;
-    __shared__ OutBars obars;
-    __shared__ uint32_t tmem_base;
-    __shared__ int s_unit, s_ok;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int H = pp.H;
-    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
-    const int C = doc_slot0[pp.num_seqs];
-    const int total = 2 * C * H;
-    if (tid == 0) {
-        prep_bars_init(&pbars);
-        tc::mbar_init(&obars.load, 1);
-        tc::mbar_init(&obars.sload, 1);
-        tc::mbar_init(&obars.mma, 1);
-        tc::fence_mbar_init();
-    }
-    if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 256);
-        tc::tmem_relinquish();
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = tmem_base;
-    uint32_t nprep = 0, nout = 0;
-    int32_t *pending = nullptr;  // the last record this CTA prepared, not yet published
-    if (tid == 0 && f.stagger_ns > 0) {
-        // Workers start in groups of H, one chain step apart: the first chunk slots are prepared by
-        // fewer CTAs at a time, so their records (which the state pass needs first) come out sooner,
-        // and the later groups fall into step behind them.
-        const uint64_t t_start = tc::globaltimer_ns();
-        const uint64_t delay = (uint64_t)((blockIdx.x - f.n_state) / H) * (uint64_t)f.stagger_ns;
-        while (tc::globaltimer_ns() - t_start < delay) __nanosleep(256);
-    }
-    for (;;) {
-        if (tid == 0) s_unit = atomicAdd(f.counter, 1);
-        __syncthreads();
-        const int u = s_unit;
-        if (u >= total) break;
-        bool out;
-        int slot, h, doc, t0, Lc;
-        decode_unit(u, C, H, f.lag, &out, &slot, &h);
-        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
-        if (!out) {
-            // the previous record is published once this unit's loads are issued; this one's stays pending
-            const bool ok = prepare_unit(pp, slot, h, t0, Lc, sm, &pbars, nprep & 1u, tmem, -1, 0, pending);
-            ++nprep;
-            if (!ok) break;
-            pending = f.ready + (size_t)slot * H + h;
-        } else {
-            if (tid == 0 && pending) publish_record(pending);
-            pending = nullptr;
-            if (tid == 0) {
-                // the record itself (its own publication) and every column tile's image of S_c
-                s_ok = tc::wait_flag_geq(f.ready + (size_t)slot * H + h, 1) &&
-                       tc::wait_flag_geq(f.sdone + (size_t)slot * H + h, kNTile);
-                tc::fence_proxy_async_global();
-            }
-            __syncthreads();
-            if (!s_ok) {
-                if (tid == 0) flag_timeout(pp.ws);
-                break;
-            }
-            __shared__ int s_uok;
-            const bool ok = output_unit(pp.cu, H, f.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, sm,
-                                        &obars, nout & 1u, tmem, OutGroup{tid, 0u, &s_uok});
-            ++nout;
-            if (!ok) break;
-        }
-    }
-    if (tid == 0 && pending) publish_record(pending);
-    tc::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 256);
-}
-
-__global__ void __launch_bounds__(kPrepThreads, 2)
-prefill_fused_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                 const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
-                 char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, FusedArgs f) {
-    extern __shared__ uint8_t smem_raw[];
-    tc::grid_dep_wait();  // the chunk index kernel: slots, status word, cleared flags
-    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
-    uint8_t *sm = align1024(smem_raw);
-    const PrepParams pp{&tm_q, &tm_k, &tm_v, &tm_g, beta, cu, num_seqs, H, ws, doc_slot0_off, records_off, record_bytes};
-    if ((int)blockIdx.x < f.n_state)
-        fused_state(pp, f, sm);
-    else
-        fused_worker(pp, f, sm);
-}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -1702,11 +1360,48 @@ bool make_gate_map(CUtensorMap *map, const float *base, int total_tokens, int H)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The four tensor maps of a call, remembered for the (q, k, v, g, T, H) they were encoded for: a serving
+// loop that reuses its buffers pays for the encoding once.  A tensor map holds only the base address, sizes
+// and strides, so an entry stays valid for as long as the same addresses describe the same shapes.
+struct InputMaps {
+    CUtensorMap q, k, v, g;
+};
+bool input_maps(const void *q, const void *k, const void *v, const float *g, int T, int H, InputMaps *out) {
+    struct Entry {
+        const void *q, *k, *v, *g;
+        int T, H;
+        InputMaps maps;
+    };
+    constexpr int kEntries = 16;
+    static std::mutex lock;
+    static Entry cache[kEntries];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> guard(lock);
+        for (int i = 0; i < used; ++i) {
+            const Entry &e = cache[i];
+            if (e.q == q && e.k == k && e.v == v && e.g == g && e.T == T && e.H == H) {
+                *out = e.maps;
+                return true;
+            }
+        }
+    }
+    InputMaps m;
+    if (!make_input_map(&m.q, q, T, H) || !make_input_map(&m.k, k, T, H) || !make_input_map(&m.v, v, T, H) ||
+        !make_gate_map(&m.g, g, T, H))
+        return false;
+    std::lock_guard<std::mutex> guard(lock);
+    cache[next] = Entry{q, k, v, g, T, H, m};
+    next = (next + 1) % kEntries;
+    used = used < kEntries ? used + 1 : kEntries;
+    *out = m;
+    return true;
+}
+
 // CTAs of `kernel` that fit on the whole device at once (0 if unknown), cached per device: the smallest of
 // what the SM's registers, shared memory (dynamic + static + the per-CTA reserve), threads and tensor
 // memory (512 columns, `tmem_cols` per CTA) allow, times the SM count.  Worked out here from the
-// kernel's attributes because the runtime's occupancy query answers 1 per SM for these kernels
-// although two or three of them run side by side on an SM.
+// kernel's attributes because the runtime's occupancy query does not know about tensor memory.
 template <typename K>
 int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
     static std::mutex lock;
@@ -1734,44 +1429,96 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
     return cached[dev];
 }
 
+constexpr int kPrepSmem = PrepSmem::bytes + 1024;
+constexpr int kStateSmem = StateSmem::bytes + 1024;
+constexpr int kOutSmem = OutSmem::bytes + 1024;
+
+// Per-device facts the launches need, worked out (and the kernels' shared-memory limits raised) once per
+// device rather than on every call.
+struct DeviceSetup {
+    cudaError_t err = cudaErrorNotReady;
+    int sms = 0;
+    int prep_resident = 0, out_resident = 0;
+};
+const DeviceSetup &device_setup() {
+    static std::mutex lock;
+    static DeviceSetup setups[64];
+    int dev = 0;
+    static DeviceSetup none;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        none.err = cudaErrorInvalidDevice;
+        return none;
+    }
+    std::lock_guard<std::mutex> g(lock);
+    DeviceSetup &d = setups[dev];
+    if (d.err == cudaErrorNotReady) {
+        cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (!e) e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+        if (!e) e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+        if (!e) e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+        if (!e) e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
+        if (!e) {
+            cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+            cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+            d.prep_resident = resident_ctas(prefill_prepare_tc, kPrepThreads, kPrepSmem, 256);
+            d.out_resident = resident_ctas(prefill_output_tc, 128, kOutSmem, 128);
+        }
+        d.err = e;
+    }
+    return d;
+}
+
+// Test hooks (include/kda_testing.h): a forced launch plan and an injected fault with a short wait bound.
+std::atomic<int> g_test_plan{-1};
+std::atomic<int> g_test_fault{0};
+std::atomic<long long> g_test_wait_ns{0};
+
+// Launches `kernel` as a cooperative grid (every CTA co-resident, or the launch fails), allowed to start while
+// the previous kernel in the stream finishes where the runtime accepts both attributes together.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge) return e;
+    cudaGetLastError();  // the pair of attributes was refused: a plain cooperative launch instead
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
-// CTAs of the chain-and-output launch: one per SM (its shared memory allows no more), 0 if unknown.
-int chain_ctas() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
-        return 0;
-    return sms;
+// Testing hooks (not part of the product path; see include/kda_testing.h).
+void testing_set_plan(int plan) { g_test_plan.store(plan); }
+void testing_set_fault(int fault, long long wait_ns) {
+    g_test_fault.store(fault);
+    g_test_wait_ns.store(wait_ns);
 }
 
 TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
-    // KDA_TC_PLAN = three | fused | chain picks a plan wherever it can run; KDA_TC_FUSED = 0 / 1 is the same
-    // as three / fused.  Otherwise (kAutoPlan): the chain plan when the chains leave at least
-    // kChainMinWorkers SMs for the output groups, else three kernels.
+    // The chain plan when the chains leave at least kChainMinWorkers SMs for the output groups, else three
+    // kernels; a plan forced by the test hook is taken wherever it can run.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
+    const int forced = g_test_plan.load();
+    if (forced == TC_THREE) return TC_THREE;
+    const DeviceSetup &d = device_setup();
+    if (d.err) return TC_THREE;
     const int n_state = num_seqs * H * kNTile;
-    const char *plan = getenv("KDA_TC_PLAN");
-    const char *fused_env = getenv("KDA_TC_FUSED");
-    int want = -1;  // -1 automatic
-    if (plan && !strcmp(plan, "three")) want = TC_THREE;
-    else if (plan && !strcmp(plan, "fused")) want = TC_FUSED;
-    else if (plan && !strcmp(plan, "chain")) want = TC_CHAIN;
-    else if (fused_env && fused_env[0] == '0') want = TC_THREE;
-    else if (fused_env && fused_env[0] == '1') want = TC_FUSED;
-    if (want == TC_THREE) return TC_THREE;
-    if (want == TC_CHAIN || (want < 0 && kAutoPlan == TC_CHAIN)) {
-        if (n_state + kChainMinWorkers <= chain_ctas()) return TC_CHAIN;
-        return TC_THREE;
-    }
-    if (want < 0 && n_state > kFusedMaxChains) return TC_THREE;
-    const int smem_f = (int)fused_smem_bytes();
-    if (cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_f) != cudaSuccess)
-        return TC_THREE;
-    cudaFuncSetAttribute(prefill_fused_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         (int)cudaSharedmemCarveoutMaxShared);
-    return resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256) >= n_state + kFusedMinWorkers ? TC_FUSED
-                                                                                                     : TC_THREE;
+    return n_state + kChainMinWorkers <= d.sms ? TC_CHAIN : TC_THREE;
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -1779,86 +1526,47 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks) {
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
+    const DeviceSetup &dset = device_setup();
+    if (dset.err) return dset.err;
     cudaError_t e;
-    // The fused plan (chosen by tc_plan, its flags zeroed by the chunk index kernel).
-    if (plan == TC_FUSED) {
-        const int n_state = num_seqs * H * kNTile;
-        const int smem_f = (int)fused_smem_bytes();
-        const int resident = resident_ctas(prefill_fused_tc, kPrepThreads, smem_f, 256);
-        {
-            CUtensorMap mq, mk, mv, mg;
-            if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
-                !make_input_map(&mv, v, total_tokens, H) || !make_gate_map(&mg, g, total_tokens, H))
-                return cudaErrorInvalidValue;
-            int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
-            const size_t nflag = (size_t)lay.max_slots * H;
-            FusedArgs f;
-            f.S0 = S0;
-            f.S_final = S_final;
-            f.o = static_cast<__nv_bfloat16 *>(o);
-            f.ready = flags;
-            f.sdone = flags + nflag;
-            f.counter = flags + 2 * nflag;
-            f.n_state = n_state;
-            // outputs trail the preparations by about the chunk slots the workers hold at once, so that an
-            // output's chunk has usually passed the state pass when claimed while its record is still in L2
-            f.lag = max(2, (resident - n_state) / H + 1);
-            f.stagger_ns = kFusedStaggerNs;
-            // One CTA per resident slot.  The state CTAs have the lowest indices, so they are placed first;
-            // worker CTAs take units from a counter, so one that starts late only finds less to do; and
-            // no wait outlasts its time bound even if a CTA could not be placed.
-            marks.before(st, "prefill_fused_tc");
-            return launch_dependent(prefill_fused_tc, dim3((unsigned)resident), dim3(kPrepThreads), (size_t)smem_f, st,
-                                    mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
-                                    lay.record_bytes, f);
-        }
-    }
     if (lay.max_slots > 0 && total_tokens > 0) {
-        CUtensorMap mq, mk, mv, mg;
-        if (!make_input_map(&mq, q, total_tokens, H) || !make_input_map(&mk, k, total_tokens, H) ||
-            !make_input_map(&mv, v, total_tokens, H) || !make_gate_map(&mg, g, total_tokens, H))
-            return cudaErrorInvalidValue;
-        const int smem = PrepSmem::bytes + 1024;
-        if ((e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
-            return e;
-        cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-        const int resident = resident_ctas(prefill_prepare_tc, kPrepThreads, smem, 256);
+        InputMaps m;
+        if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
         marks.before(st, "prefill_prepare_tc");
         if ((e = launch_dependent(prefill_prepare_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(kPrepThreads),
-                                  (size_t)smem, st, mq, mk, mv, mg, beta, cu, num_seqs, H, w, lay.doc_slot0_off,
-                                  lay.records_off, lay.record_bytes, resident)))
+                                  (size_t)kPrepSmem, st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.prep_resident)))
             return e;
     }
     if (num_seqs == 0) return cudaSuccess;
-    const int smem = StateSmem::bytes + 1024;
     if (plan == TC_CHAIN) {
-        if ((e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
         int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
         const size_t nflag = (size_t)lay.max_slots * H;
         const int n_state = num_seqs * H * kNTile;
+        const long long wait = g_test_wait_ns.load();
+        const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
+        // Cooperative: the output groups wait for the chain CTAs' publications, so every CTA must be resident.
         marks.before(st, "prefill_chain_tc");
-        return launch_dependent(prefill_chain_tc, dim3((unsigned)chain_ctas()), dim3(kStateThreads), (size_t)smem, st,
-                                cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off,
-                                lay.records_off, lay.record_bytes, n_state, flags + nflag, flags + 2 * nflag);
+        e = launch_cooperative(prefill_chain_tc, dim3((unsigned)dset.sms), dim3(kStateThreads), (size_t)kStateSmem,
+                               st, cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o), w,
+                               lay.doc_slot0_off, lay.records_off, lay.record_bytes, n_state, flags, flags + nflag,
+                               flag_wait, g_test_fault.load());
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        // Fewer SMs are available to this context than the device has: nothing was launched; run the state
+        // pass and the output pass as separate kernels instead.
+        cudaGetLastError();
+        marks.n--;
     }
-    if ((e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
     marks.before(st, "prefill_state_tc");
     if ((e = launch_dependent(prefill_state_tc, dim3((unsigned)((size_t)num_seqs * H * kNTile)), dim3(kStateThreads),
-                              (size_t)smem, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off,
-                              lay.record_bytes)))
+                              (size_t)kStateSmem, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off,
+                              lay.records_off, lay.record_bytes)))
         return e;
     if (lay.max_slots > 0 && total_tokens > 0) {
-        const int smem_o = OutSmem::bytes + 1024;
-        if ((e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_o)))
-            return e;
-        cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-        const int resident = resident_ctas(prefill_output_tc, 128, smem_o, 128);
         marks.before(st, "prefill_output_tc");
         if ((e = launch_dependent(prefill_output_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(128),
-                                  (size_t)smem_o, st, cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w,
-                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, resident)))
+                                  (size_t)kOutSmem, st, cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w,
+                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.out_resident)))
             return e;
     }
     return cudaSuccess;

@@ -18,7 +18,12 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_F32, KDA_BF16 = 0, 1
 
 SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_chunked_profiled",
-           "kda_prefill_check", "kda_decode_step")
+           "kda_prefill_check", "kda_decode_step", "kda_prefill_chunked_noalloc", "kda_prefill_noalloc_check",
+           "kda_decode_step_indexed", "kda_state_snapshot", "kda_state_restore")
+# include/kda_testing.h (test hooks)
+TESTING_SYMBOLS = ("kda_testing_set_plan", "kda_testing_set_fault")
+PLAN_AUTO, PLAN_THREE, PLAN_CHAIN = -1, 0, 2
+FAULT_NONE, FAULT_NO_PUBLISH = 0, 1
 PREFILL_MAX_KERNELS = 4
 
 _lib = None
@@ -59,6 +64,21 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.kda_prefill_check.argtypes = [vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, i32, i32, i32, i32, ctypes.c_int, fp, vp, vp]
+    lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
+    lib.kda_prefill_chunked_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
+                                                i32, vp, vp, vp, vp]
+    lib.kda_prefill_noalloc_check.restype = ctypes.c_int
+    lib.kda_prefill_noalloc_check.argtypes = [vp]
+    lib.kda_decode_step_indexed.restype = ctypes.c_int
+    lib.kda_decode_step_indexed.argtypes = [vp, vp, vp, fp, fp, vp, i32, i32, i32, i32, i32, ctypes.c_int, fp, vp,
+                                            vp, vp]
+    for name in ("kda_state_snapshot", "kda_state_restore"):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = [fp, vp, i32, i32, i32, i32, i32, fp, vp, vp]
+    lib.kda_testing_set_plan.restype = ctypes.c_int
+    lib.kda_testing_set_plan.argtypes = [i32]
+    lib.kda_testing_set_fault.restype = ctypes.c_int
+    lib.kda_testing_set_fault.argtypes = [i32, ctypes.c_int64]
     _lib = lib
     return lib
 
@@ -143,6 +163,24 @@ def kda_prefill_check(workspace, stream=None) -> int:
     return int(load().kda_prefill_check(_ptr(workspace), _stream(stream)))
 
 
+def kda_prefill_noalloc_check(stream=None) -> int:
+    return int(load().kda_prefill_noalloc_check(_stream(stream)))
+
+
+def testing_set_plan(plan: int) -> None:
+    """Test hook (include/kda_testing.h): force a launch plan of the tensor-core prefill (PLAN_AUTO restores)."""
+    rc = load().kda_testing_set_plan(int(plan))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_testing_set_plan")
+
+
+def testing_set_fault(fault: int, wait_limit_ns: int = 0) -> None:
+    """Test hook (include/kda_testing.h): inject a fault and bound the flag waits (FAULT_NONE, 0 restores)."""
+    rc = load().kda_testing_set_fault(int(fault), int(wait_limit_ns))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_testing_set_fault")
+
+
 def kda_decode_step(q, k, v, g, beta, S_inout, o, stream=None) -> None:
     """Calls kda_decode_step on caller-owned device tensors (see include/kda.h)."""
     N, H, d_k = q.shape
@@ -151,6 +189,35 @@ def kda_decode_step(q, k, v, g, beta, S_inout, o, stream=None) -> None:
                                 _ptr(S_inout), _ptr(o), _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
+
+
+def kda_decode_step_indexed(q, k, v, g, beta, seq_idx, S_pool, o, status=None, stream=None) -> None:
+    """Calls kda_decode_step_indexed: one token for each listed pool slot (see include/kda.h)."""
+    A, H, d_k = q.shape
+    d_v = v.shape[2]
+    rc = load().kda_decode_step_indexed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seq_idx), A,
+                                        S_pool.shape[0], H, d_k, d_v, _dtype_code(q), _ptr(S_pool), _ptr(o),
+                                        _ptr(status), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step_indexed")
+
+
+def kda_state_snapshot(S_pool, seq_idx, S_saved, status=None, stream=None) -> None:
+    """S_saved[i] = S_pool[seq_idx[i]] (kda_state_snapshot)."""
+    num_slots, H, d_k, d_v = S_pool.shape
+    rc = load().kda_state_snapshot(_ptr(S_pool), _ptr(seq_idx), seq_idx.numel(), num_slots, H, d_k, d_v,
+                                   _ptr(S_saved), _ptr(status), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_state_snapshot")
+
+
+def kda_state_restore(S_saved, seq_idx, S_pool, status=None, stream=None) -> None:
+    """S_pool[seq_idx[i]] = S_saved[i] (kda_state_restore)."""
+    num_slots, H, d_k, d_v = S_pool.shape
+    rc = load().kda_state_restore(_ptr(S_saved), _ptr(seq_idx), seq_idx.numel(), num_slots, H, d_k, d_v,
+                                  _ptr(S_pool), _ptr(status), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_state_restore")
 
 
 def new_workspace(T, N, H, d_k, d_v, in_dtype, chunk_size, device) -> torch.Tensor:
@@ -179,7 +246,6 @@ def decode_step(q, k, v, g, beta, S_inout, stream=None):
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
-_noalloc_ready = False
 
 
 def kda_prefill_chunked_noalloc(q, k, v, g, beta, cu_seqlens, o, S0=None, S_final=None, chunk_size=64,
@@ -189,14 +255,7 @@ def kda_prefill_chunked_noalloc(q, k, v, g, beta, cu_seqlens, o, S0=None, S_fina
     For callers that must not allocate device memory; see include/kda.h for
     the scratch limit and the rule that overlapping calls on one GPU race.
     """
-    global _noalloc_ready
     lib = load()
-    if not _noalloc_ready:
-        vp, i32 = ctypes.c_void_p, ctypes.c_int32
-        lib.kda_prefill_chunked_noalloc.restype = ctypes.c_int
-        lib.kda_prefill_chunked_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
-                                                    i32, vp, vp, vp, vp]
-        _noalloc_ready = True
     T, H, d_k = q.shape
     N = cu_seqlens.numel() - 1
     rc = lib.kda_prefill_chunked_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H,

@@ -147,10 +147,20 @@ def workload_seed(name: str) -> int:
     return BASE_SEED + WORKLOADS[name]["index"]
 
 
-def workload_prefill(name: str, device="cpu") -> PrefillInputs:
-    """Prefill inputs of the tiny / prefill / varlen / long workloads (zero S0)."""
+def workload_prefill(name: str, device="cpu", head_block: int = 0) -> PrefillInputs:
+    """Prefill inputs of the tiny / prefill / varlen / long workloads (zero S0).
+
+    `head_block` b > 0 draws the inputs of heads [b H, (b + 1) H) of a larger problem made of several such
+    blocks side by side (block 0 is the workload itself): the same documents, inputs from their own seed.
+    """
     w = WORKLOADS[name]
     seed = workload_seed(name)
+    if head_block:
+        lengths_seed = seed
+        seed = seed + 1000 * head_block
+        if name == "varlen":
+            lengths = varlen_lengths(w["docs"], w["len_lo"], w["len_hi"], lengths_seed)
+            return prefill_inputs(lengths, w["H"], w["d"], w["dtype"], seed, device)
     if name == "varlen":
         lengths = varlen_lengths(w["docs"], w["len_lo"], w["len_hi"], seed)
     else:

@@ -54,7 +54,7 @@ typedef enum {
     KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad cu_seqlens, small workspace */
     KDA_ERR_UNSUPPORTED = 2, /* a size or dtype outside the supported set */
     KDA_ERR_CUDA = 3,        /* a CUDA launch or driver call failed */
-    KDA_ERR_TIMEOUT = 4      /* reserved: a bounded device-side wait gave up */
+    KDA_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by kda_prefill_check) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -120,9 +120,18 @@ KDA_API kda_status kda_prefill_chunked_profiled(const void *q, const void *k, co
                                         void *const *events, int32_t *num_kernels, const char **kernel_names);
 
 /*
- * Reports whether the last kda_prefill_chunked call that used this workspace
- * found cu_seqlens valid.  It copies one word back and SYNCHRONISES `stream`.
- * Returns KDA_OK or KDA_ERR_INVALID_ARG.
+ * Reports how the last kda_prefill_chunked call that used this workspace
+ * ended on the device.  It copies one status word back and SYNCHRONISES
+ * `stream` (the stream the call was enqueued on).  Returns
+ *   KDA_OK               the call completed;
+ *   KDA_ERR_INVALID_ARG  cu_seqlens was not valid: o and S_final were left
+ *                        unwritten;
+ *   KDA_ERR_TIMEOUT      a bounded wait inside a kernel gave up (a CTA of a
+ *                        cooperative launch, or an asynchronous copy, never
+ *                        arrived within its time bound of one to two
+ *                        seconds): o and S_final may be partly written.  The
+ *                        context stays usable and the next call starts afresh;
+ *   KDA_ERR_CUDA         the copy or the synchronisation failed.
  */
 KDA_API kda_status kda_prefill_check(const void *workspace, void *stream);
 
@@ -139,6 +148,48 @@ KDA_API kda_status kda_prefill_check(const void *workspace, void *stream);
 KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g, const float *beta,
                            int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
                            float *S_inout, void *o, void *stream);
+
+/*
+ * Decode step for a batch that mixes request phases (Lecture 04, section 2:
+ * the fused recurrent kernel serves the sequences that are generating, while
+ * others are still in their chunked prefill).  The states live in a pool of
+ * num_slots slots; the i-th active sequence's token updates slot
+ * seq_idx[i].  Slots that are not listed are not touched.
+ *
+ *   q, k       [num_active, H, d_k] in_dtype   v [num_active, H, d_v] in_dtype
+ *   g          [num_active, H, d_k] fp32       beta [num_active, H] fp32
+ *   seq_idx    [num_active] int32, device: distinct slots in [0, num_slots)
+ *              (listing a slot twice makes the two updates race)
+ *   S_pool     [num_slots, H, d_k, d_v] fp32, the listed slots read and
+ *              overwritten with S_t
+ *   o          [num_active, H, d_v] in_dtype, o_t = S_t^T q_t
+ *   status     optional device int32 (NULL to skip), 4-byte aligned: a slot
+ *              outside [0, num_slots) is skipped (its state and o rows are not
+ *              written) and sets *status to KDA_ERR_INVALID_ARG if it was 0.
+ */
+KDA_API kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, const float *g,
+                                           const float *beta, const int32_t *seq_idx, int32_t num_active,
+                                           int32_t num_slots, int32_t H, int32_t d_k, int32_t d_v,
+                                           kda_dtype in_dtype, float *S_pool, void *o, int32_t *status,
+                                           void *stream);
+
+/*
+ * State snapshot and restore for rollback (Lecture 11, section 2, "Serving
+ * state" row: speculative rollback must reconcile the KDA state; section 3:
+ * a run after rollback must equal a from-scratch run).  Each copies whole
+ * slots (all H heads) bit for bit:
+ *   kda_state_snapshot  S_saved[i] = S_pool[seq_idx[i]]   (i < n)
+ *   kda_state_restore   S_pool[seq_idx[i]] = S_saved[i]
+ * S_pool is [num_slots, H, d_k, d_v] fp32, S_saved [n, H, d_k, d_v] fp32, both
+ * device and 16-byte aligned; seq_idx and status as for
+ * kda_decode_step_indexed (a restore that lists a slot twice races).
+ */
+KDA_API kda_status kda_state_snapshot(const float *S_pool, const int32_t *seq_idx, int32_t n, int32_t num_slots,
+                                      int32_t H, int32_t d_k, int32_t d_v, float *S_saved, int32_t *status,
+                                      void *stream);
+KDA_API kda_status kda_state_restore(const float *S_saved, const int32_t *seq_idx, int32_t n, int32_t num_slots,
+                                     int32_t H, int32_t d_k, int32_t d_v, float *S_pool, int32_t *status,
+                                     void *stream);
 
 /*
  * Chunked prefill that allocates nothing.  The course pages have no
@@ -162,11 +213,19 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
  *     the GPU (unordered streams) race and corrupt each other's results.
  *     Calls ordered on one stream are safe.  Nothing in the array needs to
  *     start at zero.
- *   - kda_prefill_check is not available for these calls (the status word
- *     sits in the shared array); invalid cu_seqlens still leave o and S_final
- *     unwritten.
+ *   - Their device-side status (invalid cu_seqlens, a wait that ran out) is
+ *     read with kda_prefill_noalloc_check; invalid cu_seqlens leave o and
+ *     S_final unwritten.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+/*
+ * kda_prefill_check for the no-allocation entry point: reads the status word
+ * of the static scratch on the current device and SYNCHRONISES `stream`.  The
+ * word describes the last kda_prefill_chunked_noalloc call on this device and
+ * is valid until the next such call.  Same return values as
+ * kda_prefill_check.
+ */
+KDA_API kda_status kda_prefill_noalloc_check(void *stream);
 KDA_API kda_status kda_prefill_chunked_noalloc(const void *q, const void *k, const void *v, const float *g,
                                                const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                                                int32_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,

@@ -6,6 +6,9 @@ fp32 inputs and <= 2e-2 for bf16 inputs.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -40,5 +43,13 @@ def to_device(inp):
     return [x.to(d) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens)]
 
 
-def rel(x, ref):
-    return oracle.rel_err(f64(x) if torch.is_tensor(x) else x, ref)
+def rel(x, ref, label: str = ""):
+    """max|x - ref| / max|ref|.  With KDA_PARITY_LOG set, every measured error is appended there as one JSON
+    line with the running test's name, so that the margin under the tolerance can be tabulated."""
+    err = oracle.rel_err(f64(x) if torch.is_tensor(x) else x, ref)
+    path = os.environ.get("KDA_PARITY_LOG")
+    if path:
+        with open(path, "a") as fh:
+            fh.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], "label": label,
+                                 "err": err}) + "\n")
+    return err

@@ -89,3 +89,12 @@ def test_decode_rejects_bad_arguments_on_the_host():
         libkda.KDA_ERR_INVALID_ARG
     assert lib.kda_decode_step(fake, fake, fake, fake, fake, 4, 1, 128, 128, 1, fake, fake, None) == \
         libkda.KDA_ERR_INVALID_ARG  # o aliases q
+
+
+def test_testing_hooks_check_their_arguments():
+    lib = libkda.load()
+    assert lib.kda_testing_set_plan(5) == libkda.KDA_ERR_INVALID_ARG
+    assert lib.kda_testing_set_fault(3, 0) == libkda.KDA_ERR_INVALID_ARG
+    assert lib.kda_testing_set_fault(libkda.FAULT_NO_PUBLISH, -1) == libkda.KDA_ERR_INVALID_ARG
+    assert lib.kda_testing_set_plan(libkda.PLAN_AUTO) == libkda.KDA_OK
+    assert lib.kda_testing_set_fault(libkda.FAULT_NONE, 0) == libkda.KDA_OK

@@ -66,3 +66,53 @@ def test_traffic_entries_ignore_comment_edits():
     code = "int f(int x) {  // doubles x\n    /* body */ return 2 * x;\n}\n"
     assert bench._code_only(code) == bench._code_only(code.replace("doubles x", "twice x").replace("body", "b"))
     assert bench._code_only(code) != bench._code_only(code.replace("2 * x", "3 * x"))
+
+
+def _split_rank_main(rank, world, port, out):
+    """One rank of the head split: its slice of a small problem through the oracle (standing in for the GPU
+    library on CPU ranks); the test alone gathers the slices to compare them with the unsplit run."""
+    sys.path.insert(0, ROOT)
+    from gated_delta_rule_27_gb300 import shard, workloads
+    from oracle import oracle
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        H = 5
+        inp = workloads.prefill_inputs([23, 0, 17], H=H, d=16, dtype=torch.float32, seed=91, s0_std=0.3)
+        lo, hi = shard.head_range(H, world, rank)
+        part = [shard.take_heads(x, lo, hi, 1).double().numpy() for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+        S0 = shard.take_heads(inp.S0, lo, hi, 1).double().numpy()
+        o, S, _ = oracle.run(*part, inp.cu_seqlens.numpy(), S0=S0, threads=1)
+        gathered = [None] * world
+        torch.distributed.all_gather_object(gathered, (lo, hi, o, S))
+        if rank == 0:
+            o_full, S_full, _ = oracle.run(*(x.double().numpy() for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)),
+                                           inp.cu_seqlens.numpy(), S0=inp.S0.double().numpy(), threads=1)
+            import numpy as np
+            spans = [(a, b) for a, b, _, _ in gathered]
+            o_cat = np.concatenate([x for _, _, x, _ in gathered], axis=1)
+            S_cat = np.concatenate([x for _, _, _, x in gathered], axis=1)
+            out["spans"] = spans
+            out["same"] = bool(np.array_equal(o_cat, o_full) and np.array_equal(S_cat, S_full))
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_head_split_over_two_gloo_ranks_concatenates_to_the_unsplit_run():
+    world, port = 2, _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_split_rank_main, args=(world, port, out), nprocs=world, join=True)
+    assert out["spans"] == [(0, 3), (3, 5)]
+    assert out["same"]  # every chain is independent: the split changes no bit
+
+
+def test_head_ranges_cover_every_head_once():
+    sys.path.insert(0, ROOT)
+    from gated_delta_rule_27_gb300 import shard
+    for H in (1, 5, 16, 32, 33):
+        for world in (1, 2, 3, 4, 8):
+            spans = [shard.head_range(H, world, r) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == H
+            assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+            assert max(b - a for a, b in spans) - min(b - a for a, b in spans) <= 1

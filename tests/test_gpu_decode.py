@@ -65,11 +65,11 @@ def test_decode_workload_full():
     torch.cuda.synchronize()
     o_ref, S_ref, snaps = _oracle_steps(dec, chains, S0_cpu, snap_t=snap_steps)
     tol = TOL[w["dtype"]]
-    assert rel(o_all.transpose(0, 1), o_ref) <= tol
-    assert rel(S[idx_n, idx_h], S_ref) <= tol
+    assert rel(o_all.transpose(0, 1), o_ref, "o 1000 steps") <= tol
+    assert rel(S[idx_n, idx_h], S_ref, "S after 1000 steps") <= tol
     for j, t in enumerate(snap_steps):
         ref = np.stack([snaps[j, c, 0] for c in range(len(chains))])
-        assert rel(snaps_gpu[t], ref) <= tol, t
+        assert rel(snaps_gpu[t], ref, "S at step %d" % t) <= tol, t
 
 
 def test_decode_deterministic_and_guarded():

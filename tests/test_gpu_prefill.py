@@ -32,11 +32,11 @@ def test_tiny_workload_every_boundary():
     o_ref, S_ref, snaps = oracle_prefill(inp, snap_t=list(range(16, 65, 16)))
     for chunk in (16, 32, 64):
         o, S = _run(inp, chunk)
-        assert rel(o, o_ref) <= TOL[torch.float32], chunk
-        assert rel(S, S_ref) <= TOL[torch.float32], chunk
+        assert rel(o, o_ref, "o chunk %d" % chunk) <= TOL[torch.float32], chunk
+        assert rel(S, S_ref, "S chunk %d" % chunk) <= TOL[torch.float32], chunk
     for j, t in enumerate(range(16, 65, 16)):
         _, S = _run(_prefix(inp, t), w["chunk"])
-        assert rel(S, snaps[j]) <= TOL[torch.float32], t
+        assert rel(S, snaps[j], "S at %d" % t) <= TOL[torch.float32], t
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
@@ -65,11 +65,11 @@ def test_prefill_workload_full():
     bounds = [64, 128, 1024, 2048, 4032]
     o_ref, S_ref, snaps = oracle_prefill(inp, snap_t=bounds)
     o, S = _run(inp, 64)
-    assert rel(o, o_ref) <= TOL[torch.bfloat16], rel(o, o_ref)
-    assert rel(S, S_ref) <= TOL[torch.bfloat16], rel(S, S_ref)
+    assert rel(o, o_ref, "o") <= TOL[torch.bfloat16]
+    assert rel(S, S_ref, "S") <= TOL[torch.bfloat16]
     for j, t in enumerate(bounds):
         _, St = _run(_prefix(inp, t), 64)
-        assert rel(St, snaps[j]) <= TOL[torch.bfloat16], t
+        assert rel(St, snaps[j], "S at %d" % t) <= TOL[torch.bfloat16], t
 
 
 def test_varlen_workload_and_document_isolation():
@@ -78,8 +78,8 @@ def test_varlen_workload_and_document_isolation():
     o, S = _run(inp, 64)
     heads = [0, 13, 31]
     o_ref, S_ref, _ = oracle_prefill(inp, heads=heads)
-    assert rel(o[:, heads], o_ref) <= TOL[torch.bfloat16]
-    assert rel(S[:, heads], S_ref) <= TOL[torch.bfloat16]
+    assert rel(o[:, heads], o_ref, "o heads 0,13,31") <= TOL[torch.bfloat16]
+    assert rel(S[:, heads], S_ref, "S heads 0,13,31") <= TOL[torch.bfloat16]
     cu = inp.cu_seqlens.tolist()
     for i in (0, 3, 7):
         a, b = cu[i], cu[i + 1]
@@ -135,9 +135,9 @@ def test_long_workload_three_paths():
     torch.cuda.synchronize()
 
     tol = TOL[torch.bfloat16]
-    for o_x, S_x in ((o2, Sb), (o3, Sd)):
-        assert rel(o_x, f64(o1)) <= tol
-        assert rel(S_x, f64(S1)) <= tol
+    for name, o_x, S_x in (("continuation", o2, Sb), ("prefill+decode", o3, Sd)):
+        assert rel(o_x, f64(o1), "o %s vs one pass" % name) <= tol
+        assert rel(S_x, f64(S1), "S %s vs one pass" % name) <= tol
     # each path against the oracle on two sampled chains (seq 0 head 5, seq 1 head 20), one oracle call
     chains = ((0, 5), (1, 20))
     parts = [[x[seq * T:(seq + 1) * T, h:h + 1].cpu() for x in (q, k, v, g, beta)] for seq, h in chains]
@@ -146,9 +146,9 @@ def test_long_workload_three_paths():
     o_ref, S_ref, _ = oracle_prefill(both)
     for c, (seq, h) in enumerate(chains):
         sl = slice(seq * T, (seq + 1) * T)
-        for o_x, S_x in ((o1, S1), (o2, Sb), (o3, Sd)):
-            assert rel(o_x[sl, h:h + 1], o_ref[c * T:(c + 1) * T]) <= tol
-            assert rel(S_x[seq, h], S_ref[c, 0]) <= tol
+        for name, o_x, S_x in (("one pass", o1, S1), ("continuation", o2, Sb), ("prefill+decode", o3, Sd)):
+            assert rel(o_x[sl, h:h + 1], o_ref[c * T:(c + 1) * T], "o %s vs oracle" % name) <= tol
+            assert rel(S_x[seq, h], S_ref[c, 0], "S %s vs oracle" % name) <= tol
 
 
 def test_empty_and_degenerate_documents():

@@ -1,16 +1,14 @@
 """The launch plans of the tensor-core prefill agree with the oracle and with each other.
 
 bf16 inputs with d = 128 and 64-token chunks take the tensor-core path.  It runs
-as three kernels (preparation, state pass, output), as one launch that overlaps
-all three, or as the preparation followed by one launch running the state
-chains with the output units alongside; KDA_TC_PLAN (or KDA_TC_FUSED=0 / 1)
-forces a plan.  All perform the same arithmetic in the same order, so their
-results must be bitwise identical, and they must meet the bf16 tolerance
-against the fp64 oracle.
+as three kernels (preparation, state pass, output), or as the preparation
+followed by one cooperative launch running the state chains with the output
+units alongside; the test hook kda_testing_set_plan forces a plan.  Both
+perform the same arithmetic in the same order, so their results must be
+bitwise identical, and they must meet the bf16 tolerance against the fp64
+oracle.
 """
 from __future__ import annotations
-
-import os
 
 import pytest
 import torch
@@ -24,11 +22,7 @@ pytestmark = pytest.mark.gpu
 def _run(inp, plan, S0=None, poison=0x7F):
     """One call under the given launch plan, on a workspace whose every byte is `poison` beforehand, so that
     nothing a call reads before writing it can pass for a result."""
-    saved = {key: os.environ.pop(key, None) for key in ("KDA_TC_FUSED", "KDA_TC_PLAN")}
-    if plan in ("three", "fused", "chain"):
-        os.environ["KDA_TC_PLAN"] = plan
-    elif plan != "auto":
-        os.environ["KDA_TC_FUSED"] = plan
+    libkda.testing_set_plan({"auto": libkda.PLAN_AUTO, "three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN}[plan])
     try:
         q, k, v, g, beta, cu = to_device(inp)
         T, H, d = q.shape
@@ -42,10 +36,7 @@ def _run(inp, plan, S0=None, poison=0x7F):
         torch.cuda.synchronize()
         assert libkda.kda_prefill_check(ws) == 0
     finally:
-        for key, val in saved.items():
-            os.environ.pop(key, None)
-            if val is not None:
-                os.environ[key] = val
+        libkda.testing_set_plan(libkda.PLAN_AUTO)
     return o, S
 
 
@@ -64,21 +55,18 @@ CASES = {
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_fused_and_three_kernel_plans_agree(case):
+def test_chain_and_three_kernel_plans_agree(case):
     c = CASES[case]
     inp = workloads.prefill_inputs(c["lengths"], H=c["H"], d=128, dtype=torch.bfloat16, seed=300 + len(case),
                                    s0_std=c["s0"] or None)
     S0 = inp.S0
-    o3, S3 = _run(inp, "0", S0, poison=0x00)
-    of, Sf = _run(inp, "1", S0, poison=0x7F)
+    o3, S3 = _run(inp, "three", S0, poison=0x00)
     oc, Sc = _run(inp, "chain", S0, poison=0x5A)
-    assert torch.equal(o3, of), (o3.float() - of.float()).abs().max().item()
-    assert torch.equal(S3, Sf), (S3 - Sf).abs().max().item()
     assert torch.equal(o3, oc), (o3.float() - oc.float()).abs().max().item()
     assert torch.equal(S3, Sc), (S3 - Sc).abs().max().item()
     o_ref, S_ref, _ = oracle_prefill(inp, S0=S0)
-    assert rel(of, o_ref) <= TOL[torch.bfloat16], rel(of, o_ref)
-    assert rel(Sf, S_ref) <= TOL[torch.bfloat16], rel(Sf, S_ref)
+    assert rel(oc, o_ref) <= TOL[torch.bfloat16], rel(oc, o_ref)
+    assert rel(Sc, S_ref) <= TOL[torch.bfloat16], rel(Sc, S_ref)
 
 
 def test_automatic_plan_on_the_prefill_workload_twice():
@@ -97,15 +85,15 @@ def test_automatic_plan_on_the_prefill_workload_twice():
         assert libkda.kda_prefill_check(ws) == 0
         outs.append((o, S))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
-    o3, S3 = _run(inp, "0")
+    o3, S3 = _run(inp, "three")
     assert torch.equal(o3, outs[0][0]) and torch.equal(S3, outs[0][1])
 
 
-@pytest.mark.parametrize("plan", ["three", "fused", "chain"])
+@pytest.mark.parametrize("plan", ["three", "chain"])
 def test_full_prefill_workload_on_poisoned_workspaces(plan):
     """The prefill workload under each launch plan on a workspace poisoned with two different patterns: the
-    kernels overlap at their boundaries (and, in the chain and fused plans, hand data over through flags), so any
-    read of a record before it is written would show up as a difference."""
+    kernels overlap at their boundaries (and, in the chain plan, hand data over through flags), so any read of
+    a record before it is written would show up as a difference."""
     inp = workloads.workload_prefill("prefill")
     o_a, S_a = _run(inp, plan, poison=0x00)
     o_b, S_b = _run(inp, plan, poison=0x7F)
