@@ -27,6 +27,26 @@ kda_status shape_check(int32_t total_tokens, int32_t num_seqs, int32_t H, int32_
     return KDA_OK;
 }
 
+// The fused prologue / epilogue options, checked (pointers only when the call has rows to process).
+kda_status fusion_from(const kda_fusion_opts *opts, bool any_rows, const void *o, kda::Fusion *fu) {
+    *fu = kda::Fusion{};
+    if (!opts) return KDA_OK;
+    if (opts->qk_l2norm) {
+        if (!(opts->qk_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+        fu->qk_norm = 1;
+        fu->qk_eps = opts->qk_eps;
+    }
+    if (opts->out_gate) {
+        if (!(opts->out_eps > 0.f)) return KDA_ERR_INVALID_ARG;
+        if (any_rows && (!aligned16(opts->out_gate) || opts->out_gate == o)) return KDA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(opts->out_weight) & 3u) return KDA_ERR_INVALID_ARG;
+        fu->gate = opts->out_gate;
+        fu->weight = opts->out_weight;
+        fu->out_eps = opts->out_eps;
+    }
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -56,10 +76,13 @@ namespace {
 kda_status prefill_impl(const void *q, const void *k, const void *v, const float *g, const float *beta,
                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t d_k,
                         int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
-                        float *S_final, void *workspace, size_t workspace_bytes, void *stream, kda::Marks &marks) {
+                        float *S_final, void *workspace, size_t workspace_bytes, void *stream, kda::Marks &marks,
+                        const kda_fusion_opts *opts = nullptr) {
     const int32_t L = chunk_size == 0 ? 64 : chunk_size;
     kda_status st = shape_check(total_tokens, num_seqs, H, d_k, d_v, in_dtype, L);
     if (st != KDA_OK) return st;
+    kda::Fusion fu;
+    if ((st = fusion_from(opts, total_tokens > 0, o, &fu)) != KDA_OK) return st;
     if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0) {
         if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
@@ -82,10 +105,10 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (path == kda::PATH_TC)
         e = kda::launch_prefill_tc(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, S0, o, S_final, workspace,
-                                   plan, s, marks);
+                                   plan, fu, s, marks);
     else
         e = kda::launch_prefill_simt(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, in_dtype, L, S0,
-                                     o, S_final, workspace, s, marks);
+                                     o, S_final, workspace, fu, s, marks);
     marks.end(s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -101,6 +124,16 @@ kda_status kda_prefill_chunked(const void *q, const void *k, const void *v, cons
     kda::Marks marks;
     return prefill_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype, chunk_size, S0,
                         o, S_final, workspace, workspace_bytes, stream, marks);
+}
+
+kda_status kda_prefill_chunked_ex(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                  const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
+                                  int32_t d_k, int32_t d_v, kda_dtype in_dtype, int32_t chunk_size, const float *S0,
+                                  void *o, float *S_final, void *workspace, size_t workspace_bytes, void *stream,
+                                  const kda_fusion_opts *opts) {
+    kda::Marks marks;
+    return prefill_impl(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype, chunk_size, S0,
+                        o, S_final, workspace, workspace_bytes, stream, marks, opts);
 }
 
 kda_status kda_prefill_chunked_profiled(const void *q, const void *k, const void *v, const float *g,
@@ -143,7 +176,15 @@ kda_status kda_testing_set_fault(int32_t fault, int64_t wait_limit_ns) {
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g, const float *beta,
                            int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
                            float *S_inout, void *o, void *stream) {
+    return kda_decode_step_ex(q, k, v, g, beta, num_seqs, H, d_k, d_v, in_dtype, S_inout, o, stream, nullptr);
+}
+
+kda_status kda_decode_step_ex(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                              int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                              float *S_inout, void *o, void *stream, const kda_fusion_opts *opts) {
     if (num_seqs < 0 || H <= 0 || !valid_dtype(in_dtype)) return KDA_ERR_INVALID_ARG;
+    kda::Fusion fu;
+    if (kda_status st = fusion_from(opts, num_seqs > 0, o, &fu)) return st;
     if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > INT_MAX) return KDA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return KDA_OK;
@@ -153,7 +194,7 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
     if (reinterpret_cast<uintptr_t>(beta) & 3u) return KDA_ERR_INVALID_ARG;
     if (o == q || o == k || o == v || o == (const void *)S_inout) return KDA_ERR_INVALID_ARG;
     cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_seqs, H, d_k, in_dtype, S_inout, o, nullptr, num_seqs,
-                                       nullptr, static_cast<cudaStream_t>(stream));
+                                       nullptr, fu, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -173,7 +214,7 @@ kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, 
         return KDA_ERR_INVALID_ARG;
     if (o == q || o == k || o == v || o == (const void *)S_pool) return KDA_ERR_INVALID_ARG;
     cudaError_t e = kda::launch_decode(q, k, v, g, beta, num_active, H, d_k, in_dtype, S_pool, o, seq_idx, num_slots,
-                                       status, static_cast<cudaStream_t>(stream));
+                                       status, kda::Fusion{}, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -188,6 +229,43 @@ static kda_status state_copy(const float *src, float *dst, const int32_t *seq_id
         return KDA_ERR_INVALID_ARG;
     cudaError_t e = kda::launch_state_copy(src, dst, seq_idx, n, num_slots, H, d_k, scatter, status,
                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_short_conv_prefill(const void *x, const float *w, const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int32_t total_tokens, int32_t C, int32_t W, kda_dtype in_dtype,
+                                  const float *conv_state, void *y, float *conv_state_out, void *stream) {
+    if (total_tokens < 0 || num_seqs < 0 || C <= 0 || !valid_dtype(in_dtype)) return KDA_ERR_INVALID_ARG;
+    if (W < 1 || W > KDA_SHORT_CONV_MAX_W) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)total_tokens * C > INT_MAX || (int64_t)num_seqs * W * C > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    const uintptr_t el = in_dtype == KDA_BF16 ? 1u : 3u;
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!x || !w || !y || (reinterpret_cast<uintptr_t>(x) & el) ||
+                             (reinterpret_cast<uintptr_t>(y) & el) || x == y))
+        return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(conv_state) & 3u) ||
+        (reinterpret_cast<uintptr_t>(conv_state_out) & 3u))
+        return KDA_ERR_INVALID_ARG;
+    if (W > 1 && conv_state && conv_state == conv_state_out) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_conv_prefill(x, w, cu_seqlens, num_seqs, total_tokens, C, W, in_dtype,
+                                             W > 1 ? conv_state : nullptr, y, W > 1 ? conv_state_out : nullptr,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_short_conv_decode(const void *x, const float *w, int32_t N, int32_t C, int32_t W, kda_dtype in_dtype,
+                                 float *conv_state, void *y, void *stream) {
+    if (N < 0 || C <= 0 || !valid_dtype(in_dtype)) return KDA_ERR_INVALID_ARG;
+    if (W < 1 || W > KDA_SHORT_CONV_MAX_W) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * W * C > INT_MAX) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    const uintptr_t el = in_dtype == KDA_BF16 ? 1u : 3u;
+    if (!x || !w || !y || (W > 1 && !conv_state) || (reinterpret_cast<uintptr_t>(x) & el) ||
+        (reinterpret_cast<uintptr_t>(y) & el) || (reinterpret_cast<uintptr_t>(w) & 3u) ||
+        (reinterpret_cast<uintptr_t>(conv_state) & 3u) || x == y)
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_conv_decode(x, w, N, C, W, in_dtype, conv_state, y, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -34,6 +34,20 @@ namespace {
 
 constexpr int kRows = 16;  // rows of S per thread
 
+// Sum of squares of x[0, n) by the 32 lanes of a warp (every lane gets it), or by one thread, in a fixed order.
+__device__ __forceinline__ float warp_sum_squares(const float *x, int n, int lane) {
+    float ss = 0.f;
+    for (int i = lane; i < n; i += 32) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    return ss;
+}
+__device__ __forceinline__ float serial_sum_squares(const float *x, int n) {
+    float ss = 0.f;
+    for (int i = 0; i < n; ++i) ss = fmaf(x[i], x[i], ss);
+    return ss;
+}
+
 // One CTA per (active sequence, head).  With `idx` null, sequence i's state is S[i]; otherwise it is the
 // pool slot idx[i] (a slot outside [0, num_slots) is skipped and recorded in *status, when given).
 template <typename Tin, int D>
@@ -41,13 +55,14 @@ __global__ void __launch_bounds__((D / 4) * (D / kRows))
 decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ S,
                    Tin *__restrict__ o, const int32_t *__restrict__ idx, int H, int num_slots,
-                   int32_t *__restrict__ status) {
+                   int32_t *__restrict__ status, int qk_norm, float qk_eps, const Tin *__restrict__ gate,
+                   const float *__restrict__ weight, float out_eps) {
     constexpr int CG = D / 4;        // column groups (float4)
     constexpr int RG = D / kRows;    // row bands
     constexpr int NT = CG * RG;
-    __shared__ float s_q[D], s_k[D], s_dec[D], s_u[D];
+    __shared__ float s_q[D], s_k[D], s_dec[D], s_u[D], s_o[D];
     __shared__ float s_x[RG][D], s_y[RG][D];
-    __shared__ float s_qk;
+    __shared__ float s_qk, s_scale[2];
 
     const int head = blockIdx.x;  // flattened (active sequence, head): the token's inputs and output
     size_t state = (size_t)head;  // flattened (slot, head) of its state
@@ -75,6 +90,20 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
         s_dec[i] = expf(g[vec + i]);
     }
     __syncthreads();
+    if (qk_norm) {  // fused prologue: q, k L2-normalised in fp32 (warps 0 / 1, or threads 0 / 1 of a small block)
+        if (NT >= 64 && tid < 64) {
+            const float ss = warp_sum_squares(tid < 32 ? s_q : s_k, D, tid & 31);
+            if ((tid & 31) == 0) s_scale[tid >> 5] = rsqrtf(ss + qk_eps);
+        } else if (NT < 64 && tid < 2) {
+            s_scale[tid] = rsqrtf(serial_sum_squares(tid ? s_k : s_q, D) + qk_eps);
+        }
+        __syncthreads();
+        for (int i = tid; i < D; i += NT) {
+            s_q[i] *= s_scale[0];
+            s_k[i] *= s_scale[1];
+        }
+        __syncthreads();
+    }
     if (tid == 0) {
         float acc = 0.f;
         for (int i = 0; i < D; ++i) acc = fmaf(s_q[i], s_k[i], acc);
@@ -103,9 +132,22 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
         for (int r = 0; r < RG; ++r) { xs += s_x[r][c]; ys += s_y[r][c]; }
         const float u = b * (to_f32(v[vec + c]) - xs);
         s_u[c] = u;
-        o[vec + c] = from_f32<Tin>(fmaf(s_qk, u, ys));
+        const float out = fmaf(s_qk, u, ys);
+        if (gate) s_o[c] = out;
+        else o[vec + c] = from_f32<Tin>(out);
     }
     __syncthreads();
+    if (gate) {  // fused epilogue: o / rms(o) * w * sigmoid(z)
+        if (NT >= 32 && tid < 32) {
+            const float ss = warp_sum_squares(s_o, D, tid);
+            if (tid == 0) s_scale[0] = rsqrtf(ss / (float)D + out_eps);
+        } else if (NT < 32 && tid == 0) {
+            s_scale[0] = rsqrtf(serial_sum_squares(s_o, D) / (float)D + out_eps);
+        }
+        __syncthreads();
+        for (int c = tid; c < D; c += NT)
+            o[vec + c] = from_f32<Tin>(s_o[c] * s_scale[0] * (weight ? weight[c] : 1.f) * sigmoidf(to_f32(gate[vec + c])));
+    }
 
     const float4 u = *reinterpret_cast<const float4 *>(&s_u[cg * 4]);
 #pragma unroll
@@ -136,21 +178,23 @@ state_copy_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, cons
 
 template <typename Tin, int D>
 cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
-                     float *S, void *o, const int32_t *idx, int H, int num_slots, int32_t *status, cudaStream_t st) {
+                     float *S, void *o, const int32_t *idx, int H, int num_slots, int32_t *status, const Fusion &fu,
+                     cudaStream_t st) {
     constexpr int NT = (D / 4) * (D / kRows);
     decode_step_kernel<Tin, D><<<heads, NT, 0, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, S,
-                                                     (Tin *)o, idx, H, num_slots, status);
+                                                     (Tin *)o, idx, H, num_slots, status, fu.qk_norm, fu.qk_eps,
+                                                     (const Tin *)fu.gate, fu.weight, fu.out_eps);
     return cudaGetLastError();
 }
 
 template <typename Tin>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g, const float *beta, int heads,
                      int d, float *S, void *o, const int32_t *idx, int H, int num_slots, int32_t *status,
-                     cudaStream_t st) {
+                     const Fusion &fu, cudaStream_t st) {
     switch (d) {
-        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
-        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
-        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, st);
+        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, fu, st);
+        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, fu, st);
+        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, heads, S, o, idx, H, num_slots, status, fu, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -159,11 +203,12 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, const int32_t *idx,
-                          int num_slots, int32_t *status, cudaStream_t st) {
+                          int num_slots, int32_t *status, const Fusion &fu, cudaStream_t st) {
     const int heads = num_seqs * H;
     if (heads == 0) return cudaSuccess;
-    if (dt == KDA_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, st);
-    return launch_t<float>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, st);
+    if (dt == KDA_BF16)
+        return launch_t<__nv_bfloat16>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, fu, st);
+    return launch_t<float>(q, k, v, g, beta, heads, d, S, o, idx, H, num_slots, status, fu, st);
 }
 
 cudaError_t launch_state_copy(const float *src, float *dst, const int32_t *idx, int n, int num_slots, int H, int d,

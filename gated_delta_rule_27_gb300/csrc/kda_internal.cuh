@@ -126,6 +126,21 @@ __device__ __forceinline__ bool locate_slot(const int32_t *__restrict__ doc_slot
 }
 
 // ---------------------------------------------------------------------------
+// The fused prologue and epilogue of kda_fusion_opts, as the kernels take them
+// (all zero / null: neither).
+// ---------------------------------------------------------------------------
+struct Fusion {
+    int qk_norm = 0;
+    float qk_eps = 0.f;
+    const void *gate = nullptr;
+    const float *weight = nullptr;
+    float out_eps = 0.f;
+};
+
+// The logistic function in fp32 (the gate of the output normalisation).
+__device__ __forceinline__ float sigmoidf(float z) { return 1.f / (1.f + expf(-z)); }
+
+// ---------------------------------------------------------------------------
 // Optional profiling marks: an event recorded before every kernel of a call
 // and one after the last, with the kernels' names (all may be null).
 // ---------------------------------------------------------------------------
@@ -179,18 +194,27 @@ void testing_set_fault(int fault, long long wait_ns);
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
-                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st,
-                                Marks &marks);
+                                int L, const float *S0, void *o, float *S_final, void *ws, const Fusion &fu,
+                                cudaStream_t st, Marks &marks);
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks);
+                              float *S_final, void *ws, TcPlan plan, const Fusion &fu, cudaStream_t st,
+                              Marks &marks);
 
 // Decode step of num_seqs sequences; with `idx` (device, [num_seqs]) their states are the pool slots idx[i] of
 // S [num_slots, H, d, d], otherwise S[i].
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g, const float *beta,
                           int num_seqs, int H, int d, kda_dtype dt, float *S, void *o, const int32_t *idx,
-                          int num_slots, int32_t *status, cudaStream_t st);
+                          int num_slots, int32_t *status, const Fusion &fu, cudaStream_t st);
+
+// Short causal convolution (kda_conv.cu): prefill over packed documents with carried states, and one decode
+// step with a rolling state.
+cudaError_t launch_conv_prefill(const void *x, const float *w, const int32_t *cu, int num_seqs, int total_tokens, int C,
+                                int W, kda_dtype dt, const float *state_in, void *y, float *state_out,
+                                cudaStream_t st);
+cudaError_t launch_conv_decode(const void *x, const float *w, int N, int C, int W, kda_dtype dt, float *state, void *y,
+                               cudaStream_t st);
 
 // Snapshot (gather: dst[i] = src[idx[i]]) or restore (scatter: dst[idx[i]] = src[i]) of n whole slots of
 // H heads' d x d fp32 states.

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads)
 prefill_prepare_simt(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                      const float *__restrict__ g, const float *__restrict__ beta, const int32_t *__restrict__ cu,
                      int num_seqs, int H, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
-                     size_t record_bytes) {
+                     size_t record_bytes, int qk_norm, float qk_eps) {
     using SM = PrepSmem<D, L>;
     constexpr int DP = SM::DP;
     extern __shared__ float smem[];
@@ -142,6 +142,19 @@ prefill_prepare_simt(const Tin *__restrict__ q, const Tin *__restrict__ k, const
     }
     for (int r = tid; r < Lc; r += kThreads) sbeta[r] = beta[(size_t)(t0 + r) * H + h];
     __syncthreads();
+    if (qk_norm) {  // fused prologue: every q and k row L2-normalised in fp32, one warp per row
+        const int lane = tid & 31;
+        for (int rr = tid >> 5; rr < 2 * Lc; rr += kThreads / 32) {
+            float *x = (rr < Lc ? sq : sk) + (rr % Lc) * DP;
+            float ss = 0.f;
+            for (int c = lane; c < D; c += 32) ss = fmaf(x[c], x[c], ss);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss + qk_eps);
+            for (int c = lane; c < D; c += 32) x[c] *= inv;
+        }
+        __syncthreads();
+    }
     for (int c = tid; c < D; c += kThreads) {  // in-chunk cumulative log-decay
         float acc = 0.f;
         for (int r = 0; r < Lc; ++r) { acc += sb[r * DP + c]; sb[r * DP + c] = acc; }
@@ -313,10 +326,42 @@ prefill_state_simt(const int32_t *__restrict__ cu, int num_seqs, int H, const fl
     }
 }
 
+// ---------------------------------------------------------------------------
+// (4) the fused epilogue's gated output normalisation, on this path a pass of its own (the state pass writes
+// each row of o in column tiles from several CTAs): o <- o / rms(o) * w * sigmoid(z), one warp per row.
+// ---------------------------------------------------------------------------
+template <typename Tout, int D>
+__global__ void __launch_bounds__(kThreads)
+out_gated_norm_kernel(Tout *__restrict__ o, const Tout *__restrict__ gate, const float *__restrict__ weight,
+                      float eps, int rows) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    constexpr int PER = (D + 31) / 32;
+    float x[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        x[j] = c < D ? to_f32(o[(size_t)row * D + c]) : 0.f;
+        ss = fmaf(x[j], x[j], ss);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float scale = rsqrtf(ss / (float)D + eps);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        if (c < D)
+            o[(size_t)row * D + c] =
+                from_f32<Tout>(x[j] * scale * (weight ? weight[c] : 1.f) * sigmoidf(to_f32(gate[(size_t)row * D + c])));
+    }
+}
+
 template <typename Tin, int D, int L>
 cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *g, const float *beta,
                       const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                      float *S_final, void *ws, cudaStream_t st, Marks &marks) {
+                      float *S_final, void *ws, const Fusion &fu, cudaStream_t st, Marks &marks) {
     constexpr int TILE = D < 32 ? D : 32;
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, D, D, L, PATH_SIMT);
     char *w = static_cast<char *>(ws);
@@ -330,7 +375,7 @@ cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *
         marks.before(st, "prefill_prepare_simt");
         prep<<<grid, kThreads, sm_prep, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, cu,
                                               num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
-                                              lay.record_bytes);
+                                              lay.record_bytes, fu.qk_norm, fu.qk_eps);
         if ((e = cudaGetLastError())) return e;
     }
     if (num_seqs == 0) return cudaSuccess;
@@ -341,17 +386,25 @@ cudaError_t launch_dl(const void *q, const void *k, const void *v, const float *
     marks.before(st, "prefill_state_simt");
     state<<<blocks, kThreads, sm_state, st>>>(cu, num_seqs, H, S0, (Tin *)o, S_final, w, lay.doc_slot0_off,
                                               lay.records_off, lay.record_bytes);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError())) return e;
+    if (fu.gate && total_tokens > 0) {
+        const int rows = total_tokens * H;
+        marks.before(st, "out_gated_norm");
+        out_gated_norm_kernel<Tin, D><<<(rows + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, st>>>(
+            (Tin *)o, (const Tin *)fu.gate, fu.weight, fu.out_eps, rows);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 template <typename Tin, int D>
 cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g, const float *beta,
                      const int32_t *cu, int num_seqs, int total_tokens, int H, int L, const float *S0, void *o,
-                     float *S_final, void *ws, cudaStream_t st, Marks &marks) {
+                     float *S_final, void *ws, const Fusion &fu, cudaStream_t st, Marks &marks) {
     switch (L) {
-        case 16: return launch_dl<Tin, D, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
-        case 32: return launch_dl<Tin, D, 32>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
-        case 64: return launch_dl<Tin, D, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, st, marks);
+        case 16: return launch_dl<Tin, D, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, fu, st, marks);
+        case 32: return launch_dl<Tin, D, 32>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, fu, st, marks);
+        case 64: return launch_dl<Tin, D, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, S0, o, S_final, ws, fu, st, marks);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -359,11 +412,11 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const float *g
 template <typename Tin>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g, const float *beta,
                      const int32_t *cu, int num_seqs, int total_tokens, int H, int d, int L, const float *S0,
-                     void *o, float *S_final, void *ws, cudaStream_t st, Marks &marks) {
+                     void *o, float *S_final, void *ws, const Fusion &fu, cudaStream_t st, Marks &marks) {
     switch (d) {
-        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
-        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
-        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, st, marks);
+        case 16: return launch_d<Tin, 16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, fu, st, marks);
+        case 64: return launch_d<Tin, 64>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, fu, st, marks);
+        case 128: return launch_d<Tin, 128>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, L, S0, o, S_final, ws, fu, st, marks);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -386,12 +439,12 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,
-                                int L, const float *S0, void *o, float *S_final, void *ws, cudaStream_t st,
-                                Marks &marks) {
+                                int L, const float *S0, void *o, float *S_final, void *ws, const Fusion &fu,
+                                cudaStream_t st, Marks &marks) {
     if (dt == KDA_BF16)
-        return launch_t<__nv_bfloat16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st,
-                                       marks);
-    return launch_t<float>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, st, marks);
+        return launch_t<__nv_bfloat16>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, fu,
+                                       st, marks);
+    return launch_t<float>(q, k, v, g, beta, cu, num_seqs, total_tokens, H, d, L, S0, o, S_final, ws, fu, st, marks);
 }
 
 }  // namespace kda

@@ -221,11 +221,13 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
 // wide for the factorised tensor-core form: pairwise exp(b_r - b_s) <= 1
 // (s <= r).  Thread t owns row r = t / 4 and the 16 columns s of quarter t % 4.
 __device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, int Lc, int tid, float (&accA)[16],
-                         float (&accP)[16]) {
+                         float (&accP)[16], const float *invk, const float *invq) {
     const int r = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
     for (int j = 0; j < 16; ++j) { accA[j] = 0.f; accP[j] = 0.f; }
     if (r >= Lc) return;
+    // with the fused q / k normalisation, row norms enter as factors: k_r . k_s -> (k_r . k_s) ik_r ik_s
+    const float ikr = invk ? invk[r] : 1.f, iqr = invq ? invq[r] : 1.f;
     for (int c = 0; c < kD; ++c) {
         const uint8_t *panel = X + (uint32_t)(c >> 6) * 16384u;
         const float brc = B[bswz(r, c)];
@@ -242,7 +244,11 @@ __device__ void exact_ap(const uint8_t *X, const float *B, const float *s_beta, 
         }
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) accA[j] *= s_beta[r];
+    for (int j = 0; j < 16; ++j) {
+        const float iks = invk ? invk[s0 + j] : 1.f;
+        accA[j] *= s_beta[r] * ikr * iks;
+        accP[j] *= iqr * iks;
+    }
 }
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -275,6 +281,8 @@ struct PrepParams {
     int num_seqs, H;
     char *ws;
     size_t doc_slot0_off, records_off, record_bytes;
+    int qk_norm;     // fused prologue: q and k rows L2-normalised (x / sqrt(sum x^2 + qk_eps)) as they are read
+    float qk_eps;
 };
 // mbarriers of one preparation, each completing exactly once per unit: the gate tile, the k, q, v
 // tiles, and the four MMA rounds
@@ -305,6 +313,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     __shared__ __align__(16) float s_Em[kD];
     __shared__ __align__(16) float s_blast[kD];
     __shared__ float s_half[kD], s_mid[kD], s_lo[2][kD], s_hi[2][kD];
+    __shared__ float s_invk[kL], s_invq[kL];
     __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -411,9 +420,38 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         if (tid == 0) flag_timeout(ws);
         return false;
     }
+    if (p.qk_norm) {
+        // fused prologue: inverse L2 norms of the 64 k rows and 64 q rows; thread t sums row t / 4, channels
+        // 32 (t % 4) .. + 31, and the four threads of a row combine by shuffles
+        const int r = tid >> 2, qd = tid & 3;
+        const uint8_t *panel = sm + PrepSmem::X + (uint32_t)(qd >> 1) * 16384u;
+        const int c0 = (qd & 1) * 32;
+        float sk2 = 0.f, sq2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            float f[8], e[8];
+            unpack8(*reinterpret_cast<const uint4 *>(panel + tc::sw128_offset(r, c0 + j)), f);
+            unpack8(*reinterpret_cast<const uint4 *>(panel + tc::sw128_offset(64 + r, c0 + j)), e);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                sk2 = fmaf(f[u], f[u], sk2);
+                sq2 = fmaf(e[u], e[u], sq2);
+            }
+        }
+        sk2 += __shfl_xor_sync(0xffffffffu, sk2, 1);
+        sq2 += __shfl_xor_sync(0xffffffffu, sq2, 1);
+        sk2 += __shfl_xor_sync(0xffffffffu, sk2, 2);
+        sq2 += __shfl_xor_sync(0xffffffffu, sq2, 2);
+        if (qd == 0) {
+            s_invk[r] = rsqrtf(sk2 + p.qk_eps);
+            s_invq[r] = rsqrtf(sq2 + p.qk_eps);
+        }
+        __syncthreads();
+    }
     float accA[16], accP[16];
     if (unsafe) {
-        exact_ap(sm + PrepSmem::X, Gf, s_beta, Lc, tid, accA, accP);
+        exact_ap(sm + PrepSmem::X, Gf, s_beta, Lc, tid, accA, accP, p.qk_norm ? s_invk : nullptr,
+                 p.qk_norm ? s_invq : nullptr);
         __syncthreads();  // the raw k, q tiles are about to be scaled in place
     }
 
@@ -442,6 +480,14 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             float k8[8], q8[8], xk[8], xq[8], ke[8];
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
+            if (p.qk_norm) {
+                const float ik = s_invk[r], iq = s_invq[r];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    k8[u] *= ik;
+                    q8[u] *= iq;
+                }
+            }
             const float4 b0 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0));
             const float4 b1 = *reinterpret_cast<const float4 *>(Gf + bswz(r, c0 + 4));
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
@@ -769,7 +815,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
                    char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
-                   int resident) {
+                   int resident, int qk_norm, float qk_eps) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ PrepBars bars;
     __shared__ uint32_t tmem_base;
@@ -810,7 +856,8 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // CTA's place next
     const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
     const bool has_next = resident > 0 && nxt < (int)(gridDim.x * gridDim.y);
-    const PrepParams prm{&tm_q, &tm_k, &tm_v, &tm_g, beta, cu, num_seqs, H, ws, doc_slot0_off, records_off, record_bytes};
+    const PrepParams prm{&tm_q,         &tm_k,       &tm_v,          &tm_g,   beta,  cu, num_seqs, H, ws, doc_slot0_off,
+                         records_off, record_bytes, qk_norm, qk_eps};
     prepare_unit(prm, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, has_next ? nxt % (int)gridDim.x : -1,
                  has_next ? nxt / (int)gridDim.x : 0);
     __syncthreads();
@@ -1098,6 +1145,13 @@ struct OutBars {
     uint64_t load, sload, mma;  // the record's Qp, P, Ut; its state image; the MMAs
 };
 
+// The fused epilogue's gated output normalisation (gate null: o is written as it is).
+struct OutNorm {
+    const __nv_bfloat16 *gate;  // z [T, H, 128]
+    const float *weight;        // w [128] or null (ones)
+    float eps;
+};
+
 // A group of 128 threads of a CTA: thread `gtid` of it, synchronised by named
 // barrier `gbar` (0: the whole CTA is the group, __syncthreads).
 struct OutGroup {
@@ -1120,8 +1174,9 @@ struct OutGroup {
 // timeout in the status word.
 __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
-                            OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, bool dep_wait = false,
-                            const int32_t *sflag = nullptr, uint64_t flag_wait_ns = kFlagWaitNs) {
+                            OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, const OutNorm &onorm,
+                            bool dep_wait = false, const int32_t *sflag = nullptr,
+                            uint64_t flag_wait_ns = kFlagWaitNs) {
     const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
@@ -1170,12 +1225,38 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
         if (warp_all(done)) {
             const int r = tid;
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * H + h) * kD);
+            const size_t row = ((size_t)(t0 + r) * H + h) * kD;
+            uint4 *dst = reinterpret_cast<uint4 *>(o + row);
+            float scale = 1.f;
+            if (onorm.gate) {  // fused epilogue, pass 1: the row's mean square
+                float ss = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+                }
+                scale = rsqrtf(ss * (1.f / kD) + onorm.eps);
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float v[32];
                 tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
                 if (r < Lc) {
+                    if (onorm.gate) {  // pass 2: o / rms(o) * w * sigmoid(z)
+                        const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row) + q * 4;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            float z[8];
+                            unpack8(z4[u], z);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int c = q * 32 + u * 8 + i;
+                                v[u * 8 + i] *= scale * (onorm.weight ? onorm.weight[c] : 1.f) * sigmoidf(z[i]);
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) dst[q * 4 + u] = pack8_at(v + 8 * u);
                 }
@@ -1194,7 +1275,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
 __global__ void __launch_bounds__(128)
 prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o,
                   char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
-                  int resident) {
+                  int resident, OutNorm onorm) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ OutBars bars;
     __shared__ uint32_t tmem_base;
@@ -1227,7 +1308,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     tc::tc_fence_after();
     __shared__ int s_ok;
     output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base,
-                OutGroup{tid, 0u, &s_ok}, true);
+                OutGroup{tid, 0u, &s_ok}, onorm, true);
     if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
 }
 
@@ -1245,7 +1326,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  float *__restrict__ S_final, __nv_bfloat16 *__restrict__ o, char *__restrict__ ws,
                  size_t doc_slot0_off, size_t records_off, size_t record_bytes, int n_state, int32_t *sdone,
-                 int32_t *counter, unsigned long long flag_wait_ns, int fault) {
+                 int32_t *counter, unsigned long long flag_wait_ns, int fault, OutNorm onorm) {
     extern __shared__ uint8_t smem_raw[];
     if ((int)blockIdx.x < n_state) {
         // (fault == kFaultNoPublish only in tests of the timeout path: no state image is published, so the
@@ -1305,7 +1386,7 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             int doc, t0, Lc;
             locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
             if (!output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
-                             grp, false, sdone + u, flag_wait_ns))
+                             grp, onorm, false, sdone + u, flag_wait_ns))
                 break;
         }
     }
@@ -1523,7 +1604,9 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
                               const int32_t *cu, int num_seqs, int total_tokens, int H, const float *S0, void *o,
-                              float *S_final, void *ws, TcPlan plan, cudaStream_t st, Marks &marks) {
+                              float *S_final, void *ws, TcPlan plan, const Fusion &fu, cudaStream_t st,
+                              Marks &marks) {
+    const OutNorm onorm{static_cast<const __nv_bfloat16 *>(fu.gate), fu.weight, fu.out_eps};
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     char *w = static_cast<char *>(ws);
     const DeviceSetup &dset = device_setup();
@@ -1535,7 +1618,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         marks.before(st, "prefill_prepare_tc");
         if ((e = launch_dependent(prefill_prepare_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(kPrepThreads),
                                   (size_t)kPrepSmem, st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
-                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.prep_resident)))
+                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.prep_resident,
+                                  fu.qk_norm, fu.qk_eps)))
             return e;
     }
     if (num_seqs == 0) return cudaSuccess;
@@ -1550,7 +1634,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         e = launch_cooperative(prefill_chain_tc, dim3((unsigned)dset.sms), dim3(kStateThreads), (size_t)kStateSmem,
                                st, cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o), w,
                                lay.doc_slot0_off, lay.records_off, lay.record_bytes, n_state, flags, flags + nflag,
-                               flag_wait, g_test_fault.load());
+                               flag_wait, g_test_fault.load(), onorm);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the state
         // pass and the output pass as separate kernels instead.
@@ -1566,7 +1650,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         marks.before(st, "prefill_output_tc");
         if ((e = launch_dependent(prefill_output_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(128),
                                   (size_t)kOutSmem, st, cu, num_seqs, H, static_cast<__nv_bfloat16 *>(o), w,
-                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.out_resident)))
+                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.out_resident, onorm)))
             return e;
     }
     return cudaSuccess;

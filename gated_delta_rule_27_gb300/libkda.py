@@ -19,7 +19,8 @@ KDA_F32, KDA_BF16 = 0, 1
 
 SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_chunked_profiled",
            "kda_prefill_check", "kda_decode_step", "kda_prefill_chunked_noalloc", "kda_prefill_noalloc_check",
-           "kda_decode_step_indexed", "kda_state_snapshot", "kda_state_restore")
+           "kda_decode_step_indexed", "kda_state_snapshot", "kda_state_restore", "kda_prefill_chunked_ex",
+           "kda_decode_step_ex", "kda_short_conv_prefill", "kda_short_conv_decode")
 # include/kda_testing.h (test hooks)
 TESTING_SYMBOLS = ("kda_testing_set_plan", "kda_testing_set_fault")
 PLAN_AUTO, PLAN_THREE, PLAN_CHAIN = -1, 0, 2
@@ -27,6 +28,12 @@ FAULT_NONE, FAULT_NO_PUBLISH = 0, 1
 PREFILL_MAX_KERNELS = 4
 
 _lib = None
+
+
+class FusionOpts(ctypes.Structure):
+    """kda_fusion_opts (include/kda.h): the fused q/k normalisation and gated output normalisation."""
+    _fields_ = [("qk_l2norm", ctypes.c_int32), ("qk_eps", ctypes.c_float), ("out_gate", ctypes.c_void_p),
+                ("out_weight", ctypes.c_void_p), ("out_eps", ctypes.c_float)]
 
 
 class KdaError(RuntimeError):
@@ -69,6 +76,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                 i32, vp, vp, vp, vp]
     lib.kda_prefill_noalloc_check.restype = ctypes.c_int
     lib.kda_prefill_noalloc_check.argtypes = [vp]
+    lib.kda_prefill_chunked_ex.restype = ctypes.c_int
+    lib.kda_prefill_chunked_ex.argtypes = lib.kda_prefill_chunked.argtypes + [ctypes.POINTER(FusionOpts)]
+    lib.kda_decode_step_ex.restype = ctypes.c_int
+    lib.kda_decode_step_ex.argtypes = lib.kda_decode_step.argtypes + [ctypes.POINTER(FusionOpts)]
+    lib.kda_short_conv_prefill.restype = ctypes.c_int
+    lib.kda_short_conv_prefill.argtypes = [vp, fp, vp, i32, i32, i32, i32, ctypes.c_int, fp, vp, fp, vp]
+    lib.kda_short_conv_decode.restype = ctypes.c_int
+    lib.kda_short_conv_decode.argtypes = [vp, fp, i32, i32, i32, ctypes.c_int, fp, vp, vp]
     lib.kda_decode_step_indexed.restype = ctypes.c_int
     lib.kda_decode_step_indexed.argtypes = [vp, vp, vp, fp, fp, vp, i32, i32, i32, i32, i32, ctypes.c_int, fp, vp,
                                             vp, vp]
@@ -189,6 +204,63 @@ def kda_decode_step(q, k, v, g, beta, S_inout, o, stream=None) -> None:
                                 _ptr(S_inout), _ptr(o), _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
+
+
+def fusion_opts(qk_l2norm=False, qk_eps=1e-6, out_gate=None, out_weight=None, out_eps=1e-6):
+    """A kda_fusion_opts for the _ex entry points (None when nothing is fused)."""
+    if not qk_l2norm and out_gate is None:
+        return None
+    return FusionOpts(1 if qk_l2norm else 0, float(qk_eps), _ptr(out_gate), _ptr(out_weight), float(out_eps))
+
+
+def kda_prefill_chunked_ex(q, k, v, g, beta, cu_seqlens, o, S0=None, S_final=None, workspace=None, chunk_size=64,
+                           stream=None, **fusion) -> None:
+    """kda_prefill_chunked with the fused prologue / epilogue (keywords of fusion_opts)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if workspace is None:
+        workspace = new_workspace(T, N, H, d_k, d_v, dt, chunk_size, q.device)
+    opts = fusion_opts(**fusion)
+    rc = load().kda_prefill_chunked_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, H,
+                                       d_k, d_v, dt, chunk_size, _ptr(S0), _ptr(o), _ptr(S_final), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream),
+                                       None if opts is None else ctypes.byref(opts))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_chunked_ex")
+
+
+def kda_decode_step_ex(q, k, v, g, beta, S_inout, o, stream=None, **fusion) -> None:
+    """kda_decode_step with the fused prologue / epilogue (keywords of fusion_opts)."""
+    N, H, d_k = q.shape
+    opts = fusion_opts(**fusion)
+    rc = load().kda_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), N, H, d_k, v.shape[2],
+                                   _dtype_code(q), _ptr(S_inout), _ptr(o), _stream(stream),
+                                   None if opts is None else ctypes.byref(opts))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step_ex")
+
+
+def kda_short_conv_prefill(x, w, cu_seqlens, y, conv_state=None, conv_state_out=None, stream=None) -> None:
+    """kda_short_conv_prefill on x [T, C] (or [T, H, d], flattened), w [C, W]."""
+    T = x.shape[0]
+    C, W = w.shape
+    rc = load().kda_short_conv_prefill(_ptr(x), _ptr(w), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, C, W,
+                                       _dtype_code(x), _ptr(conv_state), _ptr(y), _ptr(conv_state_out),
+                                       _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_short_conv_prefill")
+
+
+def kda_short_conv_decode(x, w, conv_state, y, stream=None) -> None:
+    """kda_short_conv_decode on x [N, C]: one token per sequence, conv_state [N, W - 1, C] rolled in place."""
+    N = x.shape[0]
+    C, W = w.shape
+    rc = load().kda_short_conv_decode(_ptr(x), _ptr(w), N, C, W, _dtype_code(x), _ptr(conv_state), _ptr(y),
+                                      _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_short_conv_decode")
 
 
 def kda_decode_step_indexed(q, k, v, g, beta, seq_idx, S_pool, o, status=None, stream=None) -> None:

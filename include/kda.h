@@ -150,6 +150,41 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                            float *S_inout, void *o, void *stream);
 
 /*
+ * The steps on either side of the recurrence, fused into its kernels
+ * (Lecture 04, section 3: the sublayer runs Q/K normalisation before the
+ * recurrence and a gated normalisation on its output; fusing them saves a
+ * round trip of q, k and o through memory).  The pages name the two steps
+ * without formulas; libkda computes, per (token, head):
+ *   qk_l2norm != 0:  q <- q / sqrt(sum_c q_c^2 + qk_eps), and the same for k,
+ *                    in fp32 from the input values;
+ *   out_gate != NULL: o <- o / sqrt(mean_c o_c^2 + out_eps) * w_c * sigmoid(z_c),
+ *                    with z = out_gate [T, H, d_v] in_dtype and w = out_weight
+ *                    [d_v] fp32 (NULL: all ones); the stored o is this value.
+ * All pointers are device pointers with the alignment rules of the entry
+ * points (out_gate 16-byte, out_weight 4-byte aligned).
+ */
+typedef struct {
+    int32_t qk_l2norm;
+    float qk_eps;            /* >= 0 */
+    const void *out_gate;    /* NULL: o is the recurrence output as it is */
+    const float *out_weight; /* NULL: ones */
+    float out_eps;           /* > 0 when out_gate is given */
+} kda_fusion_opts;
+
+/* kda_prefill_chunked with the fused prologue and epilogue above (opts NULL: exactly kda_prefill_chunked). */
+KDA_API kda_status kda_prefill_chunked_ex(const void *q, const void *k, const void *v, const float *g,
+                                          const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                          int32_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                          kda_dtype in_dtype, int32_t chunk_size, const float *S0, void *o,
+                                          float *S_final, void *workspace, size_t workspace_bytes, void *stream,
+                                          const kda_fusion_opts *opts);
+
+/* kda_decode_step with the fused prologue and epilogue above (out_gate is [num_seqs, H, d_v]). */
+KDA_API kda_status kda_decode_step_ex(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                      int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                                      float *S_inout, void *o, void *stream, const kda_fusion_opts *opts);
+
+/*
  * Decode step for a batch that mixes request phases (Lecture 04, section 2:
  * the fused recurrent kernel serves the sequences that are generating, while
  * others are still in their chunked prefill).  The states live in a pool of
@@ -190,6 +225,38 @@ KDA_API kda_status kda_state_snapshot(const float *S_pool, const int32_t *seq_id
 KDA_API kda_status kda_state_restore(const float *S_saved, const int32_t *seq_idx, int32_t n, int32_t num_slots,
                                      int32_t H, int32_t d_k, int32_t d_v, float *S_pool, int32_t *status,
                                      void *stream);
+
+/*
+ * Short causal convolution on the inputs of the recurrence (Lecture 04,
+ * section 3: a small local mixing step on Q, K and/or V before the Q/K
+ * normalisation; Lecture 11, section 2, "Serving state" row: the
+ * convolution state must survive continuation and rollback like S does).
+ * The pages give no formula; libkda computes, per channel c,
+ *     y_t[c] = sum_{j < W} w[c, j] x_{t-j}[c]
+ * inside each document, positions before a document's first token reading
+ * its carried state.  fp32 arithmetic; 1 <= W <= KDA_SHORT_CONV_MAX_W.
+ *
+ *   x, y            [total_tokens, C] in_dtype (e.g. C = H * d for q laid out
+ *                   [T, H, d]); y must not alias x
+ *   w               [C, W] fp32
+ *   cu_seqlens      [num_seqs + 1] int32, device, valid as for the prefill
+ *                   (not checked here: an invalid table gives wrong values
+ *                   but no out-of-bounds access)
+ *   conv_state      [num_seqs, W - 1, C] fp32, each document's previous W - 1
+ *                   inputs, oldest first, or NULL for zeros
+ *   conv_state_out  [num_seqs, W - 1, C] fp32 or NULL: each document's last
+ *                   W - 1 inputs (older carried entries when it is shorter);
+ *                   must not alias conv_state
+ * The decode step takes one token per sequence (x, y [N, C]) and rolls
+ * conv_state [N, W - 1, C] in place.  All pointers are device pointers aligned
+ * to their element size.
+ */
+#define KDA_SHORT_CONV_MAX_W 8
+KDA_API kda_status kda_short_conv_prefill(const void *x, const float *w, const int32_t *cu_seqlens, int32_t num_seqs,
+                                          int32_t total_tokens, int32_t C, int32_t W, kda_dtype in_dtype,
+                                          const float *conv_state, void *y, float *conv_state_out, void *stream);
+KDA_API kda_status kda_short_conv_decode(const void *x, const float *w, int32_t N, int32_t C, int32_t W,
+                                         kda_dtype in_dtype, float *conv_state, void *y, void *stream);
 
 /*
  * Chunked prefill that allocates nothing.  The course pages have no
