@@ -161,8 +161,12 @@ kda_status kda_prefill_check(const void *workspace, void *stream) {
 }
 
 kda_status kda_testing_set_plan(int32_t plan) {
-    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN) return KDA_ERR_INVALID_ARG;
-    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE ? kda::TC_THREE : plan == -1 ? -1 : kda::TC_CHAIN);
+    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN && plan != KDA_TESTING_PLAN_PIPE)
+        return KDA_ERR_INVALID_ARG;
+    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE   ? kda::TC_THREE
+                          : plan == KDA_TESTING_PLAN_CHAIN ? kda::TC_CHAIN
+                          : plan == KDA_TESTING_PLAN_PIPE  ? kda::TC_PIPE
+                                                           : -1);
     return KDA_OK;
 }
 

@@ -41,8 +41,8 @@ struct WsLayout {
     size_t records_off;
     size_t record_bytes;
     int64_t max_slots;
-    size_t flags_off;    // tensor-core path: int32 [max_slots * H] state-image counters, then two int32
-                         // unit counters (chain plan)
+    size_t flags_off;    // tensor-core path: int32 [max_slots * H] record-published flags, int32 [max_slots * H]
+                         // state-image counters, then two int32 work counters (chain and pipe plans)
     size_t flags_bytes;  // 0 on the CUDA-core path
     size_t total;
 };
@@ -95,7 +95,7 @@ inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int
     w.record_bytes = path == PATH_TC ? tc_record().bytes : simt_record(L, dk, dv).bytes;
     w.max_slots = total_tokens / L + num_seqs;
     w.flags_off = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;
-    w.flags_bytes = path == PATH_TC ? align256(((size_t)w.max_slots * H + 2) * 4) : 0;
+    w.flags_bytes = path == PATH_TC ? align256(((size_t)2 * w.max_slots * H + 2) * 4) : 0;
     w.total = w.flags_off + w.flags_bytes;
     return w;
 }
@@ -182,10 +182,11 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
                                size_t clear_bytes, cudaStream_t st, Marks &marks);
 
-// Launch plans of the tensor-core prefill: three kernels (preparation, state, output), or the preparation
-// followed by one cooperative launch running the state chains with the output units alongside (chain).  The
-// chain plan needs the workspace's progress flags zeroed before it starts.
-enum TcPlan { TC_THREE = 0, TC_CHAIN = 2 };
+// Launch plans of the tensor-core prefill: three kernels (preparation, state, output); the preparation
+// followed by one cooperative launch running the state chains with the output units alongside (chain); or one
+// cooperative launch of chains beside groups that prepare the records and then form the outputs (pipe).  The
+// last two need the workspace's progress flags zeroed before they start.
+enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3 };
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.

@@ -109,12 +109,54 @@ struct PrepSmem {
     static constexpr uint32_t bytes = 98304;
 };
 
+// The 256 threads that run one preparation unit: the whole CTA (bar 0, __syncthreads), or one of two groups
+// of a 512-thread CTA synchronised by named barrier `bar`; `tid` is the thread's index within the group.
+// A group's warps are numbered from its first warp, whose index is a multiple of 4, so a warp's TMEM lane
+// quarter (physical warp index mod 4) is its group-relative index mod 4.
+struct PrepGroup {
+    int tid;
+    uint32_t bar;
+    __device__ __forceinline__ void sync() const {
+        if (bar == 0) __syncthreads();
+        else tc::named_barrier(bar, kPrepThreads);
+    }
+    // barrier that also returns whether `pred` held for any thread of the group
+    __device__ __forceinline__ bool sync_or(bool pred) const {
+        if (bar == 0) return __syncthreads_or(pred) != 0;
+        uint32_t r;
+        asm volatile(
+            "{\n"
+            ".reg .pred p, q;\n"
+            "setp.ne.u32 p, %1, 0;\n"
+            "bar.red.or.pred q, %2, %3, p;\n"
+            "selp.u32 %0, 1, 0, q;\n"
+            "}\n"
+            : "=r"(r)
+            : "r"((uint32_t)pred), "r"(bar), "r"((uint32_t)kPrepThreads)
+            : "memory");
+        return r != 0;
+    }
+};
+
+// Per-unit scratch of a preparation group (small per-channel and per-row vectors, outside the big tiles).
+struct PrepShared {
+    __align__(16) float beta[kL];
+    __align__(16) float bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
+    __align__(16) float F[kD];
+    __align__(16) float Em[kD];
+    __align__(16) float blast[kD];
+    float half[kD], mid[kD], lo[2][kD], hi[2][kD];
+    float invk[kL], invq[kL];
+    int abort;
+};
+
 // T = (I + A)^{-1} for A strictly lower triangular (compact block-major, four
 // 16-row blocks), 256 threads.  The diagonal blocks are inverted by forward
 // substitution; then, with L = I + A split into 32-row halves
 // [[L_lo, 0], [A_hl, L_hi]], each half's lower block is -T_ii A_ij T_jj and
 // the lower-left quarter is -T_hi (A_hl T_lo): four phases of 256 equal items.
-__device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid) {
+__device__ void unit_lower_inverse(const float *A, float *T, float *scr, const PrepGroup &grp) {
+    const int tid = grp.tid;
     if (tid < 64) {  // diagonal block blk, column j: (I + A_bb) x = e_j
         const int blk = tid >> 4, j = tid & 15;
         const float *Ab = A + tri_blk(blk, blk);
@@ -134,7 +176,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
 #pragma unroll
         for (int r = 0; r < 16; ++r) Td[(r << 4) + j] = x[r];
     }
-    __syncthreads();
+    grp.sync();
     {  // F = T_ii A_{i,i-1} for i = 1, 3 (scratch blocks 0, 1): item (b, row, column pair)
         const int b = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2, i = 1 + 2 * b;
         const float *Ti = T + tri_blk(i, i) + (r << 4);
@@ -153,7 +195,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
         }
         *reinterpret_cast<float2 *>(scr + (b << 8) + (r << 4) + c2) = acc;
     }
-    __syncthreads();
+    grp.sync();
     {  // T_{i,i-1} = -F T_{i-1,i-1}
         const int b = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2, i = 1 + 2 * b;
         const float *F = scr + (b << 8) + (r << 4);
@@ -172,7 +214,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
         }
         *reinterpret_cast<float2 *>(T + tri_blk(i, i - 1) + (r << 4) + c2) = make_float2(-acc.x, -acc.y);
     }
-    __syncthreads();
+    grp.sync();
     {  // X_ij = sum_{k=j}^{1} A_ik T_kj for (i, j) in {2, 3} x {0, 1} (scratch blocks 2..5)
         const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -193,7 +235,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
         }
         *reinterpret_cast<float4 *>(scr + 512 + (xb << 8) + (r << 4) + c4) = acc;
     }
-    __syncthreads();
+    grp.sync();
     {  // T_ij = -sum_{k=2}^{i} T_ik X_kj
         const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -214,7 +256,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, int tid
         }
         *reinterpret_cast<float4 *>(T + tri_blk(i, j) + (r << 4) + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-    __syncthreads();
+    grp.sync();
 }
 
 // Exact A and P on the CUDA cores for a chunk whose log-decay range is too
@@ -306,16 +348,14 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // once its bulk stores are complete) as soon as this unit's loads are on
 // their way.  Returns false after recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
-                             uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish = nullptr) {
-    __shared__ __align__(16) float s_beta[kL];
-    __shared__ __align__(16) float s_bm[kD];  // per-channel reference, exp factors (16-byte aligned for float4 reads)
-    __shared__ __align__(16) float s_F[kD];
-    __shared__ __align__(16) float s_Em[kD];
-    __shared__ __align__(16) float s_blast[kD];
-    __shared__ float s_half[kD], s_mid[kD], s_lo[2][kD], s_hi[2][kD];
-    __shared__ float s_invk[kL], s_invq[kL];
-    __shared__ int s_abort;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+                             uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish, const PrepGroup &grp,
+                             PrepShared &sh) {
+    float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
+    float *s_half = sh.half, *s_mid = sh.mid, *s_invk = sh.invk, *s_invq = sh.invq;
+    float(*s_lo)[kD] = sh.lo;
+    float(*s_hi)[kD] = sh.hi;
+    int &s_abort = sh.abort;
+    const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(p.ws + p.doc_slot0_off);
     char *ws = p.ws;
@@ -342,13 +382,13 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     }
     if (tid < kL) s_beta[tid] = tid < Lc ? p.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     tc::tc_fence_before();
-    __syncthreads();
+    grp.sync();
     tc::tc_fence_after();
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int trow = (warp & 3) * 32 + lane;  // this thread's TMEM lane
     const int hs = warp >> 2;                 // this warp's half of an accumulator's columns
     if (!tc::mbar_wait(&bars->g, ph)) s_abort = 1;
-    __syncthreads();
+    grp.sync();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
         if (tid == 0) flag_timeout(ws);
         return false;
@@ -368,7 +408,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             bcol[u] = acc;
         }
         if (hh == 0) s_half[c] = acc;
-        __syncthreads();  // all of g has been read (b may now go to its swizzled places); s_half is final
+        grp.sync();  // all of g has been read (b may now go to its swizzled places); s_half is final
         const float off = hh ? s_half[c] : 0.f;
         float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
@@ -382,7 +422,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         }
         s_lo[hh][c] = lo;
         s_hi[hh][c] = hi;
-        __syncthreads();
+        grp.sync();
         bool bad = false;
         if (tid < kD) {
             const float bm = s_mid[c];
@@ -392,7 +432,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         // Reference point of the factorised exponentials: the middle token; a chunk whose range is too
         // wide for that takes exact A and P and the chunk start as reference (exp(b_r) <= 1 for
         // non-positive gates), so no operand can overflow.
-        unsafe = __syncthreads_or(bad) != 0;
+        unsafe = grp.sync_or(bad);
         if (tid < kD) {
             const float blast = s_blast[c];
             const float bref = unsafe ? 0.f : s_mid[c];
@@ -414,7 +454,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
                 tc::tma_prefetch_3d(p.tm_v, 64, nh, nt0);
             }
         }
-        __syncthreads();
+        grp.sync();
     }
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
@@ -446,13 +486,13 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             s_invk[r] = rsqrtf(sk2 + p.qk_eps);
             s_invq[r] = rsqrtf(sq2 + p.qk_eps);
         }
-        __syncthreads();
+        grp.sync();
     }
     float accA[16], accP[16];
     if (unsafe) {
         exact_ap(sm + PrepSmem::X, Gf, s_beta, Lc, tid, accA, accP, p.qk_norm ? s_invk : nullptr,
                  p.qk_norm ? s_invq : nullptr);
-        __syncthreads();  // the raw k, q tiles are about to be scaled in place
+        grp.sync();  // the raw k, q tiles are about to be scaled in place
     }
 
     // Operand build: thread t owns channel octet o = t % 16 (channels 8 o .. 8 o + 7) of token rows
@@ -520,7 +560,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
-    __syncthreads();
+    grp.sync();
     tc::tc_fence_after();
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
@@ -608,7 +648,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     }
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
-    __syncthreads();
+    grp.sync();
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
         return false;
@@ -616,7 +656,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
 
     // triangular solve in fp32, then T diag(beta) as the bf16 round-2 B operand (K-major [r][s])
     float *Tf = reinterpret_cast<float *>(sm + PrepSmem::Tfp);
-    unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), tid);
+    unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), grp);
     {
         // thread (r, q) takes columns 16 q .. 16 q + 15 of row r (one row of a 16 x 16 block of T, absent
         // above the diagonal blocks), four at a time in an order rotated by q: the four threads of a row
@@ -638,7 +678,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
-    __syncthreads();
+    grp.sync();
     tc::tc_fence_after();
     if (tid == 0) {  // P is final: its image goes to the record for the output pass
         tc::bulk_s2g(rec + R.P, sm + PrepSmem::P, 8192);
@@ -676,7 +716,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     tc::fence_async_smem();
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
-    __syncthreads();
+    grp.sync();
     tc::tc_fence_after();
     if (s_abort) {
         if (tid == 0) {
@@ -750,7 +790,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     tc::fence_async_smem();
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
-    __syncthreads();
+    grp.sync();
     tc::tc_fence_after();
     if (s_abort) {
         if (tid == 0) {
@@ -778,7 +818,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     ok = tc::mbar_wait(&bars->r4, ph);
     tc::tc_fence_after();
     if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
-    __syncthreads();
+    grp.sync();
     if (warp_all(ok)) {
         const int c = trow;
 #pragma unroll
@@ -796,7 +836,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     tc::fence_async_smem();
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
-    __syncthreads();
+    grp.sync();
     const bool done = !s_abort;
     if (tid == 0) {
         if (done) {
@@ -818,6 +858,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    int resident, int qk_norm, float qk_eps) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ PrepBars bars;
+    __shared__ PrepShared psh;
     __shared__ uint32_t tmem_base;
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -859,7 +900,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const PrepParams prm{&tm_q,         &tm_k,       &tm_v,          &tm_g,   beta,  cu, num_seqs, H, ws, doc_slot0_off,
                          records_off, record_bytes, qk_norm, qk_eps};
     prepare_unit(prm, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, has_next ? nxt % (int)gridDim.x : -1,
-                 has_next ? nxt / (int)gridDim.x : 0);
+                 has_next ? nxt / (int)gridDim.x : 0, nullptr, PrepGroup{tid, 0u}, psh);
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
@@ -867,120 +908,141 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // ---------------------------------------------------------------------------
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
-constexpr int kNBuf = 4;  // record buffers: chunks c + 1 .. c + 3 stream in while chunk c computes
-constexpr int kNSb = 5;   // bf16 state images: multiplied, being written, up to three awaiting their copy out
-struct StateSmem {
-    static constexpr uint32_t kBuf = 43008;  // M' and gamma (33 KB) + this CTA's Bc tile (8 KB), 1 KB aligned
+// A chain is one (document, head, TN-column tile of S), TN = 32 or 64, run by one CTA sequentially over the
+// document's chunks.  Its shared memory: kNBuf record buffers (M' and gamma, then the chain's Bc tile(s)) and a
+// ring of kNSb bf16 images of S^T (the B operand of M' S).
+template <int TN>
+struct ChainCfg {
+    static_assert(TN == 32 || TN == 64, "column tile of a chain");
+    static constexpr int kNBuf = TN == 32 ? 4 : 3;             // records in flight
+    static constexpr int kNSb = TN == 32 ? 5 : 3;              // images: multiplied, being written, awaiting copy
+    static constexpr uint32_t kBc = (uint32_t)TN * kD * 2;     // the chain's Bc tiles: 8 / 16 KB
     static constexpr uint32_t Mc = 0, gam = 32768, Bc = 33792;
-    // S^T operand, K-major [32 rows][128 K] in 2 panels of 4 KB, a ring of kNSb: chunk c's MMAs
-    // read image c % kNSb, which the publisher warp also copies to chunk c's record for the output
-    // pass, while the epilogue writes image (c + 1) % kNSb.
+    static constexpr uint32_t kBuf = Bc + kBc;                 // a multiple of 1 KB (operand alignment)
+    static constexpr uint32_t kPanel = (uint32_t)TN * 128;     // one 64-wide K panel of the image
+    static constexpr uint32_t kImg = 2 * kPanel;
     static constexpr uint32_t SB = kNBuf * kBuf;
-    static constexpr uint32_t bytes = SB + kNSb * 8192;
+    static constexpr uint32_t bytes = SB + kNSb * kImg;
+    static constexpr int kCols = TN / 2;                       // columns of S per epilogue thread
+    static_assert(kBuf % 1024 == 0 && kImg % 1024 == 0, "1 KB aligned operands");
 };
 
+template <int TN>
 __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int tile, uint64_t *bar) {
     constexpr TcRecord R = tc_record();
-    tc::mbar_arrive_expect_tx(bar, (uint32_t)R.state_part + 8192u);
+    constexpr uint32_t kBc = ChainCfg<TN>::kBc;
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)R.state_part + kBc);
     tc::bulk_g2s(buf, rec, (uint32_t)R.state_part, bar);
-    tc::bulk_g2s(buf + StateSmem::Bc, rec + R.Bc + (size_t)tile * 8192, 8192, bar);
+    tc::bulk_g2s(buf + ChainCfg<TN>::Bc, rec + R.Bc + (size_t)tile * kBc, kBc, bar);
 }
 
-// Writes S[i][16 h + j] (j < 16, this thread's half h of the tile's columns)
-// into the K-major S^T operand, element (16 h + j, i).  Rows i and i ^ 1 (lanes
-// of one warp) trade values so that each stores whole 4-byte words holding
-// rows (i & ~1, i | 1) of one column: the even lane columns 16 h + u, the odd
-// lane columns 16 h + 8 + ((u + 4) mod 8), which keeps the 32 stores of a warp
-// instruction on 32 distinct banks.
-__device__ __forceinline__ void store_state_half(uint8_t *SB, int i, int h, const float (&S)[16]) {
-    uint8_t *p = SB + (uint32_t)(i >> 6) * 4096u;
+// Writes S[i][jbase + j] (j < NC, this thread's columns) into the K-major S^T image (element (jbase + j, i),
+// K panels `panel_bytes` apart).  Rows i and i ^ 1 (lanes of one warp) trade values so that each stores whole
+// 4-byte words holding rows (i & ~1, i | 1) of one column: the even lane the columns j < NC / 2, the odd lane
+// the others in a rotated order, which keeps a warp's 32 stores on 32 distinct banks.
+template <int NC>
+__device__ __forceinline__ void store_state_cols(uint8_t *SB, uint32_t panel_bytes, int i, int jbase,
+                                                 const float (&S)[NC]) {
+    constexpr int HALF = NC / 2;
+    uint8_t *p = SB + (uint32_t)(i >> 6) * panel_bytes;
     const int odd = i & 1, ie = i & ~1;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int ja = u, jb = 8 + ((u + 4) & 7);  // the even and the odd lane's column of this step
-        const float give = odd ? S[ja] : S[jb];   // what the partner needs from this row
+    for (int u = 0; u < HALF; ++u) {
+        const int ja = u, jb = HALF + ((u + HALF / 2) % HALF);  // the even and the odd lane's column of this step
+        const float give = odd ? S[ja] : S[jb];                  // what the partner needs from this row
         const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-        const int j = 16 * h + (odd ? jb : ja);
+        const int j = jbase + (odd ? jb : ja);
         const float lo = odd ? got : S[ja], hi = odd ? S[jb] : got;
         *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
     }
 }
 
-// One CTA per (document, head, 32-column tile of S), 352 threads:
+// One CTA per chain, kStateThreads threads:
 //   warps 0-7   epilogue: thread <-> state row i = 32 (w % 4) + lane (its TMEM lane) and column half
-//               h = w / 4; S[i][16 h ..] stays fp32 in registers
-//   warps 8, 9  lane 0 issues M' S over K panel w - 8 of S; warp 9 also keeps records streaming
-//               three chunks ahead
+//               h = w / 4; S[i][TN/2 h ..] stays fp32 in registers
+//   warps 8, 9  lane 0 issues M' S over K panel w - 8 of S
 //   warp 10     publisher: copies each chunk's S image to its record and, when asked, publishes it
-// Per chunk c:  issuers (after the epilogue warps' arrival on the operand barrier) -> MMAs ->
-// a_bar -> epilogue S <- gamma S + Bc + M' S, image of S_{c+1} -> arrival on the operand barrier
-// and on img_full.  The publisher hands each image slot back through img_free; it runs behind the
-// chain by up to kNSb - 2 images without holding it up.
+//   warp 11     loader: streams the records in, up to kNBuf - 1 chunks ahead, each once its buffer is free
+//               and, when asked, once the record is published
+// Per chunk c:  issuers (after the epilogue warps' arrival on the operand barrier) -> MMAs -> a_bar ->
+// epilogue S <- gamma S + Bc + M' S, image of S_{c+1} -> arrivals on the operand barrier, img_full and the
+// buffer's empty barrier.  The publisher hands each image slot back through img_free.
 constexpr int kStateEpiWarps = 8;
 constexpr int kStatePubWarp = kStateEpiWarps + 2;
-constexpr int kStateThreads = (kStatePubWarp + 1) * 32;
+constexpr int kStateLoadWarp = kStatePubWarp + 1;
+constexpr int kStateThreads = (kStateLoadWarp + 1) * 32;
 constexpr uint32_t kBarOperand = 1;  // named barrier: the next S image is complete
 constexpr int kBarOperandThreads = (kStateEpiWarps + 2) * 32;  // epilogue and issuer warps
 constexpr int kStatePubLag = 2;    // images are published once the copy two chunks later is issued ...
 constexpr int kStatePubBatch = 4;  // ... four at a time, behind one release fence
 constexpr int kChainOutGroups = 2;  // output groups of 128 threads in each non-chain CTA of the chain plan
 
-// Chain j (document, head, column tile) by a CTA of kStateThreads threads over `smem_raw` (StateSmem).
-// With `sdone` set, each chunk's state image is also published there (a count per (slot, head), raised
-// after a GPU-scope release fence, in batches of kStatePubBatch) once its copy to the record is complete,
-// for output units running alongside.
+// Hand-offs of a chain with the rest of a launch (all null / true when it runs alone).
+struct ChainLinks {
+    int32_t *sdone = nullptr;        // publish each chunk's state image there (count in 32-column units)
+    bool publish = true;             // false only in tests of the timeout path
+    const int32_t *ready = nullptr;  // wait for each record's publication flag there before loading it
+    uint64_t flag_wait_ns = kFlagWaitNs;
+};
+
+// Chain j by a CTA of at least kStateThreads threads over `smem_raw` (ChainCfg<TN>); threads beyond
+// kStateThreads take part in the CTA barriers only.
+template <int TN>
 __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                             float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off,
-                            size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw, int32_t *sdone,
-                            bool publish = true) {
-    __shared__ uint64_t full_bar[kNBuf], a_bar, img_full[kNSb], img_free[kNSb];
+                            size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw,
+                            const ChainLinks &links) {
+    using Cfg = ChainCfg<TN>;
+    constexpr int NB = Cfg::kNBuf, NS = Cfg::kNSb, NC = Cfg::kCols, NT = kD / TN;
+    __shared__ uint64_t full_bar[NB], empty_bar[NB], a_bar, img_full[NS], img_free[NS];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
-    // (the chunk index kernel's table and status word are complete: the preparation waited for them before
-    // letting this kernel start)
+    // (the chunk index kernel's table and status word are complete: the kernel before this one waited for them
+    // before letting this one start)
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool epi = warp < kStateEpiWarps;
     const bool issuer = warp == kStateEpiWarps || warp == kStateEpiWarps + 1;
     const int i = (warp & 3) * 32 + lane, hcol = (warp >> 2) & 1;
-    const int tile = j % kNTile;
-    const int h = (j / kNTile) % H;
-    const int n = j / (kNTile * H);
+    const int tile = j % NT;
+    const int h = (j / NT) % H;
+    const int n = j / (NT * H);
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
-    const int col0 = tile * kTile + 16 * hcol;
+    const int col0 = tile * TN + NC * hcol;
     const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + col0;
     constexpr TcRecord R = tc_record();
 
-    float S[16];
+    float S[NC];
 #pragma unroll
-    for (int c4 = 0; c4 < 16; c4 += 4) {
+    for (int c4 = 0; c4 < NC; c4 += 4) {
         const float4 v = (S0 && epi) ? *reinterpret_cast<const float4 *>(S0 + state_off + c4)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         S[c4] = v.x; S[c4 + 1] = v.y; S[c4 + 2] = v.z; S[c4 + 3] = v.w;
     }
     bool ok = true;
     if (nchunks > 0) {
-        if (epi) store_state_half(sm + StateSmem::SB, i, hcol, S);
+        if (epi) store_state_cols<NC>(sm + Cfg::SB, Cfg::kPanel, i, NC * hcol, S);
         tc::fence_async_smem();
         char *rec_h = ws + records_off + (size_t)h * record_bytes;  // record of (slot 0, head h)
         const size_t rec_stride = (size_t)H * record_bytes;          // one chunk slot further
         if (tid == 0) {
-            for (int b = 0; b < kNBuf; ++b) tc::mbar_init(&full_bar[b], 1);
+            for (int b = 0; b < NB; ++b) {
+                tc::mbar_init(&full_bar[b], 1);
+                tc::mbar_init(&empty_bar[b], kStateEpiWarps);  // one arrival per epilogue warp
+            }
             tc::mbar_init(&a_bar, 2);  // one commit from each issuer
-            for (int b = 0; b < kNSb; ++b) {
+            for (int b = 0; b < NS; ++b) {
                 tc::mbar_init(&img_full[b], kStateEpiWarps);  // one arrival per epilogue warp
                 tc::mbar_init(&img_free[b], 1);               // the publisher's
             }
             tc::fence_mbar_init();
             s_abort = 0;
-            tc::grid_dep_wait();  // the preparation has completed: its records are visible
-            for (int c = 0; c < kNBuf - 1 && c < nchunks; ++c)
-                issue_record(sm + c * StateSmem::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[c]);
+            tc::grid_dep_wait();  // the preparation has completed, or (pipe plan) its records are awaited by flag
         }
         if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 64);
+            tc::tmem_alloc(&tmem_base, 2 * TN);
             tc::tmem_relinquish();
         }
         tc::tc_fence_before();
@@ -989,35 +1051,49 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         // Only now (after this CTA's wait for the preparation) may the output pass start: it reads the
         // preparation's part of each record before it waits for this kernel.
         tc::grid_dep_launch();
-        // TMEM: M' S over the two K panels in cols 0..31 and 32..63
+        // TMEM: M' S over the two K panels in cols 0 .. TN - 1 and TN .. 2 TN - 1
         const uint32_t tmem = tmem_base;
 
-        if (issuer) {
+        if (warp == kStateLoadWarp) {
+            if (lane == 0) {
+                int issued = 0;
+                for (int c = 0; c < nchunks; ++c) {
+                    const int b = c % NB;
+                    if (c >= NB) ok = ok && tc::mbar_wait(&empty_bar[b], (uint32_t)((c / NB - 1) & 1));
+                    if (ok && links.ready) {
+                        ok = tc::wait_flag_geq(links.ready + (size_t)(first + c) * H + h, 1, links.flag_wait_ns);
+                        tc::fence_proxy_async_global();
+                    }
+                    if (!ok) break;
+                    issue_record<TN>(sm + b * Cfg::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[b]);
+                    issued = c + 1;
+                }
+                if (!ok) {  // copies already on their way land before the CTA's shared memory can go away
+                    for (int c = max(0, issued - NB); c < issued; ++c)
+                        tc::mbar_wait(&full_bar[c % NB], (uint32_t)((c / NB) & 1), 10000000ull);
+                }
+            }
+            __syncwarp();
+        } else if (issuer) {
             const uint32_t panel = (uint32_t)(warp - kStateEpiWarps);
             constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-            constexpr uint32_t idN = tc::idesc_bf16_f32(128, kTile, false, false);
+            constexpr uint32_t idN = tc::idesc_bf16_f32(128, TN, false, false);
             for (int c = 0; c < nchunks; ++c) {
-                const int bsel = c % kNBuf;
-                uint8_t *buf = sm + bsel * StateSmem::kBuf;
-                uint8_t *sbc = sm + StateSmem::SB + (uint32_t)(c % kNSb) * 8192u;
+                const int bsel = c % NB;
+                uint8_t *buf = sm + bsel * Cfg::kBuf;
+                uint8_t *sbc = sm + Cfg::SB + (uint32_t)(c % NS) * Cfg::kImg;
                 if (c > 0) tc::named_barrier(kBarOperand, kBarOperandThreads);  // S_c's image is complete
                 tc::tc_fence_after();
                 if (lane == 0) {
-                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / NB) & 1));
                     if (ok) {
-                        const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + StateSmem::Mc + panel * 16384u));
-                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * 4096u));
+                        const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + Cfg::Mc + panel * 16384u));
+                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * Cfg::kPanel));
                         for (int s = 0; s < 4; ++s)  // K steps of 16: +32 bytes, +2 in the start-address field
-                            tc::mma_bf16(tmem + 32u * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, s > 0);
+                            tc::mma_bf16(tmem + (uint32_t)TN * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s,
+                                         idN, s > 0);
                     }
                     tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
-                    if (panel == 1 && ok) {
-                        // the buffer chunk c - 1 used was released by the operand barrier of this chunk
-                        const int cn = c + kNBuf - 1;
-                        if (cn < nchunks)
-                            issue_record(sm + (cn % kNBuf) * StateSmem::kBuf,
-                                         rec_h + (size_t)(first + cn) * rec_stride, tile, &full_bar[cn % kNBuf]);
-                    }
                 }
                 __syncwarp();
             }
@@ -1025,106 +1101,128 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             if (lane == 0) {
                 int pub = 0;  // images published so far
                 for (int c = 0; c < nchunks; ++c) {
-                    const int sl = c % kNSb;
+                    const int sl = c % NS;
                     // image 0 was written before the CTA barrier; image c >= 1 by chunk c - 1's epilogue
-                    if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / kNSb) & 1));
+                    if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / NS) & 1));
                     if (ok) {
-                        // S_c's image, tile rows of both panels, into chunk c's record
-                        const uint8_t *sbc = sm + StateSmem::SB + (uint32_t)sl * 8192u;
+                        // S_c's image, this chain's rows of both panels, into chunk c's record
+                        const uint8_t *sbc = sm + Cfg::SB + (uint32_t)sl * Cfg::kImg;
                         char *rec = rec_h + (size_t)(first + c) * rec_stride;
-                        tc::bulk_s2g(rec + R.S + (size_t)tile * 4096, sbc, 4096);
-                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * 4096, sbc + 4096, 4096);
+                        tc::bulk_s2g(rec + R.S + (size_t)tile * Cfg::kPanel, sbc, Cfg::kPanel);
+                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * Cfg::kPanel, sbc + Cfg::kPanel, Cfg::kPanel);
                         tc::bulk_commit();
                         tc::bulk_wait_read();  // the slot may be rewritten
                     }
                     tc::mbar_arrive(&img_free[sl]);  // always: the epilogue counts on one per image
-                    if (ok && sdone && publish && c + 1 - kStatePubLag - pub >= kStatePubBatch) {
+                    if (ok && links.sdone && links.publish && c + 1 - kStatePubLag - pub >= kStatePubBatch) {
                         // the copies of S_pub .. S_{c-2} have completed: publish them
                         static_assert(kStatePubLag == 2, "wait_group below");
                         tc::bulk_wait_all_but_two();
                         tc::fence_proxy_async_global();
                         tc::fence_acq_rel_gpu();
                         for (; pub <= c - kStatePubLag; ++pub)
-                            tc::red_relaxed_gpu_add(sdone + (size_t)(first + pub) * H + h, 1);
+                            tc::red_relaxed_gpu_add(links.sdone + (size_t)(first + pub) * H + h, TN / 32);
                     }
                 }
                 tc::bulk_wait_all();  // shared memory must outlive the image copies
-                if (sdone && publish && ok) {
+                if (links.sdone && links.publish && ok) {
                     tc::fence_proxy_async_global();
                     tc::fence_acq_rel_gpu();
-                    for (; pub < nchunks; ++pub) tc::red_relaxed_gpu_add(sdone + (size_t)(first + pub) * H + h, 1);
+                    for (; pub < nchunks; ++pub)
+                        tc::red_relaxed_gpu_add(links.sdone + (size_t)(first + pub) * H + h, TN / 32);
                 }
             }
             __syncwarp();
-        } else {
-            const uint32_t tacc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 16u * (uint32_t)hcol;
+        } else if (epi) {
+            const uint32_t tacc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(NC * hcol);
             for (int c = 0; c < nchunks; ++c) {
-                const int bsel = c % kNBuf;
-                const uint8_t *buf = sm + bsel * StateSmem::kBuf;
-                // gamma and this thread's 16 Bc values, read while the MMAs run
-                ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / kNBuf) & 1));
-                const float gam = reinterpret_cast<const float *>(buf + StateSmem::gam)[i];
+                const int bsel = c % NB;
+                const uint8_t *buf = sm + bsel * Cfg::kBuf;
+                // gamma and this thread's NC Bc values, read while the MMAs run
+                ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / NB) & 1));
+                const float gam = reinterpret_cast<const float *>(buf + Cfg::gam)[i];
                 const int nb = c + 1;                // the image this chunk writes: S_{c+1}, needed by chunk c + 1
                 const bool img = nb < nchunks;
-                uint8_t *sbn = sm + StateSmem::SB + (uint32_t)(nb % kNSb) * 8192u;
-                float bc[16];
-                {
-                    const uint8_t *brow = buf + StateSmem::Bc + i * 64;
+                uint8_t *sbn = sm + Cfg::SB + (uint32_t)(nb % NS) * Cfg::kImg;
+                // Bc is stored per 32-column tile: rows of 64 bytes, 16-byte chunk k at k ^ ((row / 2) mod 4)
+                const uint8_t *brow = buf + Cfg::Bc + (NC == 32 ? (uint32_t)hcol * 8192u : 0u) + i * 64;
+                const int k0 = NC == 32 ? 0 : 2 * hcol;
+                auto bc8 = [&](int kk, float (&f)[8]) {
+                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((k0 + kk) ^ ((i >> 1) & 3)) << 4)), f);
+                };
+                float bc[16];  // 16 columns: read while the MMAs run
+                if constexpr (NC == 16) {
                     float f[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((2 * hcol) ^ ((i >> 1) & 3)) << 4)), f);
+                    bc8(0, f);
 #pragma unroll
                     for (int u = 0; u < 8; ++u) bc[u] = f[u];
-                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((2 * hcol + 1) ^ ((i >> 1) & 3)) << 4)), f);
+                    bc8(1, f);
 #pragma unroll
                     for (int u = 0; u < 8; ++u) bc[8 + u] = f[u];
                 }
-                // the slot's previous image, S_{c+1-kNSb}, has been copied out
-                if (img && nb >= kNSb) ok = ok && tc::mbar_wait(&img_free[nb % kNSb], (uint32_t)((nb / kNSb - 1) & 1));
+                // the slot's previous image, S_{c+1-NS}, has been copied out
+                if (img && nb >= NS) ok = ok && tc::mbar_wait(&img_free[nb % NS], (uint32_t)((nb / NS - 1) & 1));
                 ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
                 tc::tc_fence_after();
                 if (warp_all(ok)) {
-                    float t0[16], t1[16];
-                    tc::tmem_ld16x2(tacc, tacc + 32u, t0, t1);
+                    // S <- gamma S + (Bc + (P0 + P1)), P0 / P1 the two K panels' products
+                    float t0[NC];
+                    if constexpr (NC == 16) {
+                        float t1[16];
+                        tc::tmem_ld16x2(tacc, tacc + TN, t0, t1);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) S[j] = fmaf(gam, S[j], bc[j] + (t0[j] + t1[j]));
-                    if (img) store_state_half(sbn, i, hcol, S);
+                        for (int q = 0; q < 16; ++q) S[q] = fmaf(gam, S[q], bc[q] + (t0[q] + t1[q]));
+                    } else {
+                        // 32 columns: the second panel and Bc in halves, to stay within the register budget
+                        tc::tmem_ld32(tacc, t0);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float t1[16];
+                            tc::tmem_ld16(tacc + TN + 16u * (uint32_t)hh, t1);
+                            float f[8];
+                            bc8(2 * hh, f);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                S[16 * hh + q] = fmaf(gam, S[16 * hh + q], f[q] + (t0[16 * hh + q] + t1[q]));
+                            bc8(2 * hh + 1, f);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                S[16 * hh + 8 + q] = fmaf(gam, S[16 * hh + 8 + q], f[q] + (t0[16 * hh + 8 + q] + t1[8 + q]));
+                        }
+                    }
+                    if (img) store_state_cols<NC>(sbn, Cfg::kPanel, i, NC * hcol, S);
                 }
                 tc::fence_async_smem();
                 tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&empty_bar[bsel]);  // the MMAs and this warp are done with it
                 if (img) {
                     tc::named_barrier_arrive(kBarOperand, kBarOperandThreads);
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&img_full[nb % kNSb]);
+                    if (lane == 0) tc::mbar_arrive(&img_full[nb % NS]);
                 }
             }
         }
         if (!ok) s_abort = 1;
         __syncthreads();
-        if (s_abort) {
-            // let any record copy still in flight land before the CTA's shared memory goes away
-            if (tid == 0) {
-                flag_timeout(ws);
-                for (int b = 0; b < kNBuf; ++b) tc::mbar_wait(&full_bar[b], 0, 10000000ull);
-            }
-            __syncthreads();
-        }
-        if (warp == 0) tc::tmem_dealloc(tmem, 64);
+        if (s_abort && tid == 0) flag_timeout(ws);
+        if (warp == 0) tc::tmem_dealloc(tmem, 2 * TN);
         if (s_abort) return;
     }
     if (S_final && epi) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(S_final + state_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        for (int q = 0; q < NC; q += 4)
+            *reinterpret_cast<float4 *>(S_final + state_off + q) = make_float4(S[q], S[q + 1], S[q + 2], S[q + 3]);
     }
 }
 
+template <int TN>
 __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
                  size_t record_bytes) {
     extern __shared__ uint8_t smem_raw[];
-    state_chain(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x, smem_raw,
-                nullptr);
+    state_chain<TN>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
+                    smem_raw, ChainLinks{});
 }
 
 // ---------------------------------------------------------------------------
@@ -1176,7 +1274,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
                             OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, const OutNorm &onorm,
                             bool dep_wait = false, const int32_t *sflag = nullptr,
-                            uint64_t flag_wait_ns = kFlagWaitNs) {
+                            uint64_t flag_wait_ns = kFlagWaitNs, const int32_t *rflag = nullptr) {
     const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
@@ -1184,10 +1282,15 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
                   "output pass loads the record tail as one image");
     const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
     if (tid == 0) {
-        // Qp, P, Ut (written by the preparation) ...
+        // Qp, P, Ut (written by the preparation; in the pipe plan, once published) ...
+        bool rok = true;
+        if (rflag) {
+            rok = tc::wait_flag_geq(rflag, 1, flag_wait_ns);
+            tc::fence_proxy_async_global();
+        }
         tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
         tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
-        bool ok = tc::mbar_wait(&bars->load, ph);
+        bool ok = tc::mbar_wait(&bars->load, ph) && rok;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
         constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
         constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, false);
@@ -1331,12 +1434,15 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     if ((int)blockIdx.x < n_state) {
         // (fault == kFaultNoPublish only in tests of the timeout path: no state image is published, so the
         // output groups' bounded waits run out)
-        state_chain(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
-                    smem_raw, sdone, fault != kFaultNoPublish);
+        ChainLinks links;
+        links.sdone = sdone;
+        links.publish = fault != kFaultNoPublish;
+        state_chain<kTile>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes,
+                           (int)blockIdx.x, smem_raw, links);
         return;
     }
     constexpr int kGroups = kChainOutGroups;
-    static_assert(kGroups * 128 <= kStateThreads && kGroups * OutSmem::bytes + 1024 <= StateSmem::bytes + 1024 &&
+    static_assert(kGroups * 128 <= kStateThreads && kGroups * OutSmem::bytes <= ChainCfg<kTile>::bytes &&
                       OutSmem::bytes % 1024 == 0,
                   "output groups fit the chain CTA");
     __shared__ OutBars bars[kGroups];
@@ -1396,6 +1502,141 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
 }
 
 constexpr int kChainMinWorkers = 48;  // output CTAs alongside the chains, at least
+
+// ---------------------------------------------------------------------------
+// Pipe plan: preparation, state chains and outputs in one cooperative launch
+// ---------------------------------------------------------------------------
+// One CTA of kPipeThreads per SM.  CTAs [0, n_chain) each run one chain of 64 columns (state_chain<64>), which
+// loads each chunk's record as soon as its publication flag is raised and publishes each chunk's state image;
+// every other CTA holds two groups of 256 threads that take work from one counter: first the preparation
+// units in chunk-slot order (each publishes its record with a GPU-scope release once its bulk stores are
+// complete), then the output units in the same order (each waits for its record and for its chunk's state
+// image).  So the chains run on whole SMs while later chunks are still being prepared, and the chains' work
+// leaves the preparation's critical path.
+//
+// Progress: every CTA is resident (cooperative launch).  A preparation waits for nothing but its own copies
+// and MMAs; a chain waits only for records, all of which belong to preparation units claimed before any
+// output unit; an output unit waits for a record and for the chains.  Every wait is bounded.
+constexpr int kPipeThreads = 512;
+constexpr int kPipeChainMax = 38;  // automatic choice: at most this many chains of 64 columns
+constexpr size_t kPipeSmemBytes = (ChainCfg<64>::bytes > 2 * PrepSmem::bytes ? ChainCfg<64>::bytes
+                                                                               : 2 * PrepSmem::bytes) +
+                                  1024;
+static_assert(PrepSmem::bytes % 1024 == 0 && OutSmem::bytes <= PrepSmem::bytes, "a group's region holds a unit");
+
+struct PipeArgs {
+    const float *S0;
+    float *S_final;
+    __nv_bfloat16 *o;
+    int32_t *ready;    // [slot * H + h]: the record is published
+    int32_t *sdone;    // [slot * H + h]: columns (in 32s) whose state image is published
+    int32_t *counter;  // next work item
+    int n_chain;
+    unsigned long long flag_wait_ns;
+    int fault;  // kFaultNoPublish only in tests of the timeout path
+    OutNorm onorm;
+};
+
+__device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm) {
+    __shared__ PrepBars pbars[2];
+    __shared__ OutBars obars[2];
+    __shared__ PrepShared psh[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_unit[2], s_ok[2];
+    const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255, gwarp = gtid >> 5;
+    const int H = pp.H;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
+    const int units = doc_slot0[pp.num_seqs] * H;  // preparation units, then as many output units
+    if (gtid == 0) {
+        prep_bars_init(&pbars[g]);
+        tc::mbar_init(&obars[g].load, 1);
+        tc::mbar_init(&obars[g].sload, 1);
+        tc::mbar_init(&obars[g].mma, 1);
+        tc::fence_mbar_init();
+    }
+    if (tid < 32) {  // one allocation for both groups (the permit is given up once, for the whole CTA)
+        tc::tmem_alloc(&tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const PrepGroup grp{gtid, 1u + (uint32_t)g};
+    uint8_t *gsm = sm + (uint32_t)g * PrepSmem::bytes;
+    const uint32_t tmem = tmem_base + 256u * (uint32_t)g;
+    uint32_t nprep = 0, nout = 0;
+    int32_t *pending = nullptr;  // the last record this group prepared, not yet published
+    for (;;) {
+        if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);
+        grp.sync();
+        const int u = s_unit[g];
+        grp.sync();  // every thread has read s_unit before the next claim overwrites it
+        if (u >= 2 * units) break;
+        int doc, t0, Lc;
+        if (u < units) {
+            const int slot = u / H, h = u % H;
+            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+            // the previous record is published once this unit's loads are issued; this one's stays pending
+            const bool ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, -1, 0, pending, grp,
+                                         psh[g]);
+            ++nprep;
+            if (!ok) break;
+            pending = a.ready + (size_t)slot * H + h;
+        } else {
+            if (gtid == 0 && pending) {
+                tc::bulk_wait_all();
+                tc::fence_proxy_async_global();
+                tc::st_release_gpu(pending, 1);
+            }
+            pending = nullptr;
+            const int v = u - units, slot = v / H, h = v % H;
+            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+            bool ok = true;
+            if (gtid < 128) {
+                ok = output_unit(pp.cu, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
+                                 &obars[g], nout & 1u, tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, a.onorm,
+                                 false, a.sdone + (size_t)slot * H + h, a.flag_wait_ns,
+                                 a.ready + (size_t)slot * H + h);
+            }
+            ++nout;
+            grp.sync();
+            if (!s_ok[g]) break;
+        }
+    }
+    if (gtid == 0 && pending) {
+        tc::bulk_wait_all();
+        tc::fence_proxy_async_global();
+        tc::st_release_gpu(pending, 1);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid < 32) tc::tmem_dealloc(tmem_base, 512);
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1)
+prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
+                char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, int qk_norm,
+                float qk_eps, PipeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    tc::grid_dep_wait();  // the chunk index kernel: slot table, status word, cleared flags
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    uint8_t *sm = align1024(smem_raw);
+    if ((int)blockIdx.x < a.n_chain) {
+        ChainLinks links;
+        links.sdone = a.sdone;
+        links.publish = a.fault != kFaultNoPublish;
+        links.ready = a.ready;
+        links.flag_wait_ns = a.flag_wait_ns;
+        state_chain<64>(cu, num_seqs, H, a.S0, a.S_final, ws, doc_slot0_off, records_off, record_bytes,
+                        (int)blockIdx.x, sm, links);
+        return;
+    }
+    const PrepParams pp{&tm_q,       &tm_k,        &tm_v,   &tm_g,  beta, cu, num_seqs, H, ws, doc_slot0_off,
+                        records_off, record_bytes, qk_norm, qk_eps};
+    pipe_worker(pp, a, sm);
+}
 
 
 // ---------------------------------------------------------------------------
@@ -1511,7 +1752,8 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
 }
 
 constexpr int kPrepSmem = PrepSmem::bytes + 1024;
-constexpr int kStateSmem = StateSmem::bytes + 1024;
+constexpr int kStateSmem = ChainCfg<32>::bytes + 1024;
+constexpr int kStateSmem64 = ChainCfg<64>::bytes + 1024;
 constexpr int kOutSmem = OutSmem::bytes + 1024;
 
 // Per-device facts the launches need, worked out (and the kernels' shared-memory limits raised) once per
@@ -1535,9 +1777,13 @@ const DeviceSetup &device_setup() {
     if (d.err == cudaErrorNotReady) {
         cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (!e) e = cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-        if (!e) e = cudaFuncSetAttribute(prefill_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+        if (!e) e = cudaFuncSetAttribute(prefill_state_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_state_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem64);
         if (!e) e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
         if (!e) e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPipeSmemBytes);
         if (!e) {
             cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1590,16 +1836,22 @@ void testing_set_fault(int fault, long long wait_ns) {
 }
 
 TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
-    // The chain plan when the chains leave at least kChainMinWorkers SMs for the output groups, else three
-    // kernels; a plan forced by the test hook is taken wherever it can run.
+    // Few chains: the pipe plan (at most kPipeChainMax chains of 64 columns); then the chain plan while the
+    // chains of 32 columns leave at least kChainMinWorkers SMs for the output groups; else three kernels.  A
+    // plan forced by the test hook is taken wherever it can run.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int forced = g_test_plan.load();
     if (forced == TC_THREE) return TC_THREE;
     const DeviceSetup &d = device_setup();
     if (d.err) return TC_THREE;
-    const int n_state = num_seqs * H * kNTile;
-    return n_state + kChainMinWorkers <= d.sms ? TC_CHAIN : TC_THREE;
+    const long long chains32 = (long long)num_seqs * H * kNTile, chains64 = chains32 / 2;
+    const bool pipe_fits = chains64 + 2 * kChainMinWorkers / 3 <= d.sms;
+    const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
+    if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
+    if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
+    if (pipe_fits && chains64 <= kPipeChainMax) return TC_PIPE;
+    return chain_fits ? TC_CHAIN : TC_THREE;
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -1612,6 +1864,35 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const DeviceSetup &dset = device_setup();
     if (dset.err) return dset.err;
     cudaError_t e;
+    int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
+    const size_t nflag = (size_t)lay.max_slots * H;
+    const long long wait = g_test_wait_ns.load();
+    const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
+    if (plan == TC_PIPE) {
+        InputMaps m;
+        if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
+        PipeArgs a;
+        a.S0 = S0;
+        a.S_final = S_final;
+        a.o = static_cast<__nv_bfloat16 *>(o);
+        a.ready = flags;
+        a.sdone = flags + nflag;
+        a.counter = flags + 2 * nflag;
+        a.n_chain = num_seqs * H * 2;
+        a.flag_wait_ns = flag_wait;
+        a.fault = g_test_fault.load();
+        a.onorm = onorm;
+        marks.before(st, "prefill_pipe_tc");
+        e = launch_cooperative(prefill_pipe_tc, dim3((unsigned)dset.sms), dim3(kPipeThreads), kPipeSmemBytes, st, m.q,
+                               m.k, m.v, m.g, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
+                               lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        // Fewer SMs are available to this context than the device has: nothing was launched; run the three
+        // kernels instead.
+        cudaGetLastError();
+        marks.n--;
+        plan = TC_THREE;
+    }
     if (lay.max_slots > 0 && total_tokens > 0) {
         InputMaps m;
         if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
@@ -1624,28 +1905,31 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     if (num_seqs == 0) return cudaSuccess;
     if (plan == TC_CHAIN) {
-        int32_t *flags = reinterpret_cast<int32_t *>(w + lay.flags_off);
-        const size_t nflag = (size_t)lay.max_slots * H;
         const int n_state = num_seqs * H * kNTile;
-        const long long wait = g_test_wait_ns.load();
-        const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
         // Cooperative: the output groups wait for the chain CTAs' publications, so every CTA must be resident.
         marks.before(st, "prefill_chain_tc");
         e = launch_cooperative(prefill_chain_tc, dim3((unsigned)dset.sms), dim3(kStateThreads), (size_t)kStateSmem,
                                st, cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o), w,
-                               lay.doc_slot0_off, lay.records_off, lay.record_bytes, n_state, flags, flags + nflag,
-                               flag_wait, g_test_fault.load(), onorm);
+                               lay.doc_slot0_off, lay.records_off, lay.record_bytes, n_state, flags + nflag,
+                               flags + 2 * nflag, flag_wait, g_test_fault.load(), onorm);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the state
         // pass and the output pass as separate kernels instead.
         cudaGetLastError();
         marks.n--;
     }
+    // Chains of 32 columns while they fit on the SMs at once, else of 64 (half as many: fewer waves of chains)
+    const size_t chains32 = (size_t)num_seqs * H * kNTile;
     marks.before(st, "prefill_state_tc");
-    if ((e = launch_dependent(prefill_state_tc, dim3((unsigned)((size_t)num_seqs * H * kNTile)), dim3(kStateThreads),
-                              (size_t)kStateSmem, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off,
-                              lay.records_off, lay.record_bytes)))
-        return e;
+    if (chains32 <= (size_t)dset.sms)
+        e = launch_dependent(prefill_state_tc<32>, dim3((unsigned)chains32), dim3(kStateThreads), (size_t)kStateSmem,
+                             st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off,
+                             lay.record_bytes);
+    else
+        e = launch_dependent(prefill_state_tc<64>, dim3((unsigned)(chains32 / 2)), dim3(kStateThreads),
+                             (size_t)kStateSmem64, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off,
+                             lay.records_off, lay.record_bytes);
+    if (e) return e;
     if (lay.max_slots > 0 && total_tokens > 0) {
         marks.before(st, "prefill_output_tc");
         if ((e = launch_dependent(prefill_output_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(128),

@@ -25,14 +25,17 @@ extern "C" {
 #define KDA_TESTING_PLAN_THREE 0    /* preparation, state pass and output pass as three kernels */
 #define KDA_TESTING_PLAN_CHAIN 2    /* preparation, then one cooperative launch of the state chains with the
                                        output units alongside; falls back to THREE where it cannot run */
+#define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains of 64 columns beside groups that
+                                       prepare the records in chunk order and then form the outputs; falls back
+                                       to THREE where it cannot run */
 
 /* Forces a launch plan for later calls.  KDA_ERR_INVALID_ARG for an unknown plan. */
 KDA_API kda_status kda_testing_set_plan(int32_t plan);
 
 /* Faults for tests of the failure path. */
 #define KDA_TESTING_FAULT_NONE 0        /* the default */
-#define KDA_TESTING_FAULT_NO_PUBLISH 1  /* chain plan: the state chains publish none of their state images, so
-                                           the output units' bounded waits on them run out */
+#define KDA_TESTING_FAULT_NO_PUBLISH 1  /* chain and pipe plans: the state chains publish none of their state
+                                           images, so the output units' bounded waits on them run out */
 
 /*
  * Injects `fault` into later calls and bounds the device-side waits on

@@ -4,10 +4,10 @@ Every wait of one CTA on another in libkda's kernels is bounded in time; when
 a bound runs out, the waiting kernel records KDA_ERR_TIMEOUT in the call's
 status word, stops touching the outputs it cannot finish, and returns, so
 that the context stays usable and kda_prefill_check can report the failure.
-Here the test hook kda_testing_set_fault stops the chain plan's state chains
-from publishing their state images, with a short (20 ms) bound on the output
-units' waits for them: nothing hangs, nothing faults, the wait simply runs
-out.
+Here the test hook kda_testing_set_fault stops the state chains of the chain
+and pipe plans from publishing their state images, with a short (20 ms)
+bound on the output units' waits for them: nothing hangs, nothing faults,
+the wait simply runs out.
 """
 from __future__ import annotations
 
@@ -31,13 +31,14 @@ def _call(q, k, v, g, beta, cu, ws, S0):
     return o, S
 
 
-def test_wait_that_runs_out_is_reported_and_the_next_call_is_correct():
+@pytest.mark.parametrize("plan", ["chain", "pipe"])
+def test_wait_that_runs_out_is_reported_and_the_next_call_is_correct(plan):
     inp = workloads.prefill_inputs([300, 77], H=4, d=128, dtype=torch.bfloat16, seed=41, s0_std=0.1)
     q, k, v, g, beta, cu = to_device(inp)
     S0 = inp.S0.to(dev())
     T, H, d = q.shape
     ws = libkda.new_workspace(T, 2, H, d, d, libkda.KDA_BF16, 64, dev())
-    libkda.testing_set_plan(libkda.PLAN_CHAIN)
+    libkda.testing_set_plan(libkda.PLAN_CHAIN if plan == "chain" else libkda.PLAN_PIPE)
     libkda.testing_set_fault(libkda.FAULT_NO_PUBLISH, 20_000_000)
     try:
         t0 = time.perf_counter()
