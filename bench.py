@@ -375,6 +375,50 @@ def bench_decode_indexed(libkda, steps, warmup, dev):
     return dict(us=us, bytes=nbytes, slots=slots, active=active, H=H, d=d, steps=steps)
 
 
+def bench_sublayer(steps, warmup, dev):
+    """Whole-sublayer timing with synthetic weights (measurement only): the stages around the recurrence --
+    projections (cuBLAS bf16 GEMMs), short convolution, recurrence with the fused normalisations, output
+    projection -- each bracketed by events, for the prefill workload's shape and for one decode step of the
+    decode workload's shape.  Hidden size H * d."""
+    from gated_delta_rule_27_gb300 import sublayer
+    stages = ["projections", "short_conv", "recurrence", "output_projection"]
+    out = {}
+    cases = (("prefill", 1, 4096, 16), ("decode", 256, 1, 32))
+    for name, N, T, H in cases:
+        d = 128
+        D = H * d
+        w = sublayer.synthetic_weights(D, H, d, seed=workloads.BASE_SEED + 21, device=dev)
+        gen = torch.Generator(device="cpu").manual_seed(workloads.BASE_SEED + 22)
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        if name == "prefill":
+            x = torch.randn((T, D), generator=gen).to(torch.bfloat16).to(dev)
+            cu = workloads.cu_from_lengths([T], device=dev)
+            run = lambda ev: sublayer.prefill_forward(x, cu, w, H, d, events=ev)
+        else:
+            x = torch.randn((N, D), generator=gen).to(torch.bfloat16).to(dev)
+            S = torch.empty((N, H, d, d), device=dev).normal_(0.0, 0.1)
+            cst = [torch.zeros((N, sublayer.CONV_W - 1, D), device=dev) for _ in range(3)]
+            run = lambda ev: sublayer.decode_forward(x, S, cst, w, H, d, events=ev)
+        per = {k: [] for k in stages}
+        for i in range(warmup + steps):
+            ev = new_events(5)
+            flush.zero_()
+            run(ev)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                for j, k in enumerate(stages):
+                    per[k].append(ev[j].elapsed_time(ev[j + 1]))
+        ms = {k: statistics.median(v) for k, v in per.items()}
+        total = sum(ms.values())
+        out[name] = {"shape": "N=%d T=%d H=%d d=%d hidden=%d bf16, synthetic weights" % (N, T, H, d, D),
+                     "ms": {k: round(v, 5) for k, v in ms.items()}, "total_ms": total,
+                     "recurrence_share": ms["recurrence"] / total,
+                     "note": "projections are cuBLAS GEMMs (q, k, v, decay gate, write gate, output gate) plus "
+                             "torch gate activations; short_conv, recurrence (with the q/k L2 norm and the gated "
+                             "output norm fused) are libkda kernels; L2 flushed before every step"}
+    return out
+
+
 def barrier():
     if torch.distributed.is_available() and torch.distributed.is_initialized():
         torch.distributed.barrier()
@@ -498,6 +542,7 @@ def run_libkda(args):
             steps = min(args.steps, 10 if name == "varlen" else 5)
             others[name] = bench_prefill(libkda, steps, 3, dev, rank, name=name, head_block=rank)
         di = bench_decode_indexed(libkda, 50, 3, dev)
+        sub = bench_sublayer(min(args.steps, 10), 3, dev)
     e2e = bench_e2e(libkda, args.steps, args.warmup, dev, pf["inp"])
 
     T = pf["T"]
@@ -550,6 +595,7 @@ def run_libkda(args):
             "us_per_step_median": di["us"], "steps": di["steps"],
             "roofline": {"bound": "hbm", "achieved": di_gbs, "peak": hbm, "unit": "GB/s", "frac": di_gbs / hbm,
                          "algorithmic_bytes": di["bytes"], "peak_source": pk_src}}
+        line["sublayer"] = sub
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pf["inp"])
         line["decode"]["cpu_baseline"] = cpu_baseline_decode(dc["dec"])

@@ -78,5 +78,50 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def _demangle(name: str) -> str:
+    """The kernel's name and template arguments, without namespaces and parameter types."""
+    try:
+        full = subprocess.run(["c++filt", name], capture_output=True, text=True).stdout.strip() or name
+    except OSError:
+        return name
+    full = full.replace("(anonymous namespace)::", "").split("(")[0]
+    return full.replace("void ", "").split("::")[-1]
+
+
+def resource_report() -> str:
+    """Registers, spills, stack and shared memory of every kernel, as ptxas reports them for sm_103a
+    (`-Xptxas -v`), one Markdown table row per kernel."""
+    import re
+    rows = []
+    for src in _sources():
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-Xptxas", "-v", "-c", src, "-o", os.devnull]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed on %s:\n%s" % (src, r.stderr))
+        name = None
+        for line in r.stderr.splitlines():
+            m = re.search(r"Compiling entry function '([^']+)'", line)
+            if m:
+                name = m.group(1)
+                continue
+            m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m and name:
+                stack, st, ld = m.groups()
+                continue
+            m = re.search(r"Used (\d+) registers", line)
+            if m and name:
+                sm = re.search(r"(\d+) bytes smem", line)
+                rows.append((os.path.basename(src), _demangle(name), m.group(1), stack, st, ld,
+                             sm.group(1) if sm else "0"))
+                name = None
+    out = ["| source | kernel | registers | stack B | spill stores B | spill loads B | static smem B |",
+           "|---|---|---|---|---|---|---|"]
+    out += ["| %s | `%s` | %s | %s | %s | %s | %s |" % r for r in rows]
+    return "\n".join(out)
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--resources" in sys.argv:
+        print(resource_report())
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

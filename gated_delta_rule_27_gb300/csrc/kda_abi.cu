@@ -161,12 +161,14 @@ kda_status kda_prefill_check(const void *workspace, void *stream) {
 }
 
 kda_status kda_testing_set_plan(int32_t plan) {
-    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN && plan != KDA_TESTING_PLAN_PIPE)
+    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN &&
+        plan != KDA_TESTING_PLAN_PIPE && plan != KDA_TESTING_PLAN_PIPE64)
         return KDA_ERR_INVALID_ARG;
-    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE   ? kda::TC_THREE
-                          : plan == KDA_TESTING_PLAN_CHAIN ? kda::TC_CHAIN
-                          : plan == KDA_TESTING_PLAN_PIPE  ? kda::TC_PIPE
-                                                           : -1);
+    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE    ? kda::TC_THREE
+                          : plan == KDA_TESTING_PLAN_CHAIN  ? kda::TC_CHAIN
+                          : plan == KDA_TESTING_PLAN_PIPE   ? kda::TC_PIPE
+                          : plan == KDA_TESTING_PLAN_PIPE64 ? kda::TC_PIPE64
+                                                            : -1);
     return KDA_OK;
 }
 

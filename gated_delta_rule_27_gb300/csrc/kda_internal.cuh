@@ -186,7 +186,7 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 // followed by one cooperative launch running the state chains with the output units alongside (chain); or one
 // cooperative launch of chains beside groups that prepare the records and then form the outputs (pipe).  The
 // last two need the workspace's progress flags zeroed before they start.
-enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3 };
+enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3, TC_PIPE64 = 4 };  // pipe: chains of 32 / 64 columns
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.

@@ -344,7 +344,7 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // columns start at `tmem`; `ph` is the parity of this unit's barrier phases (units
 // a CTA has prepared before, mod 2).  (nslot, nh) is a unit that is likely to
 // follow on this SM (nslot < 0: none): its tiles are pulled into L2.  If
-// `publish` is set, the CTA's previous record is published there (release,
+// `publish` is set, the group's previous record is published there (release,
 // once its bulk stores are complete) as soon as this unit's loads are on
 // their way.  Returns false after recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
@@ -374,7 +374,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         tc::tma_load_3d(sm + PrepSmem::X + 24576, p.tm_q, 64, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V, p.tm_v, 0, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V + 8192, p.tm_v, 64, h, t0, &bars->load);
-        if (publish) {
+        if (publish) {  // the previous record, once its bulk stores are complete (they overlap these loads)
             tc::bulk_wait_all();
             tc::fence_proxy_async_global();
             tc::st_release_gpu(publish, 1);
@@ -1518,11 +1518,28 @@ constexpr int kChainMinWorkers = 48;  // output CTAs alongside the chains, at le
 // and MMAs; a chain waits only for records, all of which belong to preparation units claimed before any
 // output unit; an output unit waits for a record and for the chains.  Every wait is bounded.
 constexpr int kPipeThreads = 512;
-constexpr int kPipeChainMax = 38;  // automatic choice: at most this many chains of 64 columns
-constexpr size_t kPipeSmemBytes = (ChainCfg<64>::bytes > 2 * PrepSmem::bytes ? ChainCfg<64>::bytes
-                                                                               : 2 * PrepSmem::bytes) +
-                                  1024;
+constexpr int kPipeChainMax = 32;   // automatic choice: at most this many chains of 32 columns
+template <int TN>
+constexpr size_t pipe_smem_bytes() {
+    return (ChainCfg<TN>::bytes > 2 * PrepSmem::bytes ? ChainCfg<TN>::bytes : 2 * PrepSmem::bytes) + 1024;
+}
 static_assert(PrepSmem::bytes % 1024 == 0 && OutSmem::bytes <= PrepSmem::bytes, "a group's region holds a unit");
+
+// Work item w of the pipe workers -> (output?, slot, head): the preparations of the first `lag` chunk slots,
+// then alternately one slot's preparations and the outputs of the slot `lag` earlier, then the last outputs.
+__device__ __forceinline__ void pipe_item(int w, int C, int H, int lag, bool *out, int *slot, int *h) {
+    const int D = min(lag, C);
+    const int lead = D * H, mid = (C - D) * 2 * H;
+    if (w < lead) {
+        *out = false; *slot = w / H; *h = w % H;
+    } else if (w < lead + mid) {
+        const int q = w - lead, b = q / (2 * H), r = q % (2 * H);
+        *out = r >= H; *slot = r < H ? D + b : b; *h = r < H ? r : r - H;
+    } else {
+        const int q = w - lead - mid;
+        *out = true; *slot = C - D + q / H; *h = q % H;
+    }
+}
 
 struct PipeArgs {
     const float *S0;
@@ -1531,7 +1548,7 @@ struct PipeArgs {
     int32_t *ready;    // [slot * H + h]: the record is published
     int32_t *sdone;    // [slot * H + h]: columns (in 32s) whose state image is published
     int32_t *counter;  // next work item
-    int n_chain;
+    int n_chain, lag;
     unsigned long long flag_wait_ns;
     int fault;  // kFaultNoPublish only in tests of the timeout path
     OutNorm onorm;
@@ -1546,7 +1563,8 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255, gwarp = gtid >> 5;
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
-    const int units = doc_slot0[pp.num_seqs] * H;  // preparation units, then as many output units
+    const int C = doc_slot0[pp.num_seqs];
+    const int units = C * H;  // preparation units, and as many output units
     if (gtid == 0) {
         prep_bars_init(&pbars[g]);
         tc::mbar_init(&obars[g].load, 1);
@@ -1566,19 +1584,31 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     const uint32_t tmem = tmem_base + 256u * (uint32_t)g;
     uint32_t nprep = 0, nout = 0;
     int32_t *pending = nullptr;  // the last record this group prepared, not yet published
+    // items are claimed one ahead, so that a preparation can pull the next one's input tiles into L2
+    if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);
     for (;;) {
-        if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);
         grp.sync();
         const int u = s_unit[g];
         grp.sync();  // every thread has read s_unit before the next claim overwrites it
         if (u >= 2 * units) break;
-        int doc, t0, Lc;
-        if (u < units) {
-            const int slot = u / H, h = u % H;
+        if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);  // the next item (read after the next barrier)
+        bool is_out;
+        int slot, h, doc, t0, Lc;
+        pipe_item(u, C, H, a.lag, &is_out, &slot, &h);
+        if (!is_out) {
             locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+            int nslot = -1, nh = 0;
+            if (gtid == 0) {  // only thread 0 issues the prefetch; it alone has claimed the next item
+                const int un = s_unit[g];
+                bool n_out;
+                if (un < 2 * units) {
+                    pipe_item(un, C, H, a.lag, &n_out, &nslot, &nh);
+                    if (n_out) nslot = -1;
+                }
+            }
             // the previous record is published once this unit's loads are issued; this one's stays pending
-            const bool ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, -1, 0, pending, grp,
-                                         psh[g]);
+            const bool ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, nslot, nh, pending,
+                                         grp, psh[g]);
             ++nprep;
             if (!ok) break;
             pending = a.ready + (size_t)slot * H + h;
@@ -1589,7 +1619,6 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
                 tc::st_release_gpu(pending, 1);
             }
             pending = nullptr;
-            const int v = u - units, slot = v / H, h = v % H;
             locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
             bool ok = true;
             if (gtid < 128) {
@@ -1613,6 +1642,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     if (tid < 32) tc::tmem_dealloc(tmem_base, 512);
 }
 
+template <int TN>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -1629,7 +1659,7 @@ prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         links.publish = a.fault != kFaultNoPublish;
         links.ready = a.ready;
         links.flag_wait_ns = a.flag_wait_ns;
-        state_chain<64>(cu, num_seqs, H, a.S0, a.S_final, ws, doc_slot0_off, records_off, record_bytes,
+        state_chain<TN>(cu, num_seqs, H, a.S0, a.S_final, ws, doc_slot0_off, records_off, record_bytes,
                         (int)blockIdx.x, sm, links);
         return;
     }
@@ -1783,7 +1813,11 @@ const DeviceSetup &device_setup() {
         if (!e) e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
         if (!e) e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
         if (!e)
-            e = cudaFuncSetAttribute(prefill_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPipeSmemBytes);
+            e = cudaFuncSetAttribute(prefill_pipe_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)pipe_smem_bytes<32>());
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_pipe_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)pipe_smem_bytes<64>());
         if (!e) {
             cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1846,11 +1880,13 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     const DeviceSetup &d = device_setup();
     if (d.err) return TC_THREE;
     const long long chains32 = (long long)num_seqs * H * kNTile, chains64 = chains32 / 2;
-    const bool pipe_fits = chains64 + 2 * kChainMinWorkers / 3 <= d.sms;
+    const bool pipe_fits = chains32 + 2 * kChainMinWorkers / 3 <= d.sms;
+    const bool pipe64_fits = chains64 + 2 * kChainMinWorkers / 3 <= d.sms;
     const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
     if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
+    if (forced == TC_PIPE64) return pipe64_fits ? TC_PIPE64 : TC_THREE;
     if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
-    if (pipe_fits && chains64 <= kPipeChainMax) return TC_PIPE;
+    if (pipe_fits && chains32 <= kPipeChainMax) return TC_PIPE;
     return chain_fits ? TC_CHAIN : TC_THREE;
 }
 
@@ -1868,7 +1904,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const size_t nflag = (size_t)lay.max_slots * H;
     const long long wait = g_test_wait_ns.load();
     const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
-    if (plan == TC_PIPE) {
+    if (plan == TC_PIPE || plan == TC_PIPE64) {
+        const int tn = plan == TC_PIPE ? 32 : 64;
         InputMaps m;
         if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
         PipeArgs a;
@@ -1878,14 +1915,21 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         a.ready = flags;
         a.sdone = flags + nflag;
         a.counter = flags + 2 * nflag;
-        a.n_chain = num_seqs * H * 2;
+        a.n_chain = num_seqs * H * (kD / tn);
+        // outputs trail their preparations by about the chunk slots the worker groups hold at once
+        a.lag = 2 * (dset.sms - a.n_chain) / H + 4;
         a.flag_wait_ns = flag_wait;
         a.fault = g_test_fault.load();
         a.onorm = onorm;
         marks.before(st, "prefill_pipe_tc");
-        e = launch_cooperative(prefill_pipe_tc, dim3((unsigned)dset.sms), dim3(kPipeThreads), kPipeSmemBytes, st, m.q,
-                               m.k, m.v, m.g, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
-                               lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
+        e = tn == 32 ? launch_cooperative(prefill_pipe_tc<32>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
+                                          pipe_smem_bytes<32>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                                          lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm,
+                                          fu.qk_eps, a)
+                     : launch_cooperative(prefill_pipe_tc<64>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
+                                          pipe_smem_bytes<64>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                                          lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm,
+                                          fu.qk_eps, a);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the three
         // kernels instead.

@@ -25,9 +25,10 @@ extern "C" {
 #define KDA_TESTING_PLAN_THREE 0    /* preparation, state pass and output pass as three kernels */
 #define KDA_TESTING_PLAN_CHAIN 2    /* preparation, then one cooperative launch of the state chains with the
                                        output units alongside; falls back to THREE where it cannot run */
-#define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains of 64 columns beside groups that
-                                       prepare the records in chunk order and then form the outputs; falls back
-                                       to THREE where it cannot run */
+#define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains of 32 columns beside groups that
+                                       prepare the records in chunk order and form the outputs behind the
+                                       chains; falls back to THREE where it cannot run */
+#define KDA_TESTING_PLAN_PIPE64 4   /* the same with chains of 64 columns (half as many chains) */
 
 /* Forces a launch plan for later calls.  KDA_ERR_INVALID_ARG for an unknown plan. */
 KDA_API kda_status kda_testing_set_plan(int32_t plan);

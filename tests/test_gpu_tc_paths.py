@@ -25,7 +25,7 @@ def _run(inp, plan, S0=None, poison=0x7F):
     """One call under the given launch plan, on a workspace whose every byte is `poison` beforehand, so that
     nothing a call reads before writing it can pass for a result."""
     libkda.testing_set_plan({"auto": libkda.PLAN_AUTO, "three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN,
-                             "pipe": libkda.PLAN_PIPE}[plan])
+                             "pipe": libkda.PLAN_PIPE, "pipe64": libkda.PLAN_PIPE64}[plan])
     try:
         q, k, v, g, beta, cu = to_device(inp)
         T, H, d = q.shape
@@ -65,19 +65,20 @@ def test_chain_and_three_kernel_plans_agree(case):
     S0 = inp.S0
     o3, S3 = _run(inp, "three", S0, poison=0x00)
     oc, Sc = _run(inp, "chain", S0, poison=0x5A)
-    op, Sp = _run(inp, "pipe", S0, poison=0x7F)
     assert torch.equal(o3, oc), (o3.float() - oc.float()).abs().max().item()
     assert torch.equal(S3, Sc), (S3 - Sc).abs().max().item()
-    assert torch.equal(o3, op), (o3.float() - op.float()).abs().max().item()
-    assert torch.equal(S3, Sp), (S3 - Sp).abs().max().item()
+    for plan in ("pipe", "pipe64"):
+        op, Sp = _run(inp, plan, S0, poison=0x7F)
+        assert torch.equal(o3, op), (plan, (o3.float() - op.float()).abs().max().item())
+        assert torch.equal(S3, Sp), (plan, (S3 - Sp).abs().max().item())
     o_ref, S_ref, _ = oracle_prefill(inp, S0=S0)
     assert rel(oc, o_ref) <= TOL[torch.bfloat16], rel(oc, o_ref)
     assert rel(Sc, S_ref) <= TOL[torch.bfloat16], rel(Sc, S_ref)
 
 
 def test_automatic_plan_on_the_prefill_workload_twice():
-    """The prefill workload (which picks the pipe plan by itself) twice on one workspace: the progress
-    flags start from zero every call, so both calls match bit for bit and the three-kernel plan."""
+    """The prefill workload twice on one workspace with the automatic plan: the progress flags start from zero
+    every call, so both calls match bit for bit and the three-kernel plan."""
     inp = workloads.workload_prefill("prefill")
     q, k, v, g, beta, cu = to_device(inp)
     T, H, d = q.shape
@@ -95,7 +96,7 @@ def test_automatic_plan_on_the_prefill_workload_twice():
     assert torch.equal(o3, outs[0][0]) and torch.equal(S3, outs[0][1])
 
 
-@pytest.mark.parametrize("plan", ["three", "chain", "pipe"])
+@pytest.mark.parametrize("plan", ["three", "chain", "pipe", "pipe64"])
 def test_full_prefill_workload_on_poisoned_workspaces(plan):
     """The prefill workload under each launch plan on a workspace poisoned with two different patterns: the
     kernels overlap at their boundaries (and, in the chain and pipe plans, hand data over through flags), so any
@@ -155,10 +156,10 @@ def test_chain_plan_at_its_worker_threshold(extra_heads):
 
 @pytest.mark.parametrize("extra_heads", [0, 1])
 def test_pipe_plan_at_its_threshold(extra_heads):
-    """One document with 19 heads (38 chains of 64 columns, the most the automatic pipe plan takes) and with 20
+    """One document with 8 heads (32 chains of 32 columns, the most the automatic pipe plan takes) and with 9
     heads (the chain plan then): the automatic choice is the expected plan, matches the three-kernel plan bit
     for bit and meets the bf16 tolerance against the oracle."""
-    H = 19 + extra_heads
+    H = 8 + extra_heads
     inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=97 + extra_heads, s0_std=0.1)
     names = _kernel_names(inp, inp.S0)
     assert ("prefill_pipe_tc" in names) == (extra_heads == 0), names
