@@ -58,6 +58,7 @@ const char *kda_status_string(kda_status status) {
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_BOUNDS: return "KDA_ERR_BOUNDS";
         default: return "KDA_ERR_UNKNOWN";
     }
 }
@@ -173,7 +174,9 @@ kda_status kda_testing_set_plan(int32_t plan) {
 }
 
 kda_status kda_testing_set_fault(int32_t fault, int64_t wait_limit_ns) {
-    if ((fault != KDA_TESTING_FAULT_NONE && fault != KDA_TESTING_FAULT_NO_PUBLISH) || wait_limit_ns < 0)
+    if ((fault != KDA_TESTING_FAULT_NONE && fault != KDA_TESTING_FAULT_NO_PUBLISH &&
+         fault != KDA_TESTING_FAULT_CHUNK_TABLE) ||
+        wait_limit_ns < 0)
         return KDA_ERR_INVALID_ARG;
     kda::testing_set_fault(fault, (long long)wait_limit_ns);
     return KDA_OK;

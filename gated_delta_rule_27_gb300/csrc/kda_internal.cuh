@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "kda.h"
+#include "kda_check.cuh"
 
 namespace kda {
 
@@ -105,7 +106,13 @@ inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int
 inline kda_status status_from_word(int32_t word) {
     if (word == 0) return KDA_OK;
     if (word == (int32_t)KDA_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
+    if (word == (int32_t)KDA_ERR_BOUNDS) return KDA_ERR_BOUNDS;
     return KDA_ERR_INVALID_ARG;
+}
+
+// Chunk slots of a call, bounded by its arguments: the record of (slot, head) exists iff slot < max_slots.
+__device__ __forceinline__ int max_chunk_slots(const int32_t *cu, int num_seqs, int L) {
+    return cu[num_seqs] / L + num_seqs;
 }
 
 // Locates the document and chunk of a chunk slot by binary search over the
@@ -192,6 +199,8 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.
 void testing_set_plan(int plan);
 void testing_set_fault(int fault, long long wait_ns);
+int testing_fault();
+constexpr int kFaultChunkTable = 2;  // test hook of the bounds-checking build (KDA_TESTING_FAULT_CHUNK_TABLE)
 
 cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g, const float *beta,
                                 const int32_t *cu, int num_seqs, int total_tokens, int H, int d, kda_dtype dt,

@@ -39,7 +39,7 @@ constexpr int kThreads = 256;
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_tokens, int L, int32_t *status,
-                   int32_t *doc_slot0, uint4 *clear, int clear_vec) {
+                   int32_t *doc_slot0, uint4 *clear, int clear_vec, int fault) {
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ int s_carry;
@@ -90,6 +90,14 @@ chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_token
     if (tid == 0) {
         doc_slot0[num_seqs] = s_carry;
         *status = 0;
+        status[1] = 0;
+#ifdef KDA_DEBUG_BOUNDS
+        // test hook of the bounds-checking build only: a chunk table that claims more chunks than exist, which
+        // the later kernels' checks must catch (the release build ignores it)
+        if (fault == kFaultChunkTable) doc_slot0[num_seqs] = s_carry + 1000;
+#else
+        (void)fault;
+#endif
     }
 }
 
@@ -126,6 +134,10 @@ prefill_prepare_simt(const Tin *__restrict__ q, const Tin *__restrict__ k, const
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     int doc, t0, Lc;
     if (!locate_slot(doc_slot0, cu, num_seqs, L, slot, &doc, &t0, &Lc)) return;
+    if (!KDA_IN_BOUNDS(slot < max_chunk_slots(cu, num_seqs, L) && t0 >= 0 && Lc >= 1 && Lc <= L &&
+                           t0 + Lc <= cu[num_seqs],
+                       reinterpret_cast<int32_t *>(ws)))
+        return;
     const SimtRecord R = simt_record(L, D, D);
     char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
     float *gW = reinterpret_cast<float *>(rec + R.W), *gUt = reinterpret_cast<float *>(rec + R.Ut);
@@ -274,6 +286,9 @@ prefill_state_simt(const int32_t *__restrict__ cu, int num_seqs, int H, const fl
         sS[i] = S0 ? S0[state_off + (size_t)c * D + col0 + j] : 0.f;
     }
     const int first = doc_slot0[n], last = doc_slot0[n + 1];
+    if (!KDA_IN_BOUNDS(first >= 0 && last >= first && last <= max_chunk_slots(cu, num_seqs, L),
+                       reinterpret_cast<int32_t *>(const_cast<char *>(ws))))
+        return;
     for (int slot = first; slot < last; ++slot) {
         const int t0 = cu[n] + (slot - first) * L;
         const int Lc = min(L, cu[n + 1] - t0);
@@ -307,7 +322,8 @@ prefill_state_simt(const int32_t *__restrict__ cu, int num_seqs, int H, const fl
                 y = fmaf(sQ[r * DP + c], s, y);
             }
             sU[i] = sUt[i] - x;
-            o[((size_t)(t0 + r) * H + h) * D + col0 + j] = from_f32<Tout>(y + sOl[i]);
+            if (KDA_IN_BOUNDS(t0 + r < cu[num_seqs], reinterpret_cast<int32_t *>(const_cast<char *>(ws))))
+                o[((size_t)(t0 + r) * H + h) * D + col0 + j] = from_f32<Tout>(y + sOl[i]);
         }
         __syncthreads();
         for (int i = tid; i < D * TILE; i += kThreads) {
@@ -425,6 +441,7 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens, int L, void *ws, void *clear,
                                size_t clear_bytes, cudaStream_t st, Marks &marks) {
+    const int fault = testing_fault();
     char *w = static_cast<char *>(ws);
     const size_t doc_off = 256;
     const int clear_vec = (int)(clear_bytes / 16);
@@ -433,7 +450,7 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
     marks.before(st, "chunk_index");
     chunk_index_kernel<<<1, threads, 0, st>>>(cu, num_seqs, total_tokens, L, reinterpret_cast<int32_t *>(w),
                                               reinterpret_cast<int32_t *>(w + doc_off), static_cast<uint4 *>(clear),
-                                              clear_vec);
+                                              clear_vec, fault);
     return cudaGetLastError();
 }
 

@@ -361,6 +361,11 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     char *ws = p.ws;
     constexpr TcRecord R = tc_record();
     char *rec = ws + p.records_off + ((size_t)slot * H + h) * p.record_bytes;
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    if (!KDA_IN_BOUNDS(slot >= 0 && slot < max_chunk_slots(p.cu, p.num_seqs, kL) && h >= 0 && h < H && t0 >= 0 &&
+                           Lc >= 1 && Lc <= kL && t0 + Lc <= p.cu[p.num_seqs],
+                       status))
+        return false;  // (uniform: every thread of the group evaluates the same condition)
 
     if (tid == 0) {
         s_abort = 0;
@@ -517,6 +522,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             const int r = orow + 16 * i;
             const bool valid = r < Lc;
             const uint32_t off_k = tc::sw128_offset(r, ocol), off_q = tc::sw128_offset(64 + r, ocol);
+            if (!KDA_IN_BOUNDS(r < kL && off_q + 16 <= 16384u, status)) continue;
             float k8[8], q8[8], xk[8], xq[8], ke[8];
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
             unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
@@ -609,7 +615,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
 #pragma unroll
                 for (int qb = 0; qb < 2; ++qb) {
                     const int q4 = 2 * hs + qb;
-                    if (q4 <= (r >> 4)) {
+                    if (q4 <= (r >> 4) && KDA_IN_BOUNDS(tri_blk(r >> 4, q4) + 256 <= 2560, status)) {
                         float *dst = Af + tri_blk(r >> 4, q4) + ((r & 15) << 4);
 #pragma unroll
                         for (int i = 0; i < 16; i += 4) {
@@ -1010,6 +1016,10 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
     const int n = j / (NT * H);
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
+    if (!KDA_IN_BOUNDS(n < num_seqs && first >= 0 && nchunks >= 0 &&
+                           first + nchunks <= max_chunk_slots(cu, num_seqs, kL),
+                       reinterpret_cast<int32_t *>(ws)))
+        return;  // (uniform over the CTA)
     const int col0 = tile * TN + NC * hcol;
     const size_t state_off = ((size_t)n * H + h) * kD * kD + (size_t)i * kD + col0;
     constexpr TcRecord R = tc_record();
@@ -1270,7 +1280,7 @@ struct OutGroup {
 // previous kernel), or through its publication count at `sflag` (all column
 // tiles), else it must already be complete.  Returns false after recording a
 // timeout in the status word.
-__device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16 *__restrict__ o, char *ws,
+__device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
                             OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, const OutNorm &onorm,
                             bool dep_wait = false, const int32_t *sflag = nullptr,
@@ -1281,6 +1291,13 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
                       R.S - R.Qp == OutSmem::S,
                   "output pass loads the record tail as one image");
     const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
+#ifdef KDA_DEBUG_BOUNDS
+    const int total_tokens = cu[num_seqs];
+#endif
+    if (!KDA_IN_BOUNDS(slot >= 0 && slot < max_chunk_slots(cu, num_seqs, kL) && h >= 0 && h < H && t0 >= 0 &&
+                           Lc >= 1 && Lc <= kL && t0 + Lc <= total_tokens,
+                       reinterpret_cast<int32_t *>(ws)))
+        return false;  // (uniform over the group)
     if (tid == 0) {
         // Qp, P, Ut (written by the preparation; in the pipe plan, once published) ...
         bool rok = true;
@@ -1330,6 +1347,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
             const size_t row = ((size_t)(t0 + r) * H + h) * kD;
             uint4 *dst = reinterpret_cast<uint4 *>(o + row);
+            const bool row_ok = KDA_IN_BOUNDS(r >= Lc || t0 + r < total_tokens, reinterpret_cast<int32_t *>(ws));
             float scale = 1.f;
             if (onorm.gate) {  // fused epilogue, pass 1: the row's mean square
                 float ss = 0.f;
@@ -1346,7 +1364,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int H, __nv_bfloat16
             for (int q = 0; q < 4; ++q) {
                 float v[32];
                 tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
-                if (r < Lc) {
+                if (r < Lc && row_ok) {
                     if (onorm.gate) {  // pass 2: o / rms(o) * w * sigmoid(z)
                         const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row) + q * 4;
 #pragma unroll
@@ -1410,7 +1428,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     __syncthreads();
     tc::tc_fence_after();
     __shared__ int s_ok;
-    output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base,
+    output_unit(cu, num_seqs, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, sm, &bars, 0u, tmem_base,
                 OutGroup{tid, 0u, &s_ok}, onorm, true);
     if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
 }
@@ -1491,7 +1509,7 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
             const int slot = u / H, h = u % H;
             int doc, t0, Lc;
             locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
-            if (!output_unit(cu, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
+            if (!output_unit(cu, num_seqs, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
                              grp, onorm, false, sdone + u, flag_wait_ns))
                 break;
         }
@@ -1622,7 +1640,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
             locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
             bool ok = true;
             if (gtid < 128) {
-                ok = output_unit(pp.cu, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
+                ok = output_unit(pp.cu, pp.num_seqs, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
                                  &obars[g], nout & 1u, tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, a.onorm,
                                  false, a.sdone + (size_t)slot * H + h, a.flag_wait_ns,
                                  a.ready + (size_t)slot * H + h);
@@ -1868,6 +1886,7 @@ void testing_set_fault(int fault, long long wait_ns) {
     g_test_fault.store(fault);
     g_test_wait_ns.store(wait_ns);
 }
+int testing_fault() { return g_test_fault.load(); }
 
 TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     // Few chains: the pipe plan (at most kPipeChainMax chains of 64 columns); then the chain plan while the

@@ -14,7 +14,7 @@ import torch
 
 from . import build as _build
 
-KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_BOUNDS = range(6)
 KDA_F32, KDA_BF16 = 0, 1
 
 SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunked", "kda_prefill_chunked_profiled",
@@ -24,7 +24,7 @@ SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunk
 # include/kda_testing.h (test hooks)
 TESTING_SYMBOLS = ("kda_testing_set_plan", "kda_testing_set_fault")
 PLAN_AUTO, PLAN_THREE, PLAN_CHAIN, PLAN_PIPE, PLAN_PIPE64 = -1, 0, 2, 3, 4
-FAULT_NONE, FAULT_NO_PUBLISH = 0, 1
+FAULT_NONE, FAULT_NO_PUBLISH, FAULT_CHUNK_TABLE = 0, 1, 2
 PREFILL_MAX_KERNELS = 4
 
 _lib = None
@@ -55,7 +55,18 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         _build.build()
     if not os.path.exists(_build.LIB):
         raise RuntimeError("libkda.so is not built (%s); run gated_delta_rule_27_gb300.build" % _build.LIB)
-    lib = ctypes.CDLL(_build.LIB)
+    _lib = _declare(ctypes.CDLL(_build.LIB))
+    return _lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """Loads the bounds-checking build, libkda_debug.so (built on first use): the same C ABI, for tests."""
+    _build.build(debug=True)
+    return _declare(ctypes.CDLL(_build.DEBUG_LIB))
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Sets the argument and result types of libkda's entry points on a loaded library."""
     vp, i32, fp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -94,7 +105,6 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.kda_testing_set_plan.argtypes = [i32]
     lib.kda_testing_set_fault.restype = ctypes.c_int
     lib.kda_testing_set_fault.argtypes = [i32, ctypes.c_int64]
-    _lib = lib
     return lib
 
 

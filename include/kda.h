@@ -54,7 +54,8 @@ typedef enum {
     KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, bad cu_seqlens, small workspace */
     KDA_ERR_UNSUPPORTED = 2, /* a size or dtype outside the supported set */
     KDA_ERR_CUDA = 3,        /* a CUDA launch or driver call failed */
-    KDA_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by kda_prefill_check) */
+    KDA_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (reported by kda_prefill_check) */
+    KDA_ERR_BOUNDS = 5       /* debug build only: a checked index was out of bounds (kda_prefill_check) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -131,6 +132,10 @@ KDA_API kda_status kda_prefill_chunked_profiled(const void *q, const void *k, co
  *                        arrived within its time bound of one to two
  *                        seconds): o and S_final may be partly written.  The
  *                        context stays usable and the next call starts afresh;
+ *   KDA_ERR_BOUNDS       (the debug build, libkda_debug.so, only) a checked
+ *                        index was out of bounds; the access was skipped and
+ *                        the source line of the first failing check is the
+ *                        workspace's second int32 word;
  *   KDA_ERR_CUDA         the copy or the synchronisation failed.
  */
 KDA_API kda_status kda_prefill_check(const void *workspace, void *stream);

@@ -37,6 +37,9 @@ KDA_API kda_status kda_testing_set_plan(int32_t plan);
 #define KDA_TESTING_FAULT_NONE 0        /* the default */
 #define KDA_TESTING_FAULT_NO_PUBLISH 1  /* chain and pipe plans: the state chains publish none of their state
                                            images, so the output units' bounded waits on them run out */
+#define KDA_TESTING_FAULT_CHUNK_TABLE 2 /* bounds-checking build (libkda_debug.so) only: the chunk table claims
+                                           1000 chunks more than exist, which the kernels' bounds checks must
+                                           catch (KDA_ERR_BOUNDS); the release build ignores this fault */
 
 /*
  * Injects `fault` into later calls and bounds the device-side waits on
