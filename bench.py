@@ -162,6 +162,8 @@ KERNEL_SOURCES = {
     "prefill_state_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_output_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_chain_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_pipe_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "out_gated_norm": "gated_delta_rule_27_gb300/csrc/kda_prefill_simt.cu",
     "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
 }
 

@@ -588,15 +588,17 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             *reinterpret_cast<uint4 *>(Pb + tc::sw128_offset(r, s0 + j8)) = pack8(w);
         }
     } else {
-        // round 1: [beta k e1 ; q e1] x (k / e1)^T (rows 0-63 A, 64-127 P), the two K panels
-        // issued by warps 0 and 1 into TMEM cols 0..63 and 128..191
+        // round 1: [beta k e1 ; q e1] x (k / e1)^T (rows 0-63 A, 64-127 P) into TMEM cols 0..63, both K panels
+        // accumulated by one issuer (lane 0 of warp 0; warp 1 only commits, the barrier counting two commits)
         if (lane == 0 && warp < 2) {
-            constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, false, false);
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t ka = (uint32_t)warp * 16384u + (uint32_t)s * 32u;
-                const uint32_t kb = (uint32_t)warp * 8192u + (uint32_t)s * 32u;
-                tc::mma_bf16(tmem + 128u * (uint32_t)warp, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::X + ka)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + kb)), id, s > 0);
+            if (warp == 0) {
+                constexpr uint32_t id = tc::idesc_bf16_f32(128, 64, false, false);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t ka = (uint32_t)(s >> 2) * 16384u + (uint32_t)(s & 3) * 32u;
+                    const uint32_t kb = (uint32_t)(s >> 2) * 8192u + (uint32_t)(s & 3) * 32u;
+                    tc::mma_bf16(tmem, tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::X + ka)),
+                                 tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Y + kb)), id, s > 0);
+                }
             }
             tc::mma_commit(&bars->r1);
         }
@@ -604,11 +606,8 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         ok = tc::mbar_wait(&bars->r1, ph);
         tc::tc_fence_after();
         if (warp_all(ok)) {  // the MMAs are complete: their operand Y may be overwritten by P
-            float v[32], v2[32];
+            float v[32];
             tc::tmem_ld32(tmem + lane_base + 32u * (uint32_t)hs, v);
-            tc::tmem_ld32(tmem + lane_base + 128u + 32u * (uint32_t)hs, v2);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += v2[i];
             if (trow < 64) {
                 const int r = trow;
                 const float br = s_beta[r];  // A = diag(beta) (k e1)(k / e1)^T, strictly lower
@@ -823,7 +822,10 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     __syncwarp();
     ok = tc::mbar_wait(&bars->r4, ph);
     tc::tc_fence_after();
-    if (tid == 0) tc::bulk_wait_read();  // round 3's images have left X: it can stage Bc
+    // Bc is staged in V (tiles 0, 1; round 4 has consumed Ut^T) and Y (tiles 2, 3: P and the identity are done
+    // with), whose copies out (P, Ut^T) are older than round 3's and have long been read: no wait for round 3's
+    // images, which are still leaving X and W'^T
+    if (tid == 0) tc::bulk_wait_read_all_but_one();
     grp.sync();
     if (warp_all(ok)) {
         const int c = trow;
@@ -833,7 +835,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             const int t = 2 * hs + tt;
             float bv[32];
             tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(t * 32), bv);
-            uint8_t *BcS = sm + PrepSmem::X + t * 8192 + c * 64;
+            uint8_t *BcS = sm + (hs ? PrepSmem::Y : PrepSmem::V) + tt * 8192 + c * 64;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 *reinterpret_cast<uint4 *>(BcS + ((k ^ ((c >> 1) & 3)) << 4)) = pack8_at(bv + 8 * k);
@@ -846,7 +848,8 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     const bool done = !s_abort;
     if (tid == 0) {
         if (done) {
-            tc::bulk_s2g(rec + R.Bc, sm + PrepSmem::X, 32768);
+            tc::bulk_s2g(rec + R.Bc, sm + PrepSmem::V, 16384);
+            tc::bulk_s2g(rec + R.Bc + 16384, sm + PrepSmem::Y, 16384);
             tc::bulk_commit();
         } else {
             flag_timeout(ws);
@@ -989,6 +992,9 @@ struct ChainLinks {
     bool publish = true;             // false only in tests of the timeout path
     const int32_t *ready = nullptr;  // wait for each record's publication flag there before loading it
     uint64_t flag_wait_ns = kFlagWaitNs;
+    // Records are streamed in by the loader warp (required with `ready`), else by the second MMA issuer right
+    // behind its MMAs; which is faster depends on what else the launch runs (measured per plan).
+    bool loader = true;
 };
 
 // Chain j by a CTA of at least kStateThreads threads over `smem_raw` (ChainCfg<TN>); threads beyond
@@ -1050,6 +1056,12 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             tc::fence_mbar_init();
             s_abort = 0;
             tc::grid_dep_wait();  // the preparation has completed, or (pipe plan) its records are awaited by flag
+            if (!links.loader) {  // records already complete: the first kNBuf - 1 stream in at once
+                char *rec0 = ws + records_off + (size_t)h * record_bytes;
+                for (int c = 0; c < NB - 1 && c < nchunks; ++c)
+                    issue_record<TN>(sm + c * Cfg::kBuf, rec0 + (size_t)(first + c) * H * record_bytes, tile,
+                                     &full_bar[c]);
+            }
         }
         if (warp == 0) {
             tc::tmem_alloc(&tmem_base, 2 * TN);
@@ -1065,7 +1077,9 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         const uint32_t tmem = tmem_base;
 
         if (warp == kStateLoadWarp) {
-            if (lane == 0) {
+            // (with records that are complete before the launch, the second issuer streams them in instead,
+            // right behind its MMAs, which costs less per chunk than a hand-off to this warp)
+            if (lane == 0 && links.loader) {
                 int issued = 0;
                 for (int c = 0; c < nchunks; ++c) {
                     const int b = c % NB;
@@ -1104,6 +1118,13 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                                          idN, s > 0);
                     }
                     tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
+                    if (!links.loader && panel == 1 && ok) {
+                        // the buffer chunk c - 1 used was released by the operand barrier of this chunk
+                        const int cn = c + NB - 1;
+                        if (cn < nchunks)
+                            issue_record<TN>(sm + (cn % NB) * Cfg::kBuf, rec_h + (size_t)(first + cn) * rec_stride,
+                                             tile, &full_bar[cn % NB]);
+                    }
                 }
                 __syncwarp();
             }
@@ -1205,7 +1226,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 tc::fence_async_smem();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&empty_bar[bsel]);  // the MMAs and this warp are done with it
+                if (lane == 0 && links.loader) tc::mbar_arrive(&empty_bar[bsel]);  // the MMAs and this warp are done
                 if (img) {
                     tc::named_barrier_arrive(kBarOperand, kBarOperandThreads);
                     if (lane == 0) tc::mbar_arrive(&img_full[nb % NS]);
@@ -1214,7 +1235,17 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         }
         if (!ok) s_abort = 1;
         __syncthreads();
-        if (s_abort && tid == 0) flag_timeout(ws);
+        if (s_abort && tid == 0) {
+            flag_timeout(ws);
+            if (!links.loader) {
+                // record copies the issuer may still have on their way land before shared memory goes away
+                // (best effort, 10 ms per buffer: the last chunk that could use each one)
+                for (int b = 0; b < NB && b < nchunks; ++b) {
+                    const int last = b + ((nchunks - 1 - b) / NB) * NB;
+                    tc::mbar_wait(&full_bar[b], (uint32_t)((last / NB) & 1), 10000000ull);
+                }
+            }
+        }
         if (warp == 0) tc::tmem_dealloc(tmem, 2 * TN);
         if (s_abort) return;
     }
@@ -1455,6 +1486,7 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
         ChainLinks links;
         links.sdone = sdone;
         links.publish = fault != kFaultNoPublish;
+        links.loader = false;
         state_chain<kTile>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes,
                            (int)blockIdx.x, smem_raw, links);
         return;
