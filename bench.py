@@ -395,12 +395,14 @@ def bench_sublayer(steps, warmup, dev):
         if name == "prefill":
             x = torch.randn((T, D), generator=gen).to(torch.bfloat16).to(dev)
             cu = workloads.cu_from_lengths([T], device=dev)
-            run = lambda ev: sublayer.prefill_forward(x, cu, w, H, d, events=ev)
+            bufs = sublayer.Buffers(T, N, H, d, dev)
+            run = lambda ev: sublayer.prefill_forward(x, cu, w, H, d, events=ev, bufs=bufs)
         else:
             x = torch.randn((N, D), generator=gen).to(torch.bfloat16).to(dev)
             S = torch.empty((N, H, d, d), device=dev).normal_(0.0, 0.1)
             cst = [torch.zeros((N, sublayer.CONV_W - 1, D), device=dev) for _ in range(3)]
-            run = lambda ev: sublayer.decode_forward(x, S, cst, w, H, d, events=ev)
+            bufs = sublayer.Buffers(N, N, H, d, dev)
+            run = lambda ev: sublayer.decode_forward(x, S, cst, w, H, d, events=ev, bufs=bufs)
         per = {k: [] for k in stages}
         for i in range(warmup + steps):
             ev = new_events(5)
@@ -417,7 +419,8 @@ def bench_sublayer(steps, warmup, dev):
                      "recurrence_share": ms["recurrence"] / total,
                      "note": "projections are cuBLAS GEMMs (q, k, v, decay gate, write gate, output gate) plus "
                              "torch gate activations; short_conv, recurrence (with the q/k L2 norm and the gated "
-                             "output norm fused) are libkda kernels; L2 flushed before every step"}
+                             "output norm fused) are libkda kernels; buffers allocated once; L2 flushed before "
+                             "every step; stage times are event intervals, so they include any wait for the host"}
     return out
 
 

@@ -162,14 +162,12 @@ kda_status kda_prefill_check(const void *workspace, void *stream) {
 }
 
 kda_status kda_testing_set_plan(int32_t plan) {
-    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN &&
-        plan != KDA_TESTING_PLAN_PIPE && plan != KDA_TESTING_PLAN_PIPE64)
+    if (plan != -1 && plan != KDA_TESTING_PLAN_THREE && plan != KDA_TESTING_PLAN_CHAIN && plan != KDA_TESTING_PLAN_PIPE)
         return KDA_ERR_INVALID_ARG;
-    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE    ? kda::TC_THREE
-                          : plan == KDA_TESTING_PLAN_CHAIN  ? kda::TC_CHAIN
-                          : plan == KDA_TESTING_PLAN_PIPE   ? kda::TC_PIPE
-                          : plan == KDA_TESTING_PLAN_PIPE64 ? kda::TC_PIPE64
-                                                            : -1);
+    kda::testing_set_plan(plan == KDA_TESTING_PLAN_THREE   ? kda::TC_THREE
+                          : plan == KDA_TESTING_PLAN_CHAIN ? kda::TC_CHAIN
+                          : plan == KDA_TESTING_PLAN_PIPE  ? kda::TC_PIPE
+                                                           : -1);
     return KDA_OK;
 }
 

@@ -16,15 +16,17 @@
 // Both kernels are bound by HBM: every input is read once (plus a halo of
 // W - 1 rows per tile, served by L1/L2) and every output written once.  One
 // thread owns one channel over a tile of tokens, so a warp's loads and stores
-// are 32 consecutive channels of one token row (coalesced), and each input
-// row is loaded once per tile and kept in a register window.
+// are 32 consecutive channels of one token row (coalesced).  The tile's
+// inputs are all loaded before any arithmetic (into the thread's own column
+// of a shared-memory tile), so that every thread has its whole tile of loads
+// in flight at once; the arithmetic then walks a register window.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kConvTile = 64;  // tokens per thread
+constexpr int kConvTile = 32;  // tokens per thread
 constexpr int kMaxW = 8;
 
 // The document of token t: the last n with cu[n] <= t (documents may be empty).
@@ -42,10 +44,14 @@ __global__ void __launch_bounds__(kConvThreads)
 conv_prefill_kernel(const T *__restrict__ x, const float *__restrict__ w, const int32_t *__restrict__ cu,
                     int num_seqs, int total_tokens, int C, int W, const float *__restrict__ state_in, T *__restrict__ y,
                     float *__restrict__ state_out) {
+    __shared__ float xs[kConvTile][kConvThreads];  // column threadIdx.x: this thread's inputs
     const int c = blockIdx.x * kConvThreads + threadIdx.x;
     const int t_begin = blockIdx.y * kConvTile;
     if (c >= C || t_begin >= total_tokens) return;
     const int t_end = min(t_begin + kConvTile, total_tokens);
+#pragma unroll
+    for (int j = 0; j < kConvTile; ++j)
+        if (t_begin + j < t_end) xs[j][threadIdx.x] = to_f32(x[(size_t)(t_begin + j) * C + c]);
     float wc[kMaxW];
 #pragma unroll
     for (int j = 0; j < kMaxW; ++j) wc[j] = j < W ? w[(size_t)c * W + j] : 0.f;
@@ -73,7 +79,7 @@ conv_prefill_kernel(const T *__restrict__ x, const float *__restrict__ w, const 
 #pragma unroll
             for (int i = 1; i < kMaxW; ++i) win[i] = (i < W) ? input_at(t - i) : 0.f;
         }
-        win[0] = to_f32(x[(size_t)t * C + c]);
+        win[0] = xs[t - t_begin][threadIdx.x];
         float acc = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxW; ++j) acc = fmaf(wc[j], win[j], acc);
@@ -111,12 +117,23 @@ conv_decode_kernel(const T *__restrict__ x, const float *__restrict__ w, int N, 
     const int n = (int)(i / C), c = (int)(i % C);
     float *st = state + (size_t)n * (W - 1) * C + c;
     const float xin = to_f32(x[i]);
+    // win[s]: state slot s (oldest first), the input W - 1 - s tokens back, weighted by w[c][W - 1 - s];
+    // every load is issued before any arithmetic
+    float win[kMaxW], wr[kMaxW];
+#pragma unroll
+    for (int s = 0; s < kMaxW; ++s) {
+        win[s] = s < W - 1 ? st[(size_t)s * C] : 0.f;
+        wr[s] = s < W - 1 ? w[(size_t)c * W + (W - 1 - s)] : 0.f;
+    }
     float acc = w[(size_t)c * W] * xin;
-    for (int j = 1; j < W; ++j) acc = fmaf(w[(size_t)c * W + j], st[(size_t)(W - 1 - j) * C], acc);
+#pragma unroll
+    for (int s = kMaxW - 1; s >= 0; --s)  // the newest state slot first: the same order as the prefill kernel
+        if (s < W - 1) acc = fmaf(wr[s], win[s], acc);
     y[i] = from_f32<T>(acc);
     // roll: drop the oldest input, append this one
-    for (int s = 0; s + 1 < W - 1; ++s) st[(size_t)s * C] = st[(size_t)(s + 1) * C];
-    if (W > 1) st[(size_t)(W - 2) * C] = xin;
+#pragma unroll
+    for (int s = 0; s < kMaxW - 1; ++s)
+        if (s < W - 1) st[(size_t)s * C] = s + 1 < W - 1 ? win[s + 1] : xin;
 }
 
 template <typename T>

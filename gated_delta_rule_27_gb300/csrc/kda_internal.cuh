@@ -68,25 +68,25 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
 }
 
 // Tensor-core record (d = 128, L = 64).  Every operand is stored as the exact
-// shared-memory image its consumer loads (bf16, 128-byte swizzled unless
-// noted), so each consumer moves its part of a record with one or two bulk
-// copies.  The state pass reads [Mc, Bc) plus its own column tile of Bc and
-// writes S; the output pass reads [Qp, bytes) in one piece.
+// shared-memory image its consumer loads (bf16, 128-byte swizzled), so each
+// consumer moves its part of a record with one or two bulk copies.  The state
+// pass reads [Mc, Qp) plus its column tile of Ut and writes S; the output
+// pass reads [Qp, bytes) in one piece.
 //   Mc     M' = -Kend^T W, K-major [128 d_k rows][128 d_k], 2 panels          32 KB
 //   gamma  fp32 [128], padded to 1 KB
-//   Bc     Kend^T Ut, per 32-column tile t: bf16 [128 d_k][32 d_v], 64-byte rows
-//          whose 16-byte chunks are XOR-swizzled by ((row / 2) mod 4)    4 x 8 KB
+//   Kend   the chunk's keys decayed to its end, MN-major [64 tokens][128 d_k],
+//          2 panels of 8 KB (the state pass forms Kend^T Ut from it)          16 KB
 //   Qp     MN-major [128 d_k][64 tokens]                                       16 KB
 //   P      intra-chunk scores, K-major [64 tokens][64 tokens]                   8 KB
 //   Ut     Ut^T, K-major [128 d_v][64 tokens]                                  16 KB
 //   S      the chunk's incoming state as the state pass multiplied it: bf16
 //          K-major [128 d_v rows][128 d_k], 2 panels of 16 KB (written by the
-//          state pass, tile t filling rows 32t .. 32t + 31 of both panels)     32 KB
+//          state pass, each chain filling its rows of both panels)             32 KB
 struct TcRecord {
-    size_t Mc, gamma, Bc, Qp, P, Ut, S, state_part, out_part, bytes;
+    size_t Mc, gamma, Kend, Qp, P, Ut, S, state_part, out_part, bytes;
 };
 __host__ __device__ constexpr TcRecord tc_record() {
-    return TcRecord{0, 32768, 33792, 66560, 82944, 91136, 107520, 33792, 140288 - 66560, 140288};
+    return TcRecord{0, 32768, 33792, 50176, 66560, 74752, 91136, 50176, 123904 - 50176, 123904};
 }
 
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {
@@ -193,7 +193,7 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 // followed by one cooperative launch running the state chains with the output units alongside (chain); or one
 // cooperative launch of chains beside groups that prepare the records and then form the outputs (pipe).  The
 // last two need the workspace's progress flags zeroed before they start.
-enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3, TC_PIPE64 = 4 };  // pipe: chains of 32 / 64 columns
+enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3 };
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.

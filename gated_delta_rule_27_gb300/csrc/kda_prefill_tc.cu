@@ -8,31 +8,35 @@
 //     A[r,s] = beta_r sum_c k_rc k_sc exp(b_rc - b_sc)  (s < r)
 //     P[r,s] = sum_c q_rc k_sc exp(b_rc - b_sc)         (s <= r)
 //     T = (I + A)^{-1},  W' = T X_k,  Ut = T (beta V)
-//     Qp = (X_q - P W') exp(b_m),  M' = -Kend^T W' exp(b_m),  Bc = Kend^T Ut,  gamma = exp(b_last)
+//     Qp = (X_q - P W') exp(b_m),  M' = -Kend^T W' exp(b_m),  gamma = exp(b_last)
 // and per document, chunk after chunk, with S_c the state entering chunk c:
-//     S_{c+1} = gamma S_c + M' S_c + Bc,      O_c = Qp S_c + P Ut.
+//     S_{c+1} = gamma S_c + M' S_c + Kend^T Ut,      O_c = Qp S_c + P Ut.
 //
-// Kernel 1, prefill_prepare_tc: one CTA (256 threads, two per SM) per (chunk,
-// head).  q, k, v, g tiles arrive by TMA.  The dense contractions run as four
-// rounds of tcgen05.mma with fp32 accumulators in TMEM (A and P; W' and Ut; Qp
-// and M'; Bc); the gates, their cumulative
-// sums and the triangular solve stay fp32 on the CUDA cores, and nothing
-// d_k x d_k is formed from a single token.  b_m is the chunk's middle token,
-// so every factor is bounded by exp(+-80) while the chunk's log-decay range on
-// each side of m stays within 80; a chunk outside that range takes exact
-// pairwise exponentials for A and P and reference 0 instead.  Every result is
-// written to the chunk's workspace record as a ready shared-memory image.
+// Preparation, prefill_prepare_tc: one unit per (chunk, head), 256 threads
+// (two units per SM).  q, k, v, g tiles arrive by TMA.  The dense contractions
+// run as three rounds of tcgen05.mma with fp32 accumulators in TMEM (A and P;
+// W' and Ut; Qp and M'); the gates, their cumulative sums and the triangular
+// solve stay fp32 on the CUDA cores, and nothing d_k x d_k is formed from a
+// single token.  b_m is the chunk's middle token, so every factor is bounded
+// by exp(+-80) while the chunk's log-decay range on each side of m stays
+// within 80; a chunk outside that range takes exact pairwise exponentials for
+// A and P and reference 0 instead.  Every result is written to the chunk's
+// workspace record as a ready shared-memory image.
 //
-// Kernel 2, prefill_state_tc: one CTA per (document, head, 32-column tile of
-// S), sequential over the document's chunks: one MMA group M' S per chunk,
-// S kept fp32 in registers, its bf16 image in shared memory feeding the next
-// MMA and copied to the chunk's record.
+// State pass: one CTA per (document, head, 32- or 64-column tile of S),
+// sequential over the document's chunks: per chunk one MMA group M' S on top
+// of Kend^T Ut (issued one chunk ahead, off the chain's critical path), S kept
+// fp32 in registers, its bf16 image in shared memory feeding the next MMA and
+// copied to the chunk's record.
 //
-// Kernel 3, prefill_output_tc: one CTA per (chunk, head), O = Qp S_c + P Ut
-// from the record, written as bf16.
+// Output: per (chunk, head), O = Qp S_c + P Ut from the record, written as
+// bf16 (optionally through the fused gated RMS normalisation).
 //
-// Every mbarrier wait is bounded: on expiry the kernel records
-// KDA_ERR_TIMEOUT in the workspace status word and stops.
+// Launch plans (host side, below): three kernels; the preparation then one
+// cooperative launch of chains beside output groups (chain); or one
+// cooperative launch of chains beside groups that prepare and then form
+// outputs (pipe).  Every mbarrier and flag wait is bounded: on expiry the
+// kernel records KDA_ERR_TIMEOUT in the workspace status word and stops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -327,9 +331,9 @@ struct PrepParams {
     float qk_eps;
 };
 // mbarriers of one preparation, each completing exactly once per unit: the gate tile, the k, q, v
-// tiles, and the four MMA rounds
+// tiles, and the three MMA rounds
 struct PrepBars {
-    uint64_t g, load, r1, r2, r3, r4;
+    uint64_t g, load, r1, r2, r3;
 };
 __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
     tc::mbar_init(&b->g, 1);
@@ -337,7 +341,6 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
     tc::mbar_init(&b->r1, 2);  // rounds 1-3 are issued by two warps, one commit each
     tc::mbar_init(&b->r2, 2);
     tc::mbar_init(&b->r3, 2);
-    tc::mbar_init(&b->r4, 1);
 }
 
 // One (chunk slot, head) of the preparation by a CTA of 256 threads whose 256 TMEM
@@ -806,57 +809,12 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     }
     if (tid == 0) {
         tc::bulk_s2g(rec + R.Mc, sm + PrepSmem::X, 32768);
+        tc::bulk_s2g(rec + R.Kend, sm + PrepSmem::KendS, 16384);  // round 3 has consumed it
         tc::bulk_s2g(rec + R.Qp, sm + PrepSmem::WT, 16384);
         tc::bulk_commit();
     }
-
-    // round 4:  Bc = Kend^T Ut -> cols 128..255
-    if (tid == 32) {
-        constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
-        constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
-        for (int s = 0; s < 4; ++s)
-            tc::mma_bf16(tmem + 128, tc::smem_desc(kKmn, tc::smem_u32(sm + PrepSmem::KendS + s * 2048)),
-                         tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::V + s * 32)), id128, s > 0);
-        tc::mma_commit(&bars->r4);
-    }
-    __syncwarp();
-    ok = tc::mbar_wait(&bars->r4, ph);
-    tc::tc_fence_after();
-    // Bc is staged in V (tiles 0, 1; round 4 has consumed Ut^T) and Y (tiles 2, 3: P and the identity are done
-    // with), whose copies out (P, Ut^T) are older than round 3's and have long been read: no wait for round 3's
-    // images, which are still leaving X and W'^T
-    if (tid == 0) tc::bulk_wait_read_all_but_one();
-    grp.sync();
-    if (warp_all(ok)) {
-        const int c = trow;
-#pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-            // Bc row c, columns of tile t: four 16-byte chunks, chunk k stored at k ^ ((c >> 1) & 3)
-            const int t = 2 * hs + tt;
-            float bv[32];
-            tc::tmem_ld32(tmem + lane_base + 128u + (uint32_t)(t * 32), bv);
-            uint8_t *BcS = sm + (hs ? PrepSmem::Y : PrepSmem::V) + tt * 8192 + c * 64;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(BcS + ((k ^ ((c >> 1) & 3)) << 4)) = pack8_at(bv + 8 * k);
-        }
-    }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    if (!ok) s_abort = 1;
-    grp.sync();
-    const bool done = !s_abort;
-    if (tid == 0) {
-        if (done) {
-            tc::bulk_s2g(rec + R.Bc, sm + PrepSmem::V, 16384);
-            tc::bulk_s2g(rec + R.Bc + 16384, sm + PrepSmem::Y, 16384);
-            tc::bulk_commit();
-        } else {
-            flag_timeout(ws);
-        }
-        tc::bulk_wait_read();  // shared memory must outlive the copies' reads
-    }
-    return done;
+    if (tid == 0) tc::bulk_wait_read();  // shared memory must outlive the copies' reads
+    return true;
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
@@ -923,11 +881,11 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 template <int TN>
 struct ChainCfg {
     static_assert(TN == 32 || TN == 64, "column tile of a chain");
-    static constexpr int kNBuf = TN == 32 ? 4 : 3;             // records in flight
+    static constexpr int kNBuf = 3;                            // records in flight
     static constexpr int kNSb = TN == 32 ? 5 : 3;              // images: multiplied, being written, awaiting copy
-    static constexpr uint32_t kBc = (uint32_t)TN * kD * 2;     // the chain's Bc tiles: 8 / 16 KB
-    static constexpr uint32_t Mc = 0, gam = 32768, Bc = 33792;
-    static constexpr uint32_t kBuf = Bc + kBc;                 // a multiple of 1 KB (operand alignment)
+    static constexpr uint32_t Mc = 0, gam = 32768, Kend = 33792, Ut = 50176;
+    static constexpr uint32_t kUt = (uint32_t)TN * 128;        // the chain's rows of Ut^T: 4 / 8 KB
+    static constexpr uint32_t kBuf = Ut + kUt;                 // a multiple of 1 KB (operand alignment)
     static constexpr uint32_t kPanel = (uint32_t)TN * 128;     // one 64-wide K panel of the image
     static constexpr uint32_t kImg = 2 * kPanel;
     static constexpr uint32_t SB = kNBuf * kBuf;
@@ -936,13 +894,14 @@ struct ChainCfg {
     static_assert(kBuf % 1024 == 0 && kImg % 1024 == 0, "1 KB aligned operands");
 };
 
+// A chunk's record into a chain's buffer: M', gamma and Kend in one copy, the chain's rows of Ut^T in another.
 template <int TN>
 __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int tile, uint64_t *bar) {
     constexpr TcRecord R = tc_record();
-    constexpr uint32_t kBc = ChainCfg<TN>::kBc;
-    tc::mbar_arrive_expect_tx(bar, (uint32_t)R.state_part + kBc);
+    constexpr uint32_t kUt = ChainCfg<TN>::kUt;
+    tc::mbar_arrive_expect_tx(bar, (uint32_t)R.state_part + kUt);
     tc::bulk_g2s(buf, rec, (uint32_t)R.state_part, bar);
-    tc::bulk_g2s(buf + ChainCfg<TN>::Bc, rec + R.Bc + (size_t)tile * kBc, kBc, bar);
+    tc::bulk_g2s(buf + ChainCfg<TN>::Ut, rec + R.Ut + (size_t)tile * kUt, kUt, bar);
 }
 
 // Writes S[i][jbase + j] (j < NC, this thread's columns) into the K-major S^T image (element (jbase + j, i),
@@ -1064,7 +1023,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             }
         }
         if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 2 * TN);
+            tc::tmem_alloc(&tmem_base, 4 * TN);  // two regions (chunks alternate) of two K panels
             tc::tmem_relinquish();
         }
         tc::tc_fence_before();
@@ -1073,7 +1032,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         // Only now (after this CTA's wait for the preparation) may the output pass start: it reads the
         // preparation's part of each record before it waits for this kernel.
         tc::grid_dep_launch();
-        // TMEM: M' S over the two K panels in cols 0 .. TN - 1 and TN .. 2 TN - 1
+        // TMEM: chunk c's products in region c % 2 (cols 2 TN (c % 2) ..): Kend^T Ut plus M' S over the first
+        // K panel, then M' S over the second
         const uint32_t tmem = tmem_base;
 
         if (warp == kStateLoadWarp) {
@@ -1101,7 +1061,18 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         } else if (issuer) {
             const uint32_t panel = (uint32_t)(warp - kStateEpiWarps);
             constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+            constexpr uint64_t kKendMn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
             constexpr uint32_t idN = tc::idesc_bf16_f32(128, TN, false, false);
+            constexpr uint32_t idKU = tc::idesc_bf16_f32(128, TN, true, false);
+            // Kend^T Ut of chunk c (the state-free part of its update) into panel 0 of TMEM region c % 2, ahead
+            // of the chunk's M' S MMAs, which accumulate onto it
+            auto kend_ut = [&](int c) {
+                const uint8_t *b = sm + (c % NB) * Cfg::kBuf;
+                const uint32_t d = tmem + (uint32_t)(2 * TN * (c & 1));
+                for (int s = 0; s < 4; ++s)  // K steps of 16 tokens: +2 KB of the MN-major Kend, +32 B of Ut
+                    tc::mma_bf16(d, tc::smem_desc(kKendMn, tc::smem_u32(b + Cfg::Kend + s * 2048)),
+                                 tc::smem_desc(kKmaj, tc::smem_u32(b + Cfg::Ut + s * 32)), idKU, s > 0);
+            };
             for (int c = 0; c < nchunks; ++c) {
                 const int bsel = c % NB;
                 uint8_t *buf = sm + bsel * Cfg::kBuf;
@@ -1111,13 +1082,20 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 if (lane == 0) {
                     ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / NB) & 1));
                     if (ok) {
+                        if (panel == 0 && c == 0) kend_ut(0);
                         const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + Cfg::Mc + panel * 16384u));
                         const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * Cfg::kPanel));
+                        const uint32_t d = tmem + (uint32_t)(2 * TN * (c & 1)) + (uint32_t)TN * panel;
                         for (int s = 0; s < 4; ++s)  // K steps of 16: +32 bytes, +2 in the start-address field
-                            tc::mma_bf16(tmem + (uint32_t)TN * panel, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s,
-                                         idN, s > 0);
+                            tc::mma_bf16(d, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, panel == 0 || s > 0);
                     }
                     tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
+                    if (panel == 0 && ok && c + 1 < nchunks) {
+                        // the next chunk's Kend^T Ut, while this chunk's epilogue runs: region (c + 1) % 2 was
+                        // read by chunk c - 1's epilogue before this chunk's operand barrier
+                        ok = tc::mbar_wait(&full_bar[(c + 1) % NB], (uint32_t)(((c + 1) / NB) & 1));
+                        if (ok) kend_ut(c + 1);
+                    }
                     if (!links.loader && panel == 1 && ok) {
                         // the buffer chunk c - 1 used was released by the operand barrier of this chunk
                         const int cn = c + NB - 1;
@@ -1165,60 +1143,38 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             }
             __syncwarp();
         } else if (epi) {
-            const uint32_t tacc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(NC * hcol);
+            const uint32_t tacc0 = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(NC * hcol);
             for (int c = 0; c < nchunks; ++c) {
                 const int bsel = c % NB;
                 const uint8_t *buf = sm + bsel * Cfg::kBuf;
-                // gamma and this thread's NC Bc values, read while the MMAs run
                 ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / NB) & 1));
-                const float gam = reinterpret_cast<const float *>(buf + Cfg::gam)[i];
+                const float gam = reinterpret_cast<const float *>(buf + Cfg::gam)[i];  // read while the MMAs run
                 const int nb = c + 1;                // the image this chunk writes: S_{c+1}, needed by chunk c + 1
                 const bool img = nb < nchunks;
                 uint8_t *sbn = sm + Cfg::SB + (uint32_t)(nb % NS) * Cfg::kImg;
-                // Bc is stored per 32-column tile: rows of 64 bytes, 16-byte chunk k at k ^ ((row / 2) mod 4)
-                const uint8_t *brow = buf + Cfg::Bc + (NC == 32 ? (uint32_t)hcol * 8192u : 0u) + i * 64;
-                const int k0 = NC == 32 ? 0 : 2 * hcol;
-                auto bc8 = [&](int kk, float (&f)[8]) {
-                    unpack8(*reinterpret_cast<const uint4 *>(brow + (((k0 + kk) ^ ((i >> 1) & 3)) << 4)), f);
-                };
-                float bc[16];  // 16 columns: read while the MMAs run
-                if constexpr (NC == 16) {
-                    float f[8];
-                    bc8(0, f);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) bc[u] = f[u];
-                    bc8(1, f);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) bc[8 + u] = f[u];
-                }
                 // the slot's previous image, S_{c+1-NS}, has been copied out
                 if (img && nb >= NS) ok = ok && tc::mbar_wait(&img_free[nb % NS], (uint32_t)((nb / NS - 1) & 1));
                 ok = ok && tc::mbar_wait(&a_bar, (uint32_t)(c & 1));
                 tc::tc_fence_after();
                 if (warp_all(ok)) {
-                    // S <- gamma S + (Bc + (P0 + P1)), P0 / P1 the two K panels' products
+                    // S <- gamma S + (P0 + P1): P0 = Kend^T Ut + the first K panel of M' S, P1 the second
+                    const uint32_t tacc = tacc0 + (uint32_t)(2 * TN * (c & 1));
                     float t0[NC];
                     if constexpr (NC == 16) {
                         float t1[16];
                         tc::tmem_ld16x2(tacc, tacc + TN, t0, t1);
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) S[q] = fmaf(gam, S[q], bc[q] + (t0[q] + t1[q]));
+                        for (int q = 0; q < 16; ++q) S[q] = fmaf(gam, S[q], t0[q] + t1[q]);
                     } else {
-                        // 32 columns: the second panel and Bc in halves, to stay within the register budget
+                        // 32 columns: the second panel in halves, to stay within the register budget
                         tc::tmem_ld32(tacc, t0);
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             float t1[16];
                             tc::tmem_ld16(tacc + TN + 16u * (uint32_t)hh, t1);
-                            float f[8];
-                            bc8(2 * hh, f);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                S[16 * hh + q] = fmaf(gam, S[16 * hh + q], f[q] + (t0[16 * hh + q] + t1[q]));
-                            bc8(2 * hh + 1, f);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                S[16 * hh + 8 + q] = fmaf(gam, S[16 * hh + 8 + q], f[q] + (t0[16 * hh + 8 + q] + t1[8 + q]));
+                            for (int q = 0; q < 16; ++q)
+                                S[16 * hh + q] = fmaf(gam, S[16 * hh + q], t0[16 * hh + q] + t1[q]);
                         }
                     }
                     if (img) store_state_cols<NC>(sbn, Cfg::kPanel, i, NC * hcol, S);
@@ -1246,7 +1202,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 }
             }
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 2 * TN);
+        if (warp == 0) tc::tmem_dealloc(tmem, 4 * TN);
         if (s_abort) return;
     }
     if (S_final && epi) {
@@ -1865,9 +1821,7 @@ const DeviceSetup &device_setup() {
         if (!e)
             e = cudaFuncSetAttribute(prefill_pipe_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)pipe_smem_bytes<32>());
-        if (!e)
-            e = cudaFuncSetAttribute(prefill_pipe_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)pipe_smem_bytes<64>());
+
         if (!e) {
             cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -1930,12 +1884,10 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     if (forced == TC_THREE) return TC_THREE;
     const DeviceSetup &d = device_setup();
     if (d.err) return TC_THREE;
-    const long long chains32 = (long long)num_seqs * H * kNTile, chains64 = chains32 / 2;
+    const long long chains32 = (long long)num_seqs * H * kNTile;
     const bool pipe_fits = chains32 + 2 * kChainMinWorkers / 3 <= d.sms;
-    const bool pipe64_fits = chains64 + 2 * kChainMinWorkers / 3 <= d.sms;
     const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
     if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
-    if (forced == TC_PIPE64) return pipe64_fits ? TC_PIPE64 : TC_THREE;
     if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
     if (pipe_fits && chains32 <= kPipeChainMax) return TC_PIPE;
     return chain_fits ? TC_CHAIN : TC_THREE;
@@ -1955,8 +1907,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const size_t nflag = (size_t)lay.max_slots * H;
     const long long wait = g_test_wait_ns.load();
     const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
-    if (plan == TC_PIPE || plan == TC_PIPE64) {
-        const int tn = plan == TC_PIPE ? 32 : 64;
+    if (plan == TC_PIPE) {
+        constexpr int tn = 32;
         InputMaps m;
         if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
         PipeArgs a;
@@ -1973,14 +1925,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         a.fault = g_test_fault.load();
         a.onorm = onorm;
         marks.before(st, "prefill_pipe_tc");
-        e = tn == 32 ? launch_cooperative(prefill_pipe_tc<32>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
-                                          pipe_smem_bytes<32>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
-                                          lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm,
-                                          fu.qk_eps, a)
-                     : launch_cooperative(prefill_pipe_tc<64>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
-                                          pipe_smem_bytes<64>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
-                                          lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm,
-                                          fu.qk_eps, a);
+        e = launch_cooperative(prefill_pipe_tc<tn>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
+                               pipe_smem_bytes<tn>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                               lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the three
         // kernels instead.

@@ -23,7 +23,7 @@ SYMBOLS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill_chunk
            "kda_decode_step_ex", "kda_short_conv_prefill", "kda_short_conv_decode")
 # include/kda_testing.h (test hooks)
 TESTING_SYMBOLS = ("kda_testing_set_plan", "kda_testing_set_fault")
-PLAN_AUTO, PLAN_THREE, PLAN_CHAIN, PLAN_PIPE, PLAN_PIPE64 = -1, 0, 2, 3, 4
+PLAN_AUTO, PLAN_THREE, PLAN_CHAIN, PLAN_PIPE = -1, 0, 2, 3
 FAULT_NONE, FAULT_NO_PUBLISH, FAULT_CHUNK_TABLE = 0, 1, 2
 PREFILL_MAX_KERNELS = 4
 

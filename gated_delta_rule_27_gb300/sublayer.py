@@ -57,55 +57,84 @@ def _mark(events, i):
         events[i].record()
 
 
-def prefill_forward(x, cu_seqlens, w: Weights, H: int, d: int, events=None, qk_eps=1e-6, out_eps=1e-6):
+class Buffers:
+    """Every intermediate of one sublayer step with R rows (tokens, or sequences in decode), allocated once so
+    that repeated steps allocate nothing and keep their addresses (libkda then reuses its encoded tensor
+    maps)."""
+
+    def __init__(self, R: int, N: int, H: int, d: int, device):
+        bf, f32 = torch.bfloat16, torch.float32
+        HD = H * d
+        self.q, self.k, self.v, self.z = (torch.empty((R, HD), dtype=bf, device=device) for _ in range(4))
+        self.qc, self.kc, self.vc = (torch.empty((R, HD), dtype=bf, device=device) for _ in range(3))
+        self.a = torch.empty((R, HD), dtype=bf, device=device)
+        self.b = torch.empty((R, H), dtype=bf, device=device)
+        self.g = torch.empty((R, HD), dtype=f32, device=device)
+        self.beta = torch.empty((R, H), dtype=f32, device=device)
+        self.o = torch.empty((R, H, d), dtype=bf, device=device)
+        self.S = torch.empty((N, H, d, d), dtype=f32, device=device)
+        self.conv_state = [torch.empty((N, CONV_W - 1, HD), dtype=f32, device=device) for _ in range(3)]
+
+
+def _project(x, w: Weights, bufs: Buffers):
+    torch.matmul(x, w.W_q, out=bufs.q)
+    torch.matmul(x, w.W_k, out=bufs.k)
+    torch.matmul(x, w.W_v, out=bufs.v)
+    torch.matmul(x, w.W_a, out=bufs.a)
+    torch.matmul(x, w.W_b, out=bufs.b)
+    torch.matmul(x, w.W_z, out=bufs.z)
+    torch.nn.functional.softplus(bufs.a.float(), out=bufs.g)
+    bufs.g.neg_()
+    torch.sigmoid(bufs.b.float(), out=bufs.beta)
+
+
+def prefill_forward(x, cu_seqlens, w: Weights, H: int, d: int, events=None, qk_eps=1e-6, out_eps=1e-6,
+                    bufs: Buffers = None):
     """x [T, D] bf16 -> (y [T, D] bf16, S [N, H, d, d], convolution states of q, k, v [N, CONV_W - 1, H d])
     for packed documents (zero initial states).  With `events` (five torch.cuda.Event), the stage boundaries
-    are recorded: projections | convolution | recurrence | output."""
+    are recorded: projections | convolution | recurrence | output.  `bufs` (Buffers for T rows) avoids every
+    allocation; the results then live in it."""
     T = x.shape[0]
     N = cu_seqlens.numel() - 1
-    conv_state = [torch.empty((N, CONV_W - 1, H * d), dtype=torch.float32, device=x.device) for _ in range(3)]
+    if bufs is None:
+        bufs = Buffers(T, N, H, d, x.device)
     _mark(events, 0)
-    q, k, v = x @ w.W_q, x @ w.W_k, x @ w.W_v
-    g = -torch.nn.functional.softplus((x @ w.W_a).float())
-    beta = torch.sigmoid((x @ w.W_b).float())
-    z = x @ w.W_z
+    _project(x, w, bufs)
     _mark(events, 1)
-    qc, kc, vc = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for src, cw, dst, st in ((q, w.conv_q, qc, conv_state[0]), (k, w.conv_k, kc, conv_state[1]),
-                             (v, w.conv_v, vc, conv_state[2])):
+    for src, cw, dst, st in ((bufs.q, w.conv_q, bufs.qc, bufs.conv_state[0]), (bufs.k, w.conv_k, bufs.kc,
+                                                                               bufs.conv_state[1]),
+                             (bufs.v, w.conv_v, bufs.vc, bufs.conv_state[2])):
         libkda.kda_short_conv_prefill(src, cw, cu_seqlens, dst, conv_state_out=st)
     _mark(events, 2)
-    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=x.device)
-    S = torch.empty((N, H, d, d), dtype=torch.float32, device=x.device)
-    libkda.kda_prefill_chunked_ex(qc.view(T, H, d), kc.view(T, H, d), vc.view(T, H, d), g.view(T, H, d).contiguous(),
-                                  beta.contiguous(), cu_seqlens, o, S_final=S, qk_l2norm=True, qk_eps=qk_eps,
-                                  out_gate=z.view(T, H, d), out_weight=w.out_weight, out_eps=out_eps)
+    libkda.kda_prefill_chunked_ex(bufs.qc.view(T, H, d), bufs.kc.view(T, H, d), bufs.vc.view(T, H, d),
+                                  bufs.g.view(T, H, d), bufs.beta, cu_seqlens, bufs.o, S_final=bufs.S,
+                                  qk_l2norm=True, qk_eps=qk_eps, out_gate=bufs.z.view(T, H, d),
+                                  out_weight=w.out_weight, out_eps=out_eps)
     _mark(events, 3)
-    y = o.view(T, H * d) @ w.W_o
+    y = bufs.o.view(T, H * d) @ w.W_o
     _mark(events, 4)
-    return y, S, conv_state
+    return y, bufs.S, bufs.conv_state
 
 
-def decode_forward(x, S, conv_state, w: Weights, H: int, d: int, events=None, qk_eps=1e-6, out_eps=1e-6):
+def decode_forward(x, S, conv_state, w: Weights, H: int, d: int, events=None, qk_eps=1e-6, out_eps=1e-6,
+                   bufs: Buffers = None):
     """One token per sequence: x [N, D] bf16, S [N, H, d, d] and conv_state (q, k, v states, each
-    [N, CONV_W - 1, H d]) updated in place; returns y [N, D]."""
+    [N, CONV_W - 1, H d]) updated in place; returns y [N, D].  `bufs` (Buffers for N rows) avoids every
+    allocation."""
     N = x.shape[0]
+    if bufs is None:
+        bufs = Buffers(N, N, H, d, x.device)
     _mark(events, 0)
-    q, k, v = x @ w.W_q, x @ w.W_k, x @ w.W_v
-    g = -torch.nn.functional.softplus((x @ w.W_a).float())
-    beta = torch.sigmoid((x @ w.W_b).float())
-    z = x @ w.W_z
+    _project(x, w, bufs)
     _mark(events, 1)
-    qc, kc, vc = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for src, cw, st, dst in ((q, w.conv_q, conv_state[0], qc), (k, w.conv_k, conv_state[1], kc),
-                             (v, w.conv_v, conv_state[2], vc)):
+    for src, cw, st, dst in ((bufs.q, w.conv_q, conv_state[0], bufs.qc), (bufs.k, w.conv_k, conv_state[1], bufs.kc),
+                             (bufs.v, w.conv_v, conv_state[2], bufs.vc)):
         libkda.kda_short_conv_decode(src, cw, st, dst)
     _mark(events, 2)
-    o = torch.empty((N, H, d), dtype=torch.bfloat16, device=x.device)
-    libkda.kda_decode_step_ex(qc.view(N, H, d), kc.view(N, H, d), vc.view(N, H, d), g.view(N, H, d).contiguous(),
-                              beta.contiguous(), S, o, qk_l2norm=True, qk_eps=qk_eps, out_gate=z.view(N, H, d),
-                              out_weight=w.out_weight, out_eps=out_eps)
+    libkda.kda_decode_step_ex(bufs.qc.view(N, H, d), bufs.kc.view(N, H, d), bufs.vc.view(N, H, d),
+                              bufs.g.view(N, H, d), bufs.beta, S, bufs.o, qk_l2norm=True, qk_eps=qk_eps,
+                              out_gate=bufs.z.view(N, H, d), out_weight=w.out_weight, out_eps=out_eps)
     _mark(events, 3)
-    y = o.view(N, H * d) @ w.W_o
+    y = bufs.o.view(N, H * d) @ w.W_o
     _mark(events, 4)
     return y

@@ -28,7 +28,6 @@ extern "C" {
 #define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains of 32 columns beside groups that
                                        prepare the records in chunk order and form the outputs behind the
                                        chains; falls back to THREE where it cannot run */
-#define KDA_TESTING_PLAN_PIPE64 4   /* the same with chains of 64 columns (half as many chains) */
 
 /* Forces a launch plan for later calls.  KDA_ERR_INVALID_ARG for an unknown plan. */
 KDA_API kda_status kda_testing_set_plan(int32_t plan);

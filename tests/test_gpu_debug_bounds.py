@@ -53,7 +53,7 @@ def test_debug_build_passes_every_check_and_matches_the_release_build(name, leng
     dbg = libkda.load_debug()
     rel = libkda.load()
     inp = workloads.prefill_inputs(lengths, H=H, d=d, dtype=dtype, seed=171, s0_std=0.1)
-    plans = [libkda.PLAN_THREE, libkda.PLAN_CHAIN, libkda.PLAN_PIPE, libkda.PLAN_PIPE64] if d == 128 else \
+    plans = [libkda.PLAN_THREE, libkda.PLAN_CHAIN, libkda.PLAN_PIPE] if d == 128 else \
         [libkda.PLAN_AUTO]
     for plan in plans:
         o_d, S_d, st, line = _prefill(dbg, inp, chunk, plan)

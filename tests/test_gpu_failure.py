@@ -31,14 +31,14 @@ def _call(q, k, v, g, beta, cu, ws, S0):
     return o, S
 
 
-@pytest.mark.parametrize("plan", ["chain", "pipe", "pipe64"])
+@pytest.mark.parametrize("plan", ["chain", "pipe"])
 def test_wait_that_runs_out_is_reported_and_the_next_call_is_correct(plan):
     inp = workloads.prefill_inputs([300, 77], H=4, d=128, dtype=torch.bfloat16, seed=41, s0_std=0.1)
     q, k, v, g, beta, cu = to_device(inp)
     S0 = inp.S0.to(dev())
     T, H, d = q.shape
     ws = libkda.new_workspace(T, 2, H, d, d, libkda.KDA_BF16, 64, dev())
-    libkda.testing_set_plan({"chain": libkda.PLAN_CHAIN, "pipe": libkda.PLAN_PIPE, "pipe64": libkda.PLAN_PIPE64}[plan])
+    libkda.testing_set_plan({"chain": libkda.PLAN_CHAIN, "pipe": libkda.PLAN_PIPE}[plan])
     libkda.testing_set_fault(libkda.FAULT_NO_PUBLISH, 20_000_000)
     try:
         t0 = time.perf_counter()

@@ -25,7 +25,7 @@ def _run(inp, plan, S0=None, poison=0x7F):
     """One call under the given launch plan, on a workspace whose every byte is `poison` beforehand, so that
     nothing a call reads before writing it can pass for a result."""
     libkda.testing_set_plan({"auto": libkda.PLAN_AUTO, "three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN,
-                             "pipe": libkda.PLAN_PIPE, "pipe64": libkda.PLAN_PIPE64}[plan])
+                             "pipe": libkda.PLAN_PIPE}[plan])
     try:
         q, k, v, g, beta, cu = to_device(inp)
         T, H, d = q.shape
@@ -67,7 +67,7 @@ def test_chain_and_three_kernel_plans_agree(case):
     oc, Sc = _run(inp, "chain", S0, poison=0x5A)
     assert torch.equal(o3, oc), (o3.float() - oc.float()).abs().max().item()
     assert torch.equal(S3, Sc), (S3 - Sc).abs().max().item()
-    for plan in ("pipe", "pipe64"):
+    for plan in ("pipe",):
         op, Sp = _run(inp, plan, S0, poison=0x7F)
         assert torch.equal(o3, op), (plan, (o3.float() - op.float()).abs().max().item())
         assert torch.equal(S3, Sp), (plan, (S3 - Sp).abs().max().item())
@@ -96,7 +96,7 @@ def test_automatic_plan_on_the_prefill_workload_twice():
     assert torch.equal(o3, outs[0][0]) and torch.equal(S3, outs[0][1])
 
 
-@pytest.mark.parametrize("plan", ["three", "chain", "pipe", "pipe64"])
+@pytest.mark.parametrize("plan", ["three", "chain", "pipe"])
 def test_full_prefill_workload_on_poisoned_workspaces(plan):
     """The prefill workload under each launch plan on a workspace poisoned with two different patterns: the
     kernels overlap at their boundaries (and, in the chain and pipe plans, hand data over through flags), so any
