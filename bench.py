@@ -379,48 +379,106 @@ def bench_decode_indexed(libkda, steps, warmup, dev):
 
 def bench_sublayer(steps, warmup, dev):
     """Whole-sublayer timing with synthetic weights (measurement only): the stages around the recurrence --
-    projections (cuBLAS bf16 GEMMs), short convolution, recurrence with the fused normalisations, output
-    projection -- each bracketed by events, for the prefill workload's shape and for one decode step of the
-    decode workload's shape.  Hidden size H * d."""
-    from gated_delta_rule_27_gb300 import sublayer
+    projections (cuBLAS bf16 GEMMs and the gate activations), short convolution, recurrence with the fused
+    normalisations, output projection -- each bracketed by events, for the prefill workload's shape and for
+    one decode step of the decode workload's shape.  Hidden size H * d.  The stages made of many small
+    launches (projections, convolution, output projection) are replayed from CUDA graphs, so that their
+    intervals are device time rather than the host's launch latency; the recurrence is enqueued while the GPU
+    is still busy with the stages before it."""
+    from gated_delta_rule_27_gb300 import libkda, sublayer
     stages = ["projections", "short_conv", "recurrence", "output_projection"]
     out = {}
     cases = (("prefill", 1, 4096, 16), ("decode", 256, 1, 32))
+
+    def graph_of(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
     for name, N, T, H in cases:
         d = 128
         D = H * d
+        R = T * N if name == "prefill" else N
         w = sublayer.synthetic_weights(D, H, d, seed=workloads.BASE_SEED + 21, device=dev)
         gen = torch.Generator(device="cpu").manual_seed(workloads.BASE_SEED + 22)
         flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        x = torch.randn((R, D), generator=gen).to(torch.bfloat16).to(dev)
+        b = sublayer.Buffers(R, N, H, d, dev)
+        y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+        HD = H * d
         if name == "prefill":
-            x = torch.randn((T, D), generator=gen).to(torch.bfloat16).to(dev)
             cu = workloads.cu_from_lengths([T], device=dev)
-            bufs = sublayer.Buffers(T, N, H, d, dev)
-            run = lambda ev: sublayer.prefill_forward(x, cu, w, H, d, events=ev, bufs=bufs)
+            ws = libkda.new_workspace(T, 1, H, d, d, libkda.KDA_BF16, 64, dev)
+
+            def conv():
+                for src, cw, dst, st in ((b.q, w.conv_q, b.qc, b.conv_state[0]), (b.k, w.conv_k, b.kc,
+                                                                                 b.conv_state[1]),
+                                         (b.v, w.conv_v, b.vc, b.conv_state[2])):
+                    libkda.kda_short_conv_prefill(src, cw, cu, dst, conv_state_out=st)
+
+            def rec():
+                libkda.kda_prefill_chunked_ex(b.qc.view(T, H, d), b.kc.view(T, H, d), b.vc.view(T, H, d),
+                                              b.g.view(T, H, d), b.beta, cu, b.o, S_final=b.S, workspace=ws,
+                                              qk_l2norm=True, qk_eps=1e-6, out_gate=b.z.view(T, H, d),
+                                              out_weight=w.out_weight, out_eps=1e-6)
         else:
-            x = torch.randn((N, D), generator=gen).to(torch.bfloat16).to(dev)
-            S = torch.empty((N, H, d, d), device=dev).normal_(0.0, 0.1)
-            cst = [torch.zeros((N, sublayer.CONV_W - 1, D), device=dev) for _ in range(3)]
-            bufs = sublayer.Buffers(N, N, H, d, dev)
-            run = lambda ev: sublayer.decode_forward(x, S, cst, w, H, d, events=ev, bufs=bufs)
+            b.S.normal_(0.0, 0.1)
+            for st in b.conv_state:
+                st.zero_()
+
+            def conv():
+                for src, cw, st, dst in ((b.q, w.conv_q, b.conv_state[0], b.qc), (b.k, w.conv_k, b.conv_state[1],
+                                                                                 b.kc),
+                                         (b.v, w.conv_v, b.conv_state[2], b.vc)):
+                    libkda.kda_short_conv_decode(src, cw, st, dst)
+
+            def rec():
+                libkda.kda_decode_step_ex(b.qc.view(N, H, d), b.kc.view(N, H, d), b.vc.view(N, H, d),
+                                          b.g.view(N, H, d), b.beta, b.S, b.o, qk_l2norm=True, qk_eps=1e-6,
+                                          out_gate=b.z.view(N, H, d), out_weight=w.out_weight, out_eps=1e-6)
+
+        proj = lambda: sublayer._project(x, w, b)
+        outp = lambda: torch.matmul(b.o.view(R, HD), w.W_o, out=y)
+        for _ in range(warmup):
+            proj(); conv(); rec(); outp()
+        g_proj, g_conv, g_out = graph_of(proj), graph_of(conv), graph_of(outp)
         per = {k: [] for k in stages}
-        for i in range(warmup + steps):
+        for _ in range(steps):
             ev = new_events(5)
-            flush.zero_()
-            run(ev)
             torch.cuda.synchronize()
-            if i >= warmup:
-                for j, k in enumerate(stages):
-                    per[k].append(ev[j].elapsed_time(ev[j + 1]))
+            flush.zero_()
+            ev[0].record()
+            g_proj.replay()
+            ev[1].record()
+            g_conv.replay()
+            ev[2].record()
+            rec()
+            ev[3].record()
+            g_out.replay()
+            ev[4].record()
+            torch.cuda.synchronize()
+            for j, k in enumerate(stages):
+                per[k].append(ev[j].elapsed_time(ev[j + 1]))
         ms = {k: statistics.median(v) for k, v in per.items()}
         total = sum(ms.values())
+        conv_bytes = 3 * R * HD * 2 * 2 + (3 * 2 * N * (sublayer.CONV_W - 1) * HD * 4 if name == "decode" else
+                                            3 * N * (sublayer.CONV_W - 1) * HD * 4)
         out[name] = {"shape": "N=%d T=%d H=%d d=%d hidden=%d bf16, synthetic weights" % (N, T, H, d, D),
                      "ms": {k: round(v, 5) for k, v in ms.items()}, "total_ms": total,
                      "recurrence_share": ms["recurrence"] / total,
+                     "short_conv_gbs": conv_bytes / (ms["short_conv"] * 1e-3) / 1e9,
                      "note": "projections are cuBLAS GEMMs (q, k, v, decay gate, write gate, output gate) plus "
                              "torch gate activations; short_conv, recurrence (with the q/k L2 norm and the gated "
                              "output norm fused) are libkda kernels; buffers allocated once; L2 flushed before "
-                             "every step; stage times are event intervals, so they include any wait for the host"}
+                             "every step; projections, convolution and output projection replayed from CUDA "
+                             "graphs"}
     return out
 
 

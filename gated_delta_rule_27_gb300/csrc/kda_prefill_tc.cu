@@ -903,6 +903,16 @@ __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int 
     tc::bulk_g2s(buf, rec, (uint32_t)R.state_part, bar);
     tc::bulk_g2s(buf + ChainCfg<TN>::Ut, rec + R.Ut + (size_t)tile * kUt, kUt, bar);
 }
+// The same parts of a later chunk's record pulled into L2 only (no shared memory, nothing to wait for), so that
+// its copy into a buffer, a few chunks later, is served from L2.
+template <int TN>
+__device__ __forceinline__ void prefetch_record(const char *rec, int tile) {
+    constexpr TcRecord R = tc_record();
+    constexpr uint32_t kUt = ChainCfg<TN>::kUt;
+    tc::bulk_prefetch_l2(rec, (uint32_t)R.state_part);
+    tc::bulk_prefetch_l2(rec + R.Ut + (size_t)tile * kUt, kUt);
+}
+constexpr int kChainL2Ahead = 3;  // records pulled into L2 this many chunks beyond the buffered ones
 
 // Writes S[i][jbase + j] (j < NC, this thread's columns) into the K-major S^T image (element (jbase + j, i),
 // K panels `panel_bytes` apart).  Rows i and i ^ 1 (lanes of one warp) trade values so that each stores whole
@@ -1020,6 +1030,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 for (int c = 0; c < NB - 1 && c < nchunks; ++c)
                     issue_record<TN>(sm + c * Cfg::kBuf, rec0 + (size_t)(first + c) * H * record_bytes, tile,
                                      &full_bar[c]);
+                for (int c = NB - 1; c < NB - 1 + kChainL2Ahead && c < nchunks; ++c)
+                    prefetch_record<TN>(rec0 + (size_t)(first + c) * H * record_bytes, tile);
             }
         }
         if (warp == 0) {
@@ -1051,6 +1063,10 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     if (!ok) break;
                     issue_record<TN>(sm + b * Cfg::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[b]);
                     issued = c + 1;
+                    // a later record that is already published goes to L2 ahead of its copy
+                    const int cp = c + kChainL2Ahead;
+                    if (!links.ready && cp < nchunks)
+                        prefetch_record<TN>(rec_h + (size_t)(first + cp) * rec_stride, tile);
                 }
                 if (!ok) {  // copies already on their way land before the CTA's shared memory can go away
                     for (int c = max(0, issued - NB); c < issued; ++c)
@@ -1102,6 +1118,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                         if (cn < nchunks)
                             issue_record<TN>(sm + (cn % NB) * Cfg::kBuf, rec_h + (size_t)(first + cn) * rec_stride,
                                              tile, &full_bar[cn % NB]);
+                        if (cn + kChainL2Ahead < nchunks)
+                            prefetch_record<TN>(rec_h + (size_t)(first + cn + kChainL2Ahead) * rec_stride, tile);
                     }
                 }
                 __syncwarp();
