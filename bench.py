@@ -10,7 +10,8 @@ steps) and the indexed decode over a state pool are timed.  Prints ONE JSON
 line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libkda|reference]
-  python bench.py --profile-case prefill|varlen|long|decode-n64 [--repeat R]   (untimed, for ncu)
+  python bench.py --profile-case prefill|varlen|long|decode-n64|conv [--repeat R]   (untimed, for ncu)
+  python bench.py --compare-plans      (pass time of each tensor-core launch plan, one JSON line each)
 
 Timing: CUDA events on the launching stream, L2 flushed (a 256 MB write)
 before every timed prefill step (the prefill inputs, 101 MB, would otherwise
@@ -24,6 +25,7 @@ same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import re
 import json
@@ -251,6 +253,102 @@ def bench_prefill(libkda, steps, warmup, dev, rank, name=WORKLOAD, head_block=0)
     alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * token_heads + N * H * d * d * 4
     return dict(name=name, T=T, H=H, d=d, N=N, chunk=w["chunk"], step_ms=step_ms, kern_ms=kern_ms, names=names,
                 wall_s=wall_s, launches=n * steps, inp=inp, alg_bytes=alg_bytes)
+
+
+def bench_host_overhead(libkda, dev, inp, calls=400):
+    """Host time of one call into the C ABI (argument checks, cached launch set-up, the launches themselves),
+    measured around the raw ctypes call with pointers marshalled once, next to the cost of a ctypes call that
+    does nothing (kda_status_string) and of the Python wrapper.  The device is drained every 8 calls, outside
+    the timed calls, so that the launch queue never fills."""
+    lib = libkda.load()
+    T, H, d = inp.q.shape
+    N = inp.num_seqs
+    o = torch.empty_like(inp.v)
+    S = torch.empty((N, H, d, d), device=dev)
+    ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, 64, dev)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    pre = (p(inp.q), p(inp.k), p(inp.v), p(inp.g), p(inp.beta), p(inp.cu_seqlens), N, T, H, d, d, libkda.KDA_BF16,
+           64, None, p(o), p(S), p(ws), ws.numel() * ws.element_size(), st)
+    dq = torch.zeros((N, H, d), dtype=torch.bfloat16, device=dev)
+    dg = torch.zeros((N, H, d), dtype=torch.float32, device=dev)
+    db = torch.zeros((N, H), dtype=torch.float32, device=dev)
+    do = torch.empty_like(dq)
+    dec = (p(dq), p(dq), p(dq), p(dg), p(db), N, H, d, d, libkda.KDA_BF16, p(S), p(do), st)
+
+    def timed(fn):
+        out = []
+        for i in range(calls):
+            if i % 8 == 0:
+                torch.cuda.synchronize()
+            t0 = time.perf_counter_ns()
+            fn()
+            out.append((time.perf_counter_ns() - t0) * 1e-3)
+        torch.cuda.synchronize()
+        return statistics.median(out[calls // 8:])
+
+    def prefill_raw():
+        if lib.kda_prefill_chunked(*pre) != libkda.KDA_OK:
+            raise RuntimeError("kda_prefill_chunked failed")
+
+    def decode_raw():
+        if lib.kda_decode_step(*dec) != libkda.KDA_OK:
+            raise RuntimeError("kda_decode_step failed")
+
+    res = {"prefill_call_us": timed(prefill_raw), "decode_call_us": timed(decode_raw),
+           "ctypes_floor_us": timed(lambda: lib.kda_status_string(0)),
+           "prefill_python_wrapper_us": timed(lambda: libkda.kda_prefill_chunked(
+               inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, o, S_final=S, workspace=ws))}
+    res["note"] = ("median host wall time per call (time.perf_counter_ns around the call, launches included, "
+                   "device drained every 8 calls outside the timed calls); the *_call_us figures call the C ABI "
+                   "through ctypes with pre-marshalled pointers")
+    return res
+
+
+def compare_plans(libkda, dev, reps=8):
+    """Pass time of each tensor-core launch plan, forced through the test hook, on the prefill workload and on
+    single documents of 4096 tokens with 8 and 19 heads (32 and 76 chains), L2 flushed before every pass."""
+    flush = torch.empty(64 << 20, device=dev)
+    cases = [("prefill", workloads.workload_prefill("prefill", device=dev))]
+    for H in (8, 19):
+        cases.append(("single document T=4096 H=%d" % H,
+                      workloads.prefill_inputs([4096], H=H, d=128, dtype=torch.bfloat16, seed=3, device=dev)))
+    plans = [("auto", libkda.PLAN_AUTO), ("three", libkda.PLAN_THREE), ("chain", libkda.PLAN_CHAIN),
+             ("pipe", libkda.PLAN_PIPE)]
+    out = []
+    try:
+        for name, inp in cases:
+            T, H, d = inp.q.shape
+            N = inp.num_seqs
+            o = torch.empty_like(inp.v)
+            S = torch.empty((N, H, d, d), device=dev)
+            ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, 64, dev)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(libkda.PREFILL_MAX_KERNELS + 1)]
+            for e in evs:
+                e.record()
+            for pname, plan in plans:
+                libkda.testing_set_plan(plan)
+                tot, per = [], {}
+                for rep in range(reps):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    libkda.kda_prefill_chunked(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, o, S_final=S,
+                                               workspace=ws)
+                    b.record()
+                    flush.zero_()
+                    names = libkda.kda_prefill_chunked_profiled(inp.q, inp.k, inp.v, inp.g, inp.beta,
+                                                                inp.cu_seqlens, o, evs, S_final=S, workspace=ws)
+                    torch.cuda.synchronize()
+                    if rep >= 2:
+                        tot.append(a.elapsed_time(b) * 1e3)
+                        for j, n in enumerate(names):
+                            per.setdefault(n, []).append(evs[j].elapsed_time(evs[j + 1]) * 1e3)
+                out.append({"case": name, "plan": pname, "us": round(statistics.median(tot), 1),
+                            "kernels_us": {n: round(statistics.median(t), 1) for n, t in per.items()}})
+    finally:
+        libkda.testing_set_plan(libkda.PLAN_AUTO)
+    return out
 
 
 def bench_e2e(libkda, steps, warmup, dev, inp):
@@ -607,6 +705,7 @@ def run_libkda(args):
         di = bench_decode_indexed(libkda, 50, 3, dev)
         sub = bench_sublayer(min(args.steps, 10), 3, dev)
     e2e = bench_e2e(libkda, args.steps, args.warmup, dev, pf["inp"])
+    host = bench_host_overhead(libkda, dev, pf["inp"])
 
     T = pf["T"]
     summ = prefill_summary(pf, pk, pk_src, world)
@@ -643,7 +742,7 @@ def run_libkda(args):
                     "frac_of_copy_floor": e2e["copy_ms"] / e2e["ms"],
                     "note": "pinned host inputs copied in and o, S_final copied out every step; consecutive "
                             "steps pipelined on copy-in / compute / copy-out streams"},
-            "gpu_launches": pf["launches"], "clocks": clocks,
+            "host_overhead": host, "gpu_launches": pf["launches"], "clocks": clocks,
             "wall_s_timed_region": pf["wall_s"]}
     for name, p in others.items():
         ps = prefill_summary(p, pk, pk_src, world)
@@ -705,7 +804,7 @@ def run_profile_case(case: str, repeat: int):
 
     'prefill', 'varlen' and 'long' run that prefill workload through kda_prefill_chunked; 'decode-n64' runs
     decode steps over a quarter of the decode workload's sequences (64 x 32 heads, 128 MiB of state), small
-    enough for a many-pass capture.
+    enough for a many-pass capture; 'conv' runs the sublayer's short convolutions (prefill and decode).
     """
     from gated_delta_rule_27_gb300 import libkda
     torch.cuda.set_device(0)
@@ -719,6 +818,22 @@ def run_profile_case(case: str, repeat: int):
         for _ in range(repeat):
             libkda.kda_prefill_chunked(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, o, S_final=S,
                                        workspace=ws)
+    elif case == "conv":
+        # the sublayer's short convolutions: q, k, v of the prefill workload's shape (4096 tokens x 2048
+        # channels) and of one decode step of the decode workload's shape (256 sequences x 4096 channels)
+        gen = torch.Generator(device="cpu").manual_seed(workloads.BASE_SEED + 23)
+        for R, C, step in ((4096, 2048, False), (256, 4096, True)):
+            x = torch.randn((R, C), generator=gen).to(torch.bfloat16).to("cuda")
+            w = torch.randn((C, 4), generator=gen).to("cuda")
+            y = torch.empty_like(x)
+            st = torch.zeros((1 if not step else R, 3, C), device="cuda")
+            cu = workloads.cu_from_lengths([R], device="cuda")
+            for _ in range(repeat):
+                for _ in range(3):
+                    if step:
+                        libkda.kda_short_conv_decode(x, w, st, y)
+                    else:
+                        libkda.kda_short_conv_prefill(x, w, cu, y, conv_state_out=st)
     else:
         dec = workloads.decode_inputs(repeat, 64, 32, 128, torch.bfloat16, seed=workloads.workload_seed("decode"),
                                       device="cuda")
@@ -739,12 +854,21 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the prefill and decode workloads (skip varlen, long, indexed decode)")
-    ap.add_argument("--profile-case", choices=["prefill", "varlen", "long", "decode-n64"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "varlen", "long", "decode-n64", "conv"], default=None,
                     help="run untimed launches of one workload for a profiler, print a status line, exit")
     ap.add_argument("--repeat", type=int, default=3)
+    ap.add_argument("--compare-plans", action="store_true",
+                    help="print the pass time of every tensor-core launch plan (one JSON line each) and exit")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args.profile_case, args.repeat)
+        return
+    if args.compare_plans:
+        from gated_delta_rule_27_gb300 import libkda
+        torch.cuda.set_device(0)
+        libkda.load()
+        for row in compare_plans(libkda, torch.device("cuda", 0)):
+            print(json.dumps(row), flush=True)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -39,7 +39,7 @@ kda_status fusion_from(const kda_fusion_opts *opts, bool any_rows, const void *o
     if (opts->out_gate) {
         if (!(opts->out_eps > 0.f)) return KDA_ERR_INVALID_ARG;
         if (any_rows && (!aligned16(opts->out_gate) || opts->out_gate == o)) return KDA_ERR_INVALID_ARG;
-        if (reinterpret_cast<uintptr_t>(opts->out_weight) & 3u) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(opts->out_weight)) return KDA_ERR_INVALID_ARG;  // (null passes)
         fu->gate = opts->out_gate;
         fu->weight = opts->out_weight;
         fu->out_eps = opts->out_eps;

@@ -1353,8 +1353,26 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
             const size_t row = ((size_t)(t0 + r) * H + h) * kD;
             uint4 *dst = reinterpret_cast<uint4 *>(o + row);
             const bool row_ok = KDA_IN_BOUNDS(r >= Lc || t0 + r < total_tokens, reinterpret_cast<int32_t *>(ws));
-            float scale = 1.f;
-            if (onorm.gate) {  // fused epilogue, pass 1: the row's mean square
+            const bool write = r < Lc && row_ok;
+            if (!onorm.gate) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                    if (write) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) dst[q * 4 + u] = pack8_at(v + 8 * u);
+                    }
+                }
+            } else {
+                // fused epilogue: o / rms(o) * w * sigmoid(z).  The row's gate inputs are fetched a quarter
+                // ahead of their use (the first quarter before the mean square), the weights are uniform
+                // across the warp (broadcast loads), the logistic function takes the fast exponential and
+                // division (bf16 output).
+                const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row);
+                uint4 zc[4], zn[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) zc[u] = write ? __ldg(z4 + u) : make_uint4(0u, 0u, 0u, 0u);
                 float ss = 0.f;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -1363,28 +1381,39 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
                 }
-                scale = rsqrtf(ss * (1.f / kD) + onorm.eps);
-            }
+                const float scale = rsqrtf(ss * (1.f / kD) + onorm.eps);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
-                if (r < Lc && row_ok) {
-                    if (onorm.gate) {  // pass 2: o / rms(o) * w * sigmoid(z)
-                        const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row) + q * 4;
+                for (int q = 0; q < 4; ++q) {
+                    if (q < 3) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            zn[u] = write ? __ldg(z4 + (q + 1) * 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    float v[32];
+                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                    if (write) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            float z[8];
-                            unpack8(z4[u], z);
+                            float z[8], wv[8];
+                            unpack8(zc[u], z);
+                            if (onorm.weight) {
+                                const float4 *w4 = reinterpret_cast<const float4 *>(onorm.weight + q * 32 + u * 8);
+                                *reinterpret_cast<float4 *>(wv) = __ldg(w4);
+                                *reinterpret_cast<float4 *>(wv + 4) = __ldg(w4 + 1);
+                            } else {
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int c = q * 32 + u * 8 + i;
-                                v[u * 8 + i] *= scale * (onorm.weight ? onorm.weight[c] : 1.f) * sigmoidf(z[i]);
+                                for (int i = 0; i < 8; ++i) wv[i] = 1.f;
                             }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                v[u * 8 + i] *= scale * wv[i] * __fdividef(1.f, 1.f + __expf(-z[i]));
+                            dst[q * 4 + u] = pack8_at(v + 8 * u);
                         }
                     }
+                    if (q < 3) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) dst[q * 4 + u] = pack8_at(v + 8 * u);
+                        for (int u = 0; u < 4; ++u) zc[u] = zn[u];
+                    }
                 }
             }
         } else if ((tid & 31) == 0) {

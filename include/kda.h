@@ -166,7 +166,7 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
  *                    with z = out_gate [T, H, d_v] in_dtype and w = out_weight
  *                    [d_v] fp32 (NULL: all ones); the stored o is this value.
  * All pointers are device pointers with the alignment rules of the entry
- * points (out_gate 16-byte, out_weight 4-byte aligned).
+ * points (out_gate and out_weight 16-byte aligned).
  */
 typedef struct {
     int32_t qk_l2norm;

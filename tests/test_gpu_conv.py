@@ -28,11 +28,13 @@ def _setup(lengths, C, W, dtype, seed):
     return x, w, st, workloads.cu_from_lengths(lengths)
 
 
+@pytest.mark.parametrize("C", [2 * 128 + 8, 2 * 128 + 6], ids=["C264", "C262"])
 @pytest.mark.parametrize("dtype,W", [(torch.bfloat16, 4), (torch.float32, 4), (torch.float32, 1), (torch.bfloat16, 8)],
                          ids=["bf16-W4", "f32-W4", "f32-W1", "bf16-W8"])
-def test_prefill_against_the_definition(dtype, W):
+def test_prefill_against_the_definition(dtype, W, C):
+    """C = 264 takes the four-channel kernel, C = 262 (not a multiple of 4) the one-channel kernel; neither is a
+    multiple of the block width."""
     lengths = [150, 0, 2, 64, 1, 300, 65]  # empty and shorter-than-window documents, tile-straddling ones
-    C = 2 * 128 + 8  # not a multiple of the block width
     x, w, st, cu = _setup(lengths, C, W, dtype, seed=11 + W)
     y = torch.empty_like(x, device=dev())
     st_out = torch.full((len(lengths), W - 1, C), float("nan"), device=dev())
@@ -72,6 +74,45 @@ def test_state_carry_and_decode_continuation():
     assert torch.equal(torch.cat([y3] + ys), y_all)  # the same fp32 sums in the same order
     y_ref, _ = sublayer.short_conv(f64(x), f64(w), [0, T])
     assert rel(y_all, y_ref, "y one pass") <= TOL[torch.bfloat16]
+
+
+def _offset_copy(x):
+    """x's values in a buffer that starts one element past a 4-element boundary (the one-channel kernels)."""
+    buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=dev())
+    v = buf[1:].view(x.shape)
+    v.copy_(x)
+    return v
+
+
+@pytest.mark.parametrize("dtype,W", [(torch.bfloat16, 4), (torch.float32, 3), (torch.bfloat16, 8), (torch.float32, 1),
+                                     (torch.bfloat16, 2)])
+def test_four_channel_and_one_channel_kernels_agree_bitwise(dtype, W):
+    """The same inputs through the four-channel kernels (aligned) and the one-channel kernels (x and y one element
+    off the 4-element alignment): identical outputs and states, prefill and decode."""
+    lengths = [150, 0, 2, 64, 1, 300, 65, 17]
+    C = 264
+    x, w, st, cu = _setup(lengths, C, W, dtype, seed=41 + W)
+    xd, wd, cud, std = x.to(dev()), w.to(dev()), cu.to(dev()), st.to(dev())
+    ys = []
+    states = []
+    for xin in (xd, _offset_copy(xd)):
+        y = _offset_copy(torch.zeros_like(xd)) if xin.data_ptr() % 8 else torch.empty_like(xd)
+        so = torch.full((len(lengths), W - 1, C), float("nan"), device=dev()) if W > 1 else None
+        libkda.kda_short_conv_prefill(xin, wd, cud, y, conv_state=std, conv_state_out=so)
+        ys.append(y.clone())
+        states.append(so)
+    assert torch.equal(ys[0], ys[1])
+    if W > 1:
+        assert torch.equal(states[0], states[1])
+    N = len(lengths)
+    xt = x[:N].to(dev()).contiguous()  # one token per sequence
+    outs = []
+    for xin in (xt, _offset_copy(xt)):
+        s = std.clone()
+        y = _offset_copy(torch.zeros_like(xt)) if xin.data_ptr() % 8 else torch.empty_like(xt)
+        libkda.kda_short_conv_decode(xin, wd, s if W > 1 else None, y)
+        outs.append((y.clone(), s))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def test_conv_rejects_bad_arguments():

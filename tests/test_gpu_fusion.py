@@ -40,25 +40,45 @@ def _reference(inp, q, k, z, w):
     return sublayer.gated_rmsnorm(o, f64(z), f64(w), EPS_OUT), S
 
 
-@pytest.mark.parametrize("dtype,d,chunk,plan", [(torch.bfloat16, 128, 64, "three"), (torch.bfloat16, 128, 64, "chain"),
-                                                (torch.float32, 64, 32, "auto"), (torch.bfloat16, 16, 16, "auto")],
-                         ids=["tc-three", "tc-chain", "simt-f32", "simt-bf16-d16"])
-def test_prefill_with_fused_norms(dtype, d, chunk, plan):
+@pytest.mark.parametrize("dtype,d,chunk,plan,weight", [
+    (torch.bfloat16, 128, 64, "three", True), (torch.bfloat16, 128, 64, "chain", True),
+    (torch.bfloat16, 128, 64, "pipe", True), (torch.bfloat16, 128, 64, "chain", False),
+    (torch.float32, 64, 32, "auto", True), (torch.bfloat16, 16, 16, "auto", True)],
+    ids=["tc-three", "tc-chain", "tc-pipe", "tc-chain-no-weight", "simt-f32", "simt-bf16-d16"])
+def test_prefill_with_fused_norms(dtype, d, chunk, plan, weight):
     inp, q, k, z, w = _raw_inputs([150, 77, 300], H=2, d=d, dtype=dtype, seed=131)
+    if not weight:
+        w = torch.ones(d)  # the reference's weight when out_weight is null
     o_ref, S_ref = _reference(inp, q, k, z, w)
     x = [t.to(dev()) for t in (q, k, inp.v, inp.g, inp.beta, inp.cu_seqlens)]
     T, H = inp.total_tokens, 2
     o = torch.empty((T, H, d), dtype=dtype, device=dev())
     S = torch.empty((3, H, d, d), device=dev())
-    libkda.testing_set_plan({"three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN, "auto": libkda.PLAN_AUTO}[plan])
+    libkda.testing_set_plan({"three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN, "pipe": libkda.PLAN_PIPE,
+                             "auto": libkda.PLAN_AUTO}[plan])
     try:
         libkda.kda_prefill_chunked_ex(*x, o, S0=inp.S0.to(dev()), S_final=S, chunk_size=chunk, qk_l2norm=True,
-                                      qk_eps=EPS_QK, out_gate=z.to(dev()), out_weight=w.to(dev()), out_eps=EPS_OUT)
+                                      qk_eps=EPS_QK, out_gate=z.to(dev()), out_weight=w.to(dev()) if weight else None,
+                                      out_eps=EPS_OUT)
         torch.cuda.synchronize()
     finally:
         libkda.testing_set_plan(libkda.PLAN_AUTO)
     assert rel(o, o_ref, "o fused") <= TOL[dtype], rel(o, o_ref)
     assert rel(S, S_ref, "S fused") <= TOL[dtype], rel(S, S_ref)
+
+
+def test_fused_options_are_checked():
+    inp, q, k, z, w = _raw_inputs([64], H=1, d=128, dtype=torch.bfloat16, seed=133)
+    x = [t.to(dev()) for t in (q, k, inp.v, inp.g, inp.beta, inp.cu_seqlens)]
+    o = torch.empty((64, 1, 128), dtype=torch.bfloat16, device=dev())
+    w_off = torch.empty(129, device=dev())[1:]  # 4 bytes past a 16-byte boundary
+    with pytest.raises(libkda.KdaError) as err:
+        libkda.kda_prefill_chunked_ex(*x, o, out_gate=z.to(dev()), out_weight=w_off, out_eps=EPS_OUT)
+    assert err.value.status == libkda.KDA_ERR_INVALID_ARG
+    with pytest.raises(libkda.KdaError):
+        libkda.kda_prefill_chunked_ex(*x, o, out_gate=z.to(dev()), out_eps=0.0)  # out_eps must be positive
+    with pytest.raises(libkda.KdaError):
+        libkda.kda_prefill_chunked_ex(*x, o, out_gate=o, out_eps=EPS_OUT)  # the gate may not alias o
 
 
 def test_prefill_ex_without_options_is_the_plain_call():
