@@ -307,10 +307,10 @@ def bench_host_overhead(libkda, dev, inp, calls=400):
 
 def compare_plans(libkda, dev, reps=8):
     """Pass time of each tensor-core launch plan, forced through the test hook, on the prefill workload and on
-    single documents of 4096 tokens with 8 and 19 heads (32 and 76 chains), L2 flushed before every pass."""
+    single documents of 4096 tokens with 8, 24 and 32 heads, L2 flushed before every pass."""
     flush = torch.empty(64 << 20, device=dev)
     cases = [("prefill", workloads.workload_prefill("prefill", device=dev))]
-    for H in (8, 19):
+    for H in (8, 24, 32):
         cases.append(("single document T=4096 H=%d" % H,
                       workloads.prefill_inputs([4096], H=H, d=128, dtype=torch.bfloat16, seed=3, device=dev)))
     plans = [("auto", libkda.PLAN_AUTO), ("three", libkda.PLAN_THREE), ("chain", libkda.PLAN_CHAIN),

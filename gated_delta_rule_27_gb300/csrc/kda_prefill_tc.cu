@@ -346,13 +346,20 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // One (chunk slot, head) of the preparation by a CTA of 256 threads whose 256 TMEM
 // columns start at `tmem`; `ph` is the parity of this unit's barrier phases (units
 // a CTA has prepared before, mod 2).  (nslot, nh) is a unit that is likely to
-// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  If
-// `publish` is set, the group's previous record is published there (release,
-// once its bulk stores are complete) as soon as this unit's loads are on
-// their way.  Returns false after recording a timeout in the status word.
+// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  With
+// `claim_counter`, the group instead claims its next unit from that counter
+// (claim_base + the counter's value) halfway through this one (into the
+// shared word `next_claim`; `units` and beyond: none left) and pulls that
+// unit's tiles into L2.  `mid_signal`, if
+// set, is raised (a shared word) at the same point, once the unit's operands
+// are built.  If `publish` is set, the group's previous record is published
+// there (release, once its bulk stores are complete) as soon as this unit's
+// gate tile has arrived.  Returns false after recording a timeout in the
+// status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
                              uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish, const PrepGroup &grp,
-                             PrepShared &sh) {
+                             PrepShared &sh, int32_t *claim_counter = nullptr, int claim_base = 0,
+                             int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
     float *s_half = sh.half, *s_mid = sh.mid, *s_invk = sh.invk, *s_invq = sh.invq;
     float(*s_lo)[kD] = sh.lo;
@@ -382,11 +389,6 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         tc::tma_load_3d(sm + PrepSmem::X + 24576, p.tm_q, 64, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V, p.tm_v, 0, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::V + 8192, p.tm_v, 64, h, t0, &bars->load);
-        if (publish) {  // the previous record, once its bulk stores are complete (they overlap these loads)
-            tc::bulk_wait_all();
-            tc::fence_proxy_async_global();
-            tc::st_release_gpu(publish, 1);
-        }
     }
     if (tid < kL) s_beta[tid] = tid < Lc ? p.beta[(size_t)(t0 + tid) * H + h] : 0.f;
     tc::tc_fence_before();
@@ -396,6 +398,13 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     const int trow = (warp & 3) * 32 + lane;  // this thread's TMEM lane
     const int hs = warp >> 2;                 // this warp's half of an accumulator's columns
     if (!tc::mbar_wait(&bars->g, ph)) s_abort = 1;
+    if (publish && tid == 0) {
+        // the previous record, once its bulk stores are complete: they were issued when that unit ended and
+        // this unit's loads and gate tile have come in since, so the wait is short
+        tc::bulk_wait_all();
+        tc::fence_proxy_async_global();
+        tc::st_release_gpu(publish, 1);
+    }
     grp.sync();
     if (s_abort) {  // a lost TMA completion: report and leave without touching the record
         if (tid == 0) flag_timeout(ws);
@@ -571,6 +580,9 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     tc::tc_fence_before();
     grp.sync();
     tc::tc_fence_after();
+    if (mid_signal && tid == 0) *reinterpret_cast<volatile int *>(mid_signal) = 1;
+    constexpr int kClaimer = 64;  // a thread of warp 2: neither issuer waits for the atomic
+    if (claim_counter && tid == kClaimer) *next_claim = claim_base + atomicAdd(claim_counter, 1);
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
     bool ok = true;
@@ -660,6 +672,20 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     if (s_abort) {
         if (tid == 0) flag_timeout(ws);
         return false;
+    }
+    if (claim_counter && tid == 0) {  // the unit claimed at the operand barrier: its tiles into L2
+        const int un = *next_claim;
+        int ndoc, nt0, nLc;
+        if (un < units && locate_slot(doc_slot0, p.cu, p.num_seqs, kL, un / H, &ndoc, &nt0, &nLc)) {
+            const int nhh = un % H;
+            tc::tma_prefetch_3d(p.tm_g, 0, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_k, 0, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_k, 64, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_q, 0, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_q, 64, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_v, 0, nhh, nt0);
+            tc::tma_prefetch_3d(p.tm_v, 64, nhh, nt0);
+        }
     }
 
     // triangular solve in fp32, then T diag(beta) as the bf16 round-2 B operand (K-major [r][s])
@@ -847,7 +873,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     tc::grid_dep_wait();    // the chunk index kernel's slot table
     tc::grid_dep_launch();  // the state pass may get ready once every CTA of this grid has started
-    int doc, t0, Lc;
+    int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
     if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
     if (tid == 0) {
         prep_bars_init(&bars);
@@ -876,13 +902,14 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
 // A chain is one (document, head, TN-column tile of S), TN = 32 or 64, run by one CTA sequentially over the
-// document's chunks.  Its shared memory: kNBuf record buffers (M' and gamma, then the chain's Bc tile(s)) and a
-// ring of kNSb bf16 images of S^T (the B operand of M' S).
-template <int TN>
+// document's chunks.  Its shared memory: NB record buffers (M', gamma and Kend, then the chain's rows of Ut^T)
+// and a ring of NS bf16 images of S^T (the B operand of M' S).
+template <int TN, int NB = 3, int NS = (TN == 32 ? 5 : 3)>
 struct ChainCfg {
     static_assert(TN == 32 || TN == 64, "column tile of a chain");
-    static constexpr int kNBuf = 3;                            // records in flight
-    static constexpr int kNSb = TN == 32 ? 5 : 3;              // images: multiplied, being written, awaiting copy
+    static_assert(NB >= 2 && NS >= 3, "a record ahead of the one in use; images multiplied, written, copied");
+    static constexpr int kNBuf = NB;                           // records in flight
+    static constexpr int kNSb = NS;                            // images: multiplied, being written, awaiting copy
     static constexpr uint32_t Mc = 0, gam = 32768, Kend = 33792, Ut = 50176;
     static constexpr uint32_t kUt = (uint32_t)TN * 128;        // the chain's rows of Ut^T: 4 / 8 KB
     static constexpr uint32_t kBuf = Ut + kUt;                 // a multiple of 1 KB (operand alignment)
@@ -966,14 +993,13 @@ struct ChainLinks {
     bool loader = true;
 };
 
-// Chain j by a CTA of at least kStateThreads threads over `smem_raw` (ChainCfg<TN>); threads beyond
-// kStateThreads take part in the CTA barriers only.
-template <int TN>
+// Chain j by the first kStateThreads threads of a CTA over `smem_raw` (Cfg, a ChainCfg<TN, ...>); the CTA's
+// other threads (if any) take part in its CTA barriers only.
+template <int TN, typename Cfg = ChainCfg<TN>>
 __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                             float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off,
                             size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw,
                             const ChainLinks &links) {
-    using Cfg = ChainCfg<TN>;
     constexpr int NB = Cfg::kNBuf, NS = Cfg::kNSb, NC = Cfg::kCols, NT = kD / TN;
     __shared__ uint64_t full_bar[NB], empty_bar[NB], a_bar, img_full[NS], img_free[NS];
     __shared__ uint32_t tmem_base;
@@ -1440,7 +1466,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
     const int tid = threadIdx.x, warp = tid >> 5;
     const int slot = blockIdx.x, h = blockIdx.y;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
-    int doc, t0, Lc;
+    int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
     if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
     if (tid == 0) {
         tc::mbar_init(&bars.load, 1);
@@ -1508,6 +1534,9 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     const int g = tid >> 7;  // output group; threads of groups >= kGroups only take part in setup and teardown
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int units = doc_slot0[num_seqs] * H;
+    // records the workspace holds (from cu_seqlens, as the host sized it): a prefetch never leaves them, even
+    // where a corrupted chunk table (bounds-checking build) claims more units
+    const int rec_units = max_chunk_slots(cu, num_seqs, kL) * H;
     const int workers = ((int)gridDim.x - n_state) * kGroups;
     if (tid == 0) {
         for (int b = 0; b < kGroups; ++b) {
@@ -1535,14 +1564,14 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 s_unit[g] = u;
                 // the unit some group will take one round later: its Qp, P, Ut into L2 meanwhile
                 const int un = u + workers;
-                if (un < units)
+                if (un < units && un < rec_units)
                     tc::bulk_prefetch_l2(ws + records_off + (size_t)un * record_bytes + tc_record().Qp, OutSmem::S);
             }
             grp.sync();
             const int u = s_unit[g];
             if (u >= units) break;
             const int slot = u / H, h = u % H;
-            int doc, t0, Lc;
+            int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
             locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
             if (!output_unit(cu, num_seqs, H, o, ws, records_off, record_bytes, slot, h, t0, Lc, gsm, &bars[g], k & 1u, tmem,
                              grp, onorm, false, sdone + u, flag_wait_ns))
@@ -1559,65 +1588,85 @@ constexpr int kChainMinWorkers = 48;  // output CTAs alongside the chains, at le
 // ---------------------------------------------------------------------------
 // Pipe plan: preparation, state chains and outputs in one cooperative launch
 // ---------------------------------------------------------------------------
-// One CTA of kPipeThreads per SM.  CTAs [0, n_chain) each run one chain of 64 columns (state_chain<64>), which
-// loads each chunk's record as soon as its publication flag is raised and publishes each chunk's state image;
-// every other CTA holds two groups of 256 threads that take work from one counter: first the preparation
-// units in chunk-slot order (each publishes its record with a GPU-scope release once its bulk stores are
-// complete), then the output units in the same order (each waits for its record and for its chunk's state
-// image).  So the chains run on whole SMs while later chunks are still being prepared, and the chains' work
-// leaves the preparation's critical path.
+// One CTA of kPipeThreads per SM.
+//   CTAs [0, n_chain): one chain each (state_chain, 32 or 64 columns), which loads each chunk's record as
+//     soon as its publication flag is raised and publishes each chunk's state image.
+//   Every other CTA: two groups of 256 threads that take the preparation units in (chunk slot, head) order
+//     (each publishes its record with a GPU-scope release once its bulk stores are complete) and, when none
+//     is left, output units from the output counter.  Group 1 starts half a unit after group 0, so that the
+//     two groups' heavy phases and waits alternate instead of coinciding.
+// So the preparation has all but the chains' SMs to itself, the chains start with the first chunk's records
+// and follow the preparation, and the outputs are formed behind the chains.  Chains of 64 columns take half
+// the SMs that chains of 32 would, at a longer step (a wider epilogue); they are used once the narrow ones
+// would take more than kPipeChain32Max SMs.
 //
 // Progress: every CTA is resident (cooperative launch).  A preparation waits for nothing but its own copies
-// and MMAs; a chain waits only for records, all of which belong to preparation units claimed before any
-// output unit; an output unit waits for a record and for the chains.  Every wait is bounded.
+// and MMAs, and a worker group publishes its last record before it takes any output unit; a chain waits only
+// for records; an output unit waits for a record and for the chains.  Every wait is bounded.
 constexpr int kPipeThreads = 512;
-constexpr int kPipeChainMax = 32;   // automatic choice: at most this many chains of 32 columns
+constexpr int kPipeChainMax = 40;    // automatic choice: at most this many chains of 64 columns ...
+constexpr int kPipeChain32Max = 32;  // ... and chains of 32 columns (a shorter step) up to this many of them
+constexpr uint32_t kPipePrepShared = 2 * PrepSmem::bytes;  // the worker groups' PrepShared, after their tiles
 template <int TN>
 constexpr size_t pipe_smem_bytes() {
-    return (ChainCfg<TN>::bytes > 2 * PrepSmem::bytes ? ChainCfg<TN>::bytes : 2 * PrepSmem::bytes) + 1024;
+    using PipeChainCfg = ChainCfg<TN>;
+    return (PipeChainCfg::bytes > kPipePrepShared + 2 * sizeof(PrepShared) ? PipeChainCfg::bytes
+                                                                          : kPipePrepShared + 2 * sizeof(PrepShared)) +
+           1024;
 }
 static_assert(PrepSmem::bytes % 1024 == 0 && OutSmem::bytes <= PrepSmem::bytes, "a group's region holds a unit");
-
-// Work item w of the pipe workers -> (output?, slot, head): the preparations of the first `lag` chunk slots,
-// then alternately one slot's preparations and the outputs of the slot `lag` earlier, then the last outputs.
-__device__ __forceinline__ void pipe_item(int w, int C, int H, int lag, bool *out, int *slot, int *h) {
-    const int D = min(lag, C);
-    const int lead = D * H, mid = (C - D) * 2 * H;
-    if (w < lead) {
-        *out = false; *slot = w / H; *h = w % H;
-    } else if (w < lead + mid) {
-        const int q = w - lead, b = q / (2 * H), r = q % (2 * H);
-        *out = r >= H; *slot = r < H ? D + b : b; *h = r < H ? r : r - H;
-    } else {
-        const int q = w - lead - mid;
-        *out = true; *slot = C - D + q / H; *h = q % H;
-    }
-}
 
 struct PipeArgs {
     const float *S0;
     float *S_final;
     __nv_bfloat16 *o;
-    int32_t *ready;    // [slot * H + h]: the record is published
-    int32_t *sdone;    // [slot * H + h]: columns (in 32s) whose state image is published
-    int32_t *counter;  // next work item
-    int n_chain, lag;
+    int32_t *ready;         // [slot * H + h]: the record is published
+    int32_t *sdone;         // [slot * H + h]: columns (in 32s) whose state image is published
+    int32_t *prep_counter;  // next preparation unit
+    int32_t *out_counter;   // next output unit
+    int n_chain;
     unsigned long long flag_wait_ns;
     int fault;  // kFaultNoPublish only in tests of the timeout path
     OutNorm onorm;
 };
 
+// Output units taken in (chunk slot, head) order from the output counter by one group of 128 threads, until
+// none is left or a wait gives up (false).  `s_unit` is a shared word of the group.
+__device__ bool pipe_outputs(const PrepParams &pp, const PipeArgs &a, uint8_t *gsm, OutBars *bars, uint32_t tmem,
+                             const OutGroup &og, int *s_unit) {
+    const int H = pp.H;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
+    const int units = doc_slot0[pp.num_seqs] * H;
+    // claimed one ahead by a thread of warp 2, which does not issue the unit's copies and MMAs nor write o
+    constexpr int kClaimer = 64;
+    if (og.gtid == kClaimer) *s_unit = atomicAdd(a.out_counter, 1);
+    for (uint32_t nout = 0;; ++nout) {
+        og.sync();
+        const int u = *s_unit;
+        og.sync();  // every thread has read s_unit before the next claim overwrites it
+        if (u >= units) return true;
+        if (og.gtid == kClaimer) *s_unit = atomicAdd(a.out_counter, 1);
+        const int slot = u / H, h = u % H;
+        int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
+        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+        if (!output_unit(pp.cu, pp.num_seqs, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
+                         bars, nout & 1u, tmem, og, a.onorm, false, a.sdone + (size_t)slot * H + h, a.flag_wait_ns,
+                         a.ready + (size_t)slot * H + h))
+            return false;
+    }
+}
+
 __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm) {
     __shared__ PrepBars pbars[2];
     __shared__ OutBars obars[2];
-    __shared__ PrepShared psh[2];
     __shared__ uint32_t tmem_base;
-    __shared__ int s_unit[2], s_ok[2];
-    const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255, gwarp = gtid >> 5;
+    PrepShared *psh = reinterpret_cast<PrepShared *>(sm + kPipePrepShared);
+    __shared__ int s_unit[2], s_ok[2], s_go;
+    const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255;
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
-    const int C = doc_slot0[pp.num_seqs];
-    const int units = C * H;  // preparation units, and as many output units
+    const int units = doc_slot0[pp.num_seqs] * H;  // preparation units, and as many output units
+    if (tid == 0) s_go = 0;
     if (gtid == 0) {
         prep_bars_init(&pbars[g]);
         tc::mbar_init(&obars[g].load, 1);
@@ -1635,61 +1684,52 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     const PrepGroup grp{gtid, 1u + (uint32_t)g};
     uint8_t *gsm = sm + (uint32_t)g * PrepSmem::bytes;
     const uint32_t tmem = tmem_base + 256u * (uint32_t)g;
-    uint32_t nprep = 0, nout = 0;
+    uint32_t nprep = 0;
+    bool ok = true;
     int32_t *pending = nullptr;  // the last record this group prepared, not yet published
-    // items are claimed one ahead, so that a preparation can pull the next one's input tiles into L2
-    if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);
+    // preparations, claimed one ahead, so that a preparation can pull the next one's input tiles into L2; the
+    // claim is made by a thread of warp 2, whose wait for the atomic overlaps the unit's first loads (the
+    // group's first thread issues them)
+    if (g == 1) {
+        // The two groups run equal units; started together they would stay in phase, and their heavy phases
+        // (operand build, solve, epilogues) and their waits would coincide.  Group 1 starts once group 0's
+        // first unit has built its operands (about half a unit), so that one group's waits overlap the other's
+        // arithmetic (bounded: group 0 raises the flag on any way out of its loop as well).
+        if (gtid == 0) {
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (*reinterpret_cast<volatile int *>(&s_go) == 0 && tc::globaltimer_ns() - t0 < 10000000ull)
+                __nanosleep(64);
+        }
+        grp.sync();
+    }
+    // Units are taken in the order the groups start them: the first 2 W (W worker CTAs) by position, group 0s
+    // before group 1s; each later one is claimed from the counter halfway through the group's current unit
+    // (which also pulls its tiles into L2).
+    const int nw = (int)gridDim.x - a.n_chain, wid = (int)blockIdx.x - a.n_chain;
+    if (gtid == 0) s_unit[g] = g * nw + wid;
     for (;;) {
         grp.sync();
         const int u = s_unit[g];
         grp.sync();  // every thread has read s_unit before the next claim overwrites it
-        if (u >= 2 * units) break;
-        if (gtid == 0) s_unit[g] = atomicAdd(a.counter, 1);  // the next item (read after the next barrier)
-        bool is_out;
-        int slot, h, doc, t0, Lc;
-        pipe_item(u, C, H, a.lag, &is_out, &slot, &h);
-        if (!is_out) {
-            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
-            int nslot = -1, nh = 0;
-            if (gtid == 0) {  // only thread 0 issues the prefetch; it alone has claimed the next item
-                const int un = s_unit[g];
-                bool n_out;
-                if (un < 2 * units) {
-                    pipe_item(un, C, H, a.lag, &n_out, &nslot, &nh);
-                    if (n_out) nslot = -1;
-                }
-            }
-            // the previous record is published once this unit's loads are issued; this one's stays pending
-            const bool ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, nslot, nh, pending,
-                                         grp, psh[g]);
-            ++nprep;
-            if (!ok) break;
-            pending = a.ready + (size_t)slot * H + h;
-        } else {
-            if (gtid == 0 && pending) {
-                tc::bulk_wait_all();
-                tc::fence_proxy_async_global();
-                tc::st_release_gpu(pending, 1);
-            }
-            pending = nullptr;
-            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
-            bool ok = true;
-            if (gtid < 128) {
-                ok = output_unit(pp.cu, pp.num_seqs, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
-                                 &obars[g], nout & 1u, tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, a.onorm,
-                                 false, a.sdone + (size_t)slot * H + h, a.flag_wait_ns,
-                                 a.ready + (size_t)slot * H + h);
-            }
-            ++nout;
-            grp.sync();
-            if (!s_ok[g]) break;
-        }
+        if (u >= units) break;
+        const int slot = u / H, h = u % H;
+        int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
+        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+        // the previous record is published once this unit's gate tile has arrived; this one's stays pending
+        ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, -1, 0, pending, grp, psh[g],
+                          a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr);
+        ++nprep;
+        if (!ok) break;
+        pending = a.ready + (size_t)slot * H + h;
     }
-    if (gtid == 0 && pending) {
+    if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
+    if (gtid == 0 && pending) {  // before any output unit: a chain may be waiting for this record
         tc::bulk_wait_all();
         tc::fence_proxy_async_global();
         tc::st_release_gpu(pending, 1);
     }
+    if (ok && gtid < 128)
+        pipe_outputs(pp, a, gsm, &obars[g], tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, &s_unit[g]);
     tc::tc_fence_before();
     __syncthreads();
     if (tid < 32) tc::tmem_dealloc(tmem_base, 512);
@@ -1706,19 +1746,19 @@ prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc::grid_dep_wait();  // the chunk index kernel: slot table, status word, cleared flags
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
-    if ((int)blockIdx.x < a.n_chain) {
-        ChainLinks links;
-        links.sdone = a.sdone;
-        links.publish = a.fault != kFaultNoPublish;
-        links.ready = a.ready;
-        links.flag_wait_ns = a.flag_wait_ns;
-        state_chain<TN>(cu, num_seqs, H, a.S0, a.S_final, ws, doc_slot0_off, records_off, record_bytes,
-                        (int)blockIdx.x, sm, links);
-        return;
-    }
     const PrepParams pp{&tm_q,       &tm_k,        &tm_v,   &tm_g,  beta, cu, num_seqs, H, ws, doc_slot0_off,
                         records_off, record_bytes, qk_norm, qk_eps};
-    pipe_worker(pp, a, sm);
+    if ((int)blockIdx.x >= a.n_chain) {
+        pipe_worker(pp, a, sm);
+        return;
+    }
+    ChainLinks links;
+    links.sdone = a.sdone;
+    links.publish = a.fault != kFaultNoPublish;
+    links.ready = a.ready;
+    links.flag_wait_ns = a.flag_wait_ns;
+    state_chain<TN>(cu, num_seqs, H, a.S0, a.S_final, ws, doc_slot0_off, records_off, record_bytes,
+                                  (int)blockIdx.x, sm, links);
 }
 
 
@@ -1868,6 +1908,9 @@ const DeviceSetup &device_setup() {
         if (!e)
             e = cudaFuncSetAttribute(prefill_pipe_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)pipe_smem_bytes<32>());
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_pipe_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)pipe_smem_bytes<64>());
 
         if (!e) {
             cudaFuncSetAttribute(prefill_prepare_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1931,12 +1974,12 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     if (forced == TC_THREE) return TC_THREE;
     const DeviceSetup &d = device_setup();
     if (d.err) return TC_THREE;
-    const long long chains32 = (long long)num_seqs * H * kNTile;
-    const bool pipe_fits = chains32 + 2 * kChainMinWorkers / 3 <= d.sms;
+    const long long chains32 = (long long)num_seqs * H * kNTile, chains64 = chains32 / 2;
+    const bool pipe_fits = chains64 + kChainMinWorkers <= d.sms;
     const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
     if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
     if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
-    if (pipe_fits && chains32 <= kPipeChainMax) return TC_PIPE;
+    if (pipe_fits && chains64 <= kPipeChainMax) return TC_PIPE;
     return chain_fits ? TC_CHAIN : TC_THREE;
 }
 
@@ -1955,7 +1998,6 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const long long wait = g_test_wait_ns.load();
     const unsigned long long flag_wait = wait > 0 ? (unsigned long long)wait : kFlagWaitNs;
     if (plan == TC_PIPE) {
-        constexpr int tn = 32;
         InputMaps m;
         if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
         PipeArgs a;
@@ -1964,17 +2006,25 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         a.o = static_cast<__nv_bfloat16 *>(o);
         a.ready = flags;
         a.sdone = flags + nflag;
-        a.counter = flags + 2 * nflag;
-        a.n_chain = num_seqs * H * (kD / tn);
-        // outputs trail their preparations by about the chunk slots the worker groups hold at once
-        a.lag = 2 * (dset.sms - a.n_chain) / H + 4;
+        a.prep_counter = flags + 2 * nflag;
+        a.out_counter = flags + 2 * nflag + 1;
+        a.n_chain = num_seqs * H * (kD / 64);
         a.flag_wait_ns = flag_wait;
         a.fault = g_test_fault.load();
         a.onorm = onorm;
         marks.before(st, "prefill_pipe_tc");
-        e = launch_cooperative(prefill_pipe_tc<tn>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
-                               pipe_smem_bytes<tn>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
-                               lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
+        // chains of 32 columns while they are few (a shorter step), else of 64 (half the SMs)
+        const long long chains32 = (long long)num_seqs * H * kNTile;
+        if (chains32 <= kPipeChain32Max) {
+            a.n_chain = (int)chains32;
+            e = launch_cooperative(prefill_pipe_tc<32>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
+                                   pipe_smem_bytes<32>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                                   lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
+        } else {
+            e = launch_cooperative(prefill_pipe_tc<64>, dim3((unsigned)dset.sms), dim3(kPipeThreads),
+                                   pipe_smem_bytes<64>(), st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
+                                   lay.doc_slot0_off, lay.records_off, lay.record_bytes, fu.qk_norm, fu.qk_eps, a);
+        }
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the three
         // kernels instead.

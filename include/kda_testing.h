@@ -25,7 +25,7 @@ extern "C" {
 #define KDA_TESTING_PLAN_THREE 0    /* preparation, state pass and output pass as three kernels */
 #define KDA_TESTING_PLAN_CHAIN 2    /* preparation, then one cooperative launch of the state chains with the
                                        output units alongside; falls back to THREE where it cannot run */
-#define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains of 32 columns beside groups that
+#define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains (32 or 64 columns) beside groups that
                                        prepare the records in chunk order and form the outputs behind the
                                        chains; falls back to THREE where it cannot run */
 

@@ -5,7 +5,8 @@ as three kernels (preparation, state pass, output); as the preparation
 followed by one cooperative launch running the state chains with the output
 units alongside (chain); or as one cooperative launch in which chains of 64
 columns run beside groups that prepare the records in chunk order and then
-form the outputs (pipe); the test hook kda_testing_set_plan forces a plan.
+form the outputs (pipe: chains of 32 columns while there are at most 32 of them, else of 64); the test hook
+kda_testing_set_plan forces a plan.
 All perform the same arithmetic in the same order, so their results must be
 bitwise identical, and they must meet the bf16 tolerance against the fp64
 oracle.
@@ -154,13 +155,14 @@ def test_chain_plan_at_its_worker_threshold(extra_heads):
     assert rel(S_a, S_ref) <= TOL[torch.bfloat16], rel(S_a, S_ref)
 
 
-@pytest.mark.parametrize("extra_heads", [0, 1])
-def test_pipe_plan_at_its_threshold(extra_heads):
-    """One document with 8 heads (32 chains of 32 columns, the most the automatic pipe plan takes) and with 9
-    heads (the chain plan then): the automatic choice is the expected plan, matches the three-kernel plan bit
-    for bit and meets the bf16 tolerance against the oracle."""
-    H = 8 + extra_heads
-    inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=97 + extra_heads, s0_std=0.1)
+@pytest.mark.parametrize("H", [8, 9, 20, 21])
+def test_pipe_plan_at_its_thresholds(H):
+    """One document with 8 heads (the most whose chains run 32 columns wide in the pipe plan) and 9 (64 wide),
+    with 20 heads (40 chains of 64 columns, the most the automatic pipe plan takes) and with 21 heads (the chain
+    plan then): the automatic choice is the expected plan, matches the three-kernel plan bit for bit and meets
+    the bf16 tolerance against the oracle."""
+    extra_heads = 1 if H == 21 else 0
+    inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=97 + H, s0_std=0.1)
     names = _kernel_names(inp, inp.S0)
     assert ("prefill_pipe_tc" in names) == (extra_heads == 0), names
     o_a, S_a = _run(inp, "auto", inp.S0, poison=0x00)
