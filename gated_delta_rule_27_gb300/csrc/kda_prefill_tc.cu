@@ -902,12 +902,14 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // Kernel 2: sequential state pass
 // ---------------------------------------------------------------------------
 // A chain is one (document, head, TN-column tile of S), TN = 32 or 64, run by one CTA sequentially over the
-// document's chunks.  Its shared memory: NB record buffers (M', gamma and Kend, then the chain's rows of Ut^T)
-// and a ring of NS bf16 images of S^T (the B operand of M' S).
-template <int TN, int NB = 3, int NS = (TN == 32 ? 5 : 3)>
+// document's chunks.  Its shared memory: NB record buffers (M', gamma and Kend, then the chain's rows of Ut^T),
+// with FOLD (the chain also forms its columns of each chunk's output) a ring of two (Qp, P) images, and a ring
+// of NS bf16 images of S^T (the B operand of M' S).
+template <int TN, int NB = 3, int NS = (TN == 32 ? 5 : 3), bool FOLD = false>
 struct ChainCfg {
     static_assert(TN == 32 || TN == 64, "column tile of a chain");
     static_assert(NB >= 2 && NS >= 3, "a record ahead of the one in use; images multiplied, written, copied");
+    static constexpr bool kFold = FOLD;
     static constexpr int kNBuf = NB;                           // records in flight
     static constexpr int kNSb = NS;                            // images: multiplied, being written, awaiting copy
     static constexpr uint32_t Mc = 0, gam = 32768, Kend = 33792, Ut = 50176;
@@ -915,8 +917,10 @@ struct ChainCfg {
     static constexpr uint32_t kBuf = Ut + kUt;                 // a multiple of 1 KB (operand alignment)
     static constexpr uint32_t kPanel = (uint32_t)TN * 128;     // one 64-wide K panel of the image
     static constexpr uint32_t kImg = 2 * kPanel;
-    static constexpr uint32_t SB = kNBuf * kBuf;
-    static constexpr uint32_t bytes = SB + kNSb * kImg;
+    static constexpr uint32_t kQP = 24576;                     // Qp (16 KB) then P (8 KB), as in the record
+    static constexpr uint32_t QB = kNBuf * kBuf;               // the (Qp, P) ring (FOLD), placed before the images
+    static constexpr uint32_t SB = QB + (FOLD ? 2 * kQP : 0);  // (the 128-row operands' unused upper rows of
+    static constexpr uint32_t bytes = SB + kNSb * kImg;        //  the second Qp, P image fall on the images)
     static constexpr int kCols = TN / 2;                       // columns of S per epilogue thread
     static_assert(kBuf % 1024 == 0 && kImg % 1024 == 0, "1 KB aligned operands");
 };
@@ -932,12 +936,13 @@ __device__ __forceinline__ void issue_record(uint8_t *buf, const char *rec, int 
 }
 // The same parts of a later chunk's record pulled into L2 only (no shared memory, nothing to wait for), so that
 // its copy into a buffer, a few chunks later, is served from L2.
-template <int TN>
+template <int TN, bool FOLD = false>
 __device__ __forceinline__ void prefetch_record(const char *rec, int tile) {
     constexpr TcRecord R = tc_record();
     constexpr uint32_t kUt = ChainCfg<TN>::kUt;
     tc::bulk_prefetch_l2(rec, (uint32_t)R.state_part);
     tc::bulk_prefetch_l2(rec + R.Ut + (size_t)tile * kUt, kUt);
+    if (FOLD) tc::bulk_prefetch_l2(rec + R.Qp, ChainCfg<TN>::kQP);  // (Qp, P): one copy
 }
 constexpr int kChainL2Ahead = 3;  // records pulled into L2 this many chunks beyond the buffered ones
 
@@ -991,6 +996,7 @@ struct ChainLinks {
     // Records are streamed in by the loader warp (required with `ready`), else by the second MMA issuer right
     // behind its MMAs; which is faster depends on what else the launch runs (measured per plan).
     bool loader = true;
+    __nv_bfloat16 *o = nullptr;  // FOLD: where the chain writes its columns of each chunk's output
 };
 
 // Chain j by the first kStateThreads threads of a CTA over `smem_raw` (Cfg, a ChainCfg<TN, ...>); the CTA's
@@ -1001,7 +1007,11 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                             size_t records_off, size_t record_bytes, int j, uint8_t *smem_raw,
                             const ChainLinks &links) {
     constexpr int NB = Cfg::kNBuf, NS = Cfg::kNSb, NC = Cfg::kCols, NT = kD / TN;
+    constexpr bool FOLD = Cfg::kFold;
+    // TMEM columns: two regions of two K panels for the state update; with FOLD two output regions after them
+    constexpr uint32_t kTmemCols = FOLD ? (TN == 64 ? 512u : 256u) : 4u * TN;
     __shared__ uint64_t full_bar[NB], empty_bar[NB], a_bar, img_full[NS], img_free[NS];
+    __shared__ uint64_t q_full[2], q_empty[2], o_full[2], o_free[2];  // FOLD: the (Qp, P) ring, output regions
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
     // (the chunk index kernel's table and status word are complete: the kernel before this one waited for them
@@ -1041,12 +1051,20 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
         if (tid == 0) {
             for (int b = 0; b < NB; ++b) {
                 tc::mbar_init(&full_bar[b], 1);
-                tc::mbar_init(&empty_bar[b], kStateEpiWarps);  // one arrival per epilogue warp
+                // one arrival per epilogue warp (and, with FOLD, the output warps' once the chunk's output MMAs,
+                // which read the chain's rows of Ut^T, have completed)
+                tc::mbar_init(&empty_bar[b], kStateEpiWarps + (FOLD ? 1 : 0));
             }
             tc::mbar_init(&a_bar, 2);  // one commit from each issuer
             for (int b = 0; b < NS; ++b) {
                 tc::mbar_init(&img_full[b], kStateEpiWarps);  // one arrival per epilogue warp
-                tc::mbar_init(&img_free[b], 1);               // the publisher's
+                tc::mbar_init(&img_free[b], 1);               // the publisher's (FOLD: the output warps')
+            }
+            for (int b = 0; b < 2; ++b) {
+                tc::mbar_init(&q_full[b], 1);
+                tc::mbar_init(&q_empty[b], 1);
+                tc::mbar_init(&o_full[b], 1);
+                tc::mbar_init(&o_free[b], 2);  // both output warps
             }
             tc::fence_mbar_init();
             s_abort = 0;
@@ -1061,7 +1079,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             }
         }
         if (warp == 0) {
-            tc::tmem_alloc(&tmem_base, 4 * TN);  // two regions (chunks alternate) of two K panels
+            tc::tmem_alloc(&tmem_base, kTmemCols);
             tc::tmem_relinquish();
         }
         tc::tc_fence_before();
@@ -1089,14 +1107,25 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     if (!ok) break;
                     issue_record<TN>(sm + b * Cfg::kBuf, rec_h + (size_t)(first + c) * rec_stride, tile, &full_bar[b]);
                     issued = c + 1;
+                    if constexpr (FOLD) {  // the chunk's (Qp, P) into its ring slot, free once output c - 2 is done
+                        if (c >= 2) ok = tc::mbar_wait(&q_empty[c & 1], (uint32_t)(((c - 2) >> 1) & 1));
+                        if (!ok) break;
+                        tc::mbar_arrive_expect_tx(&q_full[c & 1], Cfg::kQP);
+                        tc::bulk_g2s(sm + Cfg::QB + (uint32_t)(c & 1) * Cfg::kQP,
+                                     rec_h + (size_t)(first + c) * rec_stride + R.Qp, Cfg::kQP, &q_full[c & 1]);
+                    }
                     // a later record that is already published goes to L2 ahead of its copy
                     const int cp = c + kChainL2Ahead;
                     if (!links.ready && cp < nchunks)
-                        prefetch_record<TN>(rec_h + (size_t)(first + cp) * rec_stride, tile);
+                        prefetch_record<TN, FOLD>(rec_h + (size_t)(first + cp) * rec_stride, tile);
                 }
                 if (!ok) {  // copies already on their way land before the CTA's shared memory can go away
                     for (int c = max(0, issued - NB); c < issued; ++c)
                         tc::mbar_wait(&full_bar[c % NB], (uint32_t)((c / NB) & 1), 10000000ull);
+                    if constexpr (FOLD) {
+                        for (int c = max(0, issued - 2); c < issued; ++c)
+                            tc::mbar_wait(&q_full[c & 1], (uint32_t)((c >> 1) & 1), 10000000ull);
+                    }
                 }
             }
             __syncwarp();
@@ -1149,6 +1178,79 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     }
                 }
                 __syncwarp();
+            }
+        } else if (FOLD && warp == kStatePubWarp) {
+            // The chunk's output columns of this chain, O[:, tile] = P Ut[:, tile] + Qp S_c[:, tile], from the
+            // image S_c the chain multiplies and its own rows of Ut^T: one 128-lane accumulator whose lanes 0-63
+            // are the chunk's tokens (the operands' upper 64 rows fall on neighbouring images, unread).
+            if (lane == 0) {
+                constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
+                constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
+                constexpr uint32_t idK = tc::idesc_bf16_f32(128, TN, false, false);
+                constexpr uint32_t idMN = tc::idesc_bf16_f32(128, TN, true, false);
+                for (int c = 0; c < nchunks; ++c) {
+                    const int sl = c % NS, qs = c & 1, bsel = c % NB;
+                    if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / NS) & 1));
+                    ok = ok && tc::mbar_wait(&full_bar[bsel], (uint32_t)((c / NB) & 1));
+                    ok = ok && tc::mbar_wait(&q_full[qs], (uint32_t)((c >> 1) & 1));
+                    if (c >= 2) ok = ok && tc::mbar_wait(&o_free[qs], (uint32_t)(((c - 2) >> 1) & 1));
+                    if (ok) {
+                        tc::tc_fence_after();
+                        const uint8_t *qb = sm + Cfg::QB + (uint32_t)qs * Cfg::kQP;
+                        const uint8_t *buf = sm + bsel * Cfg::kBuf;
+                        const uint8_t *sbc = sm + Cfg::SB + (uint32_t)sl * Cfg::kImg;
+                        const uint32_t d = tmem + 4u * TN + (uint32_t)(TN * qs);
+                        for (int s4 = 0; s4 < 4; ++s4)  // P Ut over the chunk's tokens
+                            tc::mma_bf16(d, tc::smem_desc(kKmaj, tc::smem_u32(qb + 16384 + s4 * 32)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(buf + Cfg::Ut + s4 * 32)), idK, s4 > 0);
+                        for (int s8 = 0; s8 < 8; ++s8)  // + Qp S_c over d_k
+                            tc::mma_bf16(d, tc::smem_desc(kQpMn, tc::smem_u32(qb + s8 * 2048)),
+                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + (s8 >> 2) * Cfg::kPanel + (s8 & 3) * 32)),
+                                         idMN, true);
+                    }
+                    tc::mma_commit(&o_full[qs]);  // always: the output warps count on one completion per chunk
+                }
+            }
+            __syncwarp();
+        } else if (FOLD && warp >= kStateThreads / 32) {
+            // Output warps (TMEM lane quarters 0 and 1: the chunk's 64 tokens): each chunk's output columns of
+            // this chain, read once its MMAs complete, which also frees the image, the (Qp, P) slot and the
+            // record buffer they read.
+            const int ow = warp - kStateThreads / 32, r = ow * 32 + lane;
+            const uint32_t lane_base = (uint32_t)(ow * 32) << 16;
+            const int doc_t0 = cu[n], doc_t1 = cu[n + 1];
+            for (int c = 0; c < nchunks; ++c) {
+                const int qs = c & 1;
+                ok = ok && tc::mbar_wait(&o_full[qs], (uint32_t)((c >> 1) & 1));
+                tc::tc_fence_after();
+                if (ow == 0 && lane == 0) {
+                    tc::mbar_arrive(&img_free[c % NS]);
+                    tc::mbar_arrive(&q_empty[qs]);
+                    tc::mbar_arrive(&empty_bar[c % NB]);
+                }
+                float v[TN];
+                if (warp_all(ok)) {
+                    const uint32_t ta = tmem + lane_base + 4u * TN + (uint32_t)(TN * qs);
+                    if constexpr (TN == 32) {
+                        tc::tmem_ld32(ta, v);
+                    } else {
+                        float v1[32];
+                        tc::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(v));
+                        tc::tmem_ld32(ta + 32u, v1);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[32 + q] = v1[q];
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&o_free[qs]);  // always: the issuer counts on both warps
+                if (!warp_all(ok)) break;
+                const int t0 = doc_t0 + c * kL, Lc = min(kL, doc_t1 - t0);
+                if (r < Lc && KDA_IN_BOUNDS(t0 + r < cu[num_seqs], reinterpret_cast<int32_t *>(ws))) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(links.o + ((size_t)(t0 + r) * H + h) * kD + tile * TN);
+#pragma unroll
+                    for (int u = 0; u < TN / 8; ++u) dst[u] = pack8_at(v + 8 * u);
+                }
             }
         } else if (warp == kStatePubWarp) {
             if (lane == 0) {
@@ -1246,7 +1348,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 }
             }
         }
-        if (warp == 0) tc::tmem_dealloc(tmem, 4 * TN);
+        if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
         if (s_abort) return;
     }
     if (S_final && epi) {
@@ -1264,6 +1366,25 @@ prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
     extern __shared__ uint8_t smem_raw[];
     state_chain<TN>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
                     smem_raw, ChainLinks{});
+}
+
+// The state pass with each chain also forming its columns of every chunk's output (no output pass, no state
+// images in the records): the three-kernel plan's second kernel when the gated output normalisation (which
+// needs whole rows) is not fused.  Two record buffers, the (Qp, P) ring and two more warps, the output warps.
+constexpr int kFoldThreads = kStateThreads + 64;
+template <int TN>
+using FoldCfg = ChainCfg<TN, 2, (TN == 32 ? 5 : 3), true>;
+
+template <int TN>
+__global__ void __launch_bounds__(kFoldThreads, 1)
+prefill_state_fold_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
+                      float *__restrict__ S_final, __nv_bfloat16 *__restrict__ o, char *__restrict__ ws,
+                      size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+    extern __shared__ uint8_t smem_raw[];
+    ChainLinks links;
+    links.o = o;
+    state_chain<TN, FoldCfg<TN>>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes,
+                                 (int)blockIdx.x, smem_raw, links);
 }
 
 // ---------------------------------------------------------------------------
@@ -1877,6 +1998,8 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
 constexpr int kPrepSmem = PrepSmem::bytes + 1024;
 constexpr int kStateSmem = ChainCfg<32>::bytes + 1024;
 constexpr int kStateSmem64 = ChainCfg<64>::bytes + 1024;
+constexpr int kFoldSmem32 = FoldCfg<32>::bytes + 1024;
+constexpr int kFoldSmem64 = FoldCfg<64>::bytes + 1024;
 constexpr int kOutSmem = OutSmem::bytes + 1024;
 
 // Per-device facts the launches need, worked out (and the kernels' shared-memory limits raised) once per
@@ -1904,6 +2027,12 @@ const DeviceSetup &device_setup() {
         if (!e)
             e = cudaFuncSetAttribute(prefill_state_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem64);
         if (!e) e = cudaFuncSetAttribute(prefill_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_state_fold_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kFoldSmem32);
+        if (!e)
+            e = cudaFuncSetAttribute(prefill_state_fold_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kFoldSmem64);
         if (!e) e = cudaFuncSetAttribute(prefill_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
         if (!e)
             e = cudaFuncSetAttribute(prefill_pipe_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1964,10 +2093,14 @@ void testing_set_fault(int fault, long long wait_ns) {
 }
 int testing_fault() { return g_test_fault.load(); }
 
-TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
-    // Few chains: the pipe plan (at most kPipeChainMax chains of 64 columns); then the chain plan while the
-    // chains of 32 columns leave at least kChainMinWorkers SMs for the output groups; else three kernels.  A
-    // plan forced by the test hook is taken wherever it can run.
+TcPlan tc_plan(int num_seqs, int H, int total_tokens, bool gated) {
+    // Without the gated output normalisation: the pipe plan for at most kPipeChainMax chains of 64 columns,
+    // else the preparation and the state pass that forms the outputs itself (two kernels).  With it (whole
+    // rows needed per output): the chain plan while the chains of 32 columns leave at least kChainMinWorkers
+    // SMs for the output groups, else preparation, state pass and output pass.  Measured on one document of
+    // 4096 tokens: 16 heads pipe 103 us, chain 130, two kernels 134; 24 heads two kernels 164, chain 172,
+    // pipe 169; with the gated norm at 16 heads chain 136, pipe 141.  A plan forced by the test hook is taken
+    // wherever it can run.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int forced = g_test_plan.load();
@@ -1979,8 +2112,8 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
     if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
     if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
-    if (pipe_fits && chains64 <= kPipeChainMax) return TC_PIPE;
-    return chain_fits ? TC_CHAIN : TC_THREE;
+    if (gated) return chain_fits ? TC_CHAIN : TC_THREE;
+    return pipe_fits && chains64 <= kPipeChainMax ? TC_PIPE : TC_THREE;
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g, const float *beta,
@@ -2059,6 +2192,17 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     // Chains of 32 columns while they fit on the SMs at once, else of 64 (half as many: fewer waves of chains)
     const size_t chains32 = (size_t)num_seqs * H * kNTile;
+    if (!onorm.gate) {  // the chains form the outputs themselves: no output pass
+        marks.before(st, "prefill_state_fold_tc");
+        if (chains32 <= (size_t)dset.sms)
+            return launch_dependent(prefill_state_fold_tc<32>, dim3((unsigned)chains32), dim3(kFoldThreads),
+                                    (size_t)kFoldSmem32, st, cu, num_seqs, H, S0, S_final,
+                                    static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,
+                                    lay.record_bytes);
+        return launch_dependent(prefill_state_fold_tc<64>, dim3((unsigned)(chains32 / 2)), dim3(kFoldThreads),
+                                (size_t)kFoldSmem64, st, cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o),
+                                w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
+    }
     marks.before(st, "prefill_state_tc");
     if (chains32 <= (size_t)dset.sms)
         e = launch_dependent(prefill_state_tc<32>, dim3((unsigned)chains32), dim3(kStateThreads), (size_t)kStateSmem,

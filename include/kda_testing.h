@@ -22,7 +22,8 @@ extern "C" {
 
 /* Launch plans of the tensor-core prefill (bf16, d = 128, chunk 64). */
 #define KDA_TESTING_PLAN_AUTO (-1)  /* the library chooses (the default) */
-#define KDA_TESTING_PLAN_THREE 0    /* preparation, state pass and output pass as three kernels */
+#define KDA_TESTING_PLAN_THREE 0    /* preparation, then the state pass, which also forms the outputs (with the
+                                       gated output normalisation fused: state pass, then output pass) */
 #define KDA_TESTING_PLAN_CHAIN 2    /* preparation, then one cooperative launch of the state chains with the
                                        output units alongside; falls back to THREE where it cannot run */
 #define KDA_TESTING_PLAN_PIPE 3     /* one cooperative launch: state chains (32 or 64 columns) beside groups that

@@ -1,12 +1,14 @@
 """The launch plans of the tensor-core prefill agree with the oracle and with each other.
 
 bf16 inputs with d = 128 and 64-token chunks take the tensor-core path.  It runs
-as three kernels (preparation, state pass, output); as the preparation
-followed by one cooperative launch running the state chains with the output
-units alongside (chain); or as one cooperative launch in which chains of 64
-columns run beside groups that prepare the records in chunk order and then
-form the outputs (pipe: chains of 32 columns while there are at most 32 of them, else of 64); the test hook
-kda_testing_set_plan forces a plan.
+as the preparation followed by a state pass whose chains also form the outputs
+("three"; with the gated output normalisation fused, state pass and output
+pass); as the preparation followed by one cooperative launch running the state
+chains with output units alongside, which form the outputs from the chains'
+state images (chain); or as one cooperative launch in which chains run beside
+groups that prepare the records in chunk order and then form the outputs
+(pipe: chains of 32 columns while there are at most 32 of them, else of 64);
+the test hook kda_testing_set_plan forces a plan.
 All perform the same arithmetic in the same order, so their results must be
 bitwise identical, and they must meet the bf16 tolerance against the fp64
 oracle.
@@ -137,19 +139,20 @@ def _kernel_names(inp, S0):
 
 
 @pytest.mark.parametrize("extra_heads", [0, 1])
-def test_chain_plan_at_its_worker_threshold(extra_heads):
-    """One document with as many heads as leave exactly 48 CTAs beside the chains (4 column tiles a head),
-    the fewest output CTAs the automatic chain plan runs with, and one head more, where it falls back to
-    three kernels: the automatic choice is the expected plan, matches the three-kernel plan bit for bit
-    and meets the bf16 tolerance against the oracle."""
+def test_beyond_the_pipe_plan_the_state_pass_forms_the_outputs(extra_heads):
+    """One document with 21 heads (one past the pipe plan's 40 chains of 64 columns) and with as many heads as
+    leave 48 SMs beside chains of 32 columns, plus one: without the gated output normalisation the automatic
+    plan is the preparation and the state pass that forms the outputs itself (two kernels), which matches the
+    chain plan, whose output groups form them from the state images, bit for bit, and meets the bf16 tolerance
+    against the oracle."""
     sms = torch.cuda.get_device_properties(dev()).multi_processor_count
-    H = (sms - 48) // 4 + extra_heads
+    H = 21 if extra_heads == 0 else (sms - 48) // 4 + 1
     inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=77 + extra_heads, s0_std=0.1)
     names = _kernel_names(inp, inp.S0)
-    assert ("prefill_chain_tc" in names) == (extra_heads == 0), names
+    assert names == ["chunk_index", "prefill_prepare_tc", "prefill_state_fold_tc"], names
     o_a, S_a = _run(inp, "auto", inp.S0, poison=0x00)
-    o_3, S_3 = _run(inp, "three", inp.S0, poison=0x7F)
-    assert torch.equal(o_a, o_3) and torch.equal(S_a, S_3)
+    o_c, S_c = _run(inp, "chain" if extra_heads == 0 else "three", inp.S0, poison=0x7F)
+    assert torch.equal(o_a, o_c) and torch.equal(S_a, S_c)
     o_ref, S_ref, _ = oracle_prefill(inp, S0=inp.S0)
     assert rel(o_a, o_ref) <= TOL[torch.bfloat16], rel(o_a, o_ref)
     assert rel(S_a, S_ref) <= TOL[torch.bfloat16], rel(S_a, S_ref)
