@@ -39,6 +39,7 @@ enum Path { PATH_SIMT = 0, PATH_TC = 1 };
 
 struct WsLayout {
     size_t doc_slot0_off;
+    size_t doc_order_off;  // int32 [num_seqs]: documents by descending chunk count (long chains start first)
     size_t records_off;
     size_t record_bytes;
     int64_t max_slots;
@@ -92,7 +93,8 @@ __host__ __device__ constexpr TcRecord tc_record() {
 inline WsLayout ws_layout(int64_t total_tokens, int64_t num_seqs, int64_t H, int dk, int dv, int L, Path path) {
     WsLayout w;
     w.doc_slot0_off = 256;
-    w.records_off = w.doc_slot0_off + align256((size_t)(num_seqs + 1) * 4);
+    w.doc_order_off = w.doc_slot0_off + align256((size_t)(num_seqs + 1) * 4);
+    w.records_off = w.doc_order_off + align256((size_t)(num_seqs > 0 ? num_seqs : 1) * 4);
     w.record_bytes = path == PATH_TC ? tc_record().bytes : simt_record(L, dk, dv).bytes;
     w.max_slots = total_tokens / L + num_seqs;
     w.flags_off = w.records_off + (size_t)w.max_slots * (size_t)H * w.record_bytes;

@@ -39,10 +39,12 @@ constexpr int kThreads = 256;
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_tokens, int L, int32_t *status,
-                   int32_t *doc_slot0, uint4 *clear, int clear_vec, int fault) {
+                   int32_t *doc_slot0, int32_t *doc_order, uint4 *clear, int clear_vec, int fault) {
+    constexpr int kOrderMax = 512;  // documents ranked by chunk count up to this many (else the given order)
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ int s_carry;
+    __shared__ int s_cnt[kOrderMax];
     const int tid = threadIdx.x, nt = blockDim.x;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next kernel may get ready meanwhile
     for (int i = tid; i < clear_vec; i += nt) clear[i] = make_uint4(0, 0, 0, 0);
@@ -86,6 +88,23 @@ chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_token
         __syncthreads();
         if (tid == 0) s_carry += s_warp[nwarps - 1];
         __syncthreads();
+    }
+    // Documents by descending chunk count (ties in document order): a pass whose chains run in several waves
+    // then starts the longest ones first.
+    if (num_seqs <= kOrderMax) {
+        for (int i = tid; i < num_seqs; i += nt) s_cnt[i] = (cu[i + 1] - cu[i] + L - 1) / L;
+        __syncthreads();
+        for (int i = tid; i < num_seqs; i += nt) {
+            const int ci = s_cnt[i];
+            int rank = 0;
+            for (int j = 0; j < num_seqs; ++j) {
+                const int cj = s_cnt[j];
+                rank += (cj > ci) || (cj == ci && j < i);
+            }
+            doc_order[rank] = i;
+        }
+    } else {
+        for (int i = tid; i < num_seqs; i += nt) doc_order[i] = i;
     }
     if (tid == 0) {
         doc_slot0[num_seqs] = s_carry;
@@ -443,13 +462,15 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
                                size_t clear_bytes, cudaStream_t st, Marks &marks) {
     const int fault = testing_fault();
     char *w = static_cast<char *>(ws);
-    const size_t doc_off = 256;
+    const size_t doc_off = 256;  // (as ws_layout places the chunk table and the document order)
+    const size_t order_off = doc_off + align256((size_t)(num_seqs + 1) * 4);
     const int clear_vec = (int)(clear_bytes / 16);
     const int busy = num_seqs > clear_vec ? num_seqs : clear_vec;
     const int threads = busy >= 512 ? 1024 : (busy >= 128 ? 256 : 64);
     marks.before(st, "chunk_index");
     chunk_index_kernel<<<1, threads, 0, st>>>(cu, num_seqs, total_tokens, L, reinterpret_cast<int32_t *>(w),
-                                              reinterpret_cast<int32_t *>(w + doc_off), static_cast<uint4 *>(clear),
+                                              reinterpret_cast<int32_t *>(w + doc_off),
+                                              reinterpret_cast<int32_t *>(w + order_off), static_cast<uint4 *>(clear),
                                               clear_vec, fault);
     return cudaGetLastError();
 }

@@ -997,6 +997,9 @@ struct ChainLinks {
     // behind its MMAs; which is faster depends on what else the launch runs (measured per plan).
     bool loader = true;
     __nv_bfloat16 *o = nullptr;  // FOLD: where the chain writes its columns of each chunk's output
+    // The r-th document's chains are those of document doc_order[r] (null: r): with more chains than SMs, the
+    // documents with the most chunks then start first.
+    const int32_t *doc_order = nullptr;
 };
 
 // Chain j by the first kStateThreads threads of a CTA over `smem_raw` (Cfg, a ChainCfg<TN, ...>); the CTA's
@@ -1024,7 +1027,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
     const int i = (warp & 3) * 32 + lane, hcol = (warp >> 2) & 1;
     const int tile = j % NT;
     const int h = (j / NT) % H;
-    const int n = j / (NT * H);
+    const int rdoc = j / (NT * H);
+    const int n = links.doc_order && rdoc < num_seqs ? links.doc_order[rdoc] : rdoc;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
     const int first = doc_slot0[n], nchunks = doc_slot0[n + 1] - first;
     if (!KDA_IN_BOUNDS(n < num_seqs && first >= 0 && nchunks >= 0 &&
@@ -1362,10 +1366,12 @@ template <int TN>
 __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                  float *__restrict__ S_final, char *__restrict__ ws, size_t doc_slot0_off, size_t records_off,
-                 size_t record_bytes) {
+                 size_t record_bytes, size_t doc_order_off) {
     extern __shared__ uint8_t smem_raw[];
+    ChainLinks links;
+    links.doc_order = reinterpret_cast<const int32_t *>(ws + doc_order_off);
     state_chain<TN>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes, (int)blockIdx.x,
-                    smem_raw, ChainLinks{});
+                    smem_raw, links);
 }
 
 // The state pass with each chain also forming its columns of every chunk's output (no output pass, no state
@@ -1379,10 +1385,11 @@ template <int TN>
 __global__ void __launch_bounds__(kFoldThreads, 1)
 prefill_state_fold_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const float *__restrict__ S0,
                       float *__restrict__ S_final, __nv_bfloat16 *__restrict__ o, char *__restrict__ ws,
-                      size_t doc_slot0_off, size_t records_off, size_t record_bytes) {
+                      size_t doc_slot0_off, size_t records_off, size_t record_bytes, size_t doc_order_off) {
     extern __shared__ uint8_t smem_raw[];
     ChainLinks links;
     links.o = o;
+    links.doc_order = reinterpret_cast<const int32_t *>(ws + doc_order_off);
     state_chain<TN, FoldCfg<TN>>(cu, num_seqs, H, S0, S_final, ws, doc_slot0_off, records_off, record_bytes,
                                  (int)blockIdx.x, smem_raw, links);
 }
@@ -2198,20 +2205,20 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             return launch_dependent(prefill_state_fold_tc<32>, dim3((unsigned)chains32), dim3(kFoldThreads),
                                     (size_t)kFoldSmem32, st, cu, num_seqs, H, S0, S_final,
                                     static_cast<__nv_bfloat16 *>(o), w, lay.doc_slot0_off, lay.records_off,
-                                    lay.record_bytes);
+                                    lay.record_bytes, lay.doc_order_off);
         return launch_dependent(prefill_state_fold_tc<64>, dim3((unsigned)(chains32 / 2)), dim3(kFoldThreads),
                                 (size_t)kFoldSmem64, st, cu, num_seqs, H, S0, S_final, static_cast<__nv_bfloat16 *>(o),
-                                w, lay.doc_slot0_off, lay.records_off, lay.record_bytes);
+                                w, lay.doc_slot0_off, lay.records_off, lay.record_bytes, lay.doc_order_off);
     }
     marks.before(st, "prefill_state_tc");
     if (chains32 <= (size_t)dset.sms)
         e = launch_dependent(prefill_state_tc<32>, dim3((unsigned)chains32), dim3(kStateThreads), (size_t)kStateSmem,
                              st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off, lay.records_off,
-                             lay.record_bytes);
+                             lay.record_bytes, lay.doc_order_off);
     else
         e = launch_dependent(prefill_state_tc<64>, dim3((unsigned)(chains32 / 2)), dim3(kStateThreads),
                              (size_t)kStateSmem64, st, cu, num_seqs, H, S0, S_final, w, lay.doc_slot0_off,
-                             lay.records_off, lay.record_bytes);
+                             lay.records_off, lay.record_bytes, lay.doc_order_off);
     if (e) return e;
     if (lay.max_slots > 0 && total_tokens > 0) {
         marks.before(st, "prefill_output_tc");
