@@ -10,7 +10,7 @@ steps) and the indexed decode over a state pool are timed.  Prints ONE JSON
 line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libkda|reference]
-  python bench.py --profile-case prefill|varlen|long|decode-n64|conv [--repeat R]   (untimed, for ncu)
+  python bench.py --profile-case prefill|varlen|long|decode|decode-n64|conv [--repeat R]   (untimed, for ncu)
   python bench.py --compare-plans      (pass time of each tensor-core launch plan, one JSON line each)
 
 Timing: CUDA events on the launching stream, L2 flushed (a 256 MB write)
@@ -165,6 +165,7 @@ KERNEL_SOURCES = {
     "prefill_output_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_chain_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "prefill_pipe_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_state_fold_tc": "gated_delta_rule_27_gb300/csrc/kda_prefill_tc.cu",
     "out_gated_norm": "gated_delta_rule_27_gb300/csrc/kda_prefill_simt.cu",
     "decode_step": "gated_delta_rule_27_gb300/csrc/kda_decode.cu",
 }
@@ -802,9 +803,10 @@ def run_reference(args):
 def run_profile_case(case: str, repeat: int):
     """Untimed launches of one workload, for an external profiler (ncu) to capture.
 
-    'prefill', 'varlen' and 'long' run that prefill workload through kda_prefill_chunked; 'decode-n64' runs
-    decode steps over a quarter of the decode workload's sequences (64 x 32 heads, 128 MiB of state), small
-    enough for a many-pass capture; 'conv' runs the sublayer's short convolutions (prefill and decode).
+    'prefill', 'varlen' and 'long' run that prefill workload through kda_prefill_chunked; 'decode' runs decode
+    steps of the decode workload's size (256 x 32 heads, 512 MiB of state; one-pass captures such as DRAM bytes);
+    'decode-n64' runs them over a quarter of its sequences (64 x 32 heads, 128 MiB of state), small enough for a
+    many-pass capture; 'conv' runs the sublayer's short convolutions (prefill and decode).
     """
     from gated_delta_rule_27_gb300 import libkda
     torch.cuda.set_device(0)
@@ -835,10 +837,11 @@ def run_profile_case(case: str, repeat: int):
                     else:
                         libkda.kda_short_conv_prefill(x, w, cu, y, conv_state_out=st)
     else:
-        dec = workloads.decode_inputs(repeat, 64, 32, 128, torch.bfloat16, seed=workloads.workload_seed("decode"),
+        n = 64 if case == "decode-n64" else 256
+        dec = workloads.decode_inputs(repeat, n, 32, 128, torch.bfloat16, seed=workloads.workload_seed("decode"),
                                       device="cuda")
         S = dec.S0.clone()
-        o = torch.empty((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+        o = torch.empty((n, 32, 128), dtype=torch.bfloat16, device="cuda")
         for t in range(repeat):
             libkda.kda_decode_step(dec.q[t], dec.k[t], dec.v[t], dec.g[t], dec.beta[t], S, o)
     torch.cuda.synchronize()
@@ -854,7 +857,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the prefill and decode workloads (skip varlen, long, indexed decode)")
-    ap.add_argument("--profile-case", choices=["prefill", "varlen", "long", "decode-n64", "conv"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "varlen", "long", "decode", "decode-n64", "conv"], default=None,
                     help="run untimed launches of one workload for a profiler, print a status line, exit")
     ap.add_argument("--repeat", type=int, default=3)
     ap.add_argument("--compare-plans", action="store_true",
