@@ -26,7 +26,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // incoming state is written by the chunk-parallel pass and read by the
 // sequential state pass.
 //
-//   [0, 256)            int32 status word (0 = cu_seqlens valid), then padding
+//   [0, 256)            int32 status word (0 = cu_seqlens valid), the failing line of a
+//                       bounds check after it, the preparation's work counter at word
+//                       kPrepCounterWord (zeroed by the chunk index kernel), then padding
 //   doc_slot0           int32 [num_seqs + 1]: first chunk slot of each document
 //                       (exclusive prefix sum of ceil(len / L)), 256-byte padded
 //   records             one per (chunk slot, head), `record_bytes` each
@@ -36,6 +38,9 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // size depends only on the call's scalar arguments.
 // ---------------------------------------------------------------------------
 enum Path { PATH_SIMT = 0, PATH_TC = 1 };
+
+// int32 word of the workspace header that the persistent tensor-core preparation claims its units from
+constexpr int kPrepCounterWord = 32;
 
 struct WsLayout {
     size_t doc_slot0_off;

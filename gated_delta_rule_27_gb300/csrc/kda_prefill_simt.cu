@@ -33,9 +33,10 @@ constexpr int kThreads = 256;
 // ---------------------------------------------------------------------------
 // (1) chunk index: doc_slot0[i] = sum_{j<i} ceil(len_j / L), and validation of
 // cu_seqlens.  On invalid input every document gets zero chunks and the
-// status word is set, so the later kernels write nothing.  Also zeroes
-// `clear_vec` 16-byte words at `clear` (the progress flags of the chain
-// plan), when asked to.
+// status word is set, so the later kernels write nothing.  Zeroes the
+// preparation's work counter in the workspace header, and `clear_vec` 16-byte
+// words at `clear` (the progress flags of the chain and pipe plans) when asked
+// to.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_tokens, int L, int32_t *status,
@@ -49,6 +50,7 @@ chunk_index_kernel(const int32_t *__restrict__ cu, int num_seqs, int total_token
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next kernel may get ready meanwhile
     for (int i = tid; i < clear_vec; i += nt) clear[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
+        status[kPrepCounterWord] = 0;
         s_bad = (cu[0] != 0) || (cu[num_seqs] != total_tokens);
         s_carry = 0;
     }

@@ -343,21 +343,19 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
     tc::mbar_init(&b->r3, 2);
 }
 
-// One (chunk slot, head) of the preparation by a CTA of 256 threads whose 256 TMEM
-// columns start at `tmem`; `ph` is the parity of this unit's barrier phases (units
-// a CTA has prepared before, mod 2).  (nslot, nh) is a unit that is likely to
-// follow on this SM (nslot < 0: none): its tiles are pulled into L2.  With
-// `claim_counter`, the group instead claims its next unit from that counter
-// (claim_base + the counter's value) halfway through this one (into the
-// shared word `next_claim`; `units` and beyond: none left) and pulls that
-// unit's tiles into L2.  `mid_signal`, if
+// One (chunk slot, head) of the preparation by a group of 256 threads whose 256
+// TMEM columns start at `tmem`; `ph` is the parity of this unit's barrier phases
+// (units the group has prepared before, mod 2).  With `claim_counter`, the group
+// claims its next unit from that counter (claim_base + the counter's value)
+// halfway through this one (into the shared word `next_claim`; `units` and
+// beyond: none left) and pulls that unit's tiles into L2.  `mid_signal`, if
 // set, is raised (a shared word) at the same point, once the unit's operands
 // are built.  If `publish` is set, the group's previous record is published
 // there (release, once its bulk stores are complete) as soon as this unit's
 // gate tile has arrived.  Returns false after recording a timeout in the
 // status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
-                             uint32_t ph, uint32_t tmem, int nslot, int nh, int32_t *publish, const PrepGroup &grp,
+                             uint32_t ph, uint32_t tmem, int32_t *publish, const PrepGroup &grp,
                              PrepShared &sh, int32_t *claim_counter = nullptr, int claim_base = 0,
                              int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
@@ -459,18 +457,6 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             reinterpret_cast<float *>(rec + R.gamma)[c] = expf(blast);
         }
         if (!tc::mbar_wait(&bars->load, ph)) s_abort = 1;
-        if (tid == 0) {
-            int ndoc, nt0, nLc;
-            if (nslot >= 0 && locate_slot(doc_slot0, p.cu, p.num_seqs, kL, nslot, &ndoc, &nt0, &nLc)) {
-                tc::tma_prefetch_3d(p.tm_g, 0, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_k, 0, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_k, 64, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_q, 0, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_q, 64, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_v, 0, nh, nt0);
-                tc::tma_prefetch_3d(p.tm_v, 64, nh, nt0);
-            }
-        }
         grp.sync();
     }
     if (s_abort) {
@@ -848,36 +834,40 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const float *__restrict__ beta, const int32_t *__restrict__ cu, int num_seqs, int H,
                    char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes,
-                   int resident, int qk_norm, float qk_eps) {
+                   int qk_norm, float qk_eps) {
+    // Persistent: as many CTAs as are co-resident, each running units until none is left (its TMEM and
+    // barriers set up once).  Unit u is (chunk slot u / H, head u % H); a CTA's first unit is its own index,
+    // and each later one is claimed from the work counter halfway through the one before.
     extern __shared__ uint8_t smem_raw[];
     __shared__ PrepBars bars;
     __shared__ PrepShared psh;
     __shared__ uint32_t tmem_base;
+    __shared__ int s_unit;
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int slot = blockIdx.x, h = blockIdx.y;
-    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
-    if (tid == 0 && num_seqs == 1 && (int)(blockIdx.y * gridDim.x + blockIdx.x) < resident) {
-        // First wave of a single document: chunk slot s starts at token 64 s, so this CTA's tiles (inputs
-        // of the call, complete before it) can be pulled into L2 while the chunk index kernel still runs
-        const int64_t tok = (int64_t)slot * kL;
+    if (tid == 0 && num_seqs == 1) {
+        // A single document: chunk slot s starts at token 64 s, so the first unit's tiles (inputs of the call,
+        // complete before it) can be pulled into L2 while the chunk index kernel still runs
+        const int hh = (int)blockIdx.x % H;
+        const int64_t tok = (int64_t)((int)blockIdx.x / H) * kL;
         if (tok < (int64_t)__ldg(cu + 1)) {
-            tc::tma_prefetch_3d(&tm_g, 0, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_k, 0, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_k, 64, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_q, 0, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_q, 64, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_v, 0, h, (int)tok);
-            tc::tma_prefetch_3d(&tm_v, 64, h, (int)tok);
+            tc::tma_prefetch_3d(&tm_g, 0, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_k, 0, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_k, 64, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_q, 0, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_q, 64, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_v, 0, hh, (int)tok);
+            tc::tma_prefetch_3d(&tm_v, 64, hh, (int)tok);
         }
     }
-    tc::grid_dep_wait();    // the chunk index kernel's slot table
+    tc::grid_dep_wait();    // the chunk index kernel's slot table and zeroed work counter
     tc::grid_dep_launch();  // the state pass may get ready once every CTA of this grid has started
-    int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
-    if (!locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc)) return;
+    const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(ws + doc_slot0_off);
+    const int units = doc_slot0[num_seqs] * H;
     if (tid == 0) {
         prep_bars_init(&bars);
         tc::fence_mbar_init();
+        s_unit = (int)blockIdx.x;
     }
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 256);
@@ -886,14 +876,23 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    // CTAs start in launch order as slots free up, so the one `resident` places further on takes this
-    // CTA's place next
-    const int nxt = blockIdx.y * gridDim.x + blockIdx.x + resident;
-    const bool has_next = resident > 0 && nxt < (int)(gridDim.x * gridDim.y);
     const PrepParams prm{&tm_q,         &tm_k,       &tm_v,          &tm_g,   beta,  cu, num_seqs, H, ws, doc_slot0_off,
                          records_off, record_bytes, qk_norm, qk_eps};
-    prepare_unit(prm, slot, h, t0, Lc, sm, &bars, 0u, tmem_base, has_next ? nxt % (int)gridDim.x : -1,
-                 has_next ? nxt / (int)gridDim.x : 0, nullptr, PrepGroup{tid, 0u}, psh);
+    int32_t *counter = reinterpret_cast<int32_t *>(ws) + kPrepCounterWord;
+    const PrepGroup grp{tid, 0u};
+    for (uint32_t n = 0;; ++n) {
+        const int u = s_unit;
+        __syncthreads();  // every thread has read s_unit before the next claim overwrites it
+        if (u >= units) break;
+        const int slot = u / H, h = u % H;
+        int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
+        locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
+        if (!prepare_unit(prm, slot, h, t0, Lc, sm, &bars, n & 1u, tmem_base, nullptr, grp, psh, counter,
+                          (int)gridDim.x, &s_unit, units))
+            break;
+        __syncthreads();  // the claim is visible to every thread
+    }
+    tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
@@ -1844,7 +1843,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
         locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
         // the previous record is published once this unit's gate tile has arrived; this one's stays pending
-        ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, -1, 0, pending, grp, psh[g],
+        ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, pending, grp, psh[g],
                           a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr);
         ++nprep;
         if (!ok) break;
@@ -2176,10 +2175,12 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         InputMaps m;
         if (!input_maps(q, k, v, g, total_tokens, H, &m)) return cudaErrorInvalidValue;
         marks.before(st, "prefill_prepare_tc");
-        if ((e = launch_dependent(prefill_prepare_tc, dim3((unsigned)lay.max_slots, (unsigned)H), dim3(kPrepThreads),
-                                  (size_t)kPrepSmem, st, m.q, m.k, m.v, m.g, beta, cu, num_seqs, H, w,
-                                  lay.doc_slot0_off, lay.records_off, lay.record_bytes, dset.prep_resident,
-                                  fu.qk_norm, fu.qk_eps)))
+        // persistent: the co-resident CTAs (or one per unit, if fewer) claim the units in turn
+        const long long units = (long long)lay.max_slots * H;
+        const unsigned grid = (unsigned)std::max(1LL, std::min<long long>(dset.prep_resident, units));
+        if ((e = launch_dependent(prefill_prepare_tc, dim3(grid), dim3(kPrepThreads), (size_t)kPrepSmem, st, m.q,
+                                  m.k, m.v, m.g, beta, cu, num_seqs, H, w, lay.doc_slot0_off, lay.records_off,
+                                  lay.record_bytes, fu.qk_norm, fu.qk_eps)))
             return e;
     }
     if (num_seqs == 0) return cudaSuccess;
