@@ -69,8 +69,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // tcgen05.ld is warp-collective (.sync.aligned): every TMEM load below runs
 // under a warp-uniform condition, and per-lane conditions only guard stores.
 __device__ __forceinline__ bool warp_all(bool b) { return __all_sync(0xffffffffu, b); }
-// Records a timed-out wait in the workspace status word (first writer wins).
+// Records a timed-out wait in the workspace status word (first writer wins), once the chunk index kernel,
+// which writes that word, is complete (a thread that started before it waits for it here).
 __device__ __forceinline__ void flag_timeout(char *ws) {
+    tc::grid_dep_wait();
     atomicCAS(reinterpret_cast<int32_t *>(ws), 0, (int32_t)KDA_ERR_TIMEOUT);
 }
 
@@ -352,12 +354,15 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // set, is raised (a shared word) at the same point, once the unit's operands
 // are built.  If `publish` is set, the group's previous record is published
 // there (release, once its bulk stores are complete) as soon as this unit's
-// gate tile has arrived.  Returns false after recording a timeout in the
-// status word.
+// gate tile has arrived.  `dep_wait`: the unit started before the chunk index
+// kernel was known to be complete; the claimer and the first thread wait for
+// it before the claim and before reading its tables.  Returns false after
+// recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
                              uint32_t ph, uint32_t tmem, int32_t *publish, const PrepGroup &grp,
                              PrepShared &sh, int32_t *claim_counter = nullptr, int claim_base = 0,
-                             int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr) {
+                             int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr,
+                             bool dep_wait = false) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
     float *s_half = sh.half, *s_mid = sh.mid, *s_invk = sh.invk, *s_invq = sh.invq;
     float(*s_lo)[kD] = sh.lo;
@@ -568,7 +573,10 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     tc::tc_fence_after();
     if (mid_signal && tid == 0) *reinterpret_cast<volatile int *>(mid_signal) = 1;
     constexpr int kClaimer = 64;  // a thread of warp 2: neither issuer waits for the atomic
-    if (claim_counter && tid == kClaimer) *next_claim = claim_base + atomicAdd(claim_counter, 1);
+    if (claim_counter && tid == kClaimer) {
+        if (dep_wait) tc::grid_dep_wait();  // the counter is zeroed by the chunk index kernel
+        *next_claim = claim_base + atomicAdd(claim_counter, 1);
+    }
 
     constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
     bool ok = true;
@@ -660,6 +668,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         return false;
     }
     if (claim_counter && tid == 0) {  // the unit claimed at the operand barrier: its tiles into L2
+        if (dep_wait) tc::grid_dep_wait();  // (the slot table)
         const int un = *next_claim;
         int ndoc, nt0, nLc;
         if (un < units && locate_slot(doc_slot0, p.cu, p.num_seqs, kL, un / H, &ndoc, &nt0, &nLc)) {
@@ -1752,6 +1761,7 @@ struct PipeArgs {
     int32_t *prep_counter;  // next preparation unit
     int32_t *out_counter;   // next output unit
     int n_chain;
+    int total_tokens;
     unsigned long long flag_wait_ns;
     int fault;  // kFaultNoPublish only in tests of the timeout path
     OutNorm onorm;
@@ -1783,7 +1793,10 @@ __device__ bool pipe_outputs(const PrepParams &pp, const PipeArgs &a, uint8_t *g
     }
 }
 
-__device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm) {
+// `early`: a single document whose preparation starts before the chunk index kernel is known to be complete
+// (its slots follow from the token count); the group waits for that kernel before it claims a unit, publishes
+// a record or reads the kernel's tables.
+__device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm, bool early) {
     __shared__ PrepBars pbars[2];
     __shared__ OutBars obars[2];
     __shared__ uint32_t tmem_base;
@@ -1792,7 +1805,8 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255;
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
-    const int units = doc_slot0[pp.num_seqs] * H;  // preparation units, and as many output units
+    // preparation units, and as many output units
+    const int units = early ? (a.total_tokens + kL - 1) / kL * H : doc_slot0[pp.num_seqs] * H;
     if (tid == 0) s_go = 0;
     if (gtid == 0) {
         prep_bars_init(&pbars[g]);
@@ -1841,15 +1855,22 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         if (u >= units) break;
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
-        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+        if (early) {  // the single document's chunk slot
+            t0 = slot * kL;
+            Lc = min(kL, a.total_tokens - t0);
+        } else {
+            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
+        }
         // the previous record is published once this unit's gate tile has arrived; this one's stays pending
         ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, pending, grp, psh[g],
-                          a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr);
+                          a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr,
+                          early && nprep == 0);
         ++nprep;
         if (!ok) break;
         pending = a.ready + (size_t)slot * H + h;
     }
     if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
+    if (early) tc::grid_dep_wait();  // (a group that prepared nothing has not waited yet)
     if (gtid == 0 && pending) {  // before any output unit: a chain may be waiting for this record
         tc::bulk_wait_all();
         tc::fence_proxy_async_global();
@@ -1870,13 +1891,23 @@ prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, int qk_norm,
                 float qk_eps, PipeArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    tc::grid_dep_wait();  // the chunk index kernel: slot table, status word, cleared flags
-    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    // A single document whose cu_seqlens pass the chunk index kernel's checks (so that its status word will
+    // read valid): the workers start preparing at once and wait for that kernel only where they use what it
+    // writes (the slot table, the cleared flags and counters).
+    bool early = num_seqs == 1 && __ldg(cu) == 0 && __ldg(cu + 1) == a.total_tokens && a.total_tokens > 0;
+#ifdef KDA_DEBUG_BOUNDS
+    early = false;  // (the bounds-checking build tests its checks against the chunk table)
+#endif
+    const bool worker = (int)blockIdx.x >= a.n_chain;
+    if (!(worker && early)) {
+        tc::grid_dep_wait();  // the chunk index kernel: slot table, status word, cleared flags
+        if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    }
     uint8_t *sm = align1024(smem_raw);
     const PrepParams pp{&tm_q,       &tm_k,        &tm_v,   &tm_g,  beta, cu, num_seqs, H, ws, doc_slot0_off,
                         records_off, record_bytes, qk_norm, qk_eps};
-    if ((int)blockIdx.x >= a.n_chain) {
-        pipe_worker(pp, a, sm);
+    if (worker) {
+        pipe_worker(pp, a, sm, early);
         return;
     }
     ChainLinks links;
@@ -2148,6 +2179,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         a.prep_counter = flags + 2 * nflag;
         a.out_counter = flags + 2 * nflag + 1;
         a.n_chain = num_seqs * H * (kD / 64);
+        a.total_tokens = total_tokens;
         a.flag_wait_ns = flag_wait;
         a.fault = g_test_fault.load();
         a.onorm = onorm;
