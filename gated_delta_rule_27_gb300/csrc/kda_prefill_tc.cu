@@ -1868,6 +1868,14 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         ++nprep;
         if (!ok) break;
         pending = a.ready + (size_t)slot * H + h;
+        if (nprep == 1) {  // the group's first record: chains may be waiting for it, so it is published at once
+            if (gtid == 0) {
+                tc::bulk_wait_all();
+                tc::fence_proxy_async_global();
+                tc::st_release_gpu(pending, 1);
+            }
+            pending = nullptr;
+        }
     }
     if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
     if (early) tc::grid_dep_wait();  // (a group that prepared nothing has not waited yet)
