@@ -198,8 +198,13 @@ __device__ __forceinline__ void load_window(float (&win)[W][4], const T *__restr
 // A tile of kVecTile tokens x 4 channels per thread, the token loop unrolled: the tile's loads are issued
 // first, then each token takes its input from registers.  A document that starts inside the tile reloads the
 // window (a warp-uniform branch, rare); the document's last W - 1 inputs are written to its new state.
+// Three CTAs per SM where the tile's registers fit in the 80 that allows (bf16 inputs, W <= 5); two
+// (up to 128 registers) for fp32 inputs, whose tile is twice as many registers, and for wider filters.
 template <typename T, int W>
-__global__ void __launch_bounds__(kConvThreads, 3)
+constexpr int conv_vec_min_blocks() { return (sizeof(T) == 2 && W <= 5) ? 3 : 2; }
+
+template <typename T, int W>
+__global__ void __launch_bounds__(kConvThreads, conv_vec_min_blocks<T, W>())
 conv_prefill_vec_kernel(const T *__restrict__ x, const float *__restrict__ w, const int32_t *__restrict__ cu,
                         int num_seqs, int total_tokens, int C, const float *__restrict__ state_in, T *__restrict__ y,
                         float *__restrict__ state_out) {
