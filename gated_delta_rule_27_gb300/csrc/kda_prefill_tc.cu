@@ -69,6 +69,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // tcgen05.ld is warp-collective (.sync.aligned): every TMEM load below runs
 // under a warp-uniform condition, and per-lane conditions only guard stores.
 __device__ __forceinline__ bool warp_all(bool b) { return __all_sync(0xffffffffu, b); }
+// 2^x by the hardware's approximate base-2 exponential (a few ulp; subnormal results flushed to zero)
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
 // Records a timed-out wait in the workspace status word (first writer wins), once the chunk index kernel,
 // which writes that word, is complete (a thread that started before it waits for it here).
 __device__ __forceinline__ void flag_timeout(char *ws) {
@@ -518,6 +525,10 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         *reinterpret_cast<float4 *>(blv + 4) = *reinterpret_cast<const float4 *>(s_blast + c0 + 4);
         uint8_t *Xp = sm + PrepSmem::X + (uint32_t)opanel * 16384u;
         uint8_t *Yp = sm + PrepSmem::Y + (uint32_t)opanel * 8192u;
+        // the reference in log2 units: exp(b - b_m) = 2^(b log2(e) - b_m log2(e)), one fused multiply-add
+        float bml[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) bml[u] = bmv[u] * kLog2e;
         // beta is not applied here: it scales A's rows as they leave TMEM and T's columns in T's bf16
         // image, so that W' = T diag(beta) (k e1) and Ut = T diag(beta) v take k e1 and v as they are
 #pragma unroll 1
@@ -527,8 +538,10 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             const uint32_t off_k = tc::sw128_offset(r, ocol), off_q = tc::sw128_offset(64 + r, ocol);
             if (!KDA_IN_BOUNDS(r < kL && off_q + 16 <= 16384u, status)) continue;
             float k8[8], q8[8], xk[8], xq[8], ke[8];
-            unpack8(*reinterpret_cast<const uint4 *>(Xp + off_k), k8);
-            unpack8(*reinterpret_cast<const uint4 *>(Xp + off_q), q8);
+            uint4 kraw = *reinterpret_cast<const uint4 *>(Xp + off_k), qraw = *reinterpret_cast<const uint4 *>(Xp + off_q);
+            if (!valid) kraw = qraw = make_uint4(0u, 0u, 0u, 0u);  // rows past the chunk's end contribute nothing
+            unpack8(kraw, k8);
+            unpack8(qraw, q8);
             if (p.qk_norm) {
                 const float ik = s_invk[r], iq = s_invq[r];
 #pragma unroll
@@ -544,9 +557,8 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
                 float y8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float d = bb[u] - bmv[u];
-                    const float e1 = valid ? __expf(d) : 0.f;
-                    const float inv = valid ? __expf(-d) : 0.f;
+                    const float d = fmaf(bb[u], kLog2e, -bml[u]);
+                    const float e1 = exp2_approx(d), inv = exp2_approx(-d);
                     xk[u] = k8[u] * e1;
                     xq[u] = q8[u] * e1;
                     y8[u] = k8[u] * inv;
