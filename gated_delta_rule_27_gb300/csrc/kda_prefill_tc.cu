@@ -158,7 +158,7 @@ struct PrepShared {
     __align__(16) float F[kD];
     __align__(16) float Em[kD];
     __align__(16) float blast[kD];
-    float half[kD], mid[kD], lo[2][kD], hi[2][kD];
+    float half[kD], lo[2][kD], hi[2][kD];
     float invk[kL], invq[kL];
     int abort;
 };
@@ -371,7 +371,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
                              int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr,
                              bool dep_wait = false) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
-    float *s_half = sh.half, *s_mid = sh.mid, *s_invk = sh.invk, *s_invq = sh.invq;
+    float *s_half = sh.half, *s_invk = sh.invk, *s_invq = sh.invq;
     float(*s_lo)[kD] = sh.lo;
     float(*s_hi)[kD] = sh.hi;
     int &s_abort = sh.abort;
@@ -426,12 +426,16 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     bool unsafe;
     {
         const int c = tid & (kD - 1), hh = tid >> 7, r0 = hh * 32;
-        const int m = (Lc - 1) >> 1, last = Lc - 1;
+        if (Lc < kL) {  // a document's last, partial chunk: the rows past its end add nothing to the sums
+            for (int e = Lc * kD + tid; e < kL * kD; e += kPrepThreads) Gf[e] = 0.f;
+            grp.sync();
+        }
+        // (so every row's b is a valid row's: b_r = b_{Lc-1} past the end, inside the valid rows' range)
         float bcol[32];
         float acc = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-            acc += r0 + u < Lc ? Gf[(r0 + u) * kD + c] : 0.f;
+            acc += Gf[(r0 + u) * kD + c];
             bcol[u] = acc;
         }
         if (hh == 0) s_half[c] = acc;
@@ -440,19 +444,19 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-            const int r = r0 + u;
             const float b = bcol[u] + off;
-            if (r < Lc) { lo = fminf(lo, b); hi = fmaxf(hi, b); }
-            if (r == m) s_mid[c] = b;
-            if (r == last) s_blast[c] = b;
-            Gf[bswz(r, c)] = b;
+            lo = fminf(lo, b);
+            hi = fmaxf(hi, b);
+            Gf[bswz(r0 + u, c)] = b;
         }
+        if (hh) s_blast[c] = bcol[31] + off;  // row 63's b is the last valid row's
         s_lo[hh][c] = lo;
         s_hi[hh][c] = hi;
         grp.sync();
         bool bad = false;
+        float bm = 0.f;
         if (tid < kD) {
-            const float bm = s_mid[c];
+            bm = Gf[bswz((Lc - 1) >> 1, c)];  // the middle token's
             const float bmin = fminf(s_lo[0][c], s_lo[1][c]), bmax = fmaxf(s_hi[0][c], s_hi[1][c]);
             bad = bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY);
         }
@@ -462,7 +466,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         unsafe = grp.sync_or(bad);
         if (tid < kD) {
             const float blast = s_blast[c];
-            const float bref = unsafe ? 0.f : s_mid[c];
+            const float bref = unsafe ? 0.f : bm;
             s_bm[c] = bref;
             s_F[c] = expf(blast - bref);
             s_Em[c] = expf(bref);
