@@ -110,7 +110,7 @@ struct PrepSmem {
     static constexpr uint32_t X = 0;
     static constexpr uint32_t V = 32768;   // v tile (MN-major) as loaded; then Ut^T, K-major [j][s]
     static constexpr uint32_t G = 49152;   // g fp32 [64][128] -> b (swizzled); then A, T, T(bf16); then Kend, W'^T
-    static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB) and the identity (8 KB)
+    static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB)
     static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
     static constexpr uint32_t Tfp = G + 10240;     // compact fp32 T (10 KB)
     static constexpr uint32_t Scr = G + 20480;     // the solve's scratch (6 KB) ...
@@ -118,7 +118,6 @@ struct PrepSmem {
     static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB)
     static constexpr uint32_t WT = G + 16384;      // W'^T, K-major [c][s] (16 KB)
     static constexpr uint32_t P = Y;               // P, K-major [r][s] (8 KB)
-    static constexpr uint32_t Id = Y + 8192;       // identity, K-major [r][r'] (8 KB)
     static constexpr uint32_t bytes = 98304;
 };
 
@@ -162,6 +161,25 @@ struct PrepShared {
     float invk[kL], invq[kL];
     int abort;
 };
+
+// The 64 x 64 bf16 identity, K-major [r][r'] with the 128-byte swizzle (8 KB): round 3's operand that adds X_q.
+// Written once per CTA (by its `n` threads) into a region no unit overwrites.
+constexpr uint32_t kIdentBytes = 8192;
+__device__ __forceinline__ void write_identity(uint8_t *id, int tid, int n) {
+    for (int e = tid; e < 64 * 8; e += n) {  // 16-byte chunk e: row e / 8, columns 8 (e % 8) ..
+        const int r = e >> 3, s0 = (e & 7) * 8;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if ((r >> 3) == (e & 7)) {  // the chunk holding (r, r)
+            const uint32_t one = 0x3f80u << (16 * (r & 1));
+            const int word = (r & 7) >> 1;
+            w.x = word == 0 ? one : 0u;
+            w.y = word == 1 ? one : 0u;
+            w.z = word == 2 ? one : 0u;
+            w.w = word == 3 ? one : 0u;
+        }
+        *reinterpret_cast<uint4 *>(id + tc::sw128_offset(r, s0)) = w;
+    }
+}
 
 // T = (I + A)^{-1} for A strictly lower triangular (compact block-major, four
 // 16-row blocks), 256 threads.  The diagonal blocks are inverted by forward
@@ -366,7 +384,8 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // it before the claim and before reading its tables.  Returns false after
 // recording a timeout in the status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
-                             uint32_t ph, uint32_t tmem, int32_t *publish, const PrepGroup &grp,
+                             uint32_t ph, uint32_t tmem, const uint8_t *ident, int32_t *publish,
+                             const PrepGroup &grp,
                              PrepShared &sh, int32_t *claim_counter = nullptr, int claim_base = 0,
                              int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr,
                              bool dep_wait = false) {
@@ -665,17 +684,6 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             }
         }
     }
-    // identity (K-major [r][r']) for round 3, in the dead second half of the round-1 B operand
-    {
-        const int r = tid >> 2, s0 = (tid & 3) * 16;
-#pragma unroll
-        for (int s8 = 0; s8 < 16; s8 += 8) {
-            float w[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = (s0 + s8 + u) == r ? 1.f : 0.f;
-            *reinterpret_cast<uint4 *>(sm + PrepSmem::Id + tc::sw128_offset(r, s0 + s8)) = pack8(w);
-        }
-    }
     tc::tc_fence_before();
     if (!ok) s_abort = 1;
     grp.sync();
@@ -716,8 +724,9 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             const float4 t = blk ? *reinterpret_cast<const float4 *>(trow + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 b = *reinterpret_cast<const float4 *>(s_beta + s);
             uint2 pk;
-            pk.x = pack_bf16x2(s + 0 <= r ? t.x * b.x : 0.f, s + 1 <= r ? t.y * b.y : 0.f);
-            pk.y = pack_bf16x2(s + 2 <= r ? t.z * b.z : 0.f, s + 3 <= r ? t.w * b.w : 0.f);
+            // (T's diagonal blocks hold exact zeros above the diagonal: no mask)
+            pk.x = pack_bf16x2(t.x * b.x, t.y * b.y);
+            pk.y = pack_bf16x2(t.z * b.z, t.w * b.w);
             *reinterpret_cast<uint2 *>(Tb + tc::sw128_offset(r, s)) = pk;
         }
     }
@@ -786,7 +795,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
                              tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::P + s * 32)), id_neg, s > 0);
             for (int s = 0; s < 4; ++s)
                 tc::mma_bf16(tmem, tc::smem_desc(kXmn, tc::smem_u32(sm + PrepSmem::X + 8192 + s * 2048)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + PrepSmem::Id + s * 32)), id_xq, true);
+                             tc::smem_desc(kKmaj, tc::smem_u32(ident + s * 32)), id_xq, true);
         } else {
             constexpr uint32_t id128 = tc::idesc_bf16_f32(128, 128, true, false);
             constexpr uint64_t kKmn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
@@ -894,6 +903,9 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::fence_mbar_init();
         s_unit = (int)blockIdx.x;
     }
+    uint8_t *ident = sm + PrepSmem::bytes;
+    write_identity(ident, tid, kPrepThreads);
+    tc::fence_async_smem();
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 256);
         tc::tmem_relinquish();
@@ -912,7 +924,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
         locate_slot(doc_slot0, cu, num_seqs, kL, slot, &doc, &t0, &Lc);
-        if (!prepare_unit(prm, slot, h, t0, Lc, sm, &bars, n & 1u, tmem_base, nullptr, grp, psh, counter,
+        if (!prepare_unit(prm, slot, h, t0, Lc, sm, &bars, n & 1u, tmem_base, ident, nullptr, grp, psh, counter,
                           (int)gridDim.x, &s_unit, units))
             break;
         __syncthreads();  // the claim is visible to every thread
@@ -1759,12 +1771,12 @@ constexpr int kPipeThreads = 512;
 constexpr int kPipeChainMax = 40;    // automatic choice: at most this many chains of 64 columns ...
 constexpr int kPipeChain32Max = 32;  // ... and chains of 32 columns (a shorter step) up to this many of them
 constexpr uint32_t kPipePrepShared = 2 * PrepSmem::bytes;  // the worker groups' PrepShared, after their tiles
+// the workers' identity image, after both groups' PrepShared (1024-byte aligned)
+constexpr uint32_t kPipeIdent = (kPipePrepShared + 2 * (uint32_t)sizeof(PrepShared) + 1023u) & ~1023u;
 template <int TN>
 constexpr size_t pipe_smem_bytes() {
     using PipeChainCfg = ChainCfg<TN>;
-    return (PipeChainCfg::bytes > kPipePrepShared + 2 * sizeof(PrepShared) ? PipeChainCfg::bytes
-                                                                          : kPipePrepShared + 2 * sizeof(PrepShared)) +
-           1024;
+    return (PipeChainCfg::bytes > kPipeIdent + kIdentBytes ? PipeChainCfg::bytes : kPipeIdent + kIdentBytes) + 1024;
 }
 static_assert(PrepSmem::bytes % 1024 == 0 && OutSmem::bytes <= PrepSmem::bytes, "a group's region holds a unit");
 
@@ -1835,6 +1847,8 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         tc::tmem_alloc(&tmem_base, 512);
         tc::tmem_relinquish();
     }
+    write_identity(sm + kPipeIdent, tid, kPipeThreads);  // one identity for both groups
+    tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -1878,7 +1892,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
             locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
         }
         // the previous record is published once this unit's gate tile has arrived; this one's stays pending
-        ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, pending, grp, psh[g],
+        ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, sm + kPipeIdent, pending, grp, psh[g],
                           a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr,
                           early && nprep == 0);
         ++nprep;
@@ -2056,7 +2070,7 @@ int resident_ctas(K kernel, int threads, int smem, int tmem_cols) {
     return cached[dev];
 }
 
-constexpr int kPrepSmem = PrepSmem::bytes + 1024;
+constexpr int kPrepSmem = PrepSmem::bytes + kIdentBytes + 1024;  // a unit's tiles, then the identity
 constexpr int kStateSmem = ChainCfg<32>::bytes + 1024;
 constexpr int kStateSmem64 = ChainCfg<64>::bytes + 1024;
 constexpr int kFoldSmem32 = FoldCfg<32>::bytes + 1024;
