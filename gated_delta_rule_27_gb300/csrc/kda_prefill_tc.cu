@@ -654,21 +654,20 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
             tc::tmem_ld32(tmem + lane_base + 32u * (uint32_t)hs, v);
             if (trow < 64) {
                 const int r = trow;
-                const float br = s_beta[r];  // A = diag(beta) (k e1)(k / e1)^T, strictly lower
+                // A = diag(beta) (k e1)(k / e1)^T, strictly lower.  The blocks on and below the diagonal are
+                // stored whole: the solve reads only the entries below the diagonal, so the others (which
+                // may even overflow) need no mask.
+                const float br = s_beta[r];
 #pragma unroll
                 for (int qb = 0; qb < 2; ++qb) {
                     const int q4 = 2 * hs + qb;
                     if (q4 <= (r >> 4) && KDA_IN_BOUNDS(tri_blk(r >> 4, q4) + 256 <= 2560, status)) {
                         float *dst = Af + tri_blk(r >> 4, q4) + ((r & 15) << 4);
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4) {
-                            float4 w;
-                            w.x = q4 * 16 + i + 0 < r ? br * v[qb * 16 + i + 0] : 0.f;
-                            w.y = q4 * 16 + i + 1 < r ? br * v[qb * 16 + i + 1] : 0.f;
-                            w.z = q4 * 16 + i + 2 < r ? br * v[qb * 16 + i + 2] : 0.f;
-                            w.w = q4 * 16 + i + 3 < r ? br * v[qb * 16 + i + 3] : 0.f;
-                            *reinterpret_cast<float4 *>(dst + i) = w;
-                        }
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(br * v[qb * 16 + i], br * v[qb * 16 + i + 1], br * v[qb * 16 + i + 2],
+                                            br * v[qb * 16 + i + 3]);
                     }
                 }
             } else {
