@@ -104,7 +104,13 @@ decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
         }
         __syncthreads();
     }
-    if (tid == 0) {
+    if (NT >= 32 && tid < 32) {  // q . k by one warp (a fixed shuffle tree: deterministic)
+        float acc = 0.f;
+        for (int i = tid; i < D; i += 32) acc = fmaf(s_q[i], s_k[i], acc);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (tid == 0) s_qk = acc;
+    } else if (NT < 32 && tid == 0) {
         float acc = 0.f;
         for (int i = 0; i < D; ++i) acc = fmaf(s_q[i], s_k[i], acc);
         s_qk = acc;
