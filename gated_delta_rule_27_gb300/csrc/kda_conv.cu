@@ -143,7 +143,8 @@ conv_decode_kernel(const T *__restrict__ x, const float *__restrict__ w, int N, 
 // the scalar kernels' sums term for term (w[c][0] x_t first, then one fmaf per older input), so the two
 // kernels and the decode step agree bit for bit.
 // ---------------------------------------------------------------------------
-constexpr int kVecTile = 16;  // tokens per thread: one batch of loads in flight
+constexpr int kVecTile = 16;    // tokens per thread: one batch of loads in flight
+constexpr int kShortDocs = 64;  // documents per CTA row of the short-document state pass
 
 template <typename T> struct Vec4;
 template <> struct Vec4<float> {
@@ -209,8 +210,25 @@ conv_prefill_vec_kernel(const T *__restrict__ x, const float *__restrict__ w, co
                         int num_seqs, int total_tokens, int C, const float *__restrict__ state_in, T *__restrict__ y,
                         float *__restrict__ state_out) {
     const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 4;
+    const int tiles = (total_tokens + kVecTile - 1) / kVecTile;
+    if ((int)blockIdx.y >= tiles) {
+        // the rows past the token tiles: documents shorter than W - 1, whose new state keeps some of the
+        // carried one (slot s of the new state is old slot s + len), kShortDocs documents per row
+        if (c0 >= C || W < 2 || !state_out) return;
+        const int n0 = ((int)blockIdx.y - tiles) * kShortDocs;
+        for (int n = n0; n < min(n0 + kShortDocs, num_seqs); ++n) {
+            const int len = max(cu[n + 1] - cu[n], 0);
+            for (int s = 0; s < W - 1 - len; ++s) {
+                const float4 v = state_in ? __ldg(reinterpret_cast<const float4 *>(
+                                                state_in + ((size_t)n * (W - 1) + s + len) * C + c0))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(state_out + ((size_t)n * (W - 1) + s) * C + c0) = v;
+            }
+        }
+        return;
+    }
     const int t_begin = blockIdx.y * kVecTile;
-    if (c0 >= C || t_begin >= total_tokens) return;
+    if (c0 >= C) return;
     const int t_end = min(t_begin + kVecTile, total_tokens);
     typename Vec4<T>::raw xv[kVecTile];
 #pragma unroll
@@ -221,11 +239,32 @@ conv_prefill_vec_kernel(const T *__restrict__ x, const float *__restrict__ w, co
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < W; ++j) wc[i][j] = w[(size_t)(c0 + i) * W + j];
+    // the inputs before the tile, loaded with it (kept where they belong to the tile's first document)
+    typename Vec4<T>::raw pre[W > 1 ? W - 1 : 1];
+#pragma unroll
+    for (int j = 1; j < W; ++j)
+        if (t_begin - j >= 0) pre[j - 1] = load_vec4(x + (size_t)(t_begin - j) * C + c0);
     int m = doc_of(cu, num_seqs, t_begin);
     while (m + 1 < num_seqs && cu[m + 1] <= t_begin) ++m;  // skip empty documents ending at t_begin
     int ds = cu[m], de = cu[m + 1];
     float win[W][4];  // win[j][i]: channel c0 + i, j tokens back (j = 0 the current token)
-    load_window<T, W>(win, x, state_in, C, c0, m, ds, t_begin);
+#pragma unroll
+    for (int j = 1; j < W; ++j) {
+        const int p = t_begin - j;
+        if (p >= ds && p >= 0) {
+            Vec4<T>::to(pre[j - 1], win[j]);
+        } else {
+            const int back = ds - p;  // 1 .. j for a valid cu_seqlens
+            if (state_in && back >= 1 && back <= W - 1) {
+                const float4 s = __ldg(reinterpret_cast<const float4 *>(
+                    state_in + ((size_t)m * (W - 1) + (W - 1 - back)) * C + c0));
+                win[j][0] = s.x; win[j][1] = s.y; win[j][2] = s.z; win[j][3] = s.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) win[j][i] = 0.f;
+            }
+        }
+    }
 #pragma unroll
     for (int u = 0; u < kVecTile; ++u) {
         const int t = t_begin + u;
@@ -299,8 +338,10 @@ conv_decode_vec_kernel(const T *__restrict__ x, const float *__restrict__ w, int
 template <typename T, int W>
 cudaError_t conv_prefill_vec(const T *x, const float *w, const int32_t *cu, int num_seqs, int total_tokens, int C,
                              const float *state_in, T *y, float *state_out, cudaStream_t st) {
+    // token tiles, then (with a new state to write) rows for the documents shorter than W - 1
+    const int short_rows = state_out && W > 1 ? (num_seqs + kShortDocs - 1) / kShortDocs : 0;
     dim3 grid((unsigned)((C / 4 + kConvThreads - 1) / kConvThreads),
-              (unsigned)((total_tokens + kVecTile - 1) / kVecTile));
+              (unsigned)((total_tokens + kVecTile - 1) / kVecTile + short_rows));
     conv_prefill_vec_kernel<T, W><<<grid, kConvThreads, 0, st>>>(x, w, cu, num_seqs, total_tokens, C, state_in, y,
                                                                   state_out);
     return cudaGetLastError();
@@ -325,7 +366,8 @@ bool vec4_ok(int C, const void *x, const void *y, const float *s0, const float *
 template <typename T>
 cudaError_t conv_prefill_t(const void *x, const float *w, const int32_t *cu, int num_seqs, int total_tokens, int C,
                            int W, const float *state_in, void *y, float *state_out, cudaStream_t st) {
-    if (total_tokens > 0 && vec4_ok<T>(C, x, y, state_in, state_out)) {
+    const bool vec = total_tokens > 0 && vec4_ok<T>(C, x, y, state_in, state_out);
+    if (vec) {  // (its launch also writes the states of the documents shorter than W - 1)
         const T *xt = static_cast<const T *>(x);
         T *yt = static_cast<T *>(y);
         cudaError_t e;
@@ -347,7 +389,7 @@ cudaError_t conv_prefill_t(const void *x, const float *w, const int32_t *cu, int
                                                               state_in, (T *)y, state_out);
         if (cudaError_t e = cudaGetLastError()) return e;
     }
-    if (state_out && W > 1 && num_seqs > 0) {
+    if (!vec && state_out && W > 1 && num_seqs > 0) {
         dim3 grid((unsigned)((C + kConvThreads - 1) / kConvThreads), (unsigned)num_seqs);
         conv_short_docs_kernel<<<grid, kConvThreads, 0, st>>>(cu, num_seqs, C, W, state_in, state_out);
         return cudaGetLastError();
