@@ -99,7 +99,7 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const kda::TcPlan plan =
-        path == kda::PATH_TC ? kda::tc_plan(num_seqs, H, total_tokens, fu.gate != nullptr) : kda::TC_THREE;
+        path == kda::PATH_TC ? kda::tc_plan(num_seqs, H, total_tokens) : kda::TC_THREE;
     const bool flags = plan != kda::TC_THREE;
     cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace,
                                             flags ? static_cast<char *>(workspace) + lay.flags_off : nullptr,

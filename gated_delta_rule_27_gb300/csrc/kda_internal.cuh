@@ -199,10 +199,10 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 // Launch plans of the tensor-core prefill: three kernels (preparation, state, output); the preparation
 // followed by one cooperative launch running the state chains with the output units alongside (chain); or one
 // cooperative launch of chains beside groups that prepare the records and then form the outputs (pipe).  The
-// last two need the workspace's progress flags zeroed before they start.  `gated`: the call fuses the gated
-// output normalisation (heavier output units, which the pipe plan forms only after its preparations).
+// last two need the workspace's progress flags zeroed before they start.  The automatic choice takes the pipe
+// plan or the state pass plan; the chain plan runs when the test hook forces it.
 enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3 };
-TcPlan tc_plan(int num_seqs, int H, int total_tokens, bool gated = false);
+TcPlan tc_plan(int num_seqs, int H, int total_tokens);
 
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.
 void testing_set_plan(int plan);

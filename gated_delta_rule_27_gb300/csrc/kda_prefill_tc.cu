@@ -2167,14 +2167,13 @@ void testing_set_fault(int fault, long long wait_ns) {
 }
 int testing_fault() { return g_test_fault.load(); }
 
-TcPlan tc_plan(int num_seqs, int H, int total_tokens, bool gated) {
-    // Without the gated output normalisation: the pipe plan for at most kPipeChainMax chains of 64 columns,
-    // else the preparation and the state pass that forms the outputs itself (two kernels).  With it (whole
-    // rows needed per output): the chain plan while the chains of 32 columns leave at least kChainMinWorkers
-    // SMs for the output groups, else preparation, state pass and output pass.  Measured on one document of
-    // 4096 tokens: 16 heads pipe 103 us, chain 130, two kernels 134; 24 heads two kernels 164, chain 172,
-    // pipe 169; with the gated norm at 16 heads chain 136, pipe 141.  A plan forced by the test hook is taken
-    // wherever it can run.
+TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
+    // The pipe plan for at most kPipeChainMax chains of 64 columns, else the preparation and the state pass
+    // (which, without the gated output normalisation, forms the outputs itself; with it, an output pass
+    // follows, since that normalisation needs whole rows).  Measured on one document of 4096 tokens (pass
+    // times with the host calls): 16 heads pipe 108 us, chain 143, three 146; 24 heads three 163, pipe 170,
+    // chain 177; with the fused q/k and gated output norms, 16 heads pipe 140, chain 154, three 166; 24 heads
+    // three 205, pipe 215, chain 250.  The chain plan is taken only when the test hook forces it.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int forced = g_test_plan.load();
@@ -2186,7 +2185,6 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens, bool gated) {
     const bool chain_fits = chains32 + kChainMinWorkers <= d.sms;
     if (forced == TC_PIPE) return pipe_fits ? TC_PIPE : TC_THREE;
     if (forced == TC_CHAIN) return chain_fits ? TC_CHAIN : TC_THREE;
-    if (gated) return chain_fits ? TC_CHAIN : TC_THREE;
     return pipe_fits && chains64 <= kPipeChainMax ? TC_PIPE : TC_THREE;
 }
 
