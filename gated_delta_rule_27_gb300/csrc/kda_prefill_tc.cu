@@ -157,7 +157,7 @@ struct PrepShared {
     __align__(16) float F[kD];
     __align__(16) float Em[kD];
     __align__(16) float blast[kD];
-    float half[kD], lo[2][kD], hi[2][kD];
+    float half[kD], gabs[2][kD];
     float invk[kL], invq[kL];
     int abort;
 };
@@ -196,11 +196,13 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, const P
         for (int r = 0; r < 16; ++r) {
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int s = 0; s + 1 < r; s += 2) {
-                a0 = fmaf(Ab[(r << 4) + s], x[s], a0);
-                a1 = fmaf(Ab[(r << 4) + s + 1], x[s + 1], a1);
+            for (int s4 = 0; 4 * s4 < r; ++s4) {  // the row's entries left of the diagonal, four per load
+                const float4 av = *reinterpret_cast<const float4 *>(Ab + (r << 4) + 4 * s4);
+                a0 = fmaf(av.x, x[4 * s4], a0);
+                if (4 * s4 + 1 < r) a1 = fmaf(av.y, x[4 * s4 + 1], a1);
+                if (4 * s4 + 2 < r) a0 = fmaf(av.z, x[4 * s4 + 2], a0);
+                if (4 * s4 + 3 < r) a1 = fmaf(av.w, x[4 * s4 + 3], a1);
             }
-            if (r & 1) a0 = fmaf(Ab[(r << 4) + r - 1], x[r - 1], a0);
             x[r] = r < j ? 0.f : (r == j ? 1.f : -(a0 + a1));
         }
         float *Td = T + tri_blk(blk, blk);
@@ -391,8 +393,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
                              bool dep_wait = false) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
     float *s_half = sh.half, *s_invk = sh.invk, *s_invq = sh.invq;
-    float(*s_lo)[kD] = sh.lo;
-    float(*s_hi)[kD] = sh.hi;
+    float(*s_gabs)[kD] = sh.gabs;
     int &s_abort = sh.abort;
     const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
@@ -451,33 +452,30 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         }
         // (so every row's b is a valid row's: b_r = b_{Lc-1} past the end, inside the valid rows' range)
         float bcol[32];
-        float acc = 0.f;
+        float acc = 0.f, aabs = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-            acc += Gf[(r0 + u) * kD + c];
+            const float gv = Gf[(r0 + u) * kD + c];
+            acc += gv;
+            aabs += fabsf(gv);
             bcol[u] = acc;
         }
         if (hh == 0) s_half[c] = acc;
+        s_gabs[hh][c] = aabs;
         grp.sync();  // all of g has been read (b may now go to its swizzled places); s_half is final
         const float off = hh ? s_half[c] : 0.f;
-        float lo = INFINITY, hi = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const float b = bcol[u] + off;
-            lo = fminf(lo, b);
-            hi = fmaxf(hi, b);
-            Gf[bswz(r0 + u, c)] = b;
-        }
+        for (int u = 0; u < 32; ++u) Gf[bswz(r0 + u, c)] = bcol[u] + off;
         if (hh) s_blast[c] = bcol[31] + off;  // row 63's b is the last valid row's
-        s_lo[hh][c] = lo;
-        s_hi[hh][c] = hi;
         grp.sync();
         bool bad = false;
         float bm = 0.f;
         if (tid < kD) {
             bm = Gf[bswz((Lc - 1) >> 1, c)];  // the middle token's
-            const float bmin = fminf(s_lo[0][c], s_lo[1][c]), bmax = fmaxf(s_hi[0][c], s_hi[1][c]);
-            bad = bmax - bm > kMaxHalfRange || bm - bmin > kMaxHalfRange || !(bmax - bmin < INFINITY);
+            // |b_r - b_m| is at most the sum of |g| between r and m: within each half's sum for a full chunk
+            // (m = 31), within the whole chunk's otherwise (NaN or infinite gates fail the test as well)
+            const float a0 = s_gabs[0][c], a1 = s_gabs[1][c];
+            bad = Lc == kL ? !(a0 <= kMaxHalfRange && a1 <= kMaxHalfRange) : !(a0 + a1 <= kMaxHalfRange);
         }
         // Reference point of the factorised exponentials: the middle token; a chunk whose range is too
         // wide for that takes exact A and P and the chunk start as reference (exp(b_r) <= 1 for
