@@ -174,3 +174,31 @@ def test_pipe_plan_at_its_thresholds(H):
     o_ref, S_ref, _ = oracle_prefill(inp, S0=inp.S0)
     assert rel(o_a, o_ref) <= TOL[torch.bfloat16], rel(o_a, o_ref)
     assert rel(S_a, S_ref) <= TOL[torch.bfloat16], rel(S_a, S_ref)
+
+
+@pytest.mark.parametrize("plan", ["pipe", "three", "chain"])
+@pytest.mark.parametrize("lengths,bad", [([300], [0, 301]), ([300], [1, 300]), ([200, 100], [0, 250, 240])])
+def test_invalid_cu_seqlens_write_nothing_on_the_tensor_core_paths(plan, lengths, bad):
+    """cu_seqlens that fail the chunk index kernel's checks (not starting at 0, not ending at the token count,
+    decreasing) leave o and S_final untouched under every plan, the pipe plan's early start for a single
+    document included, and are reported; a valid call on the same workspace afterwards is right."""
+    inp = workloads.prefill_inputs(lengths, H=4, d=128, dtype=torch.bfloat16, seed=71)
+    q, k, v, g, beta, cu_ok = to_device(inp)
+    T, H, d = q.shape
+    N = len(lengths)
+    ws = libkda.new_workspace(T, N, H, d, d, libkda.KDA_BF16, 64, dev())
+    libkda.testing_set_plan({"three": libkda.PLAN_THREE, "chain": libkda.PLAN_CHAIN, "pipe": libkda.PLAN_PIPE}[plan])
+    try:
+        o = torch.full_like(v, 7.0)
+        S = torch.full((N, H, d, d), 7.0, device=dev())
+        cu = torch.tensor(bad, dtype=torch.int32, device=dev())
+        libkda.kda_prefill_chunked(q, k, v, g, beta, cu, o, S_final=S, workspace=ws, chunk_size=64)
+        assert libkda.kda_prefill_check(ws) == libkda.KDA_ERR_INVALID_ARG
+        assert bool((o == 7.0).all()) and bool((S == 7.0).all())
+        libkda.kda_prefill_chunked(q, k, v, g, beta, cu_ok, o, S_final=S, workspace=ws, chunk_size=64)
+        assert libkda.kda_prefill_check(ws) == libkda.KDA_OK
+    finally:
+        libkda.testing_set_plan(libkda.PLAN_AUTO)
+    o_ref, S_ref, _ = oracle_prefill(inp)
+    assert rel(o, o_ref) <= TOL[torch.bfloat16]
+    assert rel(S, S_ref) <= TOL[torch.bfloat16]
