@@ -1497,8 +1497,15 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
             rok = tc::wait_flag_geq(rflag, 1, flag_wait_ns);
             tc::fence_proxy_async_global();
         }
+        // a unit taken behind the chains finds its state image published already: both loads go at once
+        const bool img_now = sflag && !dep_wait && tc::ld_acquire_gpu(sflag) >= kNTile;
+        if (img_now) tc::fence_proxy_async_global();
         tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
         tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
+        if (img_now) {
+            tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
+            tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+        }
         bool ok = tc::mbar_wait(&bars->load, ph) && rok;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
         constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
@@ -1512,12 +1519,14 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
         }
         // ... then the image of S_c (written by the state pass)
         if (dep_wait) tc::grid_dep_wait();
-        if (sflag) {
-            ok = tc::wait_flag_geq(sflag, kNTile, flag_wait_ns) && ok;
-            tc::fence_proxy_async_global();
+        if (!img_now) {
+            if (sflag) {
+                ok = tc::wait_flag_geq(sflag, kNTile, flag_wait_ns) && ok;
+                tc::fence_proxy_async_global();
+            }
+            tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
+            tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
         }
-        tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
-        tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
         ok = tc::mbar_wait(&bars->sload, ph) && ok;
         *grp.ok = ok;
         if (ok) {
