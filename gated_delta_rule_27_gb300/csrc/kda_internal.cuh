@@ -74,7 +74,7 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
 }
 
 // Tensor-core record (d = 128, L = 64).  Every operand is stored as the exact
-// shared-memory image its consumer loads (bf16, 128-byte swizzled), so each
+// shared-memory image its consumer loads (bf16, swizzled), so each
 // consumer moves its part of a record with one or two bulk copies.  The state
 // pass reads [Mc, Qp) plus its column tile of Ut and writes S; the output
 // pass reads [Qp, bytes) in one piece.
@@ -86,8 +86,9 @@ __host__ __device__ inline SimtRecord simt_record(int L, int dk, int dv) {
 //   P      intra-chunk scores, K-major [64 tokens][64 tokens]                   8 KB
 //   Ut     Ut^T, K-major [128 d_v][64 tokens]                                  16 KB
 //   S      the chunk's incoming state as the state pass multiplied it: bf16
-//          K-major [128 d_v rows][128 d_k], 2 panels of 16 KB (written by the
-//          state pass, each chain filling its rows of both panels)             32 KB
+//          MN-major [128 d_k rows][128 d_v], four 32-column chunks of 8 KB with
+//          the 64-byte swizzle (written by the state pass, each chain its own
+//          chunks in one piece)                                                32 KB
 struct TcRecord {
     size_t Mc, gamma, Kend, Qp, P, Ut, S, state_part, out_part, bytes;
 };

@@ -937,7 +937,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // A chain is one (document, head, TN-column tile of S), TN = 32 or 64, run by one CTA sequentially over the
 // document's chunks.  Its shared memory: NB record buffers (M', gamma and Kend, then the chain's rows of Ut^T),
 // with FOLD (the chain also forms its columns of each chunk's output) a ring of two (Qp, P) images, and a ring
-// of NS bf16 images of S^T (the B operand of M' S).
+// of NS bf16 images of S (the MN-major B operand of M' S, in the record's layout).
 template <int TN, int NB = 3, int NS = (TN == 32 ? 5 : 3), bool FOLD = false>
 struct ChainCfg {
     static_assert(TN == 32 || TN == 64, "column tile of a chain");
@@ -948,8 +948,7 @@ struct ChainCfg {
     static constexpr uint32_t Mc = 0, gam = 32768, Kend = 33792, Ut = 50176;
     static constexpr uint32_t kUt = (uint32_t)TN * 128;        // the chain's rows of Ut^T: 4 / 8 KB
     static constexpr uint32_t kBuf = Ut + kUt;                 // a multiple of 1 KB (operand alignment)
-    static constexpr uint32_t kPanel = (uint32_t)TN * 128;     // one 64-wide K panel of the image
-    static constexpr uint32_t kImg = 2 * kPanel;
+    static constexpr uint32_t kImg = (uint32_t)TN * 256;       // the image: TN / 32 column chunks of 8 KB
     static constexpr uint32_t kQP = 24576;                     // Qp (16 KB) then P (8 KB), as in the record
     static constexpr uint32_t QB = kNBuf * kBuf;               // the (Qp, P) ring (FOLD), placed before the images
     static constexpr uint32_t SB = QB + (FOLD ? 2 * kQP : 0);  // (the 128-row operands' unused upper rows of
@@ -979,24 +978,18 @@ __device__ __forceinline__ void prefetch_record(const char *rec, int tile) {
 }
 constexpr int kChainL2Ahead = 3;  // records pulled into L2 this many chunks beyond the buffered ones
 
-// Writes S[i][jbase + j] (j < NC, this thread's columns) into the K-major S^T image (element (jbase + j, i),
-// K panels `panel_bytes` apart).  Rows i and i ^ 1 (lanes of one warp) trade values so that each stores whole
-// 4-byte words holding rows (i & ~1, i | 1) of one column: the even lane the columns j < NC / 2, the odd lane
-// the others in a rotated order, which keeps a warp's 32 stores on 32 distinct banks.
+// Writes S[i][jbase + j] (j < NC, this thread's columns) into an image of S as the MN-major B operand of the
+// state MMA: 32-column chunks of 128 rows x 64 bytes (8 KB apart), each row i holding its 32 columns in bf16,
+// rows 64 bytes apart, with the 64-byte swizzle (16-byte unit u of row i at u ^ ((i / 2) % 4)).  NC / 8
+// 16-byte stores; the 32 rows of a warp cover every bank once per 8 rows.
 template <int NC>
-__device__ __forceinline__ void store_state_cols(uint8_t *SB, uint32_t panel_bytes, int i, int jbase,
-                                                 const float (&S)[NC]) {
-    constexpr int HALF = NC / 2;
-    uint8_t *p = SB + (uint32_t)(i >> 6) * panel_bytes;
-    const int odd = i & 1, ie = i & ~1;
+__device__ __forceinline__ void store_state_rows(uint8_t *SB, int i, int jbase, const float (&S)[NC]) {
+    uint8_t *row = SB + (uint32_t)(i >> 3) * 512u + (uint32_t)(i & 7) * 64u;
+    const uint32_t sw = ((uint32_t)i >> 1) & 3u;
 #pragma unroll
-    for (int u = 0; u < HALF; ++u) {
-        const int ja = u, jb = HALF + ((u + HALF / 2) % HALF);  // the even and the odd lane's column of this step
-        const float give = odd ? S[ja] : S[jb];                  // what the partner needs from this row
-        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-        const int j = jbase + (odd ? jb : ja);
-        const float lo = odd ? got : S[ja], hi = odd ? S[jb] : got;
-        *reinterpret_cast<uint32_t *>(p + tc::sw128_offset(j, ie & 63)) = pack_bf16x2(lo, hi);
+    for (int q = 0; q < NC / 8; ++q) {
+        const uint32_t j = (uint32_t)(jbase + 8 * q);
+        *reinterpret_cast<uint4 *>(row + (j >> 5) * 8192u + ((((j >> 3) & 3u) ^ sw) << 4)) = pack8_at(S + 8 * q);
     }
 }
 
@@ -1081,7 +1074,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
     }
     bool ok = true;
     if (nchunks > 0) {
-        if (epi) store_state_cols<NC>(sm + Cfg::SB, Cfg::kPanel, i, NC * hcol, S);
+        if (epi) store_state_rows<NC>(sm + Cfg::SB, i, NC * hcol, S);
         tc::fence_async_smem();
         char *rec_h = ws + records_off + (size_t)h * record_bytes;  // record of (slot 0, head h)
         const size_t rec_stride = (size_t)H * record_bytes;          // one chunk slot further
@@ -1170,7 +1163,9 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
             const uint32_t panel = (uint32_t)(warp - kStateEpiWarps);
             constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
             constexpr uint64_t kKendMn = tc::smem_desc_base(8192, 1024, tc::SW_128B);
-            constexpr uint32_t idN = tc::idesc_bf16_f32(128, TN, false, false);
+            // the image: MN-major, 32-column chunks 8 KB apart, 8-row groups of 512 bytes
+            constexpr uint64_t kImgMn = tc::smem_desc_base(8192, 512, tc::SW_64B);
+            constexpr uint32_t idN = tc::idesc_bf16_f32(128, TN, false, true);
             constexpr uint32_t idKU = tc::idesc_bf16_f32(128, TN, true, false);
             // Kend^T Ut of chunk c (the state-free part of its update) into panel 0 of TMEM region c % 2, ahead
             // of the chunk's M' S MMAs, which accumulate onto it
@@ -1192,10 +1187,10 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     if (ok) {
                         if (panel == 0 && c == 0) kend_ut(0);
                         const uint64_t da = tc::smem_desc(kKmaj, tc::smem_u32(buf + Cfg::Mc + panel * 16384u));
-                        const uint64_t db = tc::smem_desc(kKmaj, tc::smem_u32(sbc + panel * Cfg::kPanel));
+                        const uint64_t db = tc::smem_desc(kImgMn, tc::smem_u32(sbc + panel * 4096u));  // rows 64 panel ..
                         const uint32_t d = tmem + (uint32_t)(2 * TN * (c & 1)) + (uint32_t)TN * panel;
-                        for (int s = 0; s < 4; ++s)  // K steps of 16: +32 bytes, +2 in the start-address field
-                            tc::mma_bf16(d, da + 2u * (uint32_t)s, db + 2u * (uint32_t)s, idN, panel == 0 || s > 0);
+                        for (int s = 0; s < 4; ++s)  // K steps of 16: M' +32 bytes, the image +1 KB (+2, +64 in the fields)
+                            tc::mma_bf16(d, da + 2u * (uint32_t)s, db + 64u * (uint32_t)s, idN, panel == 0 || s > 0);
                     }
                     tc::mma_commit(&a_bar);  // always: the epilogue counts on one completion per chunk
                     if (panel == 0 && ok && c + 1 < nchunks) {
@@ -1224,7 +1219,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                 constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
                 constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);
                 constexpr uint32_t idK = tc::idesc_bf16_f32(128, TN, false, false);
-                constexpr uint32_t idMN = tc::idesc_bf16_f32(128, TN, true, false);
+                constexpr uint64_t kImgMn = tc::smem_desc_base(8192, 512, tc::SW_64B);
+                constexpr uint32_t idMN = tc::idesc_bf16_f32(128, TN, true, true);
                 for (int c = 0; c < nchunks; ++c) {
                     const int sl = c % NS, qs = c & 1, bsel = c % NB;
                     if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / NS) & 1));
@@ -1242,7 +1238,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                                          tc::smem_desc(kKmaj, tc::smem_u32(buf + Cfg::Ut + s4 * 32)), idK, s4 > 0);
                         for (int s8 = 0; s8 < 8; ++s8)  // + Qp S_c over d_k
                             tc::mma_bf16(d, tc::smem_desc(kQpMn, tc::smem_u32(qb + s8 * 2048)),
-                                         tc::smem_desc(kKmaj, tc::smem_u32(sbc + (s8 >> 2) * Cfg::kPanel + (s8 & 3) * 32)),
+                                         tc::smem_desc(kImgMn, tc::smem_u32(sbc + s8 * 1024)),
                                          idMN, true);
                     }
                     tc::mma_commit(&o_full[qs]);  // always: the output warps count on one completion per chunk
@@ -1297,11 +1293,10 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                     // image 0 was written before the CTA barrier; image c >= 1 by chunk c - 1's epilogue
                     if (c > 0) ok = ok && tc::mbar_wait(&img_full[sl], (uint32_t)(((c - 1) / NS) & 1));
                     if (ok) {
-                        // S_c's image, this chain's rows of both panels, into chunk c's record
+                        // S_c's image, this chain's column chunks, into chunk c's record
                         const uint8_t *sbc = sm + Cfg::SB + (uint32_t)sl * Cfg::kImg;
                         char *rec = rec_h + (size_t)(first + c) * rec_stride;
-                        tc::bulk_s2g(rec + R.S + (size_t)tile * Cfg::kPanel, sbc, Cfg::kPanel);
-                        tc::bulk_s2g(rec + R.S + 16384 + (size_t)tile * Cfg::kPanel, sbc + Cfg::kPanel, Cfg::kPanel);
+                        tc::bulk_s2g(rec + R.S + (size_t)tile * Cfg::kImg, sbc, Cfg::kImg);
                         tc::bulk_commit();
                         tc::bulk_wait_read();  // the slot may be rewritten
                     }
@@ -1360,7 +1355,7 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
                                 S[16 * hh + q] = fmaf(gam, S[16 * hh + q], t0[16 * hh + q] + t1[q]);
                         }
                     }
-                    if (img) store_state_cols<NC>(sbn, Cfg::kPanel, i, NC * hcol, S);
+                    if (img) store_state_rows<NC>(sbn, i, NC * hcol, S);
                 }
                 tc::fence_async_smem();
                 tc::tc_fence_before();
@@ -1509,7 +1504,8 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
         bool ok = tc::mbar_wait(&bars->load, ph) && rok;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
         constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
-        constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, false);
+        constexpr uint64_t kSMn = tc::smem_desc_base(8192, 512, tc::SW_64B);     // the image, as the chains write it
+        constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, true);
         constexpr uint32_t id_k = tc::idesc_bf16_f32(128, 128, false, false);
         if (ok) {
             tc::tc_fence_after();
@@ -1533,7 +1529,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
             tc::tc_fence_after();
             for (int s = 0; s < 8; ++s)  // + Qp S_c over d_k
                 tc::mma_bf16(tmem, tc::smem_desc(kQpMn, tc::smem_u32(sm + OutSmem::Qp + s * 2048)),
-                             tc::smem_desc(kKmaj, tc::smem_u32(sm + OutSmem::S + (s >> 2) * 16384 + (s & 3) * 32)),
+                             tc::smem_desc(kSMn, tc::smem_u32(sm + OutSmem::S + s * 1024)),
                              id_mn, true);
         }
         tc::mma_commit(&bars->mma);  // arrives at once when nothing was issued
