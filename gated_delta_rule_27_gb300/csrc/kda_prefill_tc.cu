@@ -1459,19 +1459,31 @@ struct OutGroup {
     }
 };
 
+// An output group's next unit (pipe plan): thread `thread` of the group loads its record, and its state image
+// once published, into the group's shared memory as soon as the current unit's MMAs have completed, and
+// stores what it issued in *pre (0 nothing, 1 the record, 2 both) for that unit's call.
+struct OutNext {
+    const int *unit;  // the claimed unit (slot * H + head), read by `thread` only
+    int units, thread;
+    const int32_t *ready, *sdone;  // per unit: record published; state image count
+    int *pre;
+};
+
 // One (chunk slot, head) of the output pass, t0 / Lc the chunk's first token and
 // length, by a group of 128 threads (warps 0-1 of it write the 64 token rows)
 // whose TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's
 // barrier phases.  P Ut is formed first; the state image is then awaited
 // through the launch dependency with `dep_wait` (the state pass is the
 // previous kernel), or through its publication count at `sflag` (all column
-// tiles), else it must already be complete.  Returns false after recording a
+// tiles), else it must already be complete.  `pre`: what the group's previous
+// unit already loaded for this one (OutNext).  Returns false after recording a
 // timeout in the status word.
 __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bfloat16 *__restrict__ o, char *ws,
                             size_t records_off, size_t record_bytes, int slot, int h, int t0, int Lc, uint8_t *sm,
                             OutBars *bars, uint32_t ph, uint32_t tmem, const OutGroup &grp, const OutNorm &onorm,
                             bool dep_wait = false, const int32_t *sflag = nullptr,
-                            uint64_t flag_wait_ns = kFlagWaitNs, const int32_t *rflag = nullptr) {
+                            uint64_t flag_wait_ns = kFlagWaitNs, const int32_t *rflag = nullptr, int pre = 0,
+                            const OutNext *nx = nullptr) {
     const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
     static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
@@ -1488,18 +1500,21 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
     if (tid == 0) {
         // Qp, P, Ut (written by the preparation; in the pipe plan, once published) ...
         bool rok = true;
-        if (rflag) {
-            rok = tc::wait_flag_geq(rflag, 1, flag_wait_ns);
-            tc::fence_proxy_async_global();
-        }
-        // a unit taken behind the chains finds its state image published already: both loads go at once
-        const bool img_now = sflag && !dep_wait && tc::ld_acquire_gpu(sflag) >= kNTile;
-        if (img_now) tc::fence_proxy_async_global();
-        tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
-        tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
-        if (img_now) {
-            tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
-            tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+        bool img_now = pre == 2;  // (pre >= 1: the record's copy is on its way; 2: the image's too)
+        if (pre == 0) {
+            if (rflag) {
+                rok = tc::wait_flag_geq(rflag, 1, flag_wait_ns);
+                tc::fence_proxy_async_global();
+            }
+            // a unit taken behind the chains finds its state image published already: both loads go at once
+            img_now = sflag && !dep_wait && tc::ld_acquire_gpu(sflag) >= kNTile;
+            if (img_now) tc::fence_proxy_async_global();
+            tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
+            tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
+            if (img_now) {
+                tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
+                tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+            }
         }
         bool ok = tc::mbar_wait(&bars->load, ph) && rok;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
@@ -1535,6 +1550,25 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
         tc::mma_commit(&bars->mma);  // arrives at once when nothing was issued
     }
     __syncwarp();
+    if (nx && tid == nx->thread) {
+        // the next unit's copies into this shared memory, free once this unit's MMAs have completed
+        int p = 0;
+        const int un = *nx->unit;
+        if (un < nx->units && tc::mbar_wait(&bars->mma, ph) && tc::ld_acquire_gpu(nx->ready + un) >= 1) {
+            const char *nrec = ws + records_off + (size_t)un * record_bytes;
+            tc::fence_proxy_async_global();
+            tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
+            tc::bulk_g2s(sm, nrec + R.Qp, OutSmem::S, &bars->load);
+            p = 1;
+            if (tc::ld_acquire_gpu(nx->sdone + un) >= kNTile) {
+                tc::fence_proxy_async_global();
+                tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
+                tc::bulk_g2s(sm + OutSmem::S, nrec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+                p = 2;
+            }
+        }
+        *nx->pre = p;
+    }
     if (warp < 2) {
         // token row r = tid: 128 fp32 accumulators -> 256 bytes of o
         const bool done = tc::mbar_wait(&bars->mma, ph);
@@ -1800,26 +1834,48 @@ struct PipeArgs {
 // Output units taken in (chunk slot, head) order from the output counter by one group of 128 threads, until
 // none is left or a wait gives up (false).  `s_unit` is a shared word of the group.
 __device__ bool pipe_outputs(const PrepParams &pp, const PipeArgs &a, uint8_t *gsm, OutBars *bars, uint32_t tmem,
-                             const OutGroup &og, int *s_unit) {
+                             const OutGroup &og, int *s_unit, int *s_pre) {
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
     const int units = doc_slot0[pp.num_seqs] * H;
     // claimed one ahead by a thread of warp 2, which does not issue the unit's copies and MMAs nor write o
     constexpr int kClaimer = 64;
-    if (og.gtid == kClaimer) *s_unit = atomicAdd(a.out_counter, 1);
+    constexpr TcRecord R = tc_record();
+    // (the claimer pulls the claimed unit's record, the preparation's part, into L2 while the current one runs)
+    auto claim = [&]() {
+        const int un = atomicAdd(a.out_counter, 1);
+        *s_unit = un;
+        if (un < units)
+            tc::bulk_prefetch_l2(pp.ws + pp.records_off + (size_t)un * pp.record_bytes + R.Qp, (uint32_t)(R.S - R.Qp));
+    };
+    if (og.gtid == kClaimer) {
+        claim();
+        *s_pre = 0;
+    }
+    const OutNext nx{s_unit, units, kClaimer, a.ready, a.sdone, s_pre};
     for (uint32_t nout = 0;; ++nout) {
         og.sync();
-        const int u = *s_unit;
+        const int u = *s_unit, pre = *s_pre;
         og.sync();  // every thread has read s_unit before the next claim overwrites it
         if (u >= units) return true;
-        if (og.gtid == kClaimer) *s_unit = atomicAdd(a.out_counter, 1);
+        if (og.gtid == kClaimer) claim();
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
         locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
         if (!output_unit(pp.cu, pp.num_seqs, H, a.o, pp.ws, pp.records_off, pp.record_bytes, slot, h, t0, Lc, gsm,
                          bars, nout & 1u, tmem, og, a.onorm, false, a.sdone + (size_t)slot * H + h, a.flag_wait_ns,
-                         a.ready + (size_t)slot * H + h))
+                         a.ready + (size_t)slot * H + h, pre, &nx)) {
+            // copies still on their way (this unit's, if it left before waiting for them; the next one's) land
+            // before the CTA's shared memory can go away (best effort, 10 ms each)
+            if (og.gtid == kClaimer) {
+                const int pn = *s_pre;
+                if (pre >= 1) tc::mbar_wait(&bars->load, nout & 1u, 10000000ull);
+                if (pre == 2) tc::mbar_wait(&bars->sload, nout & 1u, 10000000ull);
+                if (pn >= 1) tc::mbar_wait(&bars->load, (nout + 1) & 1u, 10000000ull);
+                if (pn == 2) tc::mbar_wait(&bars->sload, (nout + 1) & 1u, 10000000ull);
+            }
             return false;
+        }
     }
 }
 
@@ -1831,7 +1887,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     __shared__ OutBars obars[2];
     __shared__ uint32_t tmem_base;
     PrepShared *psh = reinterpret_cast<PrepShared *>(sm + kPipePrepShared);
-    __shared__ int s_unit[2], s_ok[2], s_go;
+    __shared__ int s_unit[2], s_ok[2], s_go, s_pre[2];
     const int tid = threadIdx.x, g = tid >> 8, gtid = tid & 255;
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
@@ -1917,7 +1973,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         tc::st_release_gpu(pending, 1);
     }
     if (ok && gtid < 128)
-        pipe_outputs(pp, a, gsm, &obars[g], tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, &s_unit[g]);
+        pipe_outputs(pp, a, gsm, &obars[g], tmem, OutGroup{gtid, 3u + (uint32_t)g, &s_ok[g]}, &s_unit[g], &s_pre[g]);
     tc::tc_fence_before();
     __syncthreads();
     if (tid < 32) tc::tmem_dealloc(tmem_base, 512);
