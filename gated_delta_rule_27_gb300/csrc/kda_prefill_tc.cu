@@ -113,8 +113,8 @@ struct PrepSmem {
     static constexpr uint32_t Y = 81920;   // round-1 B operand (k / e1); then P (8 KB)
     static constexpr uint32_t Afp = G;             // compact fp32 A (10 KB)
     static constexpr uint32_t Tfp = G + 10240;     // compact fp32 T (10 KB)
-    static constexpr uint32_t Scr = G + 20480;     // the solve's scratch (6 KB) ...
-    static constexpr uint32_t Tb = G + 20480;      // ... then bf16 T, K-major [r][s] (8 KB)
+    static constexpr uint32_t Scr = G + 20480;     // the solve's scratch (6 KB)
+    static constexpr uint32_t Tb = Y + 8192;       // bf16 T diag(beta), K-major [r][s] (8 KB), written by the solve
     static constexpr uint32_t KendS = G;           // Kend, MN-major [s][c] (16 KB)
     static constexpr uint32_t WT = G + 16384;      // W'^T, K-major [c][s] (16 KB)
     static constexpr uint32_t P = Y;               // P, K-major [r][s] (8 KB)
@@ -186,8 +186,23 @@ __device__ __forceinline__ void write_identity(uint8_t *id, int tid, int n) {
 // substitution; then, with L = I + A split into 32-row halves
 // [[L_lo, 0], [A_hl, L_hi]], each half's lower block is -T_ii A_ij T_jj and
 // the lower-left quarter is -T_hi (A_hl T_lo): four phases of 256 equal items.
-__device__ void unit_lower_inverse(const float *A, float *T, float *scr, const PrepGroup &grp) {
+// Each block of T diag(beta) also goes, in bf16, to the K-major [r][s] image Tb
+// (round 2's B operand) in the first phase after it is final; the blocks above
+// the diagonal are zeroed there while the diagonal blocks are being solved.
+__device__ void unit_lower_inverse(const float *A, float *T, float *scr, uint8_t *Tb, const float *s_beta,
+                                   const PrepGroup &grp) {
     const int tid = grp.tid;
+    // bf16 (T[r][s] beta_s, T[r][s+1] beta_{s+1}) as one 32-bit word of the image
+    auto tb2 = [&](int r, int s, float a, float b) {
+        *reinterpret_cast<uint32_t *>(Tb + tc::sw128_offset(r, s)) = pack_bf16x2(a * s_beta[s], b * s_beta[s + 1]);
+    };
+    if (tid >= 64) {  // the image's blocks above the diagonal: 16-byte units 2.. of rows 0-15, 4.. of rows
+                      // 16-31, 6, 7 of rows 32-47: one per thread
+        const int t = tid - 64;
+        const int r = t < 96 ? t / 6 : (t < 160 ? 16 + (t - 96) / 4 : 32 + (t - 160) / 2);
+        const int u = t < 96 ? 2 + t % 6 : (t < 160 ? 4 + (t - 96) % 4 : 6 + (t - 160) % 2);
+        *reinterpret_cast<uint4 *>(Tb + (uint32_t)r * 128u + ((uint32_t)(u ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (tid < 64) {  // diagonal block blk, column j: (I + A_bb) x = e_j
         const int blk = tid >> 4, j = tid & 15;
         const float *Ab = A + tri_blk(blk, blk);
@@ -210,6 +225,12 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, const P
         for (int r = 0; r < 16; ++r) Td[(r << 4) + j] = x[r];
     }
     grp.sync();
+    {  // the diagonal blocks' image: item (block, row, four columns)
+        const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const float4 t = *reinterpret_cast<const float4 *>(T + tri_blk(blk, blk) + (r << 4) + c4);
+        tb2(16 * blk + r, 16 * blk + c4, t.x, t.y);
+        tb2(16 * blk + r, 16 * blk + c4 + 2, t.z, t.w);
+    }
     {  // F = T_ii A_{i,i-1} for i = 1, 3 (scratch blocks 0, 1): item (b, row, column pair)
         const int b = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2, i = 1 + 2 * b;
         const float *Ti = T + tri_blk(i, i) + (r << 4);
@@ -246,6 +267,7 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, const P
             }
         }
         *reinterpret_cast<float2 *>(T + tri_blk(i, i - 1) + (r << 4) + c2) = make_float2(-acc.x, -acc.y);
+        tb2(16 * i + r, 16 * (i - 1) + c2, -acc.x, -acc.y);
     }
     grp.sync();
     {  // X_ij = sum_{k=j}^{1} A_ik T_kj for (i, j) in {2, 3} x {0, 1} (scratch blocks 2..5)
@@ -287,8 +309,11 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, const P
                 }
             }
         }
-        *reinterpret_cast<float4 *>(T + tri_blk(i, j) + (r << 4) + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        tb2(16 * i + r, 16 * j + c4, -acc.x, -acc.y);  // (the last blocks: only their image is needed)
+        tb2(16 * i + r, 16 * j + c4 + 2, -acc.z, -acc.w);
     }
+    tc::fence_async_smem();  // the image is an MMA operand
+    tc::tc_fence_before();
     grp.sync();
 }
 
@@ -704,32 +729,9 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         }
     }
 
-    // triangular solve in fp32, then T diag(beta) as the bf16 round-2 B operand (K-major [r][s])
+    // triangular solve in fp32, writing T diag(beta) as the bf16 round-2 B operand (K-major [r][s])
     float *Tf = reinterpret_cast<float *>(sm + PrepSmem::Tfp);
-    unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), grp);
-    {
-        // thread (r, q) takes columns 16 q .. 16 q + 15 of row r (one row of a 16 x 16 block of T, absent
-        // above the diagonal blocks), four at a time in an order rotated by q: the four threads of a row
-        // then read distinct banks
-        const int r = tid >> 2, q = tid & 3;
-        uint8_t *Tb = sm + PrepSmem::Tb;
-        const bool blk = q <= (r >> 4);
-        const float *trow = Tf + (blk ? tri_blk(r >> 4, q) + ((r & 15) << 4) : 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int j = (k + q) & 3, s = 16 * q + 4 * j;
-            const float4 t = blk ? *reinterpret_cast<const float4 *>(trow + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 b = *reinterpret_cast<const float4 *>(s_beta + s);
-            uint2 pk;
-            // (T's diagonal blocks hold exact zeros above the diagonal: no mask)
-            pk.x = pack_bf16x2(t.x * b.x, t.y * b.y);
-            pk.y = pack_bf16x2(t.z * b.z, t.w * b.w);
-            *reinterpret_cast<uint2 *>(Tb + tc::sw128_offset(r, s)) = pk;
-        }
-    }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    grp.sync();
+    unit_lower_inverse(Af, Tf, reinterpret_cast<float *>(sm + PrepSmem::Scr), sm + PrepSmem::Tb, s_beta, grp);
     tc::tc_fence_after();
     if (tid == 0) {  // P is final: its image goes to the record for the output pass
         tc::bulk_s2g(rec + R.P, sm + PrepSmem::P, 8192);
