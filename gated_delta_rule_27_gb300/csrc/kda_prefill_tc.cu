@@ -437,6 +437,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         // the gates first: the cumulative sums run while k, q, v are still arriving
         tc::mbar_arrive_expect_tx(&bars->g, 32768);
         tc::tma_load_3d(sm + PrepSmem::G, p.tm_g, 0, h, t0, &bars->g);
+        tc::bulk_wait_read();  // the group's previous unit's M' copy has read X (the one copy it left pending)
         tc::mbar_arrive_expect_tx(&bars->load, 6 * 8192);
         tc::tma_load_3d(sm + PrepSmem::X, p.tm_k, 0, h, t0, &bars->load);
         tc::tma_load_3d(sm + PrepSmem::X + 8192, p.tm_q, 0, h, t0, &bars->load);
@@ -853,12 +854,16 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         return false;
     }
     if (tid == 0) {
-        tc::bulk_s2g(rec + R.Mc, sm + PrepSmem::X, 32768);
         tc::bulk_s2g(rec + R.Kend, sm + PrepSmem::KendS, 16384);  // round 3 has consumed it
         tc::bulk_s2g(rec + R.Qp, sm + PrepSmem::WT, 16384);
         tc::bulk_commit();
+        tc::bulk_s2g(rec + R.Mc, sm + PrepSmem::X, 32768);
+        tc::bulk_commit();
+        // G and V are free for the next unit's tiles once all but the M' copy have read them; that copy may
+        // still be reading X when this returns: the next unit waits for it before loading X, and the caller
+        // before it reuses the shared memory otherwise or leaves
+        tc::bulk_wait_read_all_but_one();
     }
-    if (tid == 0) tc::bulk_wait_read();  // shared memory must outlive the copies' reads
     return true;
 }
 
@@ -928,6 +933,7 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             break;
         __syncthreads();  // the claim is visible to every thread
     }
+    if (tid == 0) tc::bulk_wait_read();  // the last unit's M' copy has read shared memory
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
@@ -1968,6 +1974,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         }
     }
     if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
+    if (gtid == 0) tc::bulk_wait_read();  // the last unit's M' copy has read the group's shared memory
     if (early) tc::grid_dep_wait();  // (a group that prepared nothing has not waited yet)
     if (gtid == 0 && pending) {  // before any output unit: a chain may be waiting for this record
         tc::bulk_wait_all();
