@@ -921,9 +921,10 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                          records_off, record_bytes, qk_norm, qk_eps};
     int32_t *counter = reinterpret_cast<int32_t *>(ws) + kPrepCounterWord;
     const PrepGroup grp{tid, 0u};
+    // s_unit is read at the top of each iteration; the unit overwrites it with its claim between two of its
+    // own barriers, after every thread's read and before the unit's last barrier
     for (uint32_t n = 0;; ++n) {
         const int u = s_unit;
-        __syncthreads();  // every thread has read s_unit before the next claim overwrites it
         if (u >= units) break;
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
@@ -931,7 +932,6 @@ prefill_prepare_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (!prepare_unit(prm, slot, h, t0, Lc, sm, &bars, n & 1u, tmem_base, ident, nullptr, grp, psh, counter,
                           (int)gridDim.x, &s_unit, units))
             break;
-        __syncthreads();  // the claim is visible to every thread
     }
     if (tid == 0) tc::bulk_wait_read();  // the last unit's M' copy has read shared memory
     tc::tc_fence_before();
@@ -1944,10 +1944,11 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     // (which also pulls its tiles into L2).
     const int nw = (int)gridDim.x - a.n_chain, wid = (int)blockIdx.x - a.n_chain;
     if (gtid == 0) s_unit[g] = g * nw + wid;
+    grp.sync();
+    // s_unit is read at the top of each iteration; the unit overwrites it with its claim between two of its
+    // own barriers, after every thread's read and before the unit's last barrier
     for (;;) {
-        grp.sync();
         const int u = s_unit[g];
-        grp.sync();  // every thread has read s_unit before the next claim overwrites it
         if (u >= units) break;
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
@@ -1973,6 +1974,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
             pending = nullptr;
         }
     }
+    grp.sync();  // every thread has read s_unit before the output phase claims into it
     if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
     if (gtid == 0) tc::bulk_wait_read();  // the last unit's M' copy has read the group's shared memory
     if (early) tc::grid_dep_wait();  // (a group that prepared nothing has not waited yet)
