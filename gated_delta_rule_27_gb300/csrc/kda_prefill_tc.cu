@@ -270,47 +270,71 @@ __device__ void unit_lower_inverse(const float *A, float *T, float *scr, uint8_t
         tb2(16 * i + r, 16 * (i - 1) + c2, -acc.x, -acc.y);
     }
     grp.sync();
-    {  // X_ij = sum_{k=j}^{1} A_ik T_kj for (i, j) in {2, 3} x {0, 1} (scratch blocks 2..5)
-        const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = j; k < 2; ++k) {
-            const float *Ai = A + tri_blk(i, k) + (r << 4);
-            const float *Tk = T + tri_blk(k, j) + c4;
+    {  // X_ij = sum_{k=j}^{1} A_ik T_kj, (i, j) in {2, 3} x {0, 1} (scratch blocks 2..5): item (i, row, column
+       // pair) forms X_i0 (two block products) and X_i1 (one), the same work for every thread
+        const int i = 2 + (tid >> 7), r = (tid >> 3) & 15, c2 = (tid & 7) * 2;
+        const float *A0 = A + tri_blk(i, 0) + (r << 4), *A1 = A + tri_blk(i, 1) + (r << 4);
+        const float *T00 = T + tri_blk(0, 0) + c2, *T10 = T + tri_blk(1, 0) + c2, *T11 = T + tri_blk(1, 1) + c2;
+        float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int k4 = 0; k4 < 16; k4 += 4) {
-                const float4 a = *reinterpret_cast<const float4 *>(Ai + k4);
-                const float av[4] = {a.x, a.y, a.z, a.w};
+        for (int k4 = 0; k4 < 16; k4 += 4) {  // k = 0 for X_i0, k = 1 for X_i1
+            const float4 a0 = *reinterpret_cast<const float4 *>(A0 + k4);
+            const float4 a1 = *reinterpret_cast<const float4 *>(A1 + k4);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 t = *reinterpret_cast<const float4 *>(Tk + ((k4 + u) << 4));
-                    acc.x = fmaf(av[u], t.x, acc.x); acc.y = fmaf(av[u], t.y, acc.y);
-                    acc.z = fmaf(av[u], t.z, acc.z); acc.w = fmaf(av[u], t.w, acc.w);
-                }
+            for (int u = 0; u < 4; ++u) {
+                const float2 t0 = *reinterpret_cast<const float2 *>(T00 + ((k4 + u) << 4));
+                const float2 t1 = *reinterpret_cast<const float2 *>(T11 + ((k4 + u) << 4));
+                x0.x = fmaf(av0[u], t0.x, x0.x); x0.y = fmaf(av0[u], t0.y, x0.y);
+                x1.x = fmaf(av1[u], t1.x, x1.x); x1.y = fmaf(av1[u], t1.y, x1.y);
             }
         }
-        *reinterpret_cast<float4 *>(scr + 512 + (xb << 8) + (r << 4) + c4) = acc;
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {  // k = 1 for X_i0
+            const float4 a1 = *reinterpret_cast<const float4 *>(A1 + k4);
+            const float av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 t = *reinterpret_cast<const float2 *>(T10 + ((k4 + u) << 4));
+                x0.x = fmaf(av1[u], t.x, x0.x); x0.y = fmaf(av1[u], t.y, x0.y);
+            }
+        }
+        float *Xi = scr + 512 + (((i - 2) << 1) << 8) + (r << 4) + c2;
+        *reinterpret_cast<float2 *>(Xi) = x0;
+        *reinterpret_cast<float2 *>(Xi + 256) = x1;
     }
     grp.sync();
-    {  // T_ij = -sum_{k=2}^{i} T_ik X_kj
-        const int xb = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4, i = 2 + (xb >> 1), j = xb & 1;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 2; k <= i; ++k) {
-            const float *Ti = T + tri_blk(i, k) + (r << 4);
-            const float *Xk = scr + 512 + ((((k - 2) << 1) + j) << 8) + c4;
+    {  // T_ij = -sum_{k=2}^{i} T_ik X_kj: item (j, row, column pair) forms T_2j (one block product) and T_3j
+       // (two), the same work for every thread; only their image is needed
+        const int j = tid >> 7, r = (tid >> 3) & 15, c2 = (tid & 7) * 2;
+        const float *T22 = T + tri_blk(2, 2) + (r << 4), *T32 = T + tri_blk(3, 2) + (r << 4);
+        const float *T33 = T + tri_blk(3, 3) + (r << 4);
+        const float *X2 = scr + 512 + (j << 8) + c2, *X3 = scr + 512 + ((2 + j) << 8) + c2;
+        float2 y2 = make_float2(0.f, 0.f), y3 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int k4 = 0; k4 < 16; k4 += 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(Ti + k4);
-                const float tv[4] = {t.x, t.y, t.z, t.w};
+        for (int k4 = 0; k4 < 16; k4 += 4) {  // k = 2
+            const float4 ta = *reinterpret_cast<const float4 *>(T22 + k4);
+            const float4 tb = *reinterpret_cast<const float4 *>(T32 + k4);
+            const float tv2[4] = {ta.x, ta.y, ta.z, ta.w}, tv3[4] = {tb.x, tb.y, tb.z, tb.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 x = *reinterpret_cast<const float4 *>(Xk + ((k4 + u) << 4));
-                    acc.x = fmaf(tv[u], x.x, acc.x); acc.y = fmaf(tv[u], x.y, acc.y);
-                    acc.z = fmaf(tv[u], x.z, acc.z); acc.w = fmaf(tv[u], x.w, acc.w);
-                }
+            for (int u = 0; u < 4; ++u) {
+                const float2 x = *reinterpret_cast<const float2 *>(X2 + ((k4 + u) << 4));
+                y2.x = fmaf(tv2[u], x.x, y2.x); y2.y = fmaf(tv2[u], x.y, y2.y);
+                y3.x = fmaf(tv3[u], x.x, y3.x); y3.y = fmaf(tv3[u], x.y, y3.y);
             }
         }
-        tb2(16 * i + r, 16 * j + c4, -acc.x, -acc.y);  // (the last blocks: only their image is needed)
-        tb2(16 * i + r, 16 * j + c4 + 2, -acc.z, -acc.w);
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {  // k = 3
+            const float4 tc4 = *reinterpret_cast<const float4 *>(T33 + k4);
+            const float tv[4] = {tc4.x, tc4.y, tc4.z, tc4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 x = *reinterpret_cast<const float2 *>(X3 + ((k4 + u) << 4));
+                y3.x = fmaf(tv[u], x.x, y3.x); y3.y = fmaf(tv[u], x.y, y3.y);
+            }
+        }
+        tb2(32 + r, 16 * j + c2, -y2.x, -y2.y);
+        tb2(48 + r, 16 * j + c2, -y3.x, -y3.y);
     }
     tc::fence_async_smem();  // the image is an MMA operand
     tc::tc_fence_before();
