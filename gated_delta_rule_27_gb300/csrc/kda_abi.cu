@@ -101,9 +101,11 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const float
     const kda::TcPlan plan =
         path == kda::PATH_TC ? kda::tc_plan(num_seqs, H, total_tokens) : kda::TC_THREE;
     const bool flags = plan != kda::TC_THREE;
-    cudaError_t e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace,
-                                            flags ? static_cast<char *>(workspace) + lay.flags_off : nullptr,
-                                            flags ? lay.flags_bytes : 0, s, marks);
+    cudaError_t e = cudaSuccess;
+    if (!(path == kda::PATH_TC && kda::pipe_self_indexed(plan, num_seqs)))
+        e = kda::launch_chunk_index(cu_seqlens, num_seqs, total_tokens, L, workspace,
+                                    flags ? static_cast<char *>(workspace) + lay.flags_off : nullptr,
+                                    flags ? lay.flags_bytes : 0, s, marks);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (path == kda::PATH_TC)
         e = kda::launch_prefill_tc(q, k, v, g, beta, cu_seqlens, num_seqs, total_tokens, H, S0, o, S_final, workspace,

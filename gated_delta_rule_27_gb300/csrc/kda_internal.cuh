@@ -41,6 +41,9 @@ enum Path { PATH_SIMT = 0, PATH_TC = 1 };
 
 // int32 word of the workspace header that the persistent tensor-core preparation claims its units from
 constexpr int kPrepCounterWord = 32;
+// 64-bit word (int32 words 40-41) of the workspace header where a self-indexed pipe launch publishes its call
+// token once its first CTA has written the slot table and the status word and cleared the flags
+constexpr int kGoWord = 40;
 
 struct WsLayout {
     size_t doc_slot0_off;
@@ -204,6 +207,9 @@ cudaError_t launch_chunk_index(const int32_t *cu, int num_seqs, int total_tokens
 // plan or the state pass plan; the chain plan runs when the test hook forces it.
 enum TcPlan { TC_THREE = 0, TC_CHAIN = 2, TC_PIPE = 3 };
 TcPlan tc_plan(int num_seqs, int H, int total_tokens);
+// Whether a call of this plan does without the chunk index kernel: the pipe plan on one document sets up its
+// own slot table, status word and flags (never in the bounds-checking build, whose tests inject faults there).
+bool pipe_self_indexed(TcPlan plan, int num_seqs);
 
 // Test hooks behind include/kda_testing.h: force a plan (-1 automatic), inject a fault with a wait bound.
 void testing_set_plan(int plan);

@@ -42,6 +42,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -430,16 +431,13 @@ __device__ __forceinline__ void prep_bars_init(PrepBars *b) {
 // set, is raised (a shared word) at the same point, once the unit's operands
 // are built.  If `publish` is set, the group's previous record is published
 // there (release, once its bulk stores are complete) as soon as this unit's
-// gate tile has arrived.  `dep_wait`: the unit started before the chunk index
-// kernel was known to be complete; the claimer and the first thread wait for
-// it before the claim and before reading its tables.  Returns false after
-// recording a timeout in the status word.
+// gate tile has arrived.  Returns false after recording a timeout in the
+// status word.
 __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int Lc, uint8_t *sm, PrepBars *bars,
                              uint32_t ph, uint32_t tmem, const uint8_t *ident, int32_t *publish,
                              const PrepGroup &grp,
                              PrepShared &sh, int32_t *claim_counter = nullptr, int claim_base = 0,
-                             int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr,
-                             bool dep_wait = false) {
+                             int *next_claim = nullptr, int units = 0, int *mid_signal = nullptr) {
     float *s_beta = sh.beta, *s_bm = sh.bm, *s_F = sh.F, *s_Em = sh.Em, *s_blast = sh.blast;
     float *s_half = sh.half, *s_invk = sh.invk, *s_invq = sh.invq;
     float(*s_gabs)[kD] = sh.gabs;
@@ -451,6 +449,7 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     constexpr TcRecord R = tc_record();
     char *rec = ws + p.records_off + ((size_t)slot * H + h) * p.record_bytes;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
+    (void)status;  // (read by the bounds checks of the bounds-checking build only)
     if (!KDA_IN_BOUNDS(slot >= 0 && slot < max_chunk_slots(p.cu, p.num_seqs, kL) && h >= 0 && h < H && t0 >= 0 &&
                            Lc >= 1 && Lc <= kL && t0 + Lc <= p.cu[p.num_seqs],
                        status))
@@ -657,7 +656,6 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
     if (mid_signal && tid == 0) *reinterpret_cast<volatile int *>(mid_signal) = 1;
     constexpr int kClaimer = 64;  // a thread of warp 2: neither issuer waits for the atomic
     if (claim_counter && tid == kClaimer) {
-        if (dep_wait) tc::grid_dep_wait();  // the counter is zeroed by the chunk index kernel
         *next_claim = claim_base + atomicAdd(claim_counter, 1);
     }
 
@@ -739,7 +737,6 @@ __device__ bool prepare_unit(const PrepParams &p, int slot, int h, int t0, int L
         return false;
     }
     if (claim_counter && tid == 0) {  // the unit claimed at the operand barrier: its tiles into L2
-        if (dep_wait) tc::grid_dep_wait();  // (the slot table)
         const int un = *next_claim;
         int ndoc, nt0, nLc;
         if (un < units && locate_slot(doc_slot0, p.cu, p.num_seqs, kL, un / H, &ndoc, &nt0, &nLc)) {
@@ -1075,8 +1072,8 @@ __device__ void state_chain(const int32_t *__restrict__ cu, int num_seqs, int H,
     __shared__ uint64_t q_full[2], q_empty[2], o_full[2], o_free[2];  // FOLD: the (Qp, P) ring, output regions
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
-    // (the chunk index kernel's table and status word are complete: the kernel before this one waited for them
-    // before letting this one start)
+    // (the slot table and the status word are complete: the kernel before this one waited for the chunk index
+    // kernel before letting this one start, or, in the pipe plan, this CTA has waited for them)
     if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1861,6 +1858,13 @@ struct PipeArgs {
     unsigned long long flag_wait_ns;
     int fault;  // kFaultNoPublish only in tests of the timeout path
     OutNorm onorm;
+    // Self-indexed launch (one document, no chunk index kernel before it): the go word, this call's token, the
+    // flags and counters to clear (16-byte words) and the document order; go null otherwise.
+    unsigned long long *go = nullptr;
+    unsigned long long token = 0;
+    uint4 *clear = nullptr;
+    int clear_vec = 0;
+    int32_t *doc_order = nullptr;
 };
 
 // Output units taken in (chunk slot, head) order from the output counter by one group of 128 threads, until
@@ -1911,10 +1915,9 @@ __device__ bool pipe_outputs(const PrepParams &pp, const PipeArgs &a, uint8_t *g
     }
 }
 
-// `early`: a single document whose preparation starts before the chunk index kernel is known to be complete
-// (its slots follow from the token count); the group waits for that kernel before it claims a unit, publishes
-// a record or reads the kernel's tables.
-__device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm, bool early) {
+// A worker CTA of the pipe plan: two groups of 256 threads, each preparing units in chunk order, then forming
+// output units, once the slot table, the status word and the cleared flags are in place.
+__device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm) {
     __shared__ PrepBars pbars[2];
     __shared__ OutBars obars[2];
     __shared__ uint32_t tmem_base;
@@ -1924,7 +1927,7 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     const int H = pp.H;
     const int32_t *doc_slot0 = reinterpret_cast<const int32_t *>(pp.ws + pp.doc_slot0_off);
     // preparation units, and as many output units
-    const int units = early ? (a.total_tokens + kL - 1) / kL * H : doc_slot0[pp.num_seqs] * H;
+    const int units = doc_slot0[pp.num_seqs] * H;
     if (tid == 0) s_go = 0;
     if (gtid == 0) {
         prep_bars_init(&pbars[g]);
@@ -1976,16 +1979,10 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
         if (u >= units) break;
         const int slot = u / H, h = u % H;
         int doc = 0, t0 = -1, Lc = 0;  // (stay out of range where the slot is not found)
-        if (early) {  // the single document's chunk slot
-            t0 = slot * kL;
-            Lc = min(kL, a.total_tokens - t0);
-        } else {
-            locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
-        }
+        locate_slot(doc_slot0, pp.cu, pp.num_seqs, kL, slot, &doc, &t0, &Lc);
         // the previous record is published once this unit's gate tile has arrived; this one's stays pending
         ok = prepare_unit(pp, slot, h, t0, Lc, gsm, &pbars[g], nprep & 1u, tmem, sm + kPipeIdent, pending, grp, psh[g],
-                          a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr,
-                          early && nprep == 0);
+                          a.prep_counter, 2 * nw, &s_unit[g], units, g == 0 && nprep == 0 ? &s_go : nullptr);
         ++nprep;
         if (!ok) break;
         pending = a.ready + (size_t)slot * H + h;
@@ -2001,7 +1998,6 @@ __device__ void pipe_worker(const PrepParams &pp, const PipeArgs &a, uint8_t *sm
     grp.sync();  // every thread has read s_unit before the output phase claims into it
     if (g == 0 && gtid == 0) *reinterpret_cast<volatile int *>(&s_go) = 1;
     if (gtid == 0) tc::bulk_wait_read();  // the last unit's M' copy has read the group's shared memory
-    if (early) tc::grid_dep_wait();  // (a group that prepared nothing has not waited yet)
     if (gtid == 0 && pending) {  // before any output unit: a chain may be waiting for this record
         tc::bulk_wait_all();
         tc::fence_proxy_async_global();
@@ -2022,23 +2018,51 @@ prefill_pipe_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 char *__restrict__ ws, size_t doc_slot0_off, size_t records_off, size_t record_bytes, int qk_norm,
                 float qk_eps, PipeArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    // A single document whose cu_seqlens pass the chunk index kernel's checks (so that its status word will
-    // read valid): the workers start preparing at once and wait for that kernel only where they use what it
-    // writes (the slot table, the cleared flags and counters).
-    bool early = num_seqs == 1 && __ldg(cu) == 0 && __ldg(cu + 1) == a.total_tokens && a.total_tokens > 0;
-#ifdef KDA_DEBUG_BOUNDS
-    early = false;  // (the bounds-checking build tests its checks against the chunk table)
-#endif
-    const bool worker = (int)blockIdx.x >= a.n_chain;
-    if (!(worker && early)) {
-        tc::grid_dep_wait();  // the chunk index kernel: slot table, status word, cleared flags
-        if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
+    if (a.go) {
+        // Self-indexed (one document, no chunk index kernel before this launch): CTA 0 checks cu_seqlens (the
+        // condition above), writes the slot table, the document order and the status word and clears the flags
+        // and counters, then publishes the call's token; the other CTAs go on once they see it, as if the chunk
+        // index kernel had completed.  Invalid cu_seqlens: every CTA leaves at once and nothing is written but
+        // the status.
+        const bool valid = num_seqs == 1 && __ldg(cu) == 0 && __ldg(cu + 1) == a.total_tokens && a.total_tokens > 0;
+        tc::grid_dep_wait();  // the previous kernel in the stream, which may use this workspace, has completed
+        int32_t *status = reinterpret_cast<int32_t *>(ws);
+        if (blockIdx.x == 0) {
+            if (valid)
+                for (int i = (int)threadIdx.x; i < a.clear_vec; i += (int)blockDim.x) a.clear[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (threadIdx.x == 0) {
+                int32_t *slot0 = reinterpret_cast<int32_t *>(ws + doc_slot0_off);
+                slot0[0] = 0;
+                slot0[1] = valid ? (a.total_tokens + kL - 1) / kL : 0;
+                a.doc_order[0] = 0;
+                status[1] = 0;
+                status[kPrepCounterWord] = 0;
+                status[0] = valid ? 0 : 1;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0 && valid) {
+                __threadfence();
+                tc::st_release_gpu_u64(a.go, a.token);
+            }
+        } else if (valid) {
+            __shared__ int s_go_ok;
+            if (threadIdx.x == 0) {
+                s_go_ok = tc::wait_u64_eq(a.go, a.token, a.flag_wait_ns);
+                if (!s_go_ok) flag_timeout(ws);
+            }
+            __syncthreads();
+            if (!s_go_ok) return;
+        }
+        if (!valid) return;
     }
+    const bool worker = (int)blockIdx.x >= a.n_chain;
+    tc::grid_dep_wait();  // the chunk index kernel (if any): slot table, status word, cleared flags
+    if (*reinterpret_cast<const volatile int32_t *>(ws) != 0) return;  // invalid cu_seqlens: write nothing
     uint8_t *sm = align1024(smem_raw);
     const PrepParams pp{&tm_q,       &tm_k,        &tm_v,   &tm_g,  beta, cu, num_seqs, H, ws, doc_slot0_off,
                         records_off, record_bytes, qk_norm, qk_eps};
     if (worker) {
-        pipe_worker(pp, a, sm, early);
+        pipe_worker(pp, a, sm);
         return;
     }
     ChainLinks links;
@@ -2222,6 +2246,17 @@ const DeviceSetup &device_setup() {
     return d;
 }
 
+// A token per self-indexed pipe launch, unique within the process (a counter from a clock-derived start), so
+// that the go word a launch waits for was written by this launch.
+unsigned long long next_call_token() {
+    static std::atomic<unsigned long long> counter{
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull};
+    unsigned long long z = counter.fetch_add(0x9E3779B97F4A7C15ull) + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;  // (the SplitMix64 finaliser)
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return (z ^ (z >> 31)) | 1ull;
+}
+
 // Test hooks (include/kda_testing.h): a forced launch plan and an injected fault with a short wait bound.
 std::atomic<int> g_test_plan{-1};
 std::atomic<int> g_test_fault{0};
@@ -2260,6 +2295,16 @@ void testing_set_fault(int fault, long long wait_ns) {
     g_test_wait_ns.store(wait_ns);
 }
 int testing_fault() { return g_test_fault.load(); }
+
+bool pipe_self_indexed(TcPlan plan, int num_seqs) {
+#ifdef KDA_DEBUG_BOUNDS
+    (void)plan;
+    (void)num_seqs;
+    return false;
+#else
+    return plan == TC_PIPE && num_seqs == 1;
+#endif
+}
 
 TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     // The pipe plan for at most kPipeChainMax chains of 64 columns, else the preparation and the state pass
@@ -2312,6 +2357,14 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         a.flag_wait_ns = flag_wait;
         a.fault = g_test_fault.load();
         a.onorm = onorm;
+        const bool self = pipe_self_indexed(plan, num_seqs);
+        if (self) {
+            a.go = reinterpret_cast<unsigned long long *>(w) + kGoWord / 2;
+            a.token = next_call_token();
+            a.clear = reinterpret_cast<uint4 *>(flags);
+            a.clear_vec = (int)(lay.flags_bytes / 16);
+            a.doc_order = reinterpret_cast<int32_t *>(w + lay.doc_order_off);
+        }
         marks.before(st, "prefill_pipe_tc");
         // chains of 32 columns while they are few (a shorter step), else of 64 (half the SMs)
         const long long chains32 = (long long)num_seqs * H * kNTile;
@@ -2327,10 +2380,12 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         }
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         // Fewer SMs are available to this context than the device has: nothing was launched; run the three
-        // kernels instead.
+        // kernels instead (after the chunk index kernel, which a self-indexed launch left out).
         cudaGetLastError();
         marks.n--;
         plan = TC_THREE;
+        if (self && (e = launch_chunk_index(cu, num_seqs, total_tokens, kL, ws, nullptr, 0, st, marks)))
+            return e;
     }
     if (lay.max_slots > 0 && total_tokens > 0) {
         InputMaps m;

@@ -147,6 +147,27 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void red_relaxed_gpu_add(int32_t *p, int32_t v) {
     asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// Polls until *p == v (acquire), giving up after timeout_ns; true if the value was seen.
+__device__ __forceinline__ bool wait_u64_eq(const unsigned long long *p, unsigned long long v,
+                                            uint64_t timeout_ns = 2000000000ull) {
+    if (ld_acquire_gpu_u64(p) == v) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(32);
+            if (ld_acquire_gpu_u64(p) == v) return true;
+        }
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
 __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
     int32_t v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
