@@ -1456,13 +1456,15 @@ prefill_state_fold_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const
 // ---------------------------------------------------------------------------
 // One CTA (128 threads) per (chunk, head):  O = Qp S_c + P Ut, with S_c the
 // state entering the chunk (its bf16 image, written by the state pass).  Both
-// products accumulate into one 128-lane TMEM tile whose lanes 0-63 are the
-// chunk's tokens: A = [Qp ; *] (MN-major) and [P ; *] (K-major) are read as
-// 128-row operands whose upper 64 rows fall on other record images and give
-// accumulator rows nobody reads.
+// products accumulate into one 128-lane TMEM tile that holds the chunk's 64
+// token rows twice: A = [Qp ; Qp] (MN-major, the stride between its two 64-row
+// halves zero) and [P ; P] (K-major, P loaded twice, one copy after the other).
+// The record's Qp and P as stored, P a second time (so that the 128-row operand [P ; P] repeats the chunk's
+// rows), Ut, the state image, and a 512-byte exchange area of the gated epilogue.
 struct OutSmem {
-    static constexpr uint32_t Qp = 0, P = 16384, Ut = 24576, S = 40960;  // the record's [Qp, end) as stored
-    static constexpr uint32_t bytes = 73728;
+    static constexpr uint32_t Qp = 0, P = 16384, P2 = 24576, Ut = 32768, S = 49152, X = 81920;
+    static constexpr uint32_t kRec = S;  // bytes of the record part (Qp, P, P, Ut)
+    static constexpr uint32_t bytes = 82944;
 };
 
 struct OutBars {
@@ -1499,8 +1501,8 @@ struct OutNext {
 };
 
 // One (chunk slot, head) of the output pass, t0 / Lc the chunk's first token and
-// length, by a group of 128 threads (warps 0-1 of it write the 64 token rows)
-// whose TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's
+// length, by a group of 128 threads (its four warps each write 32 token rows by
+// 64 columns) whose TMEM holds 128 columns at `tmem`; `ph` is the parity of this unit's
 // barrier phases.  P Ut is formed first; the state image is then awaited
 // through the launch dependency with `dep_wait` (the state pass is the
 // previous kernel), or through its publication count at `sflag` (all column
@@ -1515,9 +1517,20 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
                             const OutNext *nx = nullptr) {
     const int tid = grp.gtid, warp = tid >> 5;
     constexpr TcRecord R = tc_record();
-    static_assert(R.bytes - R.Qp == OutSmem::bytes && R.P - R.Qp == OutSmem::P && R.Ut - R.Qp == OutSmem::Ut &&
-                      R.S - R.Qp == OutSmem::S,
-                  "output pass loads the record tail as one image");
+    static_assert(R.P - R.Qp == OutSmem::P && R.Ut - R.P == OutSmem::P2 - OutSmem::P &&
+                      R.S - R.Ut == OutSmem::S - OutSmem::Ut && R.bytes - R.S == OutSmem::X - OutSmem::S,
+                  "the record's Qp, P, Ut and image in the output unit's layout");
+    // the record part: Qp and P in one copy, P again, Ut; the image in one copy
+    auto load_rec = [&](const char *rc) {
+        tc::mbar_arrive_expect_tx(&bars->load, OutSmem::kRec);
+        tc::bulk_g2s(sm, rc + R.Qp, (uint32_t)(R.Ut - R.Qp), &bars->load);
+        tc::bulk_g2s(sm + OutSmem::P2, rc + R.P, (uint32_t)(R.Ut - R.P), &bars->load);
+        tc::bulk_g2s(sm + OutSmem::Ut, rc + R.Ut, (uint32_t)(R.S - R.Ut), &bars->load);
+    };
+    auto load_img = [&](const char *rc) {
+        tc::mbar_arrive_expect_tx(&bars->sload, (uint32_t)(R.bytes - R.S));
+        tc::bulk_g2s(sm + OutSmem::S, rc + R.S, (uint32_t)(R.bytes - R.S), &bars->sload);
+    };
     const char *rec = ws + records_off + ((size_t)slot * H + h) * record_bytes;
 #ifdef KDA_DEBUG_BOUNDS
     const int total_tokens = cu[num_seqs];
@@ -1538,16 +1551,12 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
             // a unit taken behind the chains finds its state image published already: both loads go at once
             img_now = sflag && !dep_wait && tc::ld_acquire_gpu(sflag) >= kNTile;
             if (img_now) tc::fence_proxy_async_global();
-            tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
-            tc::bulk_g2s(sm, rec + R.Qp, OutSmem::S, &bars->load);
-            if (img_now) {
-                tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
-                tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
-            }
+            load_rec(rec);
+            if (img_now) load_img(rec);
         }
         bool ok = tc::mbar_wait(&bars->load, ph) && rok;
         constexpr uint64_t kKmaj = tc::smem_desc_base(16, 1024, tc::SW_128B);
-        constexpr uint64_t kQpMn = tc::smem_desc_base(16384, 1024, tc::SW_128B);  // rows 64+ -> P, Ut: unused
+        constexpr uint64_t kQpMn = tc::smem_desc_base(0, 1024, tc::SW_128B);  // rows 64-127 repeat rows 0-63
         constexpr uint64_t kSMn = tc::smem_desc_base(8192, 512, tc::SW_64B);     // the image, as the chains write it
         constexpr uint32_t id_mn = tc::idesc_bf16_f32(128, 128, true, true);
         constexpr uint32_t id_k = tc::idesc_bf16_f32(128, 128, false, false);
@@ -1564,8 +1573,7 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
                 ok = tc::wait_flag_geq(sflag, kNTile, flag_wait_ns) && ok;
                 tc::fence_proxy_async_global();
             }
-            tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
-            tc::bulk_g2s(sm + OutSmem::S, rec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+            load_img(rec);
         }
         ok = tc::mbar_wait(&bars->sload, ph) && ok;
         *grp.ok = ok;
@@ -1586,73 +1594,82 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
         if (un < nx->units && tc::mbar_wait(&bars->mma, ph) && tc::ld_acquire_gpu(nx->ready + un) >= 1) {
             const char *nrec = ws + records_off + (size_t)un * record_bytes;
             tc::fence_proxy_async_global();
-            tc::mbar_arrive_expect_tx(&bars->load, OutSmem::S);
-            tc::bulk_g2s(sm, nrec + R.Qp, OutSmem::S, &bars->load);
+            load_rec(nrec);
             p = 1;
             if (tc::ld_acquire_gpu(nx->sdone + un) >= kNTile) {
                 tc::fence_proxy_async_global();
-                tc::mbar_arrive_expect_tx(&bars->sload, OutSmem::bytes - OutSmem::S);
-                tc::bulk_g2s(sm + OutSmem::S, nrec + R.S, OutSmem::bytes - OutSmem::S, &bars->sload);
+                load_img(nrec);
                 p = 2;
             }
         }
         *nx->pre = p;
     }
-    if (warp < 2) {
-        // token row r = tid: 128 fp32 accumulators -> 256 bytes of o
+    __syncwarp();  // (the lane of warp 2 that loaded the next unit rejoins its warp)
+    {
+        // O sits twice in the accumulator (A = [Qp ; Qp] and [P ; P]): warp w writes token row 32 (w % 2) +
+        // lane, columns 64 (w / 2) .. + 63, from TMEM lane 32 w + lane.
         const bool done = tc::mbar_wait(&bars->mma, ph);
         tc::tc_fence_after();
-        if (warp_all(done)) {
-            const int r = tid;
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            const size_t row = ((size_t)(t0 + r) * H + h) * kD;
-            uint4 *dst = reinterpret_cast<uint4 *>(o + row);
-            const bool row_ok = KDA_IN_BOUNDS(r >= Lc || t0 + r < total_tokens, reinterpret_cast<int32_t *>(ws));
-            const bool write = r < Lc && row_ok;
-            if (!onorm.gate) {
+        const bool wok = warp_all(done);
+        const int lane = tid & 31, r = (warp & 1) * 32 + lane, ch = warp >> 1;
+        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(64 * ch);
+        const size_t row = ((size_t)(t0 + r) * H + h) * kD + (size_t)(64 * ch);
+        uint4 *dst = reinterpret_cast<uint4 *>(o + row);
+        const bool row_ok = KDA_IN_BOUNDS(r >= Lc || t0 + r < total_tokens, reinterpret_cast<int32_t *>(ws));
+        const bool write = wok && r < Lc && row_ok;
+        if (!onorm.gate) {
+            if (wok) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float v[32];
-                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                    tc::tmem_ld32(ta + (uint32_t)(q * 32), v);
                     if (write) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) dst[q * 4 + u] = pack8_at(v + 8 * u);
                     }
                 }
-            } else {
-                // fused epilogue: o / rms(o) * w * sigmoid(z).  The row's gate inputs are fetched a quarter
-                // ahead of their use (the first quarter before the mean square), the weights are uniform
-                // across the warp (broadcast loads), the logistic function takes the fast exponential and
-                // division (bf16 output).
-                const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row);
-                uint4 zc[4], zn[4];
+            }
+        } else {
+            // fused epilogue: o / rms(o) * w * sigmoid(z).  The mean square adds the two column halves' sums,
+            // exchanged through shared memory; the gate inputs of the second 32 columns are fetched while the
+            // first are written, the weights are uniform across the warp (broadcast loads), the logistic
+            // function takes the fast exponential and division (bf16 output).
+            const uint4 *z4 = reinterpret_cast<const uint4 *>(onorm.gate + row);
+            uint4 zc[4], zn[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) zc[u] = write ? __ldg(z4 + u) : make_uint4(0u, 0u, 0u, 0u);
-                float ss = 0.f;
+            for (int u = 0; u < 4; ++u) zc[u] = write ? __ldg(z4 + u) : make_uint4(0u, 0u, 0u, 0u);
+            float ss = 0.f;
+            if (wok) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float v[32];
-                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                    tc::tmem_ld32(ta + (uint32_t)(q * 32), v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
                 }
-                const float scale = rsqrtf(ss * (1.f / kD) + onorm.eps);
+            }
+            float *xs = reinterpret_cast<float *>(sm + OutSmem::X);
+            xs[warp * 32 + lane] = ss;
+            grp.sync();
+            const float tot = xs[(warp & 1) * 32 + lane] + xs[(2 + (warp & 1)) * 32 + lane];  // (the same order in both)
+            const float scale = rsqrtf(tot * (1.f / kD) + onorm.eps);
+            if (wok) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (q < 3) {
+                for (int q = 0; q < 2; ++q) {
+                    if (q == 0) {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            zn[u] = write ? __ldg(z4 + (q + 1) * 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+                        for (int u = 0; u < 4; ++u) zn[u] = write ? __ldg(z4 + 4 + u) : make_uint4(0u, 0u, 0u, 0u);
                     }
                     float v[32];
-                    tc::tmem_ld32(tmem + lane_base + (uint32_t)(q * 32), v);
+                    tc::tmem_ld32(ta + (uint32_t)(q * 32), v);
                     if (write) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             float z[8], wv[8];
                             unpack8(zc[u], z);
                             if (onorm.weight) {
-                                const float4 *w4 = reinterpret_cast<const float4 *>(onorm.weight + q * 32 + u * 8);
+                                const float4 *w4 =
+                                    reinterpret_cast<const float4 *>(onorm.weight + 64 * ch + q * 32 + u * 8);
                                 *reinterpret_cast<float4 *>(wv) = __ldg(w4);
                                 *reinterpret_cast<float4 *>(wv + 4) = __ldg(w4 + 1);
                             } else {
@@ -1665,15 +1682,14 @@ __device__ bool output_unit(const int32_t *__restrict__ cu, int num_seqs, int H,
                             dst[q * 4 + u] = pack8_at(v + 8 * u);
                         }
                     }
-                    if (q < 3) {
+                    if (q == 0) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) zc[u] = zn[u];
                     }
                 }
             }
-        } else if ((tid & 31) == 0) {
-            flag_timeout(ws);
         }
+        if (!wok && lane == 0) flag_timeout(ws);
     }
     tc::tc_fence_before();
     grp.sync();
@@ -1707,7 +1723,7 @@ prefill_output_tc(const int32_t *__restrict__ cu, int num_seqs, int H, __nv_bflo
         if (resident > 0 && nxt < (int)(gridDim.x * gridDim.y) && (nxt % gridDim.x) < doc_slot0[num_seqs])
             tc::bulk_prefetch_l2(ws + records_off + ((size_t)(nxt % gridDim.x) * H + nxt / gridDim.x) * record_bytes +
                                      tc_record().Qp,
-                                 OutSmem::bytes);
+                                 (uint32_t)(tc_record().bytes - tc_record().Qp));
     }
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base, 128);
@@ -1794,7 +1810,8 @@ prefill_chain_tc(const int32_t *__restrict__ cu, int num_seqs, int H, const floa
                 // the unit some group will take one round later: its Qp, P, Ut into L2 meanwhile
                 const int un = u + workers;
                 if (un < units && un < rec_units)
-                    tc::bulk_prefetch_l2(ws + records_off + (size_t)un * record_bytes + tc_record().Qp, OutSmem::S);
+                    tc::bulk_prefetch_l2(ws + records_off + (size_t)un * record_bytes + tc_record().Qp,
+                                         (uint32_t)(tc_record().S - tc_record().Qp));
             }
             grp.sync();
             const int u = s_unit[g];
