@@ -1850,7 +1850,7 @@ constexpr int kChainMinWorkers = 48;  // output CTAs alongside the chains, at le
 // and MMAs, and a worker group publishes its last record before it takes any output unit; a chain waits only
 // for records; an output unit waits for a record and for the chains.  Every wait is bounded.
 constexpr int kPipeThreads = 512;
-constexpr int kPipeChainMax = 40;    // automatic choice: at most this many chains of 64 columns ...
+constexpr int kPipeChainMax = 48;    // automatic choice: at most this many chains of 64 columns ...
 constexpr int kPipeChain32Max = 32;  // ... and chains of 32 columns (a shorter step) up to this many of them
 constexpr uint32_t kPipePrepShared = 2 * PrepSmem::bytes;  // the worker groups' PrepShared, after their tiles
 // the workers' identity image, after both groups' PrepShared (1024-byte aligned)
@@ -2327,9 +2327,9 @@ TcPlan tc_plan(int num_seqs, int H, int total_tokens) {
     // The pipe plan for at most kPipeChainMax chains of 64 columns, else the preparation and the state pass
     // (which, without the gated output normalisation, forms the outputs itself; with it, an output pass
     // follows, since that normalisation needs whole rows).  Measured on one document of 4096 tokens (pass
-    // times with the host calls): 16 heads pipe 108 us, chain 143, three 146; 24 heads three 163, pipe 170,
-    // chain 177; with the fused q/k and gated output norms, 16 heads pipe 140, chain 154, three 166; 24 heads
-    // three 205, pipe 215, chain 250.  The chain plan is taken only when the test hook forces it.
+    // times, calls queued back to back): 8 heads pipe 75 us, chain 97, three 100; 24 heads pipe 132, three
+    // 141, chain 154; 32 heads three 161, chain 162, pipe 194.  The chain plan is taken only when the test
+    // hook forces it.
     const WsLayout lay = ws_layout(total_tokens, num_seqs, H, kD, kD, kL, PATH_TC);
     if (lay.max_slots <= 0 || total_tokens <= 0) return TC_THREE;
     const int forced = g_test_plan.load();

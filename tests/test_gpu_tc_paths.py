@@ -140,13 +140,13 @@ def _kernel_names(inp, S0):
 
 @pytest.mark.parametrize("extra_heads", [0, 1])
 def test_beyond_the_pipe_plan_the_state_pass_forms_the_outputs(extra_heads):
-    """One document with 21 heads (one past the pipe plan's 40 chains of 64 columns) and with as many heads as
+    """One document with 25 heads (one past the pipe plan's 48 chains of 64 columns) and with as many heads as
     leave 48 SMs beside chains of 32 columns, plus one: without the gated output normalisation the automatic
     plan is the preparation and the state pass that forms the outputs itself (two kernels), which matches the
     chain plan, whose output groups form them from the state images, bit for bit, and meets the bf16 tolerance
     against the oracle."""
     sms = torch.cuda.get_device_properties(dev()).multi_processor_count
-    H = 21 if extra_heads == 0 else (sms - 48) // 4 + 1
+    H = 25 if extra_heads == 0 else (sms - 48) // 4 + 1
     inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=77 + extra_heads, s0_std=0.1)
     names = _kernel_names(inp, inp.S0)
     assert names == ["chunk_index", "prefill_prepare_tc", "prefill_state_fold_tc"], names
@@ -158,13 +158,13 @@ def test_beyond_the_pipe_plan_the_state_pass_forms_the_outputs(extra_heads):
     assert rel(S_a, S_ref) <= TOL[torch.bfloat16], rel(S_a, S_ref)
 
 
-@pytest.mark.parametrize("H", [8, 9, 20, 21])
+@pytest.mark.parametrize("H", [8, 9, 24, 25])
 def test_pipe_plan_at_its_thresholds(H):
     """One document with 8 heads (the most whose chains run 32 columns wide in the pipe plan) and 9 (64 wide),
-    with 20 heads (40 chains of 64 columns, the most the automatic pipe plan takes) and with 21 heads (the chain
-    plan then): the automatic choice is the expected plan, matches the three-kernel plan bit for bit and meets
-    the bf16 tolerance against the oracle."""
-    extra_heads = 1 if H == 21 else 0
+    with 24 heads (48 chains of 64 columns, the most the automatic pipe plan takes) and with 25 heads (the
+    two-kernel plan then): the automatic choice is the expected plan, matches the three-kernel plan bit for bit
+    and meets the bf16 tolerance against the oracle."""
+    extra_heads = 1 if H == 25 else 0
     inp = workloads.prefill_inputs([300], H=H, d=128, dtype=torch.bfloat16, seed=97 + H, s0_std=0.1)
     names = _kernel_names(inp, inp.S0)
     assert ("prefill_pipe_tc" in names) == (extra_heads == 0), names
