@@ -179,9 +179,10 @@ def test_pipe_plan_at_its_thresholds(H):
 @pytest.mark.parametrize("plan", ["pipe", "three", "chain"])
 @pytest.mark.parametrize("lengths,bad", [([300], [0, 301]), ([300], [1, 300]), ([200, 100], [0, 250, 240])])
 def test_invalid_cu_seqlens_write_nothing_on_the_tensor_core_paths(plan, lengths, bad):
-    """cu_seqlens that fail the chunk index kernel's checks (not starting at 0, not ending at the token count,
-    decreasing) leave o and S_final untouched under every plan, the pipe plan's early start for a single
-    document included, and are reported; a valid call on the same workspace afterwards is right."""
+    """cu_seqlens that fail the chunk index checks (not starting at 0, not ending at the token count,
+    decreasing) leave o and S_final untouched under every plan, the pipe plan's self-indexed launch for a single
+    document (which makes those checks itself) included, and are reported; a valid call on the same workspace
+    afterwards is right."""
     inp = workloads.prefill_inputs(lengths, H=4, d=128, dtype=torch.bfloat16, seed=71)
     q, k, v, g, beta, cu_ok = to_device(inp)
     T, H, d = q.shape
